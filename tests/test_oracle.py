@@ -1,0 +1,289 @@
+"""Pins for the CPU fp64 oracle, independent of the oracle's own code.
+
+Each pin comes from outside the oracle: hand-derived values (tests/golden),
+closed forms, a library attention routine (torch's scaled_dot_product_attention
+and autograd, float64), central finite differences, gradient identities, and
+the agreement of the two independent routes (plain definition vs. the CP
+step/merge procedure).
+"""
+import json
+import math
+import os
+import random
+
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from oracle import attention_backward, attention_forward, cp_attention_forward
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+F64 = torch.float64
+
+
+def _num(x):
+    if isinstance(x, (int, float)):
+        return float(x)
+    table = {"ln3": math.log(3), "ln4": math.log(4), "ln5": math.log(5), "sqrt2ln2": math.sqrt(2) * math.log(2),
+             "5/3": 5 / 3, "10/3": 10 / 3, "0.75ln3": 0.75 * math.log(3)}
+    return table[x]
+
+
+def _t(rows):
+    return torch.tensor([[_num(x) for x in row] for row in rows], dtype=F64)
+
+
+def _rand(*shape, gen, std=1.0):
+    return torch.randn(*shape, generator=gen, dtype=F64) * std
+
+
+def _library_attention(q, k, v, causal):
+    """torch SDPA in float64 with K/V heads repeated for GQA: [b,s,h,d] layout."""
+    G = q.shape[2] // k.shape[2]
+    kk = k.repeat_interleave(G, dim=2)
+    vv = v.repeat_interleave(G, dim=2)
+    out = F.scaled_dot_product_attention(q.transpose(1, 2), kk.transpose(1, 2), vv.transpose(1, 2),
+                                         is_causal=causal)
+    return out.transpose(1, 2)
+
+
+def _library_lse(q, k, causal):
+    G = q.shape[2] // k.shape[2]
+    kk = k.repeat_interleave(G, dim=2)
+    S = torch.einsum("bthd,bjhd->bhtj", q, kk) / math.sqrt(q.shape[-1])
+    if causal:
+        s = q.shape[1]
+        S = S.masked_fill(torch.ones(s, s, dtype=torch.bool).triu(1), float("-inf"))
+    return torch.logsumexp(S, dim=-1)
+
+
+# ------------------------------------------------------------ hand values
+def test_golden_forward():
+    data = json.load(open(os.path.join(GOLDEN, "hand_attention.json")))
+    for case in data["cases"]:
+        q, k, v = (_t(case[n])[None, :, None, :] for n in ("q", "k", "v"))
+        for mode, causal in (("causal", True), ("full", False)):
+            o, lse = attention_forward(q, k, v, causal=causal)
+            want_o = _t(case[mode]["o"])
+            want_l = torch.tensor([_num(x) for x in case[mode]["lse"]], dtype=F64)
+            assert torch.allclose(o[0, :, 0], want_o, atol=1e-13), (case["name"], mode)
+            assert torch.allclose(lse[0, 0], want_l, atol=1e-13), (case["name"], mode)
+
+
+def test_golden_backward():
+    data = json.load(open(os.path.join(GOLDEN, "hand_attention.json")))
+    case = data["cases"][0]
+    q, k, v = (_t(case[n])[None, :, None, :] for n in ("q", "k", "v"))
+    bw = case["backward"]
+    do = _t(bw["do"])[None, :, None, :]
+    dq, dk, dv = attention_backward(q, k, v, do, causal=True)
+    assert torch.allclose(dq[0, :, 0], _t(bw["dq"]), atol=1e-13)
+    assert torch.allclose(dk[0, :, 0], _t(bw["dk"]), atol=1e-13)
+    assert torch.allclose(dv[0, :, 0], _t(bw["dv"]), atol=1e-13)
+
+
+# ------------------------------------------------------------ library routine
+@pytest.mark.parametrize("b,s,hq,hkv,d", [(1, 1, 1, 1, 4), (2, 37, 4, 2, 8), (1, 50, 6, 3, 16), (1, 64, 8, 1, 5)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_forward_matches_library(b, s, hq, hkv, d, causal):
+    g = torch.Generator().manual_seed(s * 131 + hq)
+    q, k, v = _rand(b, s, hq, d, gen=g), _rand(b, s, hkv, d, gen=g), _rand(b, s, hkv, d, gen=g)
+    o, lse = attention_forward(q, k, v, causal=causal, row_block=16)
+    assert torch.allclose(o, _library_attention(q, k, v, causal), atol=1e-12, rtol=0)
+    assert torch.allclose(lse, _library_lse(q, k, causal), atol=1e-12, rtol=0)
+
+
+@pytest.mark.parametrize("b,s,hq,hkv,d", [(1, 19, 2, 1, 4), (2, 24, 4, 2, 8)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_backward_matches_autograd(b, s, hq, hkv, d, causal):
+    g = torch.Generator().manual_seed(7 + s)
+    q, k, v, do = (_rand(b, s, hq, d, gen=g), _rand(b, s, hkv, d, gen=g), _rand(b, s, hkv, d, gen=g),
+                   _rand(b, s, hq, d, gen=g))
+    qa, ka, va = (x.clone().requires_grad_(True) for x in (q, k, v))
+    (_library_attention(qa, ka, va, causal) * do).sum().backward()
+    dq, dk, dv = attention_backward(q, k, v, do, causal=causal, row_block=8)
+    assert torch.allclose(dq, qa.grad, atol=1e-11, rtol=0)
+    assert torch.allclose(dk, ka.grad, atol=1e-11, rtol=0)
+    assert torch.allclose(dv, va.grad, atol=1e-11, rtol=0)
+
+
+# ------------------------------------------------------------ closed forms / invariants
+def test_zero_query_gives_running_mean():
+    g = torch.Generator().manual_seed(3)
+    s, d = 33, 6
+    q = torch.zeros(1, s, 2, d, dtype=F64)
+    k, v = _rand(1, s, 1, d, gen=g), _rand(1, s, 1, d, gen=g)
+    o, lse = attention_forward(q, k, v, causal=True)
+    mean = torch.cumsum(v[0, :, 0], dim=0) / torch.arange(1, s + 1, dtype=F64)[:, None]
+    for h in range(2):
+        assert torch.allclose(o[0, :, h], mean, atol=1e-13)
+        assert torch.allclose(lse[0, h], torch.log(torch.arange(1, s + 1, dtype=F64)), atol=1e-13)
+
+
+def test_constant_values_pass_through():
+    g = torch.Generator().manual_seed(4)
+    s, d = 20, 5
+    q, k = _rand(1, s, 1, d, gen=g, std=3), _rand(1, s, 1, d, gen=g, std=3)
+    row = _rand(d, gen=g)
+    v = row.expand(1, s, 1, d).clone()
+    o, _ = attention_forward(q, k, v, causal=True)
+    assert torch.allclose(o[0, :, 0], row.expand(s, d), atol=1e-12)
+
+
+def test_probability_rows_sum_to_one_and_respect_mask():
+    # one-hot values expose the probability matrix itself: O[t] = P[t, :]
+    g = torch.Generator().manual_seed(5)
+    s = d = 12
+    q, k = _rand(1, s, 1, d, gen=g, std=2), _rand(1, s, 1, d, gen=g, std=2)
+    v = torch.eye(s, dtype=F64)[None, :, None, :]
+    P, _ = attention_forward(q, k, v, causal=True)
+    P = P[0, :, 0]
+    assert torch.allclose(P.sum(dim=1), torch.ones(s, dtype=F64), atol=1e-14)
+    assert torch.all(P.triu(1) == 0)
+    assert torch.all(P[torch.ones(s, s, dtype=torch.bool).tril()] > 0)
+
+
+def test_backward_finite_differences():
+    g = torch.Generator().manual_seed(11)
+    b, s, hq, hkv, d = 1, 6, 2, 1, 3
+    q, k, v, do = (_rand(b, s, hq, d, gen=g), _rand(b, s, hkv, d, gen=g), _rand(b, s, hkv, d, gen=g),
+                   _rand(b, s, hq, d, gen=g))
+
+    def loss(q_, k_, v_):
+        return float((attention_forward(q_, k_, v_, causal=True)[0] * do).sum())
+
+    dq, dk, dv = attention_backward(q, k, v, do, causal=True)
+    eps = 1e-6
+    for name, x, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = torch.zeros_like(x)
+        flat, nflat = x.view(-1), num.view(-1)
+        for i in range(flat.numel()):
+            old = float(flat[i])
+            flat[i] = old + eps
+            up = loss(q, k, v)
+            flat[i] = old - eps
+            dn = loss(q, k, v)
+            flat[i] = old
+            nflat[i] = (up - dn) / (2 * eps)
+        assert torch.allclose(grad, num, atol=1e-7, rtol=1e-6), name
+
+
+def test_gradient_identities():
+    g = torch.Generator().manual_seed(12)
+    b, s, hq, hkv, d = 2, 29, 4, 2, 8
+    q, k, v, do = (_rand(b, s, hq, d, gen=g), _rand(b, s, hkv, d, gen=g), _rand(b, s, hkv, d, gen=g),
+                   _rand(b, s, hq, d, gen=g))
+    _, dk, dv = attention_backward(q, k, v, do, causal=True, row_block=7)
+    G = hq // hkv
+    # rows of P sum to 1  =>  sum_j dV_j = sum over the group's heads and all t of dO_t
+    want = do.view(b, s, hkv, G, d).sum(dim=(1, 3))
+    assert torch.allclose(dv.sum(dim=1), want, atol=1e-12)
+    # rows of dS sum to 0  =>  sum_j dK_j = 0
+    assert torch.allclose(dk.sum(dim=1), torch.zeros_like(want), atol=1e-12)
+
+
+def test_row_and_head_subsets_match_full():
+    g = torch.Generator().manual_seed(13)
+    b, s, hq, hkv, d = 1, 40, 4, 2, 8
+    q, k, v, do = (_rand(b, s, hq, d, gen=g), _rand(b, s, hkv, d, gen=g), _rand(b, s, hkv, d, gen=g),
+                   _rand(b, s, hq, d, gen=g))
+    rows = [39, 0, 17, 5]
+    o_full, l_full = attention_forward(q, k, v)
+    o_s, l_s = attention_forward(q, k, v, rows=rows)
+    assert torch.equal(o_s, o_full[:, rows]) or torch.allclose(o_s, o_full[:, rows], atol=1e-14)
+    assert torch.allclose(l_s, l_full[:, :, rows], atol=1e-14)
+    dq_f, dk_f, dv_f = attention_backward(q, k, v, do)
+    dq_s, dk_s, dv_s = attention_backward(q, k, v, do, dq_rows=rows, dkv_heads=[1])
+    assert torch.allclose(dq_s, dq_f[:, rows], atol=1e-13)
+    assert torch.allclose(dk_s[:, :, 0], dk_f[:, :, 1], atol=1e-13)
+    assert torch.allclose(dv_s[:, :, 0], dv_f[:, :, 1], atol=1e-13)
+
+
+# ------------------------------------------------------------ the CP route
+def test_zigzag_split_golden():
+    data = json.load(open(os.path.join(GOLDEN, "zigzag_split.json")))
+    for case in data["cases"]:
+        if "chunks" in case:
+            assert [list(ch) for _, ch in oracle.zigzag_chunks(case["cp"])] == case["chunks"]
+        else:
+            got = oracle.zigzag_global_index(case["s"], case["cp"]).tolist()
+            assert got == case["global_of_local"]
+
+
+@pytest.mark.parametrize("cp", [1, 2, 3, 4, 5, 8, 16])
+def test_zigzag_index_is_a_balanced_bijection(cp):
+    c = 3
+    s = 2 * cp * c
+    idx = oracle.zigzag_global_index(s, cp)
+    assert sorted(idx.reshape(-1).tolist()) == list(range(s))
+    # each rank's causal work (number of visible keys) is the same
+    work = [(idx[r] + 1).sum().item() for r in range(cp)]
+    assert len(set(work)) == 1
+
+
+@pytest.mark.parametrize("cp", [1, 2, 3, 4, 6])
+@pytest.mark.parametrize("causal", [True, False])
+def test_step_plan_covers_each_pair_once(cp, causal):
+    """Brute force: the blocks of every rank's steps cover each visible
+    (query, key) pair of its rows exactly once, and no masked pair except
+    inside the causal step."""
+    c = 2
+    s = 2 * cp * c
+    for r in range(cp):
+        count = torch.zeros(s, s, dtype=torch.long)
+        for (_i, _j, q_ch, kv_ch, masked) in oracle.cp_step_plan(r, cp, causal):
+            for qc in q_ch:
+                for kc in kv_ch:
+                    for t in range(qc * c, (qc + 1) * c):
+                        for j in range(kc * c, (kc + 1) * c):
+                            if masked and j > t:
+                                continue
+                            assert not causal or j <= t, "unmasked block reaches a future key"
+                            count[t, j] += 1
+        mine = oracle.zigzag_global_index(s, cp)[r].tolist()
+        for t in range(s):
+            want = [1 if (t in mine and (j <= t or not causal)) else 0 for j in range(s)]
+            assert count[t].tolist() == want, (r, t)
+
+
+@pytest.mark.parametrize("b,s,hq,hkv,d,cp", [(1, 8, 1, 1, 4, 1), (1, 24, 2, 1, 4, 3), (2, 32, 4, 2, 8, 4),
+                                              (1, 40, 2, 2, 3, 5)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_cp_route_equals_uncut(b, s, hq, hkv, d, cp, causal):
+    g = torch.Generator().manual_seed(100 + s + cp)
+    q, k, v = _rand(b, s, hq, d, gen=g), _rand(b, s, hkv, d, gen=g), _rand(b, s, hkv, d, gen=g)
+    o_ref, l_ref = attention_forward(q, k, v, causal=causal)
+    o_cp, l_cp = cp_attention_forward(q, k, v, cp, causal=causal)
+    assert torch.allclose(o_cp, o_ref, atol=1e-12, rtol=0)
+    assert torch.allclose(l_cp, l_ref, atol=1e-12, rtol=0)
+
+
+def test_merge_is_order_independent():
+    g = torch.Generator().manual_seed(21)
+    b, s, hq, hkv, d, cp = 1, 32, 2, 1, 8, 4
+    q, k, v = _rand(b, s, hq, d, gen=g, std=2), _rand(b, s, hkv, d, gen=g, std=2), _rand(b, s, hkv, d, gen=g)
+    o0, l0 = cp_attention_forward(q, k, v, cp)
+    rng = random.Random(5)
+
+    def shuffled(idx):
+        idx = list(idx)
+        rng.shuffle(idx)
+        return idx
+
+    for order in (lambda x: list(reversed(x)), shuffled, shuffled):
+        o1, l1 = cp_attention_forward(q, k, v, cp, merge_order=order)
+        assert torch.allclose(o1, o0, atol=1e-12)
+        assert torch.allclose(l1, l0, atol=1e-12)
+
+
+def test_lse_merge_two_halves_closed_form():
+    # exp(L) of the merge is the sum of the parts' exp(L): log-add-exp by hand
+    L1, L2 = torch.tensor([0.0, 2.0], dtype=F64), torch.tensor([math.log(3.0), -1.0], dtype=F64)
+    O1, O2 = torch.tensor([[1.0], [0.0]], dtype=F64), torch.tensor([[5.0], [4.0]], dtype=F64)
+    O, L = oracle.lse_merge([(O1, L1), (O2, L2)])
+    assert abs(L[0] - math.log(4.0)) < 1e-15
+    assert abs(O[0, 0] - (1.0 * 1 / 4 + 5.0 * 3 / 4)) < 1e-14
+    w = 1.0 / (1.0 + math.exp(-3.0))
+    assert abs(L[1] - (2.0 + math.log(1 + math.exp(-3.0)))) < 1e-14
+    assert abs(O[1, 0] - 4.0 * (1 - w)) < 1e-14

@@ -1,1 +1,173 @@
-"""GB300-native context-parallel causal attention (placeholder; binding follows)."""
+"""GB300-native context-parallel causal attention.
+
+Python binding of the C-ABI library ``libcpattn.so`` (include/cpattn.h).
+This module only marshals arguments: it checks tensor properties, allocates
+outputs with PyTorch when the caller does not pass them, and hands raw device
+pointers, sizes and the current CUDA stream to the library. Every step of the
+computation runs in the library's CUDA kernels; there is no fallback. If the
+library has not been built the calls raise.
+"""
+import ctypes
+import os
+
+import torch
+
+from ._build import LIB_PATH, build  # noqa: F401
+
+__all__ = [
+    "CpattnError",
+    "cpattn_fwd",
+    "cpattn_bwd",
+    "cpattn_bwd_workspace_bytes",
+    "cpattn_zigzag_index",
+    "cpattn_device_status",
+    "library",
+]
+
+CPATTN_ERRORS = {
+    -1: "CPATTN_ERR_INVALID_ARG",
+    -2: "CPATTN_ERR_NULL_PTR",
+    -3: "CPATTN_ERR_MISALIGNED",
+    -4: "CPATTN_ERR_UNSUPPORTED_ARCH",
+    -5: "CPATTN_ERR_WORKSPACE_TOO_SMALL",
+    -6: "CPATTN_ERR_LAUNCH_FAILED",
+    -7: "CPATTN_ERR_TIMEOUT",
+    -8: "CPATTN_ERR_CUDA",
+}
+
+
+class CpattnError(RuntimeError):
+    def __init__(self, code, what):
+        self.code = code
+        lib = _LIB
+        msg = lib.cpattn_strerror(code).decode() if lib is not None else CPATTN_ERRORS.get(code, "error")
+        super().__init__(f"{what}: {CPATTN_ERRORS.get(code, code)} ({msg})")
+
+
+_LIB = None
+_i, _p, _sz = ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+
+
+def library():
+    """Load libcpattn.so (once). Raises if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with context_blockwise_causal_gb300.build()")
+        lib = ctypes.CDLL(LIB_PATH)
+        lib.cpattn_fwd.argtypes = [_p, _p, _p, _p, _p] + [_i] * 7 + [_p]
+        lib.cpattn_fwd.restype = _i
+        lib.cpattn_bwd.argtypes = [_p] * 10 + [_sz] + [_i] * 7 + [_p]
+        lib.cpattn_bwd.restype = _i
+        lib.cpattn_bwd_workspace_bytes.argtypes = [_i] * 6
+        lib.cpattn_bwd_workspace_bytes.restype = _sz
+        lib.cpattn_zigzag_index.argtypes = [_i, _i, _p]
+        lib.cpattn_zigzag_index.restype = _i
+        lib.cpattn_device_status.argtypes = [_p, ctypes.POINTER(_i)]
+        lib.cpattn_device_status.restype = _i
+        lib.cpattn_strerror.argtypes = [_i]
+        lib.cpattn_strerror.restype = ctypes.c_char_p
+        lib.cpattn_version.argtypes = []
+        lib.cpattn_version.restype = _i
+        _LIB = lib
+    return _LIB
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_act(name, t, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _dims(q, k, v):
+    _check_act("q", q)
+    if q.dim() != 4:
+        raise ValueError("q must be [b, s, hq, d]")
+    b, s, hq, d = q.shape
+    _check_act("k", k)
+    if k.dim() != 4 or k.shape[0] != b or k.shape[1] != s or k.shape[3] != d:
+        raise ValueError("k must be [b, s, hkv, d]")
+    _check_act("v", v, k.shape)
+    return b, s, hq, k.shape[2], d
+
+
+def cpattn_fwd(q, k, v, cp, causal=True, o=None, lse=None, stream=None):
+    """Context-parallel causal attention forward. Returns (o, lse).
+
+    q [b,s,hq,d], k/v [b,s,hkv,d] bf16 CUDA tensors; o like q (bf16) and lse
+    [b,hq,s] fp32 are allocated when not given.
+    """
+    b, s, hq, hkv, d = _dims(q, k, v)
+    if o is None:
+        o = torch.empty_like(q)
+    _check_act("o", o, q.shape)
+    if lse is None:
+        lse = torch.empty(b, hq, s, device=q.device, dtype=torch.float32)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (b, hq, s) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [b, hq, s] tensor")
+    rc = library().cpattn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), b, s, hq, hkv,
+                              d, int(cp), 1 if causal else 0, _stream_handle(stream))
+    if rc:
+        raise CpattnError(rc, "cpattn_fwd")
+    return o, lse
+
+
+def cpattn_bwd_workspace_bytes(b, s, hq, hkv, d, cp):
+    return int(library().cpattn_bwd_workspace_bytes(b, s, hq, hkv, d, int(cp)))
+
+
+def cpattn_bwd(q, k, v, o, lse, do, cp, causal=True, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward from the forward's saved o and lse. Returns (dq, dk, dv)."""
+    b, s, hq, hkv, d = _dims(q, k, v)
+    _check_act("o", o, q.shape)
+    _check_act("do", do, q.shape)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (b, hq, s) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [b, hq, s] tensor")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check_act("dq", dq, q.shape)
+    _check_act("dk", dk, k.shape)
+    _check_act("dv", dv, v.shape)
+    need = cpattn_bwd_workspace_bytes(b, s, hq, hkv, d, cp)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    rc = library().cpattn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                              dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(), ws_bytes, b, s, hq,
+                              hkv, d, int(cp), 1 if causal else 0, _stream_handle(stream))
+    if rc:
+        raise CpattnError(rc, "cpattn_bwd")
+    return dq, dk, dv
+
+
+def cpattn_zigzag_index(s, cp):
+    """int64 [cp, 2c] (host): global token of virtual rank r's local position."""
+    c = s // (2 * cp) if cp > 0 else 0
+    out = torch.empty(max(cp, 0), 2 * c, dtype=torch.int64)
+    rc = library().cpattn_zigzag_index(int(s), int(cp), ctypes.c_void_p(out.data_ptr()))
+    if rc:
+        raise CpattnError(rc, "cpattn_zigzag_index")
+    return out
+
+
+def cpattn_device_status(stream=None):
+    """Read and clear the library's sticky device status word (0 = clean)."""
+    st = ctypes.c_int(0)
+    rc = library().cpattn_device_status(_stream_handle(stream), ctypes.byref(st))
+    if rc not in (0, -7):
+        raise CpattnError(rc, "cpattn_device_status")
+    return int(st.value)

@@ -1,0 +1,183 @@
+// C-ABI entry points declared in include/cpattn.h: argument checks, TMA
+// tensor-map encoding and kernel launches. No device memory is allocated here.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/cpattn.h"
+#include "fwd_kernel.cuh"
+#include "tmap.h"
+
+namespace cpattn {
+
+// Sticky status word written by kernels that give up waiting.
+__device__ unsigned int g_device_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool init = false;
+  bool sm103 = false;
+  int num_sms = 0;
+  unsigned int* status = nullptr;
+  bool fwd_attr[2] = {false, false};
+};
+DeviceInfo g_devs[kMaxDevices];
+std::mutex g_mu;
+
+int device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CPATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& di = g_devs[dev];
+  if (!di.init) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return CPATTN_ERR_CUDA;
+    di.sm103 = (major == 10 && minor == 3);
+    di.num_sms = sms;
+    if (di.sm103) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return CPATTN_ERR_CUDA;
+      di.status = static_cast<unsigned int*>(p);
+    }
+    di.init = true;
+  }
+  *out = &di;
+  return di.sm103 ? CPATTN_OK : CPATTN_ERR_UNSUPPORTED_ARCH;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_geometry(int b, int s, int hq, int hkv, int d, int cp) {
+  if (b < 1 || s < 1 || hq < 1 || hkv < 1 || cp < 1) return CPATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return CPATTN_ERR_INVALID_ARG;
+  if (hq % hkv != 0) return CPATTN_ERR_INVALID_ARG;
+  if (s % (2 * cp) != 0) return CPATTN_ERR_INVALID_ARG;
+  if (int64_t(b) * s >= (int64_t(1) << 31)) return CPATTN_ERR_INVALID_ARG;
+  const int64_t units = int64_t(b) * ((hq + 1) / 2) * 2 * cp * ((s / (2 * cp) + kTile - 1) / kTile);
+  if (units >= (int64_t(1) << 31)) return CPATTN_ERR_INVALID_ARG;
+  return CPATTN_OK;
+}
+
+CpGeom make_geom(int b, int s, int hq, int hkv, int cp, int causal) {
+  CpGeom g;
+  g.b = b;
+  g.s = s;
+  g.hq = hq;
+  g.hkv = hkv;
+  g.cp = cp;
+  g.causal = causal ? 1 : 0;
+  g.c = s / (2 * cp);
+  g.tpc = (g.c + kTile - 1) / kTile;
+  g.npairs = (hq + 1) / 2;
+  return g;
+}
+
+template <int D>
+int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& args,
+               DeviceInfo* di, cudaStream_t st) {
+  using C = FwdCfg<D>;
+  const int slot = D == 128 ? 1 : 0;
+  if (!di->fwd_attr[slot]) {
+    if (cudaFuncSetAttribute(cpattn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+        cudaSuccess)
+      return CPATTN_ERR_CUDA;
+    di->fwd_attr[slot] = true;
+  }
+  const int units = fwd_num_units(args.g);
+  const int grid = units < di->num_sms ? units : di->num_sms;
+  cpattn_fwd_kernel<D><<<grid, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, args);
+  return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_LAUNCH_FAILED;
+}
+
+}  // namespace
+}  // namespace cpattn
+
+using namespace cpattn;
+
+extern "C" int cpattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int b, int s, int hq,
+                          int hkv, int d, int cp, int causal, void* stream) {
+  if (!q || !k || !v || !o || !lse) return CPATTN_ERR_NULL_PTR;
+  int rc = check_geometry(b, s, hq, hkv, d, cp);
+  if (rc) return rc;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return CPATTN_ERR_MISALIGNED;
+  DeviceInfo* di = nullptr;
+  if ((rc = device_info(&di))) return rc;
+  CUtensorMap tq, tk, tv;
+  const uint64_t rows = uint64_t(b) * s;
+  if (!encode_bf16_rows_heads_d(&tq, q, rows, hq, d, kTile) || !encode_bf16_rows_heads_d(&tk, k, rows, hkv, d, kTile) ||
+      !encode_bf16_rows_heads_d(&tv, v, rows, hkv, d, kTile))
+    return CPATTN_ERR_CUDA;
+  FwdArgs args;
+  args.g = make_geom(b, s, hq, hkv, cp, causal);
+  args.o = static_cast<__nv_bfloat16*>(o);
+  args.lse = lse;
+  args.scale_log2 = float(1.4426950408889634 / std::sqrt(double(d)));
+  args.status = di->status;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return d == 128 ? launch_fwd<128>(tq, tk, tv, args, di, st) : launch_fwd<64>(tq, tk, tv, args, di, st);
+}
+
+extern "C" size_t cpattn_bwd_workspace_bytes(int b, int s, int hq, int hkv, int d, int cp) {
+  if (check_geometry(b, s, hq, hkv, d, cp)) return 0;
+  return 0;  // backward not built yet
+}
+
+extern "C" int cpattn_bwd(const void*, const void*, const void*, const void*, const float*, const void*, void*, void*,
+                          void*, void*, size_t, int, int, int, int, int, int, int, void*) {
+  return CPATTN_ERR_INVALID_ARG;
+}
+
+extern "C" int cpattn_zigzag_index(int s, int cp, int64_t* global_of_local) {
+  if (!global_of_local) return CPATTN_ERR_NULL_PTR;
+  if (s < 1 || cp < 1 || s % (2 * cp) != 0) return CPATTN_ERR_INVALID_ARG;
+  const int64_t c = s / (2 * cp);
+  for (int64_t r = 0; r < cp; ++r) {
+    int64_t* row = global_of_local + r * 2 * c;
+    for (int64_t u = 0; u < c; ++u) row[u] = r * c + u;
+    for (int64_t u = 0; u < c; ++u) row[c + u] = (2 * cp - 1 - r) * c + u;
+  }
+  return CPATTN_OK;
+}
+
+extern "C" int cpattn_device_status(void* stream, int* status) {
+  if (!status) return CPATTN_ERR_NULL_PTR;
+  DeviceInfo* di = nullptr;
+  int rc = device_info(&di);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned int h = 0, zero = 0;
+  if (cudaMemcpyAsync(&h, di->status, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemcpyAsync(di->status, &zero, sizeof(zero), cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return CPATTN_ERR_CUDA;
+  *status = int(h);
+  return h ? CPATTN_ERR_TIMEOUT : CPATTN_OK;
+}
+
+extern "C" const char* cpattn_strerror(int code) {
+  switch (code) {
+    case CPATTN_OK: return "ok";
+    case CPATTN_ERR_INVALID_ARG: return "invalid argument (unsupported shape or size)";
+    case CPATTN_ERR_NULL_PTR: return "null pointer";
+    case CPATTN_ERR_MISALIGNED: return "device pointer not 16-byte aligned";
+    case CPATTN_ERR_UNSUPPORTED_ARCH: return "current device is not sm_103 (GB300)";
+    case CPATTN_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case CPATTN_ERR_LAUNCH_FAILED: return "kernel launch failed";
+    case CPATTN_ERR_TIMEOUT: return "a kernel gave up waiting (device status set)";
+    case CPATTN_ERR_CUDA: return "CUDA runtime or driver error";
+    default: return "unknown error";
+  }
+}
+
+extern "C" int cpattn_version(void) { return 100; }

@@ -1,0 +1,449 @@
+// Forward kernel: all virtual CP ranks in one persistent launch.
+//
+// One CTA per SM, 10 warps:
+//   warps 0-3  softmax/correction/epilogue for sub-tile 0 (one row per thread)
+//   warps 4-7  the same for sub-tile 1
+//   warp 8     TMA producer (Q tiles, and the K/V ring)
+//   warp 9     TMEM owner and tcgen05.mma issuer
+// A work unit is a 128-row query tile for a pair of query heads; the two
+// sub-tiles walk the same key tiles (CP-step order, see cp_schedule.cuh) so
+// the MMA warp can alternate between them:
+//     S0(j)=Q0 K_j^T  S1(j)=Q1 K_j^T  O0+=P0(j) V_j  S0(j+1)  O1+=P1(j) V_j  S1(j+1) ...
+// while the softmax warps of one sub-tile work on S(j) the tensor core runs
+// the other sub-tile's MMAs.
+//
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 after.
+// P (bf16, two per column) overwrites the first 64 columns of its S tile and
+// feeds the P.V MMA straight from TMEM.
+//
+// Online softmax and the CP correction ("大模型面试宝典 · Megatron-LM 篇", 3.2
+// steps 4-5; the per-step log-sum-exp merge): per row a running maximum m
+// (base-2, pre-scaled) and sum l; when a new key tile raises the maximum by
+// more than kRescaleThreshold the O accumulator and l are multiplied by
+// 2^(m_old - m_new); otherwise m is kept (exact either way, since the final
+// O/l and L = (m + log2 l) ln 2 use the same m). Merging step after step in
+// this running form is the two-stage merge L = log sum e^{L_i},
+// O = sum e^{L_i - L} O_i applied incrementally; partial O never leaves TMEM.
+#pragma once
+#include <cuda_bf16.h>
+
+#include "cp_schedule.cuh"
+#include "ptx.cuh"
+
+namespace cpattn {
+
+constexpr int kFwdThreads = 320;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+constexpr float kRescaleThreshold = 8.0f;         // log2 units (factor 256)
+
+struct FwdArgs {
+  CpGeom g;
+  __nv_bfloat16* o;
+  float* lse;
+  float scale_log2;  // log2(e) / sqrt(d)
+  unsigned int* status;
+};
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kQBytes = kTile * D * 2;  // one 128 x D bf16 tile
+  static constexpr int kKVBytes = kTile * D * 2;
+  static constexpr int kSlots = D == 128 ? 4 : 8;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffKV = 2 * kQBytes;
+  static constexpr int kOffBar = kOffKV + kSlots * kKVBytes;
+  // barriers: q_full[2] q_empty[2] s_full[2] p_full[2] o_full[2] o_empty[2]
+  //           drain, kv_full[kSlots] kv_empty[kSlots]
+  static constexpr int kNumBars = 13 + 2 * kSlots;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+  static constexpr uint32_t kColO = 256;
+};
+
+enum FwdStatusBits : unsigned int {
+  kStatusProducer = 1u << 0,
+  kStatusMma = 1u << 1,
+  kStatusSoftmax = 1u << 2,
+};
+
+template <int D>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    cpattn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv, const FwdArgs a) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + C::kOffQ;
+  uint8_t* sKV = smem + C::kOffKV;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_empty = bars + 2;
+  uint64_t* s_full = bars + 4;
+  uint64_t* p_full = bars + 6;
+  uint64_t* o_full = bars + 8;
+  uint64_t* o_empty = bars + 10;
+  uint64_t* drain = bars + 12;
+  uint64_t* kv_full = bars + 13;
+  uint64_t* kv_empty = bars + 13 + C::kSlots;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const CpGeom& g = a.g;
+  const int num_units = fwd_num_units(g);
+  const int grid = gridDim.x;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 4);
+      mbar_init(&o_full[i], 1);
+      mbar_init(&o_empty[i], 4);
+    }
+    mbar_init(drain, 1);
+    for (int i = 0; i < C::kSlots; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_desc(&tmq);
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      bool ok = true;
+      uint32_t nload = 0;
+      int ul = 0;
+      for (int rd = 0; ok; ++rd) {
+        const int idx = snake_unit(rd, blockIdx.x, grid);
+        if (idx >= num_units) break;
+        const FwdUnit U = fwd_decode_unit(g, idx);
+        if (ul > 0) {
+          ok = mbar_wait_bounded(&q_empty[0], (ul - 1) & 1, abort_flag, kWaitLimitNs) &&
+               mbar_wait_bounded(&q_empty[1], (ul - 1) & 1, abort_flag, kWaitLimitNs);
+          if (!ok) break;
+        }
+        const int qrow = U.bi * g.s + U.q_t0;
+        for (int sub = 0; sub < 2; ++sub) {
+          mbar_arrive_expect_tx(&q_full[sub], C::kQBytes);
+          const int h = sub ? U.h1 : U.h0;
+          for (int x = 0; x < D; x += 64)
+            tma_load_3d(sQ + sub * C::kQBytes + (x / 64) * (kTile * 128), &tmq, &q_full[sub], x, h, qrow);
+        }
+        const bool shared_kv = U.g0 == U.g1;
+        KvWalk w(g, U);
+        int chunk, tile;
+        bool dg;
+        auto load = [&](const CUtensorMap* map, int head, int row) -> bool {
+          const uint32_t slot = nload % C::kSlots;
+          if (nload >= (uint32_t)C::kSlots) {
+            if (!mbar_wait_bounded(&kv_empty[slot], ((nload / C::kSlots) - 1) & 1, abort_flag, kWaitLimitNs))
+              return false;
+          }
+          mbar_arrive_expect_tx(&kv_full[slot], C::kKVBytes);
+          uint8_t* dst = sKV + slot * C::kKVBytes;
+          for (int x = 0; x < D; x += 64) tma_load_3d(dst + (x / 64) * (kTile * 128), map, &kv_full[slot], x, head, row);
+          ++nload;
+          return true;
+        };
+        while (ok && w.next(chunk, tile, dg)) {
+          const int row = U.bi * g.s + chunk * g.c + tile * kTile;
+          ok = load(&tmk, U.g0, row) && (shared_kv || load(&tmk, U.g1, row)) && load(&tmv, U.g0, row) &&
+               (shared_kv || load(&tmv, U.g1, row));
+        }
+        ++ul;
+      }
+      if (!ok) atomicOr(a.status, kStatusProducer);
+      // Let every copy still in flight land before the CTA can exit.
+      const uint32_t first = nload > (uint32_t)C::kSlots ? nload - C::kSlots : 0;
+      for (uint32_t i = first; i < nload; ++i)
+        mbar_wait_bounded(&kv_full[i % C::kSlots], (i / C::kSlots) & 1, abort_flag, kWaitLimitNs);
+      if (ul > 0) {
+        mbar_wait_bounded(&q_full[0], (ul - 1) & 1, abort_flag, kWaitLimitNs);
+        mbar_wait_bounded(&q_full[1], (ul - 1) & 1, abort_flag, kWaitLimitNs);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = make_idesc_bf16(kTile, kTile, false, false);
+      constexpr uint32_t idO = make_idesc_bf16(kTile, D, false, true);
+      const uint64_t dQ[2] = {make_sdesc_sw128(smem_u32(sQ), 16, 1024),
+                              make_sdesc_sw128(smem_u32(sQ + C::kQBytes), 16, 1024)};
+      const uint64_t dKV0 = make_sdesc_sw128(smem_u32(sKV), 16, 1024);
+      const uint64_t dV0 = make_sdesc_sw128(smem_u32(sKV), 16384, 1024);
+      auto issue_S = [&](int sub, uint32_t slot) {
+        const uint64_t kb = dKV0 + ((slot * C::kKVBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;
+          umma_ss(tbase + sub * kTile, dQ[sub] + off, kb + off, idS, kk > 0);
+        }
+      };
+      auto issue_PV = [&](int sub, uint32_t slot, bool acc) {
+        const uint64_t vb = dV0 + ((slot * C::kKVBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          umma_ts(tbase + C::kColO + sub * D, tbase + sub * kTile + kk * 8, vb + ((kk * 2048) >> 4), idO,
+                  (acc || kk > 0) ? 1u : 0u);
+      };
+      uint32_t ncons = 0;
+      auto take = [&](uint32_t& slot, uint32_t& par) {
+        slot = ncons % C::kSlots;
+        par = (ncons / C::kSlots) & 1;
+        ++ncons;
+      };
+      bool ok = true;
+      uint32_t pcnt[2] = {0, 0};
+      int ul = 0;
+      for (int rd = 0; ok; ++rd) {
+        const int idx = snake_unit(rd, blockIdx.x, grid);
+        if (idx >= num_units) break;
+        const FwdUnit U = fwd_decode_unit(g, idx);
+        const bool shared_kv = U.g0 == U.g1;
+        const int n = U.n;
+        ok = mbar_wait_bounded(&q_full[0], ul & 1, abort_flag, kWaitLimitNs) &&
+             mbar_wait_bounded(&q_full[1], ul & 1, abort_flag, kWaitLimitNs);
+        if (!ok) break;
+        // prologue: S0(0), S1(0)
+        uint32_t k0, k0p, k1, k1p;
+        take(k0, k0p);
+        if (shared_kv) { k1 = k0; k1p = k0p; } else take(k1, k1p);
+        if (!(ok = mbar_wait_bounded(&kv_full[k0], k0p, abort_flag, kWaitLimitNs))) break;
+        tc_fence_after();
+        issue_S(0, k0);
+        umma_commit(&s_full[0]);
+        if (!shared_kv) umma_commit(&kv_empty[k0]);
+        if (n == 1) umma_commit(&q_empty[0]);
+        if (!shared_kv) {
+          if (!(ok = mbar_wait_bounded(&kv_full[k1], k1p, abort_flag, kWaitLimitNs))) break;
+          tc_fence_after();
+        }
+        issue_S(1, k1);
+        umma_commit(&s_full[1]);
+        umma_commit(&kv_empty[k1]);
+        if (n == 1) umma_commit(&q_empty[1]);
+        for (int j = 0; j < n && ok; ++j) {
+          uint32_t v0, v0p, v1, v1p;
+          take(v0, v0p);
+          if (shared_kv) { v1 = v0; v1p = v0p; } else take(v1, v1p);
+          // ---- sub-tile 0: O0 += P0(j) V_j, then S0(j+1)
+          ok = mbar_wait_bounded(&kv_full[v0], v0p, abort_flag, kWaitLimitNs) &&
+               mbar_wait_bounded(&p_full[0], pcnt[0] & 1, abort_flag, kWaitLimitNs) &&
+               (j > 0 || ul == 0 || mbar_wait_bounded(&o_empty[0], (ul - 1) & 1, abort_flag, kWaitLimitNs));
+          if (!ok) break;
+          ++pcnt[0];
+          tc_fence_after();
+          issue_PV(0, v0, j > 0);
+          if (!shared_kv) umma_commit(&kv_empty[v0]);
+          if (j == n - 1) umma_commit(&o_full[0]);
+          uint32_t nk0 = 0, nk0p = 0, nk1 = 0, nk1p = 0;
+          if (j + 1 < n) {
+            take(nk0, nk0p);
+            if (shared_kv) { nk1 = nk0; nk1p = nk0p; } else take(nk1, nk1p);
+            if (!(ok = mbar_wait_bounded(&kv_full[nk0], nk0p, abort_flag, kWaitLimitNs))) break;
+            tc_fence_after();
+            issue_S(0, nk0);
+            umma_commit(&s_full[0]);
+            if (!shared_kv) umma_commit(&kv_empty[nk0]);
+            if (j + 1 == n - 1) umma_commit(&q_empty[0]);
+          }
+          // ---- sub-tile 1: O1 += P1(j) V_j, then S1(j+1)
+          ok = (shared_kv || mbar_wait_bounded(&kv_full[v1], v1p, abort_flag, kWaitLimitNs)) &&
+               mbar_wait_bounded(&p_full[1], pcnt[1] & 1, abort_flag, kWaitLimitNs) &&
+               (j > 0 || ul == 0 || mbar_wait_bounded(&o_empty[1], (ul - 1) & 1, abort_flag, kWaitLimitNs));
+          if (!ok) break;
+          ++pcnt[1];
+          tc_fence_after();
+          issue_PV(1, v1, j > 0);
+          umma_commit(&kv_empty[v1]);
+          if (j == n - 1) umma_commit(&o_full[1]);
+          if (j + 1 < n) {
+            if (!shared_kv) {
+              if (!(ok = mbar_wait_bounded(&kv_full[nk1], nk1p, abort_flag, kWaitLimitNs))) break;
+              tc_fence_after();
+            }
+            issue_S(1, nk1);
+            umma_commit(&s_full[1]);
+            umma_commit(&kv_empty[nk1]);
+            if (j + 1 == n - 1) umma_commit(&q_empty[1]);
+          }
+        }
+        ++ul;
+      }
+      if (!ok) atomicOr(a.status, kStatusMma);
+      // No MMA may be in flight when TMEM is released.
+      umma_commit(drain);
+      mbar_wait_bounded(drain, 0, abort_flag, kWaitLimitNs);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int sub = warp >> 2;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t lane_off = uint32_t(wq * 32) << 16;
+    const uint32_t tS = tbase + lane_off + sub * kTile;
+    const uint32_t tO = tbase + lane_off + C::kColO + sub * D;
+    const float sl2 = a.scale_log2;
+    bool ok = true;
+    uint32_t scnt = 0;
+    int ul = 0;
+    for (int rd = 0; ok; ++rd) {
+      const int idx = snake_unit(rd, blockIdx.x, grid);
+      if (idx >= num_units) break;
+      const FwdUnit U = fwd_decode_unit(g, idx);
+      KvWalk w(g, U);
+      float m_used = -INFINITY;
+      float l = 0.f;
+      for (int j = 0; j < U.n; ++j) {
+        int chunk = 0, tile = 0;
+        bool dg = false;
+        w.next(chunk, tile, dg);
+        const int rem = g.c - tile * kTile;
+        const int n_valid = rem < kTile ? rem : kTile;
+        if (!(ok = mbar_wait_bounded(&s_full[sub], scnt & 1, abort_flag, kWaitLimitNs))) break;
+        ++scnt;
+        tc_fence_after();
+        float s[kTile];
+        {
+          uint32_t r0[64], r1[64];
+          tmem_ld64(tS, r0);
+          tmem_ld64(tS + 64, r1);
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            s[i] = __uint_as_float(r0[i]);
+            s[64 + i] = __uint_as_float(r1[i]);
+          }
+        }
+        if (dg || n_valid < kTile) {
+          const int lim = dg ? (row < n_valid - 1 ? row : n_valid - 1) : n_valid - 1;
+#pragma unroll
+          for (int i = 0; i < kTile; ++i)
+            if (i > lim) s[i] = -INFINITY;
+        }
+        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+        for (int i = 4; i < kTile; i += 4) {
+          mx0 = fmaxf(mx0, s[i]);
+          mx1 = fmaxf(mx1, s[i + 1]);
+          mx2 = fmaxf(mx2, s[i + 2]);
+          mx3 = fmaxf(mx3, s[i + 3]);
+        }
+        const float m_new = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        const bool upd = m_new > m_used + kRescaleThreshold;
+        float alpha = 1.f;
+        if (upd) {
+          alpha = (m_used == -INFINITY) ? 0.f : ex2_approx(m_used - m_new);
+          m_used = m_new;
+        }
+        const float neg = (m_used == -INFINITY) ? 0.f : -m_used;
+        // P = 2^(S*scale*log2e - m), packed to bf16 pairs as it is formed so
+        // the fp32 scores die early; the row sum uses the fp32 values.
+        uint32_t pk[kTile / 2];
+        float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < kTile / 2; ++i) {
+          const float e0 = ex2_approx(fmaf(s[2 * i], sl2, neg));
+          const float e1 = ex2_approx(fmaf(s[2 * i + 1], sl2, neg));
+          l0 += e0;
+          l1 += e1;
+          pk[i] = pack_bf16x2(e0, e1);
+        }
+        if (j > 0 && __any_sync(0xffffffffu, upd)) {
+          // This row's O accumulator is idle: P.V of step j-1 completed
+          // before S(j) was signalled, and P.V of step j waits for p_full.
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t r[32];
+            tmem_ld32(tO + c0, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st32(tO + c0, r);
+          }
+        }
+        l = l * alpha + (l0 + l1);
+        {
+          uint32_t p0[32], p1[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            p0[i] = pk[i];
+            p1[i] = pk[32 + i];
+          }
+          tmem_st32(tS, p0);
+          tmem_st32(tS + 32, p1);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[sub]);
+      }
+      if (!ok) break;
+      // ---- epilogue: O / l -> bf16, L = (m + log2 l) ln 2
+      if (!(ok = mbar_wait_bounded(&o_full[sub], ul & 1, abort_flag, kWaitLimitNs))) break;
+      tc_fence_after();
+      uint32_t ov[D];
+      if constexpr (D == 128) {
+        uint32_t r0[64], r1[64];
+        tmem_ld64(tO, r0);
+        tmem_ld64(tO + 64, r1);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          ov[i] = r0[i];
+          ov[64 + i] = r1[i];
+        }
+      } else {
+        uint32_t r0[64];
+        tmem_ld64(tO, r0);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) ov[i] = r0[i];
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_empty[sub]);
+      const bool store = row < U.q_valid && (sub == 0 || U.store1);
+      if (store) {
+        const int h = sub ? U.h1 : U.h0;
+        const int t = U.q_t0 + row;
+        const float inv = 1.f / l;
+        __nv_bfloat16* dst = a.o + ((int64_t(U.bi) * g.s + t) * g.hq + h) * D;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 8) {
+          uint4 pkv;
+          pkv.x = pack_bf16x2(__uint_as_float(ov[c0 + 0]) * inv, __uint_as_float(ov[c0 + 1]) * inv);
+          pkv.y = pack_bf16x2(__uint_as_float(ov[c0 + 2]) * inv, __uint_as_float(ov[c0 + 3]) * inv);
+          pkv.z = pack_bf16x2(__uint_as_float(ov[c0 + 4]) * inv, __uint_as_float(ov[c0 + 5]) * inv);
+          pkv.w = pack_bf16x2(__uint_as_float(ov[c0 + 6]) * inv, __uint_as_float(ov[c0 + 7]) * inv);
+          *reinterpret_cast<uint4*>(dst + c0) = pkv;
+        }
+        a.lse[(int64_t(U.bi) * g.hq + h) * g.s + t] = (m_used + log2f(l)) * 0.69314718055994530942f;
+      }
+      ++ul;
+    }
+    if (!ok && lane == 0) atomicOr(a.status, kStatusSoftmax);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+}  // namespace cpattn

@@ -1,0 +1,123 @@
+/*
+ * cpattn — context-parallel (CP) causal self-attention on one GB300 GPU.
+ *
+ * The method (web page "大模型面试宝典 · Megatron-LM 篇", question 3
+ * "Context Parallel 篇", sub-questions 3.2 and 3.4; and "超大规模集群下大语言
+ * 模型训练实操指南", section "CP 与其他技术结合"):
+ *   - the sequence of s tokens is cut into 2*cp chunks of c = s/(2cp)
+ *     tokens; virtual rank r holds chunks r and 2cp-1-r (zigzag balance);
+ *   - at step i, rank r works on the KV of rank j = (r - i) mod cp:
+ *       step 0     local Q vs local KV, causal;
+ *       1 <= i <= r all local Q vs the first half of the incoming KV, no mask;
+ *       i > r      the second half of Q vs the full incoming KV, no mask;
+ *   - each step's partial output O_i and log-sum-exp L_i are corrected and
+ *     merged: L = log(sum_i e^{L_i}), O = sum_i e^{L_i - L} O_i.
+ * The result equals plain causal softmax attention over the uncut sequence
+ * (3.2: each rank's output equals the matching part of the non-CP output).
+ * All cp virtual ranks run inside one kernel launch on one GPU; there is no
+ * KV exchange between devices. The per-step correction is carried on chip,
+ * so partial outputs never reach device memory.
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are in natural token order (the zigzag is applied inside).
+ *     q, o, dout, dq: [b, s, hq, d]; k, v, dk, dv: [b, s, hkv, d];
+ *     bf16, contiguous, head_dim fastest. lse: [b, hq, s] fp32, natural log.
+ *   - Grouped-query attention: query head h uses KV head h / (hq / hkv)
+ *     (page "Megatron 面试题（一）：模型抽象与训练数据流", item M014).
+ *   - Softmax scale is 1/sqrt(d). causal != 0 selects the causal mask
+ *     (key position <= query position); causal == 0 is full attention with
+ *     the same CP chunking (every step unmasked).
+ *   - Supported: d in {64, 128}; s divisible by 2*cp; hq divisible by hkv;
+ *     b, s, hq, hkv, cp >= 1; b*s < 2^31. Chunk length c need not be a
+ *     multiple of the 128-token tile (ragged tiles are masked).
+ *   - Pointers: device pointers unless stated otherwise; the caller owns every
+ *     buffer. Device buffers must be 16-byte aligned. The library allocates
+ *     no device memory and keeps no per-call state.
+ *   - stream: a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Calls only enqueue work and return; results are ready when the stream
+ *     is synchronised.
+ *   - Return value: 0 on success, a negative CPATTN_ERR_* code otherwise
+ *     (nothing is enqueued on an argument error). No C++ exception crosses
+ *     this interface.
+ *   - Device-side failures: every wait inside the kernels has a time limit.
+ *     A kernel that gives up records it in a sticky device status word and
+ *     returns without faulting; read it with cpattn_device_status().
+ */
+#ifndef CPATTN_H
+#define CPATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  CPATTN_OK = 0,
+  CPATTN_ERR_INVALID_ARG = -1,     /* shape/size outside the supported set   */
+  CPATTN_ERR_NULL_PTR = -2,        /* a required pointer is NULL             */
+  CPATTN_ERR_MISALIGNED = -3,      /* a device pointer is not 16-byte aligned */
+  CPATTN_ERR_UNSUPPORTED_ARCH = -4,/* current device is not sm_103            */
+  CPATTN_ERR_WORKSPACE_TOO_SMALL = -5,
+  CPATTN_ERR_LAUNCH_FAILED = -6,   /* kernel launch returned a CUDA error     */
+  CPATTN_ERR_TIMEOUT = -7,         /* a kernel gave up waiting (device status) */
+  CPATTN_ERR_CUDA = -8             /* other CUDA runtime/driver error         */
+};
+
+/*
+ * Forward pass. Writes o (bf16) and lse (fp32, natural log) for every query
+ * of every head: O[t] = sum_{j<=t} softmax_j(q_t.k_j/sqrt(d)) v_j,
+ * lse[t] = log sum_{j<=t} exp(q_t.k_j/sqrt(d)).
+ * Computed CP-style (steps 0..cp-1 per virtual rank, merge fused on chip).
+ */
+int cpattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int b, int s, int hq, int hkv,
+               int d, int cp, int causal, void* stream);
+
+/*
+ * Bytes of caller-provided device workspace cpattn_bwd needs for these sizes
+ * (an fp32 dQ accumulator and the per-row D = rowsum(dO * O) vector).
+ * Returns 0 for unsupported sizes.
+ */
+size_t cpattn_bwd_workspace_bytes(int b, int s, int hq, int hkv, int d, int cp);
+
+/*
+ * Backward pass from the forward's saved o and lse: with P = exp(S - lse),
+ *   dV = P^T dO, dP = dO V^T, dS = P * (dP - rowsum(dO * O)),
+ *   dQ = dS K / sqrt(d), dK = dS^T Q / sqrt(d),
+ * over the same CP steps and masks as the forward; dK/dV of a KV head sum
+ * over its query-head group. Writes dq, dk, dv (bf16). `workspace` must hold
+ * cpattn_bwd_workspace_bytes(...) bytes (16-byte aligned); its contents on
+ * entry do not matter and on exit are unspecified.
+ */
+int cpattn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+               void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int b, int s, int hq, int hkv,
+               int d, int cp, int causal, void* stream);
+
+/*
+ * Host helper: the zigzag index map. Fills global_of_local (HOST memory,
+ * cp * 2c int64 values, row-major [cp][2c]) with the global token position
+ * of virtual rank r's local position u: chunk r then chunk 2cp-1-r, each in
+ * natural order ("大模型面试宝典 · Megatron-LM 篇", 3.4).
+ */
+int cpattn_zigzag_index(int s, int cp, int64_t* global_of_local);
+
+/*
+ * Reads the sticky device status word of the current device into *status
+ * (0 = no kernel gave up waiting) and clears it. Synchronises `stream`.
+ * Returns CPATTN_ERR_TIMEOUT when the word was non-zero, else 0 or a CUDA
+ * error code.
+ */
+int cpattn_device_status(void* stream, int* status);
+
+/* Static description of an error code. */
+const char* cpattn_strerror(int code);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int cpattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPATTN_H */

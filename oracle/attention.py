@@ -28,9 +28,14 @@ def softmax_scale(d: int) -> float:
     return 1.0 / math.sqrt(d)
 
 
+_EXACT = (torch.bfloat16, torch.float16, torch.float32, torch.float64)
+
+
 def _check(q, k, v):
-    if q.dtype != _F64 or k.dtype != _F64 or v.dtype != _F64:
-        raise TypeError("oracle works in float64; upcast the bf16 inputs first")
+    # Inputs may be bf16/fp16/fp32/fp64: each block is upcast to float64,
+    # which is exact for all of them; all arithmetic is float64.
+    if q.dtype not in _EXACT or k.dtype not in _EXACT or v.dtype not in _EXACT:
+        raise TypeError("oracle inputs must be a float type that upcasts exactly to float64")
     if q.device.type != "cpu":
         raise ValueError("oracle runs on the CPU")
     b, s, hq, d = q.shape
@@ -57,7 +62,8 @@ def _scores(qrows, kk, t, causal, scale):
 def attention_forward(q, k, v, causal=True, rows=None, row_block=1024):
     """O and LSE of softmax attention for the query positions ``rows``.
 
-    q: [b, s, hq, d]; k, v: [b, s_kv, hkv, d]; float64 CPU tensors.
+    q: [b, s, hq, d]; k, v: [b, s_kv, hkv, d]; CPU tensors of a float type
+    that upcasts exactly (bf16, fp16, fp32, fp64); arithmetic is float64.
     Returns o [b, n, hq, d] and lse [b, hq, n] (n = len(rows), default all s).
     A row that sees no key (impossible for causal self-attention) gets
     L = -inf and O = 0.
@@ -70,19 +76,21 @@ def attention_forward(q, k, v, causal=True, rows=None, row_block=1024):
     o = torch.zeros(b, n, hq, d, dtype=_F64)
     lse = torch.empty(b, hq, n, dtype=_F64)
     for bi in range(b):
-        for h in range(hq):
-            g = h // G
-            for r0 in range(0, n, row_block):
-                t = t_all[r0:r0 + row_block]
-                nk = min(int(t.max()) + 1, skv) if causal else skv
-                S = _scores(q[bi, t, h], k[bi, :nk, g], t, causal, scale)
-                m = S.max(dim=1, keepdim=True).values
-                m_safe = torch.where(torch.isfinite(m), m, torch.zeros_like(m))
-                L = m_safe + torch.log(torch.exp(S - m_safe).sum(dim=1, keepdim=True))
-                P = torch.exp(S - torch.where(torch.isfinite(L), L, torch.zeros_like(L)))
-                P = torch.where(torch.isfinite(L), P, torch.zeros_like(P))
-                o[bi, r0:r0 + t.numel(), h] = P @ v[bi, :nk, g]
-                lse[bi, h, r0:r0 + t.numel()] = L[:, 0]
+        for g in range(hkv):
+            kk_all = k[bi, :, g].to(_F64)
+            vv_all = v[bi, :, g].to(_F64)
+            for h in range(g * G, (g + 1) * G):
+                for r0 in range(0, n, row_block):
+                    t = t_all[r0:r0 + row_block]
+                    nk = min(int(t.max()) + 1, skv) if causal else skv
+                    S = _scores(q[bi, t, h].to(_F64), kk_all[:nk], t, causal, scale)
+                    m = S.max(dim=1, keepdim=True).values
+                    m_safe = torch.where(torch.isfinite(m), m, torch.zeros_like(m))
+                    L = m_safe + torch.log(torch.exp(S - m_safe).sum(dim=1, keepdim=True))
+                    P = torch.exp(S - torch.where(torch.isfinite(L), L, torch.zeros_like(L)))
+                    P = torch.where(torch.isfinite(L), P, torch.zeros_like(P))
+                    o[bi, r0:r0 + t.numel(), h] = P @ vv_all[:nk]
+                    lse[bi, h, r0:r0 + t.numel()] = L[:, 0]
     return o, lse
 
 
@@ -104,8 +112,8 @@ def attention_backward(q, k, v, do, causal=True, dq_rows=None, dkv_heads=None, r
     dk/dv carry only the requested heads, in the order given.
     """
     b, s, hq, d, skv, hkv = _check(q, k, v)
-    if do.shape != q.shape or do.dtype != _F64:
-        raise ValueError("do must match q (float64)")
+    if do.shape != q.shape or do.dtype not in _EXACT:
+        raise ValueError("do must match q")
     G = hq // hkv
     scale = softmax_scale(d)
     t_dq = _rows_tensor(dq_rows, s)
@@ -114,32 +122,35 @@ def attention_backward(q, k, v, do, causal=True, dq_rows=None, dkv_heads=None, r
     dk = torch.zeros(b, skv, len(heads), d, dtype=_F64)
     dv = torch.zeros(b, skv, len(heads), d, dtype=_F64)
 
-    def grads_for_rows(bi, h, t):
-        g = h // G
+    def grads_for_rows(qq, kk, vv, dd, t):
         nk = min(int(t.max()) + 1, skv) if causal else skv
-        S = _scores(q[bi, t, h], k[bi, :nk, g], t, causal, scale)
+        S = _scores(qq, kk[:nk], t, causal, scale)
         m = S.max(dim=1, keepdim=True).values
         P = torch.exp(S - m)
         P = P / P.sum(dim=1, keepdim=True)
-        dP = do[bi, t, h] @ v[bi, :nk, g].T
+        dP = dd @ vv[:nk].T
         dS = P * (dP - (P * dP).sum(dim=1, keepdim=True))
         return nk, P, dS
 
     for bi in range(b):
-        for h in range(hq):
-            g = h // G
-            # dQ on the requested rows
-            for r0 in range(0, t_dq.numel(), row_block):
-                t = t_dq[r0:r0 + row_block]
-                nk, P, dS = grads_for_rows(bi, h, t)
-                dq[bi, r0:r0 + t.numel(), h] = scale * (dS @ k[bi, :nk, g])
-            # dK / dV of the requested KV heads: every row of this query head
-            if g in heads:
-                slot = heads.index(g)
-                t_all = torch.arange(s, dtype=torch.long)
-                for r0 in range(0, s, row_block):
-                    t = t_all[r0:r0 + row_block]
-                    nk, P, dS = grads_for_rows(bi, h, t)
-                    dv[bi, :nk, slot] += P.T @ do[bi, t, h]
-                    dk[bi, :nk, slot] += scale * (dS.T @ q[bi, t, h])
+        for g in range(hkv):
+            kk = k[bi, :, g].to(_F64)
+            vv = v[bi, :, g].to(_F64)
+            for h in range(g * G, (g + 1) * G):
+                # dQ on the requested rows
+                for r0 in range(0, t_dq.numel(), row_block):
+                    t = t_dq[r0:r0 + row_block]
+                    nk, P, dS = grads_for_rows(q[bi, t, h].to(_F64), kk, vv, do[bi, t, h].to(_F64), t)
+                    dq[bi, r0:r0 + t.numel(), h] = scale * (dS @ kk[:nk])
+                # dK / dV of the requested KV heads: every row of this query head
+                if g in heads:
+                    slot = heads.index(g)
+                    t_all = torch.arange(s, dtype=torch.long)
+                    for r0 in range(0, s, row_block):
+                        t = t_all[r0:r0 + row_block]
+                        qq = q[bi, t, h].to(_F64)
+                        dd = do[bi, t, h].to(_F64)
+                        nk, P, dS = grads_for_rows(qq, kk, vv, dd, t)
+                        dv[bi, :nk, slot] += P.T @ dd
+                        dk[bi, :nk, slot] += scale * (dS.T @ qq)
     return dq, dk, dv

@@ -1,0 +1,45 @@
+"""CPU test of the kernels' work decomposition (zigzag units, CP-step key walk).
+
+Compiles tests/schedule_check.cpp against the kernels' schedule header with
+the host compiler and checks, by brute force, that every allowed (query, key)
+pair is computed exactly once.
+"""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+GEOMS = [
+    # b, s, hq, hkv, cp, causal, grid
+    (1, 256, 2, 2, 1, 1, 3),
+    (1, 512, 4, 4, 2, 1, 148),
+    (2, 1024, 4, 2, 2, 1, 5),
+    (1, 960, 6, 2, 3, 1, 7),
+    (1, 640, 3, 1, 2, 1, 4),
+    (1, 1536, 8, 1, 4, 1, 152),
+    (1, 96, 2, 2, 3, 1, 2),
+    (1, 2048, 2, 2, 8, 1, 11),
+    (1, 768, 4, 4, 3, 0, 6),
+    (2, 384, 2, 1, 1, 0, 3),
+    (1, 1280, 2, 1, 5, 1, 9),
+]
+
+
+@pytest.fixture(scope="module")
+def checker(tmp_path_factory):
+    cxx = shutil.which("g++") or shutil.which("c++")
+    if cxx is None:
+        pytest.skip("no host C++ compiler")
+    exe = str(tmp_path_factory.mktemp("sched") / "schedule_check")
+    subprocess.run([cxx, "-O2", "-std=c++17", "-o", exe, os.path.join(HERE, "schedule_check.cpp")], check=True)
+    return exe
+
+
+def test_every_allowed_pair_once(checker):
+    args = [str(x) for g in GEOMS for x in g]
+    out = subprocess.run([checker, *args], capture_output=True, text=True)
+    assert out.returncode == 0, out.stdout + out.stderr
+    assert out.stdout.count("ok") == len(GEOMS)

@@ -1,0 +1,349 @@
+"""Benchmark: context-parallel causal attention forward + backward on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+cpattn_fwd (all virtual CP ranks, fused LSE merge) then cpattn_bwd
+(preprocess, main kernel, dQ conversion), through the C-ABI library.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+Prints one JSON line (rank 0). With N > 1 (torchrun) every rank runs an
+independent replica of the workload on its own GPU: the method needs no
+exchange on one GPU, so there is no collective on the data path; value is the
+work of all ranks divided by the slowest rank's time ("scaling": "weak").
+--impl reference times the CPU fp64 oracle on a bounded sample of the same
+workload on the host cores (the baseline this tier compares against).
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CP causal attention fwd/bwd TFLOP/s and % of GB300 dense BF16 peak"
+DEFAULT_WORKLOAD = "train_b1_s32768_h32kv8_d128_cp8"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"bf16_tflops": d["bf16_tflops"], "bf16_tflops_sustained": d["bf16_tflops_sustained"],
+                "hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        loaded = [x for x in sm if smax is None or x > 0.3 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _profile_traffic(kernel_file, profile_name):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source of the kernel (same sha256); else None."""
+    prof = os.path.join(ROOT, "profiles", profile_name)
+    src = os.path.join(ROOT, "context_blockwise_causal_gb300", "csrc", kernel_file)
+    if not (os.path.exists(prof) and os.path.exists(src)):
+        return None
+    text = open(prof).read()
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
+    if not (m_b and m_h):
+        return None
+    if hashlib.sha256(open(src, "rb").read()).hexdigest() != m_h.group(1):
+        return None
+    return float(m_b.group(1))
+
+
+# ------------------------------------------------------------------ CPU oracle arm
+def _oracle_sample(w, rows_n, seed):
+    """The CPU oracle on a bounded sample of workload w: forward O/LSE and the
+    backward's dQ for `rows_n` seeded random query rows of every head.
+    Returns (seconds, algorithmic FLOPs of the sample in the metric's
+    convention: 4*d per visible (query, key) pair forward, 2.5x that backward)."""
+    import oracle
+    from context_blockwise_causal_gb300.workloads import make_inputs, sample_rows
+
+    x = make_inputs(w, device="cpu")
+    rows = sample_rows(w, rows_n, seed=seed)
+    t0 = time.perf_counter()
+    oracle.attention_forward(x["q"], x["k"], x["v"], causal=w.causal, rows=rows, row_block=256)
+    oracle.attention_backward(x["q"], x["k"], x["v"], x["do"], causal=w.causal, dq_rows=rows, dkv_heads=[],
+                              row_block=256)
+    dt = time.perf_counter() - t0
+    keys = (rows + 1).double().sum().item() if w.causal else float(w.s) * rows.numel()
+    flops = 3.5 * 4.0 * w.d * keys * w.hq * w.b
+    return dt, flops
+
+
+def run_reference(args, w):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    cores = torch.get_num_threads()
+    rows_n = args.ref_rows
+    for _ in range(args.warmup):
+        _oracle_sample(w, rows_n, seed=w.seed + 5)
+    times, flops = [], 0.0
+    for i in range(args.steps):
+        dt, fl = _oracle_sample(w, rows_n, seed=w.seed + 5)
+        times.append(dt)
+        flops = fl
+    tot = sum(times)
+    value = flops * args.steps / tot / 1e12
+    sample = (f"{rows_n} seeded query rows x {w.hq} heads of {w.name}: forward O/LSE + backward dQ "
+              f"(CPU fp64 oracle, torch float64 on {cores} threads)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _config(w, args.gpus),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def _config(w, n):
+    return {"workload": w.name, "b": w.b, "s": w.s, "hq": w.hq, "hkv": w.hkv, "d": w.d, "cp": w.cp,
+            "causal": w.causal, "step": "cpattn_fwd + cpattn_bwd",
+            "l2": f"inputs larger than L2 (q,k,v,dO = {_in_bytes(w) / 1e6:.0f} MB > 129 MB)",
+            "parallelism": "replicas" if n > 1 else "single"}
+
+
+def _in_bytes(w):
+    return 2 * (2 * w.b * w.s * w.hq * w.d + 2 * w.b * w.s * w.hkv * w.d)
+
+
+def run_ours(args, w):
+    import torch.distributed as dist
+
+    from context_blockwise_causal_gb300 import (cpattn_bwd, cpattn_bwd_workspace_bytes, cpattn_device_status,
+                                                cpattn_fwd, library)
+    from context_blockwise_causal_gb300.workloads import make_inputs
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl")
+    library()
+    dev = torch.device("cuda", local)
+    x = make_inputs(w, device=dev, seed=w.seed + rank)
+    q, k, v, do = x["q"], x["k"], x["v"], x["do"]
+    o = torch.empty_like(q)
+    lse = torch.empty(w.b, w.hq, w.s, device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    wsp = torch.empty(cpattn_bwd_workspace_bytes(w.b, w.s, w.hq, w.hkv, w.d, w.cp), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = 4  # fwd kernel; bwd preprocess, main, dQ conversion
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        cpattn_fwd(q, k, v, w.cp, causal=w.causal, o=o, lse=lse, stream=stream)
+        if evs:
+            evs[1].record(stream)
+        cpattn_bwd(q, k, v, o, lse, do, w.cp, causal=w.causal, dq=dq, dk=dk, dv=dv, workspace=wsp, stream=stream)
+        if evs:
+            evs[2].record(stream)
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    if cpattn_device_status(stream) != 0:
+        raise RuntimeError("a kernel reported a timeout during warm-up")
+
+    # ---- device-timed region: inputs resident in HBM
+    evs = [[ev(), ev(), ev()] for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        barrier()
+        t_start, t_end = ev(), ev()
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t_end.record(stream)
+        barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    if cpattn_device_status(stream) != 0:
+        raise RuntimeError("a kernel reported a timeout in the timed region")
+    t = torch.tensor([total_ms], device=dev)
+    if ws > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = t.item()
+
+    # ---- end to end through the public API with host buffers
+    pin = {n: x[n].cpu().pin_memory() for n in ("q", "k", "v", "do")}
+    out_h = {n: torch.empty(tuple(tt.shape), dtype=tt.dtype).pin_memory() for n, tt in (("dq", dq), ("dk", dk), ("dv", dv))}
+    h2d = sum(tt.numel() * tt.element_size() for tt in pin.values())
+    d2h = sum(tt.numel() * tt.element_size() for tt in out_h.values())
+
+    def e2e_step():
+        for n, dst in (("q", q), ("k", k), ("v", v), ("do", do)):
+            dst.copy_(pin[n], non_blocking=True)
+        step()
+        out_h["dq"].copy_(dq, non_blocking=True)
+        out_h["dk"].copy_(dk, non_blocking=True)
+        out_h["dv"].copy_(dv, non_blocking=True)
+
+    e2e_step()
+    barrier()
+    e0, e1 = ev(), ev()
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = torch.tensor([e0.elapsed_time(e1)], device=dev)
+    if ws > 1:
+        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
+    e2e_ms = e2e_ms.item()
+
+    if rank == 0:
+        peaks = _peaks()
+        step_flops = w.fwd_flops() + w.bwd_flops()
+        value = step_flops * args.steps * ws / (total_ms * 1e-3) / 1e12
+        fwd_avg = sum(fwd_ms) / len(fwd_ms)
+        bwd_avg = sum(bwd_ms) / len(bwd_ms)
+        fwd_tf = w.fwd_flops() / (fwd_avg * 1e-3) / 1e12
+        bwd_tf = w.bwd_flops() / (bwd_avg * 1e-3) / 1e12
+        dominant = "bwd" if bwd_avg >= fwd_avg else "fwd"
+        achieved = bwd_tf if dominant == "bwd" else fwd_tf
+        peak = peaks["bf16_tflops_sustained"]
+        traffic = (_profile_traffic("bwd_kernel.cuh", f"cpattn_bwd_kernel_{w.name}.md") if dominant == "bwd" else
+                   _profile_traffic("fwd_kernel.cuh", f"cpattn_fwd_kernel_{w.name}.md"))
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": _config(w, ws),
+            "fraction_of_peak": {"vs_burst": value / ws / peaks["bf16_tflops"],
+                                 "vs_sustained": value / ws / peaks["bf16_tflops_sustained"],
+                                 "peaks": peaks["source"]},
+            "phases": {"fwd_ms": fwd_avg, "fwd_tflops": fwd_tf, "fwd_frac_burst": fwd_tf / peaks["bf16_tflops"],
+                       "bwd_ms": bwd_avg, "bwd_tflops": bwd_tf, "bwd_frac_burst": bwd_tf / peaks["bf16_tflops"],
+                       "flops": {"fwd": w.fwd_flops(), "bwd": w.bwd_flops(), "convention": "fwd 2*b*hq*s^2*d; bwd 2.5x fwd"}},
+            "roofline": {"kernel": f"cpattn_{dominant}" + ("_kernel (+ preprocess and dQ conversion in the timed span)"
+                                                            if dominant == "bwd" else "_kernel"),
+                         "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "peak_kind": f"bf16 sustained ({peaks['source']})",
+                         "frac_vs_burst": achieved / peaks["bf16_tflops"], "traffic": traffic},
+            "e2e": {"value": step_flops * args.steps * ws / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary(),
+        }
+        if not args.no_cpu_baseline:
+            dt, fl = _oracle_sample(w, args.ref_rows, seed=w.seed + 5)
+            line["cpu_baseline"] = {
+                "value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": torch.get_num_threads(), "kind": "oracle",
+                "sample": f"{args.ref_rows} seeded query rows x {w.hq} heads of {w.name}: forward O/LSE + backward "
+                          f"dQ (CPU fp64 oracle), {dt:.1f} s"}
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--ref-rows", type=int, default=48)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    from context_blockwise_causal_gb300.workloads import WORKLOADS
+
+    w = WORKLOADS[args.workload]
+    if not w.backward:
+        raise SystemExit("the bench step is forward + backward: pick a workload with a backward")
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

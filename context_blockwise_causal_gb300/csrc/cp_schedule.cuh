@@ -167,4 +167,120 @@ struct KvWalk {
   }
 };
 
+
+// ---------------------------------------------------------------- backward
+// A backward work unit is one 128-key tile (chunk kc, tile v) of one KV head
+// for one batch element. It visits every (query head of the group, query
+// tile) block that sees its keys, walking the CP steps from the key owner's
+// side: the chunk kc belongs to rank j; at step i rank r = (j + i) mod cp
+// holds it and, by the same three rules as the forward,
+//   step 0            : rank j's own query chunks (the diagonal tile masked);
+//   i >= 1, no wrap   : (r > j) rank r uses only first halves of incoming KV,
+//                       so chunk kc counts only if it is j's first half, and
+//                       then against both of r's query chunks;
+//   i >= 1, wrap      : (r < j) only r's second query chunk 2cp-1-r, against
+//                       both of j's chunks.
+// The set of blocks is exactly the forward's; dK/dV of the tile accumulate
+// over all of them on chip.
+struct BwdUnit {
+  int bi, g;      // batch element, KV head
+  int kc, v;      // key chunk and tile within it
+  int j, khalf;   // owning rank of the chunk, and which of its two chunks
+  int k_t0;       // first key token
+  int k_valid;    // keys of the tile inside the chunk
+  int nq;         // number of query tiles that see the tile
+  int items;      // nq * (hq / hkv)
+};
+
+__host__ __device__ inline int bwd_num_units(const CpGeom& g) { return g.b * g.hkv * 2 * g.cp * g.tpc; }
+
+// Longest-first: the key tile with global tile index gt is seen by ntile-gt
+// query tiles (causal), so unit 0 is the first tile of the sequence.
+__host__ __device__ inline BwdUnit bwd_decode_unit(const CpGeom& g, int idx) {
+  BwdUnit U;
+  const int per = g.b * g.hkv;
+  const int ntile = 2 * g.cp * g.tpc;
+  const int gt = idx / per;
+  const int rest = idx % per;
+  U.bi = rest / g.hkv;
+  U.g = rest % g.hkv;
+  U.kc = gt / g.tpc;
+  U.v = gt % g.tpc;
+  U.khalf = U.kc >= g.cp ? 1 : 0;
+  U.j = U.khalf ? 2 * g.cp - 1 - U.kc : U.kc;
+  U.k_t0 = U.kc * g.c + U.v * kTile;
+  const int rem = g.c - U.v * kTile;
+  U.k_valid = rem < kTile ? rem : kTile;
+  U.nq = g.causal ? ntile - gt : ntile;
+  U.items = U.nq * (g.hq / g.hkv);
+  return U;
+}
+
+// Walks the query tiles of a backward unit in CP-step order (see above).
+struct QWalk {
+  int cp, j, khalf, kc, v, tpc, causal;
+  int step, seg, u;
+
+  __host__ __device__ QWalk(const CpGeom& g, const BwdUnit& U)
+      : cp(g.cp), j(U.j), khalf(U.khalf), kc(U.kc), v(U.v), tpc(g.tpc), causal(g.causal), step(0), seg(0), u(0) {}
+
+  // Segment `sg` of step `st`: query tiles [u0, tpc) of chunk `chunk`;
+  // the first of them is the diagonal tile when `diag`.
+  __host__ __device__ bool segment(int st, int sg, int& chunk, int& u0, bool& diag) const {
+    u0 = 0;
+    diag = false;
+    const int r = (j + st) % cp;
+    if (!causal) {
+      if (sg > 1) return false;
+      chunk = sg == 0 ? r : 2 * cp - 1 - r;
+      return true;
+    }
+    if (st == 0) {
+      if (sg == 0) {
+        chunk = kc;
+        u0 = v;
+        diag = true;
+        return true;
+      }
+      if (sg == 1 && khalf == 0) {
+        chunk = 2 * cp - 1 - j;
+        return true;
+      }
+      return false;
+    }
+    if (r > j) {  // no wrap: rank r keeps only first halves of incoming KV
+      if (khalf != 0 || sg > 1) return false;
+      chunk = sg == 0 ? r : 2 * cp - 1 - r;
+      return true;
+    }
+    if (sg > 0) return false;  // wrap: only r's second query chunk
+    chunk = 2 * cp - 1 - r;
+    return true;
+  }
+
+  __host__ __device__ bool next(int& chunk, int& tile, bool& is_diag) {
+    while (step < cp) {
+      int ch, u0;
+      bool dg;
+      if (segment(step, seg, ch, u0, dg)) {
+        if (u < u0) u = u0;
+        if (u < tpc) {
+          chunk = ch;
+          tile = u;
+          is_diag = dg && (u == u0);
+          ++u;
+          return true;
+        }
+        ++seg;
+        u = 0;
+        continue;
+      }
+      ++step;
+      seg = 0;
+      u = 0;
+    }
+    return false;
+  }
+};
+
 }  // namespace cpattn

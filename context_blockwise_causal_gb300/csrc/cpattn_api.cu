@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "../../include/cpattn.h"
+#include "bwd_kernel.cuh"
 #include "fwd_kernel.cuh"
 #include "tmap.h"
 
@@ -27,6 +28,7 @@ struct DeviceInfo {
   int num_sms = 0;
   unsigned int* status = nullptr;
   bool fwd_attr[2] = {false, false};
+  bool bwd_attr[2] = {false, false};
 };
 DeviceInfo g_devs[kMaxDevices];
 std::mutex g_mu;
@@ -128,14 +130,101 @@ extern "C" int cpattn_fwd(const void* q, const void* k, const void* v, void* o, 
   return d == 128 ? launch_fwd<128>(tq, tk, tv, args, di, st) : launch_fwd<64>(tq, tk, tv, args, di, st);
 }
 
-extern "C" size_t cpattn_bwd_workspace_bytes(int b, int s, int hq, int hkv, int d, int cp) {
-  if (check_geometry(b, s, hq, hkv, d, cp)) return 0;
-  return 0;  // backward not built yet
+namespace cpattn {
+namespace {
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct BwdLayout {
+  size_t dq_acc, lvec, dvec, total;
+  int ntp;
+};
+
+BwdLayout bwd_layout(int b, int s, int hq, int d, int cp) {
+  BwdLayout L;
+  const int c = s / (2 * cp);
+  const int tpc = (c + kTile - 1) / kTile;
+  L.ntp = 2 * cp * tpc * kTile;
+  L.dq_acc = 0;
+  L.lvec = align256(size_t(b) * s * hq * d * 4);
+  L.dvec = L.lvec + align256(size_t(b) * hq * L.ntp * 4);
+  L.total = L.dvec + align256(size_t(b) * hq * L.ntp * 4);
+  return L;
 }
 
-extern "C" int cpattn_bwd(const void*, const void*, const void*, const void*, const float*, const void*, void*, void*,
-                          void*, void*, size_t, int, int, int, int, int, int, int, void*) {
-  return CPATTN_ERR_INVALID_ARG;
+template <int D>
+int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+               const BwdArgs& args, DeviceInfo* di, cudaStream_t st) {
+  using C = BwdCfg<D>;
+  const int slot = D == 128 ? 1 : 0;
+  if (!di->bwd_attr[slot]) {
+    if (cudaFuncSetAttribute(cpattn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+        cudaSuccess)
+      return CPATTN_ERR_CUDA;
+    di->bwd_attr[slot] = true;
+  }
+  const int64_t rows = int64_t(args.g.b) * args.g.s * args.g.hq;
+  int pre_grid = int((rows + 255) / 256);
+  if (pre_grid > di->num_sms * 16) pre_grid = di->num_sms * 16;
+  cpattn_bwd_pre_kernel<D><<<pre_grid, 256, 0, st>>>(args);
+  if (cudaGetLastError() != cudaSuccess) return CPATTN_ERR_LAUNCH_FAILED;
+  const int units = bwd_num_units(args.g);
+  const int grid = units < di->num_sms ? units : di->num_sms;
+  cpattn_bwd_kernel<D><<<grid, kBwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, args);
+  if (cudaGetLastError() != cudaSuccess) return CPATTN_ERR_LAUNCH_FAILED;
+  const int64_t n4 = rows * D / 4;
+  int cv_grid = int((n4 + 255) / 256);
+  if (cv_grid > di->num_sms * 16) cv_grid = di->num_sms * 16;
+  cpattn_dq_convert_kernel<<<cv_grid, 256, 0, st>>>(args.dq_acc, args.dq, n4);
+  return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_LAUNCH_FAILED;
+}
+
+}  // namespace
+}  // namespace cpattn
+
+extern "C" size_t cpattn_bwd_workspace_bytes(int b, int s, int hq, int hkv, int d, int cp) {
+  if (check_geometry(b, s, hq, hkv, d, cp)) return 0;
+  return bwd_layout(b, s, hq, d, cp).total;
+}
+
+extern "C" int cpattn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                          const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                          int b, int s, int hq, int hkv, int d, int cp, int causal, void* stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return CPATTN_ERR_NULL_PTR;
+  int rc = check_geometry(b, s, hq, hkv, d, cp);
+  if (rc) return rc;
+  for (const void* p : {q, k, v, o, static_cast<const void*>(lse), dout, static_cast<const void*>(dq),
+                        static_cast<const void*>(dk), static_cast<const void*>(dv),
+                        static_cast<const void*>(workspace)})
+    if (!aligned16(p)) return CPATTN_ERR_MISALIGNED;
+  const BwdLayout L = bwd_layout(b, s, hq, d, cp);
+  if (workspace_bytes < L.total) return CPATTN_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInfo* di = nullptr;
+  if ((rc = device_info(&di))) return rc;
+  CUtensorMap tq, tk, tv, tdo;
+  const uint64_t rows = uint64_t(b) * s;
+  if (!encode_bf16_rows_heads_d(&tq, q, rows, hq, d, kTile) || !encode_bf16_rows_heads_d(&tk, k, rows, hkv, d, kTile) ||
+      !encode_bf16_rows_heads_d(&tv, v, rows, hkv, d, kTile) ||
+      !encode_bf16_rows_heads_d(&tdo, dout, rows, hq, d, kTile))
+    return CPATTN_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  BwdArgs args;
+  args.g = make_geom(b, s, hq, hkv, cp, causal);
+  args.ntp = L.ntp;
+  args.o = static_cast<const __nv_bfloat16*>(o);
+  args.dout = static_cast<const __nv_bfloat16*>(dout);
+  args.lse = lse;
+  args.dq_acc = reinterpret_cast<float*>(ws + L.dq_acc);
+  args.lvec = reinterpret_cast<float*>(ws + L.lvec);
+  args.dvec = reinterpret_cast<float*>(ws + L.dvec);
+  args.dq = static_cast<__nv_bfloat16*>(dq);
+  args.dk = static_cast<__nv_bfloat16*>(dk);
+  args.dv = static_cast<__nv_bfloat16*>(dv);
+  args.scale = float(1.0 / std::sqrt(double(d)));
+  args.scale_log2 = float(1.4426950408889634 / std::sqrt(double(d)));
+  args.status = di->status;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return d == 128 ? launch_bwd<128>(tq, tk, tv, tdo, args, di, st) : launch_bwd<64>(tq, tk, tv, tdo, args, di, st);
 }
 
 extern "C" int cpattn_zigzag_index(int s, int cp, int64_t* global_of_local) {

@@ -33,7 +33,6 @@
 namespace cpattn {
 
 constexpr int kFwdThreads = 320;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr float kRescaleThreshold = 8.0f;         // log2 units (factor 256)
 
 struct FwdArgs {

@@ -7,11 +7,14 @@
 // Prints "ok" per geometry or the first violation, exit code 1 on failure.
 #include <cstdio>
 #include <cstdlib>
+#include <algorithm>
 #include <vector>
 
 #include "../context_blockwise_causal_gb300/csrc/cp_schedule.cuh"
 
 using namespace cpattn;
+
+static int verify(const CpGeom& g, const std::vector<unsigned char>& count, const char* what);
 
 static int check(int b, int s, int hq, int hkv, int cp, int causal, int grid) {
   CpGeom g;
@@ -59,13 +62,48 @@ static int check(int b, int s, int hq, int hkv, int cp, int causal, int grid) {
     }
     if (nt != U.n) { printf("unit %d: walk has %d tiles, n = %d\n", idx, nt, U.n); return 1; }
   }
+  if (verify(g, count, "forward")) return 1;
+  // backward: key-tile units walking the query tiles that see them
+  std::fill(count.begin(), count.end(), 0);
+  const int nb = bwd_num_units(g);
+  const int G = hq / hkv;
+  int prev_items = 1 << 30;
+  for (int idx = 0; idx < nb; ++idx) {
+    BwdUnit U = bwd_decode_unit(g, idx);
+    if (causal && U.items > prev_items) { printf("bwd units not longest-first at %d\n", idx); return 1; }
+    prev_items = U.items;
+    QWalk w(g, U);
+    int chunk, tile, nt = 0;
+    bool dg;
+    while (w.next(chunk, tile, dg)) {
+      ++nt;
+      const int rem = g.c - tile * kTile;
+      const int qv = rem < kTile ? rem : kTile;
+      for (int h = U.g * G; h < (U.g + 1) * G; ++h)
+        for (int row = 0; row < qv; ++row)
+          for (int col = 0; col < U.k_valid; ++col) {
+            if (dg && col > row) continue;
+            const int t = chunk * g.c + tile * kTile + row, j = U.k_t0 + col;
+            unsigned char& c = count[(size_t(U.bi) * hq + h) * s * s + size_t(t) * s + j];
+            if (c) { printf("bwd pair (%d,%d) head %d computed twice\n", t, j, h); return 1; }
+            c = 1;
+          }
+    }
+    if (nt != U.nq) { printf("bwd unit %d: walk has %d tiles, nq = %d\n", idx, nt, U.nq); return 1; }
+    if (U.items != nt * G) { printf("bwd unit %d: items mismatch\n", idx); return 1; }
+  }
+  return verify(g, count, "backward");
+}
+
+static int verify(const CpGeom& g, const std::vector<unsigned char>& count, const char* what) {
+  const int b = g.b, hq = g.hq, s = g.s, causal = g.causal;
   for (int bi = 0; bi < b; ++bi)
     for (int h = 0; h < hq; ++h)
       for (int t = 0; t < s; ++t)
         for (int j = 0; j < s; ++j) {
           const int want = (!causal || j <= t) ? 1 : 0;
           if (count[(size_t(bi) * hq + h) * s * s + size_t(t) * s + j] != want) {
-            printf("pair (%d,%d) batch %d head %d: count %d want %d\n", t, j, bi, h,
+            printf("%s pair (%d,%d) batch %d head %d: count %d want %d\n", what, t, j, bi, h,
                    count[(size_t(bi) * hq + h) * s * s + size_t(t) * s + j], want);
             return 1;
           }

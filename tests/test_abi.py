@@ -1,0 +1,91 @@
+"""CPU tests of the C-ABI library: it loads, exports every function that
+include/*.h declares, and its host-only logic behaves (no GPU needed: the
+calls below return before touching a device)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+import torch
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import context_blockwise_causal_gb300 as pkg
+
+    if not os.path.exists(pkg.LIB_PATH):
+        pkg.build()
+    return pkg.library()
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(cpattn_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for required in ("cpattn_fwd", "cpattn_bwd", "cpattn_bwd_workspace_bytes", "cpattn_zigzag_index"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_zigzag_index_matches_oracle(lib):
+    from context_blockwise_causal_gb300 import cpattn_zigzag_index
+
+    for s, cp in ((8, 2), (12, 3), (4096, 4), (16384, 8), (96, 3), (2, 1)):
+        got = cpattn_zigzag_index(s, cp)
+        assert got.shape == (cp, s // cp)
+        assert torch.equal(got, oracle.zigzag_global_index(s, cp))  # bit-exact
+
+
+def test_zigzag_index_errors(lib):
+    buf = (ctypes.c_int64 * 64)()
+    assert lib.cpattn_zigzag_index(10, 3, buf) == -1  # s not divisible by 2cp
+    assert lib.cpattn_zigzag_index(12, 0, buf) == -1
+    assert lib.cpattn_zigzag_index(12, 3, None) == -2
+
+
+def test_strerror_and_version(lib):
+    assert lib.cpattn_strerror(0) == b"ok"
+    for code in range(-8, 0):
+        assert lib.cpattn_strerror(code) not in (b"", b"unknown error")
+    assert lib.cpattn_strerror(-99) == b"unknown error"
+    assert lib.cpattn_version() >= 100
+
+
+def test_fwd_argument_errors_are_reported_before_any_device_work(lib):
+    p = ctypes.c_void_p(4096)  # never dereferenced: validation fails first
+    f = lib.cpattn_fwd
+    assert f(None, p, p, p, p, 1, 512, 4, 4, 64, 2, 1, None) == -2
+    assert f(p, p, p, p, p, 1, 512, 4, 4, 96, 2, 1, None) == -1    # unsupported d
+    assert f(p, p, p, p, p, 1, 510, 4, 4, 64, 2, 1, None) == -1    # s % 2cp
+    assert f(p, p, p, p, p, 1, 512, 6, 4, 64, 2, 1, None) == -1    # hq % hkv
+    assert f(p, p, p, p, p, 0, 512, 4, 4, 64, 2, 1, None) == -1
+    assert f(p, p, p, p, p, 1, 512, 4, 4, 64, 0, 1, None) == -1
+    odd = ctypes.c_void_p(4096 + 8)
+    assert f(odd, p, p, p, p, 1, 512, 4, 4, 64, 2, 1, None) == -3  # misaligned
+
+
+def test_bwd_argument_errors_and_workspace_size(lib):
+    n = lib.cpattn_bwd_workspace_bytes(1, 512, 4, 2, 64, 2)
+    # fp32 dQ accumulator + tile-padded L and D vectors (256-byte aligned pieces)
+    assert n >= 512 * 4 * 64 * 4 + 2 * 4 * 512 * 4
+    assert lib.cpattn_bwd_workspace_bytes(1, 510, 4, 2, 64, 2) == 0
+    p = ctypes.c_void_p(4096)
+    b = lib.cpattn_bwd
+    assert b(p, p, p, p, p, p, p, p, p, p, n - 1, 1, 512, 4, 2, 64, 2, 1, None) == -5
+    assert b(p, p, p, p, p, p, p, p, p, None, n, 1, 512, 4, 2, 64, 2, 1, None) == -2
+    assert b(p, p, p, p, p, p, p, p, p, p, n, 1, 512, 4, 3, 64, 2, 1, None) == -1

@@ -18,10 +18,9 @@
 //
 // Online softmax and the CP correction ("大模型面试宝典 · Megatron-LM 篇", 3.2
 // steps 4-5; the per-step log-sum-exp merge): per row a running maximum m
-// (base-2, pre-scaled) and sum l; when a new key tile raises the maximum by
-// more than kRescaleThreshold the O accumulator and l are multiplied by
-// 2^(m_old - m_new); otherwise m is kept (exact either way, since the final
-// O/l and L = (m + log2 l) ln 2 use the same m). Merging step after step in
+// (base-2, pre-scaled) and sum l; when a new key tile raises the maximum the
+// O accumulator and l are multiplied by 2^(m_old - m_new) (a warp skips the
+// TMEM round trip when none of its rows moved). Merging step after step in
 // this running form is the two-stage merge L = log sum e^{L_i},
 // O = sum e^{L_i - L} O_i applied incrementally; partial O never leaves TMEM.
 #pragma once
@@ -33,7 +32,12 @@
 namespace cpattn {
 
 constexpr int kFwdThreads = 320;
-constexpr float kRescaleThreshold = 8.0f;         // log2 units (factor 256)
+// A row's running max is moved (and O, l rescaled) as soon as a key tile
+// raises it. The largest P of the row is then exactly 1, which bf16 holds
+// exactly; with a lagging max (FA4's thresholded rescale) that dominant P
+// exceeds 1 and is rounded, which measured about twice the output error on
+// peaky rows (Q, K ~ N(0, 4)) for a 2-4% gain in speed.
+constexpr float kRescaleThreshold = 0.0f;  // log2 units
 
 struct FwdArgs {
   CpGeom g;

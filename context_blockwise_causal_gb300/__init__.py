@@ -59,6 +59,10 @@ def library():
         lib.cpattn_fwd.restype = _i
         lib.cpattn_bwd.argtypes = [_p] * 10 + [_sz] + [_i] * 7 + [_p]
         lib.cpattn_bwd.restype = _i
+        lib.cpattn_bwd_noalloc.argtypes = [_p] * 9 + [_i] * 7 + [_p]
+        lib.cpattn_bwd_noalloc.restype = _i
+        lib.cpattn_bwd_noalloc_max_scratch_bytes.argtypes = []
+        lib.cpattn_bwd_noalloc_max_scratch_bytes.restype = _sz
         lib.cpattn_bwd_workspace_bytes.argtypes = [_i] * 6
         lib.cpattn_bwd_workspace_bytes.restype = _sz
         lib.cpattn_zigzag_index.argtypes = [_i, _i, _p]

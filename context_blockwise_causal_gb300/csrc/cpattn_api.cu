@@ -18,6 +18,12 @@ namespace cpattn {
 // Sticky status word written by kernels that give up waiting.
 __device__ unsigned int g_device_status;
 
+// Backward scratch for cpattn_bwd_noalloc (see include/cpattn.h): a fixed
+// device array in this library's module, so that entry point needs no
+// allocation. Every device that loads the library holds it until exit.
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -226,6 +232,78 @@ extern "C" int cpattn_bwd(const void* q, const void* k, const void* v, const voi
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return d == 128 ? launch_bwd<128>(tq, tk, tv, tdo, args, di, st) : launch_bwd<64>(tq, tk, tv, tdo, args, di, st);
 }
+
+namespace cpattn {
+namespace {
+
+void* g_noalloc_addr[kMaxDevices];
+std::mutex g_noalloc_mu;
+
+// Device address of g_noalloc_scratch on the current device. The array's
+// name is only a host-side stand-in, so it is resolved here once per device,
+// with that device current.
+void* noalloc_scratch_address() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    g_noalloc_addr[dev] = p;
+  }
+  return g_noalloc_addr[dev];
+}
+
+}  // namespace
+}  // namespace cpattn
+
+// Backward for callers that cannot allocate device memory: the workspace is
+// the library's own fixed 64 MiB scratch array instead of a caller buffer.
+extern "C" int cpattn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                  const void* dout, void* dq, void* dk, void* dv, int b, int s, int hq, int hkv,
+                                  int d, int cp, int causal, void* stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return CPATTN_ERR_NULL_PTR;
+  int rc = check_geometry(b, s, hq, hkv, d, cp);
+  if (rc) return rc;
+  for (const void* p : {q, k, v, o, static_cast<const void*>(lse), dout, static_cast<const void*>(dq),
+                        static_cast<const void*>(dk), static_cast<const void*>(dv)})
+    if (!aligned16(p)) return CPATTN_ERR_MISALIGNED;
+  const BwdLayout L = bwd_layout(b, s, hq, d, cp);
+  if (L.total > kNoAllocScratchBytes) return CPATTN_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInfo* di = nullptr;
+  if ((rc = device_info(&di))) return rc;
+  void* scratch = noalloc_scratch_address();  // first call on a device resolves it
+  if (!scratch) return CPATTN_ERR_CUDA;
+  CUtensorMap tq, tk, tv, tdo;
+  const uint64_t rows = uint64_t(b) * s;
+  if (!encode_bf16_rows_heads_d(&tq, q, rows, hq, d, kTile) || !encode_bf16_rows_heads_d(&tk, k, rows, hkv, d, kTile) ||
+      !encode_bf16_rows_heads_d(&tv, v, rows, hkv, d, kTile) ||
+      !encode_bf16_rows_heads_d(&tdo, dout, rows, hq, d, kTile))
+    return CPATTN_ERR_CUDA;
+  // The preprocess kernel zeroes the dQ accumulator part and rewrites the
+  // L/D vectors on every call, so stale contents of the shared array from an
+  // earlier call do not matter.
+  uint8_t* ws = static_cast<uint8_t*>(scratch);
+  BwdArgs args;
+  args.g = make_geom(b, s, hq, hkv, cp, causal);
+  args.ntp = L.ntp;
+  args.o = static_cast<const __nv_bfloat16*>(o);
+  args.dout = static_cast<const __nv_bfloat16*>(dout);
+  args.lse = lse;
+  args.dq_acc = reinterpret_cast<float*>(ws + L.dq_acc);
+  args.lvec = reinterpret_cast<float*>(ws + L.lvec);
+  args.dvec = reinterpret_cast<float*>(ws + L.dvec);
+  args.dq = static_cast<__nv_bfloat16*>(dq);
+  args.dk = static_cast<__nv_bfloat16*>(dk);
+  args.dv = static_cast<__nv_bfloat16*>(dv);
+  args.scale = float(1.0 / std::sqrt(double(d)));
+  args.scale_log2 = float(1.4426950408889634 / std::sqrt(double(d)));
+  args.status = di->status;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return d == 128 ? launch_bwd<128>(tq, tk, tv, tdo, args, di, st) : launch_bwd<64>(tq, tk, tv, tdo, args, di, st);
+}
+
+extern "C" size_t cpattn_bwd_noalloc_max_scratch_bytes(void) { return kNoAllocScratchBytes; }
 
 extern "C" int cpattn_zigzag_index(int s, int cp, int64_t* global_of_local) {
   if (!global_of_local) return CPATTN_ERR_NULL_PTR;

@@ -31,8 +31,9 @@
  *     b, s, hq, hkv, cp >= 1; b*s < 2^31. Chunk length c need not be a
  *     multiple of the 128-token tile (ragged tiles are masked).
  *   - Pointers: device pointers unless stated otherwise; the caller owns every
- *     buffer. Device buffers must be 16-byte aligned. The library allocates
- *     no device memory and keeps no per-call state.
+ *     buffer. Device buffers must be 16-byte aligned. No call allocates
+ *     device memory and none keeps per-call state (the one fixed scratch
+ *     array, used only by cpattn_bwd_noalloc, is part of the loaded module).
  *   - stream: a cudaStream_t passed as void* (NULL = legacy default stream).
  *     Calls only enqueue work and return; results are ready when the stream
  *     is synchronised.
@@ -93,6 +94,35 @@ size_t cpattn_bwd_workspace_bytes(int b, int s, int hq, int hkv, int d, int cp);
 int cpattn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int b, int s, int hq, int hkv,
                int d, int cp, int causal, void* stream);
+
+/*
+ * cpattn_bwd without a workspace argument. The pages describe nothing like
+ * it: it exists for callers that cannot allocate device memory when they
+ * call the backward -- code that runs under a device-memory budget fixed at
+ * start-up, threads that must not enter an allocator, or bindings with no
+ * device allocator of their own -- and so cannot hand cpattn_bwd its
+ * workspace. The caller still passes every input and output buffer.
+ *
+ * The workspace is instead a fixed scratch array of
+ * cpattn_bwd_noalloc_max_scratch_bytes() bytes (64 MiB) inside the library,
+ * held by every device that loads the library until the process exits.
+ * Sizes whose workspace (cpattn_bwd_workspace_bytes) exceeds it are rejected
+ * with CPATTN_ERR_WORKSPACE_TOO_SMALL before any device work.
+ * This entry point calls no cudaMalloc/cudaFree and no allocating routine.
+ *
+ * The first call of this entry point on a device looks up the scratch
+ * array's device address; make that first call before any stream capture. All calls share the one array and each call
+ * re-initialises what it needs, but calls that overlap on the GPU (on
+ * different streams, or from different threads without ordering) race on
+ * it and give wrong results: order them.
+ * Arguments, layouts and errors are otherwise those of cpattn_bwd.
+ */
+int cpattn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                       const void* dout, void* dq, void* dk, void* dv, int b, int s, int hq, int hkv, int d, int cp,
+                       int causal, void* stream);
+
+/* Size in bytes of the scratch array cpattn_bwd_noalloc uses. */
+size_t cpattn_bwd_noalloc_max_scratch_bytes(void);
 
 /*
  * Host helper: the zigzag index map. Fills global_of_local (HOST memory,

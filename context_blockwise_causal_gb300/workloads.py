@@ -60,6 +60,10 @@ WORKLOADS = {
                  k_std=2.0, seed=1003, check_rows=1024),
         Workload("train_b1_s32768_h32kv8_d128_cp8", b=1, s=32768, hq=32, hkv=8, d=128, cp=8, backward=True,
                  seed=1004, check_rows=512, check_dkv_heads=4),
+        # half-length training shape: the size the kernels are profiled on
+        # (inputs still exceed L2; a launch stays well under a second)
+        Workload("train_b1_s16384_h32kv8_d128_cp8", b=1, s=16384, hq=32, hkv=8, d=128, cp=8, backward=True,
+                 seed=1005, check_rows=512, check_dkv_heads=2),
     ]
 }
 

@@ -70,6 +70,11 @@ class ClockSampler:
                  "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            # let nvidia-smi initialise before the timed region starts
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 5.0:
+                time.sleep(0.02)
+            self.lines.clear()
         except (OSError, ValueError):
             self.proc = None
         return self

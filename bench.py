@@ -131,6 +131,9 @@ def _profile_traffic(kernel_file, profile_name):
 
 
 # ------------------------------------------------------------------ CPU oracle arm
+_CPU_INPUTS = {}
+
+
 def _oracle_sample(w, rows_n, seed):
     """The CPU oracle on a bounded sample of workload w: forward O/LSE and the
     backward's dQ for `rows_n` seeded random query rows of every head.
@@ -139,7 +142,9 @@ def _oracle_sample(w, rows_n, seed):
     import oracle
     from context_blockwise_causal_gb300.workloads import make_inputs, sample_rows
 
-    x = make_inputs(w, device="cpu")
+    if w.name not in _CPU_INPUTS:
+        _CPU_INPUTS[w.name] = make_inputs(w, device="cpu")
+    x = _CPU_INPUTS[w.name]
     rows = sample_rows(w, rows_n, seed=seed)
     t0 = time.perf_counter()
     oracle.attention_forward(x["q"], x["k"], x["v"], causal=w.causal, rows=rows, row_block=256)
@@ -334,7 +339,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--ref-rows", type=int, default=48)
+    ap.add_argument("--ref-rows", type=int, default=1024)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -9,9 +9,12 @@
 //                             and computes, on tcgen05 tensor cores,
 //                               S^T = K Q^T, dP^T = V dO^T          (TMEM)
 //                               P^T = 2^(S^T*scale*log2e - L*log2e)
-//                               dS^T = scale * P^T (dP^T - D)
+//                               dS^T = P^T (dP^T - D)
 //                               dV += P^T dO, dK += dS^T Q          (TMEM)
-//                               dQ  = dS K  -> fp32 atomics into the accumulator
+//                               dQ^T = K^T dS^T -> fp32 reductions into the
+//                               accumulator (d = 64: dQ = dS K)
+//                             with 1/sqrt(d) applied once to dK at the end and
+//                             to dQ in the conversion,
 //                             dK/dV of the tile stay in TMEM across all its
 //                             blocks and are written once.
 //   cpattn_dq_convert_kernel  fp32 dQ accumulator -> bf16 dq.     (HBM-bound)
@@ -29,7 +32,8 @@
 //   warp 9     TMEM owner and MMA issuer
 // TMEM: A [0,128) S^T, then P^T (bf16 pairs: queries 0-63 in columns 0-31,
 // 64-127 in columns 64-95); B [128,256) dP^T, then dQ; dV [256,256+D);
-// dK [256+D, 256+2D).
+// dK [256+D, 256+2D). Units walk query tiles from the end of the sequence
+// down (see QWalk), which keeps the dQ rows being reduced into L2-resident.
 // Shared memory: K, V tiles; two stages of (Q, dO, L, D); dS^T (bf16,
 // 128 keys x 128 queries, laid out as two 64-query blocks of 128-byte
 // swizzled rows: K-major for dK's A operand and MN-major for dQ's A operand).
@@ -96,13 +100,15 @@ __global__ void __launch_bounds__(256) cpattn_bwd_pre_kernel(const BwdArgs a) {
 }
 
 // ---------------------------------------------------------------- dQ convert
+// dq = bf16(scale * acc): the main kernel accumulates dS K with dS unscaled.
 __global__ void __launch_bounds__(256) cpattn_dq_convert_kernel(const float* __restrict__ acc,
-                                                                __nv_bfloat16* __restrict__ dq, int64_t n4) {
+                                                                __nv_bfloat16* __restrict__ dq, int64_t n4,
+                                                                float scale) {
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += int64_t(gridDim.x) * blockDim.x) {
     const float4 x = reinterpret_cast<const float4*>(acc)[i];
     uint2 p;
-    p.x = pack_bf16x2(x.x, x.y);
-    p.y = pack_bf16x2(x.z, x.w);
+    p.x = pack_bf16x2(x.x * scale, x.y * scale);
+    p.y = pack_bf16x2(x.z * scale, x.w * scale);
     reinterpret_cast<uint2*>(dq)[i] = p;
   }
 }
@@ -275,7 +281,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idS = make_idesc_bf16(kTile, kTile, false, false);  // S^T, dP^T
       constexpr uint32_t idKV = make_idesc_bf16(kTile, D, false, true);      // dV, dK
-      constexpr uint32_t idQ = make_idesc_bf16(kTile, D, true, true);        // dQ
+      constexpr uint32_t idQ = make_idesc_bf16(kTile, D == 128 ? kTile : D, true, true);  // dQ^T / dQ
       const uint64_t dK_km = make_sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dV_km = make_sdesc_sw128(smem_u32(sV), 16, 1024);
       const uint64_t dK_mn = make_sdesc_sw128(smem_u32(sK), 16384, 1024);
@@ -333,10 +339,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;
             umma_ss(tdK, ddS_km + off, dQ_mn + so + ((kk * 2048) >> 4), idKV, acc | (kk > 0));
           }
-          // dQ = dS K  -> region B
+          // dQ -> region B. d = 128: dQ^T = K^T dS^T (TMEM lanes = head dim, so
+          // each warp's reduction into the accumulator is one 128-byte line);
+          // d = 64: dQ = dS K (lanes = queries).
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            umma_ss(tB, ddS_mn + ((kk * 2048) >> 4), dK_mn + ((kk * 2048) >> 4), idQ, kk > 0);
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            if constexpr (D == 128)
+              umma_ss(tB, dK_mn + ((kk * 2048) >> 4), ddS_mn + ((kk * 2048) >> 4), idQ, kk > 0);
+            else
+              umma_ss(tB, ddS_mn + ((kk * 2048) >> 4), dK_mn + ((kk * 2048) >> 4), idQ, kk > 0);
+          }
           umma_commit(&q_empty[st]);
           umma_commit(ds_empty);
           umma_commit(dq_full);
@@ -384,9 +396,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         const float* Lv = sLD + st * (2 * kTile);
         const float* Dv = Lv + kTile;
+        // Blocks away from the diagonal and from ragged chunk ends need no mask.
+        const bool full = !dg && q_valid == kTile && U.k_valid == kTile;
         const bool key_ok = jr < U.k_valid;
         // the previous dQ/dK MMAs must be done reading dS^T
         if (item > 0 && !(ok = mbar_wait_bounded(ds_empty, (item - 1) & 1, abort_flag, kWaitLimitNs))) break;
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
         for (int sc = 0; sc < 2; ++sc) {
           const int c0 = hf * 64 + sc * 32;  // first query column of this chunk
@@ -396,19 +411,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           uint32_t pp[16], pd[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            float p2[2], d2[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int c = c0 + 2 * i + e;
-              const bool valid = key_ok && c < q_valid && !(dg && jr > c);
+            const int c = c0 + 2 * i;
+            // P = 2^(S*scale*log2e - L*log2e); dS (unscaled) = P (dP - D)
+            const uint64_t x = f2_fma(f2_pack(__uint_as_float(rs[2 * i]), __uint_as_float(rs[2 * i + 1])), sl2x2,
+                                      f2_pack(-Lv[c], -Lv[c + 1]));
+            float x0, x1;
+            f2_unpack(x, x0, x1);
+            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            const uint64_t t = f2_sub(f2_pack(__uint_as_float(rp[2 * i]), __uint_as_float(rp[2 * i + 1])),
+                                      f2_pack(Dv[c], Dv[c + 1]));
+            float d0, d1;
+            f2_unpack(f2_mul(f2_pack(p0, p1), t), d0, d1);
+            if (!full) {
               // padded rows of L/D hold arbitrary values: select, never multiply
-              const float p = ex2_approx(fmaf(__uint_as_float(rs[2 * i + e]), sl2, -Lv[c]));
-              const float ds = p * (__uint_as_float(rp[2 * i + e]) - Dv[c]) * scale;
-              p2[e] = valid ? p : 0.f;
-              d2[e] = valid ? ds : 0.f;
+              const bool v0 = key_ok && c < q_valid && !(dg && jr > c);
+              const bool v1 = key_ok && c + 1 < q_valid && !(dg && jr > c + 1);
+              p0 = v0 ? p0 : 0.f;
+              d0 = v0 ? d0 : 0.f;
+              p1 = v1 ? p1 : 0.f;
+              d1 = v1 ? d1 : 0.f;
             }
-            pp[i] = pack_bf16x2(p2[0], p2[1]);
-            pd[i] = pack_bf16x2(d2[0], d2[1]);
+            pp[i] = pack_bf16x2(p0, p1);
+            pd[i] = pack_bf16x2(d0, d1);
           }
           tmem_st16(tA + hf * 64 + sc * 16, pp);
           // dS^T row jr, query block hf, 16-byte chunks 4*sc .. 4*sc+3 (swizzled)
@@ -424,31 +448,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full);
-        // ---- drain dQ of this block into the fp32 accumulator
+        // ---- drain dQ of this block into the fp32 accumulator (unscaled;
+        // the conversion kernel applies 1/sqrt(d))
         if (!(ok = mbar_wait_bounded(dq_full, item & 1, abort_flag, kWaitLimitNs))) break;
         tc_fence_after();
-        uint32_t rq[D / 2];
-        if constexpr (D == 128) {
+        uint32_t rq[64];
+        {
           uint32_t r0[32], r1[32];
-          tmem_ld32(tB + hf * 64, r0);
-          tmem_ld32(tB + hf * 64 + 32, r1);
+          if constexpr (D == 128) {
+            tmem_ld32(tB + hf * 64, r0);
+            tmem_ld32(tB + hf * 64 + 32, r1);
+          } else {
+            tmem_ld32(tB + hf * 32, r0);
+          }
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             rq[i] = r0[i];
-            rq[32 + i] = r1[i];
+            if constexpr (D == 128) rq[32 + i] = r1[i];
           }
-        } else {
-          uint32_t r0[32];
-          tmem_ld32(tB + hf * 32, r0);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) rq[i] = r0[i];
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(dq_empty);
-        if (jr < q_valid) {
-          const int t = chunk * g.c + tile * kTile + jr;
-          float* dst = a.dq_acc + ((int64_t(U.bi) * g.s + t) * g.hq + h) * D + hf * (D / 2);
+        const int t0 = chunk * g.c + tile * kTile;
+        if constexpr (D == 128) {
+          // lane jr holds dQ^T[d = jr][queries hf*64 ..]: a warp adds one
+          // contiguous 128-byte line per query row
+          float* base = a.dq_acc + ((int64_t(U.bi) * g.s + t0 + hf * 64) * g.hq + h) * D + jr;
+          const int64_t row_stride = int64_t(g.hq) * D;
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (hf * 64 + i < q_valid) red_add_f32(base + i * row_stride, __uint_as_float(rq[i]));
+        } else if (jr < q_valid) {
+          float* dst = a.dq_acc + ((int64_t(U.bi) * g.s + t0 + jr) * g.hq + h) * D + hf * (D / 2);
 #pragma unroll
           for (int i = 0; i < D / 2; i += 4)
             red_add_v4(dst + i, __uint_as_float(rq[i]), __uint_as_float(rq[i + 1]), __uint_as_float(rq[i + 2]),
@@ -483,10 +515,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           pv.y = pack_bf16x2(__uint_as_float(rv[i + 2]), __uint_as_float(rv[i + 3]));
           pv.z = pack_bf16x2(__uint_as_float(rv[i + 4]), __uint_as_float(rv[i + 5]));
           pv.w = pack_bf16x2(__uint_as_float(rv[i + 6]), __uint_as_float(rv[i + 7]));
-          pk.x = pack_bf16x2(__uint_as_float(rk[i]), __uint_as_float(rk[i + 1]));
-          pk.y = pack_bf16x2(__uint_as_float(rk[i + 2]), __uint_as_float(rk[i + 3]));
-          pk.z = pack_bf16x2(__uint_as_float(rk[i + 4]), __uint_as_float(rk[i + 5]));
-          pk.w = pack_bf16x2(__uint_as_float(rk[i + 6]), __uint_as_float(rk[i + 7]));
+          // dK accumulated dS^T Q with dS unscaled: apply 1/sqrt(d) here
+          pk.x = pack_bf16x2(__uint_as_float(rk[i]) * scale, __uint_as_float(rk[i + 1]) * scale);
+          pk.y = pack_bf16x2(__uint_as_float(rk[i + 2]) * scale, __uint_as_float(rk[i + 3]) * scale);
+          pk.z = pack_bf16x2(__uint_as_float(rk[i + 4]) * scale, __uint_as_float(rk[i + 5]) * scale);
+          pk.w = pack_bf16x2(__uint_as_float(rk[i + 6]) * scale, __uint_as_float(rk[i + 7]) * scale);
           *reinterpret_cast<uint4*>(a.dv + off + i) = pv;
           *reinterpret_cast<uint4*>(a.dk + off + i) = pk;
         }

@@ -170,22 +170,20 @@ struct KvWalk {
 
 // ---------------------------------------------------------------- backward
 // A backward work unit is one 128-key tile (chunk kc, tile v) of one KV head
-// for one batch element. It visits every (query head of the group, query
-// tile) block that sees its keys, walking the CP steps from the key owner's
-// side: the chunk kc belongs to rank j; at step i rank r = (j + i) mod cp
-// holds it and, by the same three rules as the forward,
-//   step 0            : rank j's own query chunks (the diagonal tile masked);
-//   i >= 1, no wrap   : (r > j) rank r uses only first halves of incoming KV,
-//                       so chunk kc counts only if it is j's first half, and
-//                       then against both of r's query chunks;
-//   i >= 1, wrap      : (r < j) only r's second query chunk 2cp-1-r, against
-//                       both of j's chunks.
-// The set of blocks is exactly the forward's; dK/dV of the tile accumulate
-// over all of them on chip.
+// for one batch element. It visits every (query tile, query head of the
+// group) block that sees its keys. By the forward's CP rules those blocks
+// are: the rank's own step-0 block (the one diagonal tile, masked), and every
+// query tile of a later position (steps 1..cp-1, unmasked) -- i.e. all query
+// tiles at or after the key tile in global order. The unit walks them from
+// the end of the sequence down to its own diagonal tile: every running unit
+// then starts at the same query tiles and moves down at the same pace, so
+// the dQ rows being accumulated (and the Q/dO tiles being read) are shared
+// by the CTAs in flight and stay in L2. dK/dV of the tile accumulate on chip
+// over all its blocks.
 struct BwdUnit {
   int bi, g;      // batch element, KV head
   int kc, v;      // key chunk and tile within it
-  int j, khalf;   // owning rank of the chunk, and which of its two chunks
+  int gt;         // global tile index of the key tile: kc * tpc + v
   int k_t0;       // first key token
   int k_valid;    // keys of the tile inside the chunk
   int nq;         // number of query tiles that see the tile
@@ -204,10 +202,9 @@ __host__ __device__ inline BwdUnit bwd_decode_unit(const CpGeom& g, int idx) {
   const int rest = idx % per;
   U.bi = rest / g.hkv;
   U.g = rest % g.hkv;
+  U.gt = gt;
   U.kc = gt / g.tpc;
   U.v = gt % g.tpc;
-  U.khalf = U.kc >= g.cp ? 1 : 0;
-  U.j = U.khalf ? 2 * g.cp - 1 - U.kc : U.kc;
   U.k_t0 = U.kc * g.c + U.v * kTile;
   const int rem = g.c - U.v * kTile;
   U.k_valid = rem < kTile ? rem : kTile;
@@ -216,70 +213,20 @@ __host__ __device__ inline BwdUnit bwd_decode_unit(const CpGeom& g, int idx) {
   return U;
 }
 
-// Walks the query tiles of a backward unit in CP-step order (see above).
+// Walks the query tiles of a backward unit, last tile first.
 struct QWalk {
-  int cp, j, khalf, kc, v, tpc, causal;
-  int step, seg, u;
+  int tpc, lo, gt_k, causal, gt;
 
   __host__ __device__ QWalk(const CpGeom& g, const BwdUnit& U)
-      : cp(g.cp), j(U.j), khalf(U.khalf), kc(U.kc), v(U.v), tpc(g.tpc), causal(g.causal), step(0), seg(0), u(0) {}
-
-  // Segment `sg` of step `st`: query tiles [u0, tpc) of chunk `chunk`;
-  // the first of them is the diagonal tile when `diag`.
-  __host__ __device__ bool segment(int st, int sg, int& chunk, int& u0, bool& diag) const {
-    u0 = 0;
-    diag = false;
-    const int r = (j + st) % cp;
-    if (!causal) {
-      if (sg > 1) return false;
-      chunk = sg == 0 ? r : 2 * cp - 1 - r;
-      return true;
-    }
-    if (st == 0) {
-      if (sg == 0) {
-        chunk = kc;
-        u0 = v;
-        diag = true;
-        return true;
-      }
-      if (sg == 1 && khalf == 0) {
-        chunk = 2 * cp - 1 - j;
-        return true;
-      }
-      return false;
-    }
-    if (r > j) {  // no wrap: rank r keeps only first halves of incoming KV
-      if (khalf != 0 || sg > 1) return false;
-      chunk = sg == 0 ? r : 2 * cp - 1 - r;
-      return true;
-    }
-    if (sg > 0) return false;  // wrap: only r's second query chunk
-    chunk = 2 * cp - 1 - r;
-    return true;
-  }
+      : tpc(g.tpc), lo(g.causal ? U.gt : 0), gt_k(U.gt), causal(g.causal), gt(2 * g.cp * g.tpc - 1) {}
 
   __host__ __device__ bool next(int& chunk, int& tile, bool& is_diag) {
-    while (step < cp) {
-      int ch, u0;
-      bool dg;
-      if (segment(step, seg, ch, u0, dg)) {
-        if (u < u0) u = u0;
-        if (u < tpc) {
-          chunk = ch;
-          tile = u;
-          is_diag = dg && (u == u0);
-          ++u;
-          return true;
-        }
-        ++seg;
-        u = 0;
-        continue;
-      }
-      ++step;
-      seg = 0;
-      u = 0;
-    }
-    return false;
+    if (gt < lo) return false;
+    chunk = gt / tpc;
+    tile = gt % tpc;
+    is_diag = causal && gt == gt_k;
+    --gt;
+    return true;
   }
 };
 

@@ -181,7 +181,7 @@ int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& 
   const int64_t n4 = rows * D / 4;
   int cv_grid = int((n4 + 255) / 256);
   if (cv_grid > di->num_sms * 16) cv_grid = di->num_sms * 16;
-  cpattn_dq_convert_kernel<<<cv_grid, 256, 0, st>>>(args.dq_acc, args.dq, n4);
+  cpattn_dq_convert_kernel<<<cv_grid, 256, 0, st>>>(args.dq_acc, args.dq, n4, args.scale);
   return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_LAUNCH_FAILED;
 }
 

@@ -142,18 +142,18 @@ namespace {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct BwdLayout {
-  size_t dq_acc, lvec, dvec, total;
+  size_t lvec, dvec, total;
   int ntp;
 };
 
 BwdLayout bwd_layout(int b, int s, int hq, int d, int cp) {
+  (void)d;
   BwdLayout L;
   const int c = s / (2 * cp);
   const int tpc = (c + kTile - 1) / kTile;
   L.ntp = 2 * cp * tpc * kTile;
-  L.dq_acc = 0;
-  L.lvec = align256(size_t(b) * s * hq * d * 4);
-  L.dvec = L.lvec + align256(size_t(b) * hq * L.ntp * 4);
+  L.lvec = 0;
+  L.dvec = align256(size_t(b) * hq * L.ntp * 4);
   L.total = L.dvec + align256(size_t(b) * hq * L.ntp * 4);
   return L;
 }
@@ -161,11 +161,12 @@ BwdLayout bwd_layout(int b, int s, int hq, int d, int cp) {
 template <int D>
 int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                const BwdArgs& args, DeviceInfo* di, cudaStream_t st) {
-  using C = BwdCfg<D>;
   const int slot = D == 128 ? 1 : 0;
   if (!di->bwd_attr[slot]) {
-    if (cudaFuncSetAttribute(cpattn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(cpattn_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DkdvCfg<D>::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(cpattn_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DqCfg<D>::kSmemBytes) != cudaSuccess)
       return CPATTN_ERR_CUDA;
     di->bwd_attr[slot] = true;
   }
@@ -174,14 +175,13 @@ int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& 
   if (pre_grid > di->num_sms * 16) pre_grid = di->num_sms * 16;
   cpattn_bwd_pre_kernel<D><<<pre_grid, 256, 0, st>>>(args);
   if (cudaGetLastError() != cudaSuccess) return CPATTN_ERR_LAUNCH_FAILED;
-  const int units = bwd_num_units(args.g);
-  const int grid = units < di->num_sms ? units : di->num_sms;
-  cpattn_bwd_kernel<D><<<grid, kBwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, args);
+  const int kv_units = bwd_num_units(args.g);
+  cpattn_bwd_dkdv_kernel<D><<<kv_units < di->num_sms ? kv_units : di->num_sms, kBwdThreads, DkdvCfg<D>::kSmemBytes,
+                              st>>>(tq, tk, tv, tdo, args);
   if (cudaGetLastError() != cudaSuccess) return CPATTN_ERR_LAUNCH_FAILED;
-  const int64_t n4 = rows * D / 4;
-  int cv_grid = int((n4 + 255) / 256);
-  if (cv_grid > di->num_sms * 16) cv_grid = di->num_sms * 16;
-  cpattn_dq_convert_kernel<<<cv_grid, 256, 0, st>>>(args.dq_acc, args.dq, n4, args.scale);
+  const int q_units = dq_num_units(args.g);
+  cpattn_bwd_dq_kernel<D><<<q_units < di->num_sms ? q_units : di->num_sms, kBwdThreads, DqCfg<D>::kSmemBytes, st>>>(
+      tq, tk, tv, tdo, args);
   return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_LAUNCH_FAILED;
 }
 
@@ -220,7 +220,6 @@ extern "C" int cpattn_bwd(const void* q, const void* k, const void* v, const voi
   args.o = static_cast<const __nv_bfloat16*>(o);
   args.dout = static_cast<const __nv_bfloat16*>(dout);
   args.lse = lse;
-  args.dq_acc = reinterpret_cast<float*>(ws + L.dq_acc);
   args.lvec = reinterpret_cast<float*>(ws + L.lvec);
   args.dvec = reinterpret_cast<float*>(ws + L.dvec);
   args.dq = static_cast<__nv_bfloat16*>(dq);
@@ -290,7 +289,6 @@ extern "C" int cpattn_bwd_noalloc(const void* q, const void* k, const void* v, c
   args.o = static_cast<const __nv_bfloat16*>(o);
   args.dout = static_cast<const __nv_bfloat16*>(dout);
   args.lse = lse;
-  args.dq_acc = reinterpret_cast<float*>(ws + L.dq_acc);
   args.lvec = reinterpret_cast<float*>(ws + L.lvec);
   args.dvec = reinterpret_cast<float*>(ws + L.dvec);
   args.dq = static_cast<__nv_bfloat16*>(dq);

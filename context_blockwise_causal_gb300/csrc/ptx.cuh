@@ -289,4 +289,44 @@ __device__ __forceinline__ void red_add_f32(float* gaddr, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(gaddr), "f"(v) : "memory");
 }
 
+
+// Two TMEM loads of 32 columns (from two addresses) with a single wait.
+#define CPATTN_RA8(i) "=r"(ra[i + 0]), "=r"(ra[i + 1]), "=r"(ra[i + 2]), "=r"(ra[i + 3]), \
+                      "=r"(ra[i + 4]), "=r"(ra[i + 5]), "=r"(ra[i + 6]), "=r"(ra[i + 7])
+#define CPATTN_RB8(i) "=r"(rb[i + 0]), "=r"(rb[i + 1]), "=r"(rb[i + 2]), "=r"(rb[i + 3]), \
+                      "=r"(rb[i + 4]), "=r"(rb[i + 5]), "=r"(rb[i + 6]), "=r"(rb[i + 7])
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, uint32_t (&ra)[32], uint32_t (&rb)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : CPATTN_RA8(0), CPATTN_RA8(8), CPATTN_RA8(16), CPATTN_RA8(24), CPATTN_RB8(0), CPATTN_RB8(8),
+        CPATTN_RB8(16), CPATTN_RB8(24)
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+#undef CPATTN_RA8
+#undef CPATTN_RB8
+
+
+// Four TMEM loads of 32 columns (from four addresses) with a single wait.
+#define CPATTN_RX8(r, i) "=r"(r[i + 0]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
+                         "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
+__device__ __forceinline__ void tmem_ld32x4(uint32_t ta, uint32_t tb, uint32_t tc, uint32_t td, uint32_t (&ra)[32],
+                                            uint32_t (&rb)[32], uint32_t (&rc)[32], uint32_t (&rd)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%128];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%129];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, [%130];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%131];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : CPATTN_RX8(ra, 0), CPATTN_RX8(ra, 8), CPATTN_RX8(ra, 16), CPATTN_RX8(ra, 24), CPATTN_RX8(rb, 0),
+        CPATTN_RX8(rb, 8), CPATTN_RX8(rb, 16), CPATTN_RX8(rb, 24), CPATTN_RX8(rc, 0), CPATTN_RX8(rc, 8),
+        CPATTN_RX8(rc, 16), CPATTN_RX8(rc, 24), CPATTN_RX8(rd, 0), CPATTN_RX8(rd, 8), CPATTN_RX8(rd, 16),
+        CPATTN_RX8(rd, 24)
+      : "r"(ta), "r"(tb), "r"(tc), "r"(td)
+      : "memory");
+}
+#undef CPATTN_RX8
+
 }  // namespace cpattn

@@ -77,8 +77,8 @@ int cpattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
 
 /*
  * Bytes of caller-provided device workspace cpattn_bwd needs for these sizes
- * (an fp32 dQ accumulator and the per-row D = rowsum(dO * O) vector).
- * Returns 0 for unsupported sizes.
+ * (two fp32 vectors per query row and head: lse * log2(e) and
+ * D = rowsum(dO * O), in 128-row tile order). Returns 0 for unsupported sizes.
  */
 size_t cpattn_bwd_workspace_bytes(int b, int s, int hq, int hkv, int d, int cp);
 

@@ -81,8 +81,10 @@ def test_fwd_argument_errors_are_reported_before_any_device_work(lib):
 
 def test_bwd_argument_errors_and_workspace_size(lib):
     n = lib.cpattn_bwd_workspace_bytes(1, 512, 4, 2, 64, 2)
-    # fp32 dQ accumulator + tile-padded L and D vectors (256-byte aligned pieces)
-    assert n >= 512 * 4 * 64 * 4 + 2 * 4 * 512 * 4
+    # two fp32 vectors (L*log2e and D) per query row and head, tile-padded
+    assert n == 2 * 4 * 512 * 4
+    # ragged chunks pad each chunk to whole 128-row tiles: c = 160 -> 256 rows
+    assert lib.cpattn_bwd_workspace_bytes(1, 640, 2, 1, 64, 2) == 2 * 2 * (4 * 256) * 4
     assert lib.cpattn_bwd_workspace_bytes(1, 510, 4, 2, 64, 2) == 0
     p = ctypes.c_void_p(4096)
     b = lib.cpattn_bwd

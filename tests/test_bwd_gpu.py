@@ -67,9 +67,9 @@ def test_bwd_workspace_contents_do_not_matter():
     g1 = cpattn_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], w.cp, workspace=ws1)
     g2 = cpattn_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], w.cp, workspace=ws2)
     torch.cuda.synchronize()
-    # dK/dV are written once from TMEM (deterministic); dQ sums fp32 atomics
-    assert torch.equal(g1[1], g2[1]) and torch.equal(g1[2], g2[2])
-    assert rel_l2(g1[0].float(), g2[0].double()) < 1e-3
+    # every gradient is accumulated on chip and written once: deterministic
+    for a_, b_ in zip(g1, g2):
+        assert torch.equal(a_, b_)
 
 
 def test_bwd_full_size_training_workload():

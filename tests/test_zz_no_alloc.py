@@ -54,7 +54,7 @@ def test_noalloc_matches_workspace_backward_twice(b, s, hq, hkv, d, cp):
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     lib = library()
     cap = lib.cpattn_bwd_noalloc_max_scratch_bytes()
-    b, s, hq, hkv, d, cp = 1, 32768, 32, 8, 128, 8
+    b, s, hq, hkv, d, cp = 1, 131072, 128, 8, 128, 16
     assert lib.cpattn_bwd_workspace_bytes(b, s, hq, hkv, d, cp) > cap
     p = ctypes.c_void_p(4096)  # never dereferenced: the size check comes first
     rc = lib.cpattn_bwd_noalloc(p, p, p, p, p, p, p, p, p, b, s, hq, hkv, d, cp, 1, None)

@@ -59,6 +59,8 @@ def library():
         lib.cpattn_fwd.restype = _i
         lib.cpattn_bwd.argtypes = [_p] * 10 + [_sz] + [_i] * 7 + [_p]
         lib.cpattn_bwd.restype = _i
+        lib.cpattn_bwd_stage.argtypes = [_i] + [_p] * 10 + [_sz] + [_i] * 7 + [_p]
+        lib.cpattn_bwd_stage.restype = _i
         lib.cpattn_bwd_noalloc.argtypes = [_p] * 9 + [_i] * 7 + [_p]
         lib.cpattn_bwd_noalloc.restype = _i
         lib.cpattn_bwd_noalloc_max_scratch_bytes.argtypes = []
@@ -131,8 +133,13 @@ def cpattn_bwd_workspace_bytes(b, s, hq, hkv, d, cp):
     return int(library().cpattn_bwd_workspace_bytes(b, s, hq, hkv, d, int(cp)))
 
 
-def cpattn_bwd(q, k, v, o, lse, do, cp, causal=True, dq=None, dk=None, dv=None, workspace=None, stream=None):
-    """Backward from the forward's saved o and lse. Returns (dq, dk, dv)."""
+def cpattn_bwd(q, k, v, o, lse, do, cp, causal=True, dq=None, dk=None, dv=None, workspace=None, stream=None,
+               stage=None):
+    """Backward from the forward's saved o and lse. Returns (dq, dk, dv).
+
+    ``stage`` (0, 1 or 2) runs only that stage of the backward (see
+    cpattn_bwd_stage in include/cpattn.h); None runs all three.
+    """
     b, s, hq, hkv, d = _dims(q, k, v)
     _check_act("o", o, q.shape)
     _check_act("do", do, q.shape)
@@ -150,11 +157,15 @@ def cpattn_bwd(q, k, v, o, lse, do, cp, causal=True, dq=None, dk=None, dv=None, 
     if not workspace.is_cuda or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous CUDA tensor")
     ws_bytes = workspace.numel() * workspace.element_size()
-    rc = library().cpattn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
-                              dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(), ws_bytes, b, s, hq,
-                              hkv, d, int(cp), 1 if causal else 0, _stream_handle(stream))
+    ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(), dq.data_ptr(),
+            dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(), ws_bytes, b, s, hq, hkv, d, int(cp),
+            1 if causal else 0, _stream_handle(stream))
+    if stage is None:
+        rc = library().cpattn_bwd(*ptrs)
+    else:
+        rc = library().cpattn_bwd_stage(int(stage), *ptrs)
     if rc:
-        raise CpattnError(rc, "cpattn_bwd")
+        raise CpattnError(rc, "cpattn_bwd" if stage is None else "cpattn_bwd_stage")
     return dq, dk, dv
 
 

@@ -143,8 +143,8 @@ struct DkdvCfg {
   static constexpr int kOffLD = kOffdO + 2 * kTileBytes;
   static constexpr int kLDBytes = 2 * kTile * 4;  // L[128], D[128] fp32 per stage
   static constexpr int kOffBar = kOffLD + 2 * kLDBytes;
-  // kv_full kv_empty q_full[2] q_empty[2] s_full p_full dkv_full dkv_empty drain
-  static constexpr int kNumBars = 11;
+  // kv_full kv_empty q_full[2] q_empty[2] s_full p_full dkv_full dkv_empty drain dp_free
+  static constexpr int kNumBars = 12;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
   static constexpr uint32_t kColA = 0, kColB = 128, kColdV = 256, kColdK = 256 + D;
@@ -156,8 +156,12 @@ struct DkdvCfg {
 //              columns of dK/dV)
 //   warp 8     TMA producer (K/V per unit; Q, dO, L, D per block, 2 stages)
 //   warp 9     TMEM owner and MMA issuer
-// TMEM: A [0,128) S^T, then P^T (bf16 pairs: queries 0-63 in columns 0-31,
-// 64-127 in 64-95); B [128,256) dP^T, then dS^T (same packing); dV, dK.
+// TMEM: A [0,128) S^T, then P^T and dS^T packed bf16 (the warp of column
+// half h writes P^T of its 64 queries to columns [64h, 64h+32) and dS^T to
+// [64h+32, 64h+64), inside the range it read); B [128,256) dP^T; dV; dK.
+// Because dP^T is only read (never overwritten) by the element-wise warps,
+// dP^T of the next block is issued as soon as they have loaded it and runs
+// under their arithmetic; S^T of the next block follows the dV/dK MMAs.
 // Units walk their query tiles from the end of the sequence down (QWalk), so
 // the CTAs in flight read the same Q/dO tiles from L2.
 template <int D>
@@ -183,6 +187,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* dkv_full = bars + 8;
   uint64_t* dkv_empty = bars + 9;
   uint64_t* drain = bars + 10;
+  uint64_t* dp_free = bars + 11;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -206,6 +211,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(dkv_full, 1);
     mbar_init(dkv_empty, 8);
     mbar_init(drain, 1);
+    mbar_init(dp_free, 8);
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -298,41 +304,64 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int idx = snake_unit(rd, blockIdx.x, grid);
         if (idx >= num_units) break;
         const BwdUnit U = bwd_decode_unit(g, idx);
-        for (int it = 0; it < U.items && ok; ++it, ++item) {
-          const uint32_t st = item & 1;
+        // S^T = K Q^T into A, dP^T = V dO^T into B, for block `blk` (stage st)
+        auto issue_s = [&](uint32_t st) {
           const uint64_t so = (st * C::kTileBytes) >> 4;
-          ok = mbar_wait_bounded(&q_full[st], (item >> 1) & 1, abort_flag, kWaitLimitNs) &&
-               (it > 0 || mbar_wait_bounded(kv_full, ul & 1, abort_flag, kWaitLimitNs));
-          if (!ok) break;
-          tc_fence_after();
-          // S^T = K Q^T, dP^T = V dO^T. Regions A and B are free: the previous
-          // block's dV / dK MMAs (issued earlier, executed in order) read the
-          // P^T / dS^T they held.
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;
             umma_ss(tA, dK_km + off, dQ_km + so + off, idS, kk > 0);
           }
+        };
+        auto issue_dp = [&](uint32_t st) {
+          const uint64_t so = (st * C::kTileBytes) >> 4;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;
             umma_ss(tB, dV_km + off, ddO_km + so + off, idS, kk > 0);
           }
-          umma_commit(s_full);
+        };
+        for (int it = 0; it < U.items && ok; ++it, ++item) {
+          const uint32_t st = item & 1;
+          const uint64_t so = (st * C::kTileBytes) >> 4;
+          if (it == 0) {
+            // first block of a unit (new K/V): S^T and dP^T issued here
+            ok = mbar_wait_bounded(&q_full[st], (item >> 1) & 1, abort_flag, kWaitLimitNs) &&
+                 mbar_wait_bounded(kv_full, ul & 1, abort_flag, kWaitLimitNs) &&
+                 (item == 0 || mbar_wait_bounded(dp_free, (item - 1) & 1, abort_flag, kWaitLimitNs));
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(st);  // A is free: the previous dV/dK MMAs were issued first
+            issue_dp(st);
+            umma_commit(s_full);
+          }
+          if (it + 1 < U.items) {
+            // dP^T of the next block as soon as this block's dP^T is in registers
+            ok = mbar_wait_bounded(dp_free, item & 1, abort_flag, kWaitLimitNs) &&
+                 mbar_wait_bounded(&q_full[st ^ 1], ((item + 1) >> 1) & 1, abort_flag, kWaitLimitNs);
+            if (!ok) break;
+            tc_fence_after();
+            issue_dp(st ^ 1);
+          }
           ok = mbar_wait_bounded(p_full, item & 1, abort_flag, kWaitLimitNs) &&
                (it > 0 || ul == 0 || mbar_wait_bounded(dkv_empty, (ul - 1) & 1, abort_flag, kWaitLimitNs));
           if (!ok) break;
           tc_fence_after();
           const uint32_t acc = it > 0 ? 1u : 0u;
-          // dV += P^T dO, dK += dS^T Q   (A operands straight from TMEM)
+          // dV += P^T dO, dK += dS^T Q   (A operands straight from TMEM region A)
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
             umma_ts(tdV, tA + half_split_col(kk), ddO_mn + so + ((kk * 2048) >> 4), idKV, acc | (kk > 0));
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            umma_ts(tdK, tB + half_split_col(kk), dQ_mn + so + ((kk * 2048) >> 4), idKV, acc | (kk > 0));
+            umma_ts(tdK, tA + 32 + half_split_col(kk), dQ_mn + so + ((kk * 2048) >> 4), idKV, acc | (kk > 0));
           umma_commit(&q_empty[st]);
-          if (it == U.items - 1) {
+          if (it + 1 < U.items) {
+            // S^T of the next block, after dV/dK have read region A; its
+            // completion also covers the dP^T issued above
+            issue_s(st ^ 1);
+            umma_commit(s_full);
+          } else {
             umma_commit(kv_empty);
             umma_commit(dkv_full);
           }
@@ -373,30 +402,48 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
              mbar_wait_bounded(s_full, item & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
         tc_fence_after();
-        const float* Lv = sLD + st * (2 * kTile) + hf * 64;
-        const float* Dv = Lv + kTile;
+        uint32_t rs0[32], rs1[32], rp0[32], rp1[32];
+        tmem_ld32x4(tA + hf * 64, tA + hf * 64 + 32, tB + hf * 64, tB + hf * 64 + 32, rs0, rs1, rp0, rp1);
+        // dP^T is in registers: the MMA may now compute the next block's dP^T
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(dp_free);
+        const float4* L4 = reinterpret_cast<const float4*>(sLD + st * (2 * kTile) + hf * 64);
+        const float4* D4 = reinterpret_cast<const float4*>(sLD + st * (2 * kTile) + kTile + hf * 64);
         // Blocks away from the diagonal and from ragged chunk ends need no mask.
         const bool full = !dg && q_valid == kTile && U.k_valid == kTile;
-#pragma unroll
-        for (int sc = 0; sc < 2; ++sc) {
-          const int c0 = hf * 64 + sc * 32;  // first query column of this chunk
-          uint32_t rs[32], rp[32];
-          tmem_ld32x2(tA + c0, tB + c0, rs, rp);
-          uint32_t pp[16], pd[16];
-          auto lf = [&](int i) { return Lv[sc * 32 + i]; };
-          auto df = [&](int i) { return Dv[sc * 32 + i]; };
-          if (full) {
-            softmax_grad32<false>(rs, rp, sl2, lf, df, [](int) { return true; }, pp, pd);
-          } else {
-            auto valid = [&](int i) {
-              const int c = c0 + i;
-              return key_ok && c < q_valid && !(dg && jr > c);
-            };
-            softmax_grad32<true>(rs, rp, sl2, lf, df, valid, pp, pd);
-          }
-          tmem_st16(tA + hf * 64 + sc * 16, pp);
-          tmem_st16(tB + hf * 64 + sc * 16, pd);
+        uint32_t pp0[16], pd0[16], pp1[16], pd1[16];
+        auto l4 = [&](int base) {
+          return [=](int i) {
+            const float4 v = L4[(base + i) >> 2];
+            const int e = (base + i) & 3;
+            return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+          };
+        };
+        auto d4 = [&](int base) {
+          return [=](int i) {
+            const float4 v = D4[(base + i) >> 2];
+            const int e = (base + i) & 3;
+            return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+          };
+        };
+        if (full) {
+          softmax_grad32<false>(rs0, rp0, sl2, l4(0), d4(0), [](int) { return true; }, pp0, pd0);
+          softmax_grad32<false>(rs1, rp1, sl2, l4(32), d4(32), [](int) { return true; }, pp1, pd1);
+        } else {
+          auto v0 = [&](int i) {
+            const int c = hf * 64 + i;
+            return key_ok && c < q_valid && !(dg && jr > c);
+          };
+          auto v1 = [&](int i) {
+            const int c = hf * 64 + 32 + i;
+            return key_ok && c < q_valid && !(dg && jr > c);
+          };
+          softmax_grad32<true>(rs0, rp0, sl2, l4(0), d4(0), v0, pp0, pd0);
+          softmax_grad32<true>(rs1, rp1, sl2, l4(32), d4(32), v1, pp1, pd1);
         }
+        // P^T -> [64h, 64h+32), dS^T -> [64h+32, 64h+64) of region A
+        tmem_st16x4(tA + hf * 64, tA + hf * 64 + 16, tA + hf * 64 + 32, tA + hf * 64 + 48, pp0, pp1, pd0, pd1);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full);

@@ -159,8 +159,8 @@ BwdLayout bwd_layout(int b, int s, int hq, int d, int cp) {
 }
 
 template <int D>
-int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-               const BwdArgs& args, DeviceInfo* di, cudaStream_t st) {
+int launch_bwd_stage(int stage, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                     const CUtensorMap& tdo, const BwdArgs& args, DeviceInfo* di, cudaStream_t st) {
   const int slot = D == 128 ? 1 : 0;
   if (!di->bwd_attr[slot]) {
     if (cudaFuncSetAttribute(cpattn_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -170,19 +170,31 @@ int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& 
       return CPATTN_ERR_CUDA;
     di->bwd_attr[slot] = true;
   }
-  const int64_t rows = int64_t(args.g.b) * args.g.s * args.g.hq;
-  int pre_grid = int((rows + 255) / 256);
-  if (pre_grid > di->num_sms * 16) pre_grid = di->num_sms * 16;
-  cpattn_bwd_pre_kernel<D><<<pre_grid, 256, 0, st>>>(args);
-  if (cudaGetLastError() != cudaSuccess) return CPATTN_ERR_LAUNCH_FAILED;
-  const int kv_units = bwd_num_units(args.g);
-  cpattn_bwd_dkdv_kernel<D><<<kv_units < di->num_sms ? kv_units : di->num_sms, kBwdThreads, DkdvCfg<D>::kSmemBytes,
-                              st>>>(tq, tk, tv, tdo, args);
-  if (cudaGetLastError() != cudaSuccess) return CPATTN_ERR_LAUNCH_FAILED;
-  const int q_units = dq_num_units(args.g);
-  cpattn_bwd_dq_kernel<D><<<q_units < di->num_sms ? q_units : di->num_sms, kBwdThreads, DqCfg<D>::kSmemBytes, st>>>(
-      tq, tk, tv, tdo, args);
+  if (stage == 0) {
+    const int64_t rows = int64_t(args.g.b) * args.g.s * args.g.hq;
+    int pre_grid = int((rows + 255) / 256);
+    if (pre_grid > di->num_sms * 16) pre_grid = di->num_sms * 16;
+    cpattn_bwd_pre_kernel<D><<<pre_grid, 256, 0, st>>>(args);
+  } else if (stage == 1) {
+    const int units = bwd_num_units(args.g);
+    cpattn_bwd_dkdv_kernel<D><<<units < di->num_sms ? units : di->num_sms, kBwdThreads, DkdvCfg<D>::kSmemBytes,
+                                st>>>(tq, tk, tv, tdo, args);
+  } else {
+    const int units = dq_num_units(args.g);
+    cpattn_bwd_dq_kernel<D><<<units < di->num_sms ? units : di->num_sms, kBwdThreads, DqCfg<D>::kSmemBytes, st>>>(
+        tq, tk, tv, tdo, args);
+  }
   return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_LAUNCH_FAILED;
+}
+
+template <int D>
+int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+               const BwdArgs& args, DeviceInfo* di, cudaStream_t st) {
+  for (int stage = 0; stage < 3; ++stage) {
+    const int rc = launch_bwd_stage<D>(stage, tq, tk, tv, tdo, args, di, st);
+    if (rc) return rc;
+  }
+  return CPATTN_OK;
 }
 
 }  // namespace
@@ -193,9 +205,13 @@ extern "C" size_t cpattn_bwd_workspace_bytes(int b, int s, int hq, int hkv, int 
   return bwd_layout(b, s, hq, d, cp).total;
 }
 
-extern "C" int cpattn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                          const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
-                          int b, int s, int hq, int hkv, int d, int cp, int causal, void* stream) {
+namespace cpattn {
+namespace {
+
+// Argument checks and tensor maps shared by cpattn_bwd and cpattn_bwd_stage.
+int prepare_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int b, int s, int hq, int hkv,
+                int d, int cp, int causal, CUtensorMap* maps, BwdArgs* args, DeviceInfo** di) {
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return CPATTN_ERR_NULL_PTR;
   int rc = check_geometry(b, s, hq, hkv, d, cp);
   if (rc) return rc;
@@ -205,31 +221,61 @@ extern "C" int cpattn_bwd(const void* q, const void* k, const void* v, const voi
     if (!aligned16(p)) return CPATTN_ERR_MISALIGNED;
   const BwdLayout L = bwd_layout(b, s, hq, d, cp);
   if (workspace_bytes < L.total) return CPATTN_ERR_WORKSPACE_TOO_SMALL;
-  DeviceInfo* di = nullptr;
-  if ((rc = device_info(&di))) return rc;
-  CUtensorMap tq, tk, tv, tdo;
+  if ((rc = device_info(di))) return rc;
   const uint64_t rows = uint64_t(b) * s;
-  if (!encode_bf16_rows_heads_d(&tq, q, rows, hq, d, kTile) || !encode_bf16_rows_heads_d(&tk, k, rows, hkv, d, kTile) ||
-      !encode_bf16_rows_heads_d(&tv, v, rows, hkv, d, kTile) ||
-      !encode_bf16_rows_heads_d(&tdo, dout, rows, hq, d, kTile))
+  if (!encode_bf16_rows_heads_d(&maps[0], q, rows, hq, d, kTile) ||
+      !encode_bf16_rows_heads_d(&maps[1], k, rows, hkv, d, kTile) ||
+      !encode_bf16_rows_heads_d(&maps[2], v, rows, hkv, d, kTile) ||
+      !encode_bf16_rows_heads_d(&maps[3], dout, rows, hq, d, kTile))
     return CPATTN_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  args->g = make_geom(b, s, hq, hkv, cp, causal);
+  args->ntp = L.ntp;
+  args->o = static_cast<const __nv_bfloat16*>(o);
+  args->dout = static_cast<const __nv_bfloat16*>(dout);
+  args->lse = lse;
+  args->lvec = reinterpret_cast<float*>(ws + L.lvec);
+  args->dvec = reinterpret_cast<float*>(ws + L.dvec);
+  args->dq = static_cast<__nv_bfloat16*>(dq);
+  args->dk = static_cast<__nv_bfloat16*>(dk);
+  args->dv = static_cast<__nv_bfloat16*>(dv);
+  args->scale = float(1.0 / std::sqrt(double(d)));
+  args->scale_log2 = float(1.4426950408889634 / std::sqrt(double(d)));
+  args->status = (*di)->status;
+  return CPATTN_OK;
+}
+
+}  // namespace
+}  // namespace cpattn
+
+extern "C" int cpattn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                          const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                          int b, int s, int hq, int hkv, int d, int cp, int causal, void* stream) {
+  CUtensorMap maps[4];
   BwdArgs args;
-  args.g = make_geom(b, s, hq, hkv, cp, causal);
-  args.ntp = L.ntp;
-  args.o = static_cast<const __nv_bfloat16*>(o);
-  args.dout = static_cast<const __nv_bfloat16*>(dout);
-  args.lse = lse;
-  args.lvec = reinterpret_cast<float*>(ws + L.lvec);
-  args.dvec = reinterpret_cast<float*>(ws + L.dvec);
-  args.dq = static_cast<__nv_bfloat16*>(dq);
-  args.dk = static_cast<__nv_bfloat16*>(dk);
-  args.dv = static_cast<__nv_bfloat16*>(dv);
-  args.scale = float(1.0 / std::sqrt(double(d)));
-  args.scale_log2 = float(1.4426950408889634 / std::sqrt(double(d)));
-  args.status = di->status;
+  DeviceInfo* di = nullptr;
+  const int rc = prepare_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, b, s, hq, hkv, d, cp,
+                             causal, maps, &args, &di);
+  if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return d == 128 ? launch_bwd<128>(tq, tk, tv, tdo, args, di, st) : launch_bwd<64>(tq, tk, tv, tdo, args, di, st);
+  return d == 128 ? launch_bwd<128>(maps[0], maps[1], maps[2], maps[3], args, di, st)
+                  : launch_bwd<64>(maps[0], maps[1], maps[2], maps[3], args, di, st);
+}
+
+extern "C" int cpattn_bwd_stage(int stage, const void* q, const void* k, const void* v, const void* o,
+                                const float* lse, const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                                size_t workspace_bytes, int b, int s, int hq, int hkv, int d, int cp, int causal,
+                                void* stream) {
+  if (stage < 0 || stage > 2) return CPATTN_ERR_INVALID_ARG;
+  CUtensorMap maps[4];
+  BwdArgs args;
+  DeviceInfo* di = nullptr;
+  const int rc = prepare_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, b, s, hq, hkv, d, cp,
+                             causal, maps, &args, &di);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return d == 128 ? launch_bwd_stage<128>(stage, maps[0], maps[1], maps[2], maps[3], args, di, st)
+                  : launch_bwd_stage<64>(stage, maps[0], maps[1], maps[2], maps[3], args, di, st);
 }
 
 namespace cpattn {

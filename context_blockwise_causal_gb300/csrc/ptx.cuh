@@ -329,4 +329,28 @@ __device__ __forceinline__ void tmem_ld32x4(uint32_t ta, uint32_t tb, uint32_t t
 }
 #undef CPATTN_RX8
 
+
+// Four TMEM stores of 16 columns (to four addresses) with a single wait.
+#define CPATTN_W4(r) "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+__device__ __forceinline__ void tmem_st16x4(uint32_t ta, uint32_t tb, uint32_t tc, uint32_t td,
+                                            const uint32_t (&ra)[16], const uint32_t (&rb)[16],
+                                            const uint32_t (&rc)[16], const uint32_t (&rd)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19};\n\t"
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%1], {%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35};\n\t"
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%2], {%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51};\n\t"
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%3], {%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(ta), "r"(tb), "r"(tc), "r"(td),
+      "r"(ra[0]), "r"(ra[1]), "r"(ra[2]), "r"(ra[3]), "r"(ra[4]), "r"(ra[5]), "r"(ra[6]), "r"(ra[7]),
+      "r"(ra[8]), "r"(ra[9]), "r"(ra[10]), "r"(ra[11]), "r"(ra[12]), "r"(ra[13]), "r"(ra[14]), "r"(ra[15]),
+      "r"(rb[0]), "r"(rb[1]), "r"(rb[2]), "r"(rb[3]), "r"(rb[4]), "r"(rb[5]), "r"(rb[6]), "r"(rb[7]),
+      "r"(rb[8]), "r"(rb[9]), "r"(rb[10]), "r"(rb[11]), "r"(rb[12]), "r"(rb[13]), "r"(rb[14]), "r"(rb[15]),
+      "r"(rc[0]), "r"(rc[1]), "r"(rc[2]), "r"(rc[3]), "r"(rc[4]), "r"(rc[5]), "r"(rc[6]), "r"(rc[7]),
+      "r"(rc[8]), "r"(rc[9]), "r"(rc[10]), "r"(rc[11]), "r"(rc[12]), "r"(rc[13]), "r"(rc[14]), "r"(rc[15]),
+      "r"(rd[0]), "r"(rd[1]), "r"(rd[2]), "r"(rd[3]), "r"(rd[4]), "r"(rd[5]), "r"(rd[6]), "r"(rd[7]),
+      "r"(rd[8]), "r"(rd[9]), "r"(rd[10]), "r"(rd[11]), "r"(rd[12]), "r"(rd[13]), "r"(rd[14]), "r"(rd[15])
+      : "memory");
+}
+#undef CPATTN_W4
+
 }  // namespace cpattn

@@ -87,3 +87,20 @@ def test_bwd_full_size_training_workload():
     e_dk = rel_l2(dk.float().cpu()[:, :, heads], dk_r)
     e_dv = rel_l2(dv.float().cpu()[:, :, heads], dv_r)
     assert e_dq <= REL_L2 and e_dk <= REL_L2 and e_dv <= REL_L2, (e_dq, e_dk, e_dv)
+
+
+def test_bwd_stages_in_any_order_match_the_whole():
+    """cpattn_bwd_stage: stage 0, then 2 and 1 swapped, equals cpattn_bwd."""
+    w = Workload("stages", b=1, s=1536, hq=4, hkv=2, d=128, cp=3, backward=True, seed=23)
+    x = make_inputs(w, device="cuda")
+    o, lse = cpattn_fwd(x["q"], x["k"], x["v"], w.cp)
+    ref = cpattn_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], w.cp)
+    dq, dk, dv = (torch.full_like(t, float("nan")) for t in (x["q"], x["k"], x["v"]))
+    n = cpattn_bwd_workspace_bytes(w.b, w.s, w.hq, w.hkv, w.d, w.cp)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    for stage in (0, 2, 1):
+        cpattn_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], w.cp, dq=dq, dk=dk, dv=dv, workspace=ws, stage=stage)
+    torch.cuda.synchronize()
+    assert cpattn_device_status() == 0
+    for got, want in zip((dq, dk, dv), ref):
+        assert torch.equal(got, want)

@@ -326,13 +326,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_after();
         float s[kTile];
         {
-          uint32_t r0[64], r1[64];
-          tmem_ld64(tS, r0);
-          tmem_ld64(tS + 64, r1);
+          uint32_t r0[32], r1[32], r2[32], r3[32];
+          tmem_ld32x4(tS, tS + 32, tS + 64, tS + 96, r0, r1, r2, r3);
 #pragma unroll
-          for (int i = 0; i < 64; ++i) {
+          for (int i = 0; i < 32; ++i) {
             s[i] = __uint_as_float(r0[i]);
-            s[64 + i] = __uint_as_float(r1[i]);
+            s[32 + i] = __uint_as_float(r1[i]);
+            s[64 + i] = __uint_as_float(r2[i]);
+            s[96 + i] = __uint_as_float(r3[i]);
           }
         }
         if (dg || n_valid < kTile) {
@@ -343,11 +344,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-        for (int i = 4; i < kTile; i += 4) {
-          mx0 = fmaxf(mx0, s[i]);
-          mx1 = fmaxf(mx1, s[i + 1]);
-          mx2 = fmaxf(mx2, s[i + 2]);
-          mx3 = fmaxf(mx3, s[i + 3]);
+        for (int i = 4; i < kTile; i += 8) {
+          mx0 = fmax3(mx0, s[i], s[i + 1]);
+          mx1 = fmax3(mx1, s[i + 2], s[i + 3]);
+          mx2 = fmax3(mx2, s[i + 4], s[i + 5]);
+          mx3 = fmax3(mx3, s[i + 6], s[i + 7]);
         }
         const float m_new = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
         const bool upd = m_new > m_used + kRescaleThreshold;
@@ -359,15 +360,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const float neg = (m_used == -INFINITY) ? 0.f : -m_used;
         // P = 2^(S*scale*log2e - m), packed to bf16 pairs as it is formed so
         // the fp32 scores die early; the row sum uses the fp32 values.
-        uint32_t pk[kTile / 2];
-        float l0 = 0.f, l1 = 0.f;
+        uint32_t pk0[32], pk1[32];
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), negx2 = f2_pack(neg, neg);
+        uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0, acc2 = acc0, acc3 = acc0;
 #pragma unroll
         for (int i = 0; i < kTile / 2; ++i) {
-          const float e0 = ex2_approx(fmaf(s[2 * i], sl2, neg));
-          const float e1 = ex2_approx(fmaf(s[2 * i + 1], sl2, neg));
-          l0 += e0;
-          l1 += e1;
-          pk[i] = pack_bf16x2(e0, e1);
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(s[2 * i], s[2 * i + 1]), sl2x2, negx2), x0, x1);
+          const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+          const uint64_t e = f2_pack(e0, e1);
+          if ((i & 3) == 0) acc0 = f2_add(acc0, e);
+          else if ((i & 3) == 1) acc1 = f2_add(acc1, e);
+          else if ((i & 3) == 2) acc2 = f2_add(acc2, e);
+          else acc3 = f2_add(acc3, e);
+          if (i < 32) pk0[i] = pack_bf16x2(e0, e1);
+          else pk1[i - 32] = pack_bf16x2(e0, e1);
         }
         if (j > 0 && __any_sync(0xffffffffu, upd)) {
           // This row's O accumulator is idle: P.V of step j-1 completed
@@ -381,17 +388,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             tmem_st32(tO + c0, r);
           }
         }
-        l = l * alpha + (l0 + l1);
-        {
-          uint32_t p0[32], p1[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            p0[i] = pk[i];
-            p1[i] = pk[32 + i];
-          }
-          tmem_st32(tS, p0);
-          tmem_st32(tS + 32, p1);
-        }
+        float a0, a1, b0, b1;
+        f2_unpack(f2_add(f2_add(acc0, acc1), f2_add(acc2, acc3)), a0, a1);
+        (void)b0;
+        (void)b1;
+        l = l * alpha + (a0 + a1);
+        tmem_st32x2(tS, tS + 32, pk0, pk1);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[sub]);

@@ -353,4 +353,26 @@ __device__ __forceinline__ void tmem_st16x4(uint32_t ta, uint32_t tb, uint32_t t
 }
 #undef CPATTN_W4
 
+
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// Three-input fp32 maximum.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// Two TMEM stores of 32 columns (to two addresses) with a single wait.
+__device__ __forceinline__ void tmem_st32x2(uint32_t ta, uint32_t tb, const uint32_t (&ra)[32],
+                                            const uint32_t (&rb)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33};\n\t"
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%1], {%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(ta), "r"(tb), "r"(ra[0]), "r"(ra[1]), "r"(ra[2]), "r"(ra[3]), "r"(ra[4]), "r"(ra[5]), "r"(ra[6]), "r"(ra[7]), "r"(ra[8]), "r"(ra[9]), "r"(ra[10]), "r"(ra[11]), "r"(ra[12]), "r"(ra[13]), "r"(ra[14]), "r"(ra[15]), "r"(ra[16]), "r"(ra[17]), "r"(ra[18]), "r"(ra[19]), "r"(ra[20]), "r"(ra[21]), "r"(ra[22]), "r"(ra[23]), "r"(ra[24]), "r"(ra[25]), "r"(ra[26]), "r"(ra[27]), "r"(ra[28]), "r"(ra[29]), "r"(ra[30]), "r"(ra[31]), "r"(rb[0]), "r"(rb[1]), "r"(rb[2]), "r"(rb[3]), "r"(rb[4]), "r"(rb[5]), "r"(rb[6]), "r"(rb[7]), "r"(rb[8]), "r"(rb[9]), "r"(rb[10]), "r"(rb[11]), "r"(rb[12]), "r"(rb[13]), "r"(rb[14]), "r"(rb[15]), "r"(rb[16]), "r"(rb[17]), "r"(rb[18]), "r"(rb[19]), "r"(rb[20]), "r"(rb[21]), "r"(rb[22]), "r"(rb[23]), "r"(rb[24]), "r"(rb[25]), "r"(rb[26]), "r"(rb[27]), "r"(rb[28]), "r"(rb[29]), "r"(rb[30]), "r"(rb[31])
+      : "memory");
+}
+
 }  // namespace cpattn

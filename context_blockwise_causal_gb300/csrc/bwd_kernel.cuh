@@ -286,7 +286,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // (the whole warp runs this role; elect.sync picks the issuing lane)
+    {
       constexpr uint32_t idS = make_idesc_bf16(kTile, kTile, false, false);  // S^T, dP^T
       constexpr uint32_t idKV = make_idesc_bf16(kTile, D, false, true);      // dV, dK
       const uint64_t dK_km = make_sdesc_sw128(smem_u32(sK), 16, 1024);
@@ -310,7 +311,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;
-            umma_ss(tA, dK_km + off, dQ_km + so + off, idS, kk > 0);
+            umma_ss_w(tA, dK_km + off, dQ_km + so + off, idS, kk > 0);
           }
         };
         auto issue_dp = [&](uint32_t st) {
@@ -318,7 +319,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;
-            umma_ss(tB, dV_km + off, ddO_km + so + off, idS, kk > 0);
+            umma_ss_w(tB, dV_km + off, ddO_km + so + off, idS, kk > 0);
           }
         };
         for (int it = 0; it < U.items && ok; ++it, ++item) {
@@ -326,51 +327,51 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const uint64_t so = (st * C::kTileBytes) >> 4;
           if (it == 0) {
             // first block of a unit (new K/V): S^T and dP^T issued here
-            ok = mbar_wait_bounded(&q_full[st], (item >> 1) & 1, abort_flag, kWaitLimitNs) &&
-                 mbar_wait_bounded(kv_full, ul & 1, abort_flag, kWaitLimitNs) &&
-                 (item == 0 || mbar_wait_bounded(dp_free, (item - 1) & 1, abort_flag, kWaitLimitNs));
+            ok = mbar_wait_warp(&q_full[st], (item >> 1) & 1, abort_flag, kWaitLimitNs) &&
+                 mbar_wait_warp(kv_full, ul & 1, abort_flag, kWaitLimitNs) &&
+                 (item == 0 || mbar_wait_warp(dp_free, (item - 1) & 1, abort_flag, kWaitLimitNs));
             if (!ok) break;
-            tc_fence_after();
+            tc_fence_after();  // dp_free orders the element-wise warps' TMEM reads
             issue_s(st);  // A is free: the previous dV/dK MMAs were issued first
             issue_dp(st);
-            umma_commit(s_full);
+            umma_commit_w(s_full);
           }
           if (it + 1 < U.items) {
             // dP^T of the next block as soon as this block's dP^T is in registers
-            ok = mbar_wait_bounded(dp_free, item & 1, abort_flag, kWaitLimitNs) &&
-                 mbar_wait_bounded(&q_full[st ^ 1], ((item + 1) >> 1) & 1, abort_flag, kWaitLimitNs);
+            ok = mbar_wait_warp(dp_free, item & 1, abort_flag, kWaitLimitNs) &&
+                 mbar_wait_warp(&q_full[st ^ 1], ((item + 1) >> 1) & 1, abort_flag, kWaitLimitNs);
             if (!ok) break;
             tc_fence_after();
             issue_dp(st ^ 1);
           }
-          ok = mbar_wait_bounded(p_full, item & 1, abort_flag, kWaitLimitNs) &&
-               (it > 0 || ul == 0 || mbar_wait_bounded(dkv_empty, (ul - 1) & 1, abort_flag, kWaitLimitNs));
+          ok = mbar_wait_warp(p_full, item & 1, abort_flag, kWaitLimitNs) &&
+               (it > 0 || ul == 0 || mbar_wait_warp(dkv_empty, (ul - 1) & 1, abort_flag, kWaitLimitNs));
           if (!ok) break;
           tc_fence_after();
           const uint32_t acc = it > 0 ? 1u : 0u;
           // dV += P^T dO, dK += dS^T Q   (A operands straight from TMEM region A)
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            umma_ts(tdV, tA + half_split_col(kk), ddO_mn + so + ((kk * 2048) >> 4), idKV, acc | (kk > 0));
+            umma_ts_w(tdV, tA + half_split_col(kk), ddO_mn + so + ((kk * 2048) >> 4), idKV, acc | (kk > 0));
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            umma_ts(tdK, tA + 32 + half_split_col(kk), dQ_mn + so + ((kk * 2048) >> 4), idKV, acc | (kk > 0));
-          umma_commit(&q_empty[st]);
+            umma_ts_w(tdK, tA + 32 + half_split_col(kk), dQ_mn + so + ((kk * 2048) >> 4), idKV, acc | (kk > 0));
+          umma_commit_w(&q_empty[st]);
           if (it + 1 < U.items) {
             // S^T of the next block, after dV/dK have read region A; its
             // completion also covers the dP^T issued above
             issue_s(st ^ 1);
-            umma_commit(s_full);
+            umma_commit_w(s_full);
           } else {
-            umma_commit(kv_empty);
-            umma_commit(dkv_full);
+            umma_commit_w(kv_empty);
+            umma_commit_w(dkv_full);
           }
         }
         ++ul;
       }
-      if (!ok) atomicOr(a.status, kStatusBwdMma);
-      umma_commit(drain);
-      mbar_wait_bounded(drain, 0, abort_flag, kWaitLimitNs);
+      if (!ok && lane == 0) atomicOr(a.status, kStatusBwdMma);
+      umma_commit_w(drain);
+      mbar_wait_warp(drain, 0, abort_flag, kWaitLimitNs);
     }
   } else {
     // ------------------------------------------------------------ element-wise
@@ -673,7 +674,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // (the whole warp runs this role; elect.sync picks the issuing lane)
+    {
       constexpr uint32_t idS = make_idesc_bf16(kTile, kTile, false, false);  // S, dP
       constexpr uint32_t idQ = make_idesc_bf16(kTile, D, false, true);       // dQ += dS K
       const uint64_t dQ_km = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
@@ -694,12 +696,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;
-          umma_ss(tS, dQ_km + off, kb + off, idS, kk > 0);
+          umma_ss_w(tS, dQ_km + off, kb + off, idS, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;
-          umma_ss(tdP, ddO_km + off, vb + off, idS, kk > 0);
+          umma_ss_w(tdP, ddO_km + off, vb + off, idS, kk > 0);
         }
       };
       bool ok = true;
@@ -710,39 +712,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (idx >= num_units) break;
         const FwdUnit U = dq_decode_unit(g, idx);
         const int n = U.n;
-        if (!(ok = mbar_wait_bounded(q_full, ul & 1, abort_flag, kWaitLimitNs))) break;
+        if (!(ok = mbar_wait_warp(q_full, ul & 1, abort_flag, kWaitLimitNs))) break;
         // prologue: S(0), dP(0). The dP region is free once the previous
         // tile's element-wise warps have read it.
         uint32_t ks, kp, vs, vp;
         take(vs, vp);
         take(ks, kp);
-        ok = mbar_wait_bounded(&kv_full[ks], kp, abort_flag, kWaitLimitNs) &&
-             mbar_wait_bounded(&kv_full[vs], vp, abort_flag, kWaitLimitNs) &&
-             (jt == 0 || mbar_wait_bounded(dp_free, (jt - 1) & 1, abort_flag, kWaitLimitNs));
+        ok = mbar_wait_warp(&kv_full[ks], kp, abort_flag, kWaitLimitNs) &&
+             mbar_wait_warp(&kv_full[vs], vp, abort_flag, kWaitLimitNs) &&
+             (jt == 0 || mbar_wait_warp(dp_free, (jt - 1) & 1, abort_flag, kWaitLimitNs));
         if (!ok) break;
         tc_fence_after();
         issue_sdp(jt, ks, vs);
-        umma_commit(s_full);
-        umma_commit(&kv_empty[vs]);
-        if (n == 1) umma_commit(q_empty);
+        umma_commit_w(s_full);
+        umma_commit_w(&kv_empty[vs]);
+        if (n == 1) umma_commit_w(q_empty);
         for (int j = 0; j < n && ok; ++j, ++jt) {
           const uint32_t cur_ks = ks;
           if (j + 1 < n) {
             take(vs, vp);
             take(ks, kp);
-            ok = mbar_wait_bounded(dp_free, jt & 1, abort_flag, kWaitLimitNs) &&
-                 mbar_wait_bounded(&kv_full[ks], kp, abort_flag, kWaitLimitNs) &&
-                 mbar_wait_bounded(&kv_full[vs], vp, abort_flag, kWaitLimitNs);
+            ok = mbar_wait_warp(dp_free, jt & 1, abort_flag, kWaitLimitNs) &&
+                 mbar_wait_warp(&kv_full[ks], kp, abort_flag, kWaitLimitNs) &&
+                 mbar_wait_warp(&kv_full[vs], vp, abort_flag, kWaitLimitNs);
             if (!ok) break;
             tc_fence_after();
             // the other S buffer held dS(jt-1), read by the dQ MMA issued before
             issue_sdp(jt + 1, ks, vs);
-            umma_commit(s_full);
-            umma_commit(&kv_empty[vs]);
-            if (j + 1 == n - 1) umma_commit(q_empty);
+            umma_commit_w(s_full);
+            umma_commit_w(&kv_empty[vs]);
+            if (j + 1 == n - 1) umma_commit_w(q_empty);
           }
-          ok = mbar_wait_bounded(ds_full, jt & 1, abort_flag, kWaitLimitNs) &&
-               (j > 0 || ul == 0 || mbar_wait_bounded(dq_empty, (ul - 1) & 1, abort_flag, kWaitLimitNs));
+          ok = mbar_wait_warp(ds_full, jt & 1, abort_flag, kWaitLimitNs) &&
+               (j > 0 || ul == 0 || mbar_wait_warp(dq_empty, (ul - 1) & 1, abort_flag, kWaitLimitNs));
           if (!ok) break;
           tc_fence_after();
           // dQ += dS(jt) K_j   (dS from TMEM, K MN-major)
@@ -750,15 +752,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const uint64_t kmn = dKV_mn + ((cur_ks * C::kTileBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            umma_ts(tdQ, tS + half_split_col(kk), kmn + ((kk * 2048) >> 4), idQ, (j > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(&kv_empty[cur_ks]);
-          if (j == n - 1) umma_commit(dq_full);
+            umma_ts_w(tdQ, tS + half_split_col(kk), kmn + ((kk * 2048) >> 4), idQ, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_commit_w(&kv_empty[cur_ks]);
+          if (j == n - 1) umma_commit_w(dq_full);
         }
         ++ul;
       }
-      if (!ok) atomicOr(a.status, kStatusBwdMma);
-      umma_commit(drain);
-      mbar_wait_bounded(drain, 0, abort_flag, kWaitLimitNs);
+      if (!ok && lane == 0) atomicOr(a.status, kStatusBwdMma);
+      umma_commit_w(drain);
+      mbar_wait_warp(drain, 0, abort_flag, kWaitLimitNs);
     }
   } else {
     // ------------------------------------------------------------ element-wise

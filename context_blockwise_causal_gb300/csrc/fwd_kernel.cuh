@@ -185,7 +185,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // (the whole warp runs this role; elect.sync picks the issuing lane)
+    {
       constexpr uint32_t idS = make_idesc_bf16(kTile, kTile, false, false);
       constexpr uint32_t idO = make_idesc_bf16(kTile, D, false, true);
       const uint64_t dQ[2] = {make_sdesc_sw128(smem_u32(sQ), 16, 1024),
@@ -197,14 +198,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;
-          umma_ss(tbase + sub * kTile, dQ[sub] + off, kb + off, idS, kk > 0);
+          umma_ss_w(tbase + sub * kTile, dQ[sub] + off, kb + off, idS, kk > 0);
         }
       };
       auto issue_PV = [&](int sub, uint32_t slot, bool acc) {
         const uint64_t vb = dV0 + ((slot * C::kKVBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_ts(tbase + C::kColO + sub * D, tbase + sub * kTile + kk * 8, vb + ((kk * 2048) >> 4), idO,
+          umma_ts_w(tbase + C::kColO + sub * D, tbase + sub * kTile + kk * 8, vb + ((kk * 2048) >> 4), idO,
                   (acc || kk > 0) ? 1u : 0u);
       };
       uint32_t ncons = 0;
@@ -222,79 +223,74 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const FwdUnit U = fwd_decode_unit(g, idx);
         const bool shared_kv = U.g0 == U.g1;
         const int n = U.n;
-        ok = mbar_wait_bounded(&q_full[0], ul & 1, abort_flag, kWaitLimitNs) &&
-             mbar_wait_bounded(&q_full[1], ul & 1, abort_flag, kWaitLimitNs);
+        ok = mbar_wait_warp(&q_full[0], ul & 1, abort_flag, kWaitLimitNs) &&
+             mbar_wait_warp(&q_full[1], ul & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
         // prologue: S0(0), S1(0)
         uint32_t k0, k0p, k1, k1p;
         take(k0, k0p);
         if (shared_kv) { k1 = k0; k1p = k0p; } else take(k1, k1p);
-        if (!(ok = mbar_wait_bounded(&kv_full[k0], k0p, abort_flag, kWaitLimitNs))) break;
-        tc_fence_after();
+        // waits on TMA-filled buffers need no tcgen05 fence: the copies and
+        // the MMA operand reads are both async-proxy operations ordered by
+        // the transaction barrier
+        if (!(ok = mbar_wait_warp(&kv_full[k0], k0p, abort_flag, kWaitLimitNs))) break;
         issue_S(0, k0);
-        umma_commit(&s_full[0]);
-        if (!shared_kv) umma_commit(&kv_empty[k0]);
-        if (n == 1) umma_commit(&q_empty[0]);
-        if (!shared_kv) {
-          if (!(ok = mbar_wait_bounded(&kv_full[k1], k1p, abort_flag, kWaitLimitNs))) break;
-          tc_fence_after();
-        }
+        umma_commit_w(&s_full[0]);
+        if (!shared_kv) umma_commit_w(&kv_empty[k0]);
+        if (n == 1) umma_commit_w(&q_empty[0]);
+        if (!shared_kv && !(ok = mbar_wait_warp(&kv_full[k1], k1p, abort_flag, kWaitLimitNs))) break;
         issue_S(1, k1);
-        umma_commit(&s_full[1]);
-        umma_commit(&kv_empty[k1]);
-        if (n == 1) umma_commit(&q_empty[1]);
+        umma_commit_w(&s_full[1]);
+        umma_commit_w(&kv_empty[k1]);
+        if (n == 1) umma_commit_w(&q_empty[1]);
         for (int j = 0; j < n && ok; ++j) {
           uint32_t v0, v0p, v1, v1p;
           take(v0, v0p);
           if (shared_kv) { v1 = v0; v1p = v0p; } else take(v1, v1p);
           // ---- sub-tile 0: O0 += P0(j) V_j, then S0(j+1)
-          ok = mbar_wait_bounded(&kv_full[v0], v0p, abort_flag, kWaitLimitNs) &&
-               mbar_wait_bounded(&p_full[0], pcnt[0] & 1, abort_flag, kWaitLimitNs) &&
-               (j > 0 || ul == 0 || mbar_wait_bounded(&o_empty[0], (ul - 1) & 1, abort_flag, kWaitLimitNs));
+          ok = mbar_wait_warp(&kv_full[v0], v0p, abort_flag, kWaitLimitNs) &&
+               mbar_wait_warp(&p_full[0], pcnt[0] & 1, abort_flag, kWaitLimitNs) &&
+               (j > 0 || ul == 0 || mbar_wait_warp(&o_empty[0], (ul - 1) & 1, abort_flag, kWaitLimitNs));
           if (!ok) break;
           ++pcnt[0];
           tc_fence_after();
           issue_PV(0, v0, j > 0);
-          if (!shared_kv) umma_commit(&kv_empty[v0]);
-          if (j == n - 1) umma_commit(&o_full[0]);
+          if (!shared_kv) umma_commit_w(&kv_empty[v0]);
+          if (j == n - 1) umma_commit_w(&o_full[0]);
           uint32_t nk0 = 0, nk0p = 0, nk1 = 0, nk1p = 0;
           if (j + 1 < n) {
             take(nk0, nk0p);
             if (shared_kv) { nk1 = nk0; nk1p = nk0p; } else take(nk1, nk1p);
-            if (!(ok = mbar_wait_bounded(&kv_full[nk0], nk0p, abort_flag, kWaitLimitNs))) break;
-            tc_fence_after();
+            if (!(ok = mbar_wait_warp(&kv_full[nk0], nk0p, abort_flag, kWaitLimitNs))) break;
             issue_S(0, nk0);
-            umma_commit(&s_full[0]);
-            if (!shared_kv) umma_commit(&kv_empty[nk0]);
-            if (j + 1 == n - 1) umma_commit(&q_empty[0]);
+            umma_commit_w(&s_full[0]);
+            if (!shared_kv) umma_commit_w(&kv_empty[nk0]);
+            if (j + 1 == n - 1) umma_commit_w(&q_empty[0]);
           }
           // ---- sub-tile 1: O1 += P1(j) V_j, then S1(j+1)
-          ok = (shared_kv || mbar_wait_bounded(&kv_full[v1], v1p, abort_flag, kWaitLimitNs)) &&
-               mbar_wait_bounded(&p_full[1], pcnt[1] & 1, abort_flag, kWaitLimitNs) &&
-               (j > 0 || ul == 0 || mbar_wait_bounded(&o_empty[1], (ul - 1) & 1, abort_flag, kWaitLimitNs));
+          ok = (shared_kv || mbar_wait_warp(&kv_full[v1], v1p, abort_flag, kWaitLimitNs)) &&
+               mbar_wait_warp(&p_full[1], pcnt[1] & 1, abort_flag, kWaitLimitNs) &&
+               (j > 0 || ul == 0 || mbar_wait_warp(&o_empty[1], (ul - 1) & 1, abort_flag, kWaitLimitNs));
           if (!ok) break;
           ++pcnt[1];
           tc_fence_after();
           issue_PV(1, v1, j > 0);
-          umma_commit(&kv_empty[v1]);
-          if (j == n - 1) umma_commit(&o_full[1]);
+          umma_commit_w(&kv_empty[v1]);
+          if (j == n - 1) umma_commit_w(&o_full[1]);
           if (j + 1 < n) {
-            if (!shared_kv) {
-              if (!(ok = mbar_wait_bounded(&kv_full[nk1], nk1p, abort_flag, kWaitLimitNs))) break;
-              tc_fence_after();
-            }
+            if (!shared_kv && !(ok = mbar_wait_warp(&kv_full[nk1], nk1p, abort_flag, kWaitLimitNs))) break;
             issue_S(1, nk1);
-            umma_commit(&s_full[1]);
-            umma_commit(&kv_empty[nk1]);
-            if (j + 1 == n - 1) umma_commit(&q_empty[1]);
+            umma_commit_w(&s_full[1]);
+            umma_commit_w(&kv_empty[nk1]);
+            if (j + 1 == n - 1) umma_commit_w(&q_empty[1]);
           }
         }
         ++ul;
       }
-      if (!ok) atomicOr(a.status, kStatusMma);
+      if (!ok && lane == 0) atomicOr(a.status, kStatusMma);
       // No MMA may be in flight when TMEM is released.
-      umma_commit(drain);
-      mbar_wait_bounded(drain, 0, abort_flag, kWaitLimitNs);
+      umma_commit_w(drain);
+      mbar_wait_warp(drain, 0, abort_flag, kWaitLimitNs);
     }
   } else {
     // ------------------------------------------------------------ softmax

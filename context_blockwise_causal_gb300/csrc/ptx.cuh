@@ -69,6 +69,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// Warp-uniform bounded wait for roles run by a whole converged warp (the MMA
+// issuers): every lane waits, then the lanes agree, so a lane that timed out
+// can never leave the others at a full-mask elect.sync.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                               uint64_t limit_ns) {
+  const bool ok = mbar_wait_bounded(bar, parity, abort, limit_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -372,6 +381,40 @@ __device__ __forceinline__ void tmem_st32x2(uint32_t ta, uint32_t tb, const uint
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33};\n\t"
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%1], {%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65};\n\t"
       "tcgen05.wait::st.sync.aligned;" ::"r"(ta), "r"(tb), "r"(ra[0]), "r"(ra[1]), "r"(ra[2]), "r"(ra[3]), "r"(ra[4]), "r"(ra[5]), "r"(ra[6]), "r"(ra[7]), "r"(ra[8]), "r"(ra[9]), "r"(ra[10]), "r"(ra[11]), "r"(ra[12]), "r"(ra[13]), "r"(ra[14]), "r"(ra[15]), "r"(ra[16]), "r"(ra[17]), "r"(ra[18]), "r"(ra[19]), "r"(ra[20]), "r"(ra[21]), "r"(ra[22]), "r"(ra[23]), "r"(ra[24]), "r"(ra[25]), "r"(ra[26]), "r"(ra[27]), "r"(ra[28]), "r"(ra[29]), "r"(ra[30]), "r"(ra[31]), "r"(rb[0]), "r"(rb[1]), "r"(rb[2]), "r"(rb[3]), "r"(rb[4]), "r"(rb[5]), "r"(rb[6]), "r"(rb[7]), "r"(rb[8]), "r"(rb[9]), "r"(rb[10]), "r"(rb[11]), "r"(rb[12]), "r"(rb[13]), "r"(rb[14]), "r"(rb[15]), "r"(rb[16]), "r"(rb[17]), "r"(rb[18]), "r"(rb[19]), "r"(rb[20]), "r"(rb[21]), "r"(rb[22]), "r"(rb[23]), "r"(rb[24]), "r"(rb[25]), "r"(rb[26]), "r"(rb[27]), "r"(rb[28]), "r"(rb[29]), "r"(rb[30]), "r"(rb[31])
+      : "memory");
+}
+
+
+// Warp-collective forms of the MMA issue and commit: every lane of a
+// converged warp executes them and elect.sync picks the one lane that
+// issues. A single tcgen05 issuing thread has little slack over the tensor
+// pipe (an M=128, N=128, K=16 MMA executes in 64 cycles), and issuing from a
+// converged warp is markedly cheaper than from a lone divergent lane.
+__device__ __forceinline__ void umma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred pe, pa;\n\t.reg .b32 re;\n\t"
+      "elect.sync re|pe, 0xffffffff;\n\t"
+      "setp.ne.b32 pa, %4, 0;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pa;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred pe, pa;\n\t.reg .b32 re;\n\t"
+      "elect.sync re|pe, 0xffffffff;\n\t"
+      "setp.ne.b32 pa, %4, 0;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit_w(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred pe;\n\t.reg .b32 re;\n\t"
+      "elect.sync re|pe, 0xffffffff;\n\t"
+      "@pe tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
       : "memory");
 }
 

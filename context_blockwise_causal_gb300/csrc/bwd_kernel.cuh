@@ -101,35 +101,72 @@ __global__ void __launch_bounds__(256) cpattn_bwd_pre_kernel(const BwdArgs a) {
 // region, each written by the warp that read the fp32 values there.
 __device__ __forceinline__ uint32_t half_split_col(int kk) { return kk < 4 ? kk * 8 : 64 + (kk - 4) * 8; }
 
-// P = 2^(s*sl2 - l2), dS = P (dp - dd) for 32 consecutive elements given as
-// raw fp32 bits, packed to bf16 pairs. `valid(i)` masks element i to zero.
-template <bool kMasked, typename Valid, typename LF, typename DF>
+// One element pair: P = 2^(s*sl2 - l), dS = P (dp - d), packed to bf16x2.
+__device__ __forceinline__ void grad_pair(uint32_t s0, uint32_t s1, uint32_t dp0, uint32_t dp1, uint64_t sl2x2,
+                                          float l0, float l1, float d0, float d1, uint32_t& pp, uint32_t& pd) {
+  float x0, x1;
+  f2_unpack(f2_fma(f2_pack(__uint_as_float(s0), __uint_as_float(s1)), sl2x2, f2_pack(-l0, -l1)), x0, x1);
+  const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+  float g0, g1;
+  f2_unpack(f2_mul(f2_pack(p0, p1), f2_sub(f2_pack(__uint_as_float(dp0), __uint_as_float(dp1)), f2_pack(d0, d1))),
+            g0, g1);
+  pp = pack_bf16x2(p0, p1);
+  pd = pack_bf16x2(g0, g1);
+}
+
+// P and dS for 32 consecutive elements (raw fp32 bits of S and dP), packed
+// to bf16 pairs. L*log2e and D per element come as 8 float4 (one per 4
+// elements). When `masked`, bit i of `valid` keeps element i; masked entries
+// (which may hold arbitrary values) are selected to zero, never multiplied.
+template <bool kMasked>
 __device__ __forceinline__ void softmax_grad32(const uint32_t (&rs)[32], const uint32_t (&rp)[32], float sl2,
-                                               LF l2_of, DF d_of, Valid valid, uint32_t (&pp)[16],
-                                               uint32_t (&pd)[16]) {
+                                               const float4* l4, const float4* d4, uint32_t valid,
+                                               uint32_t (&pp)[16], uint32_t (&pd)[16]) {
   const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const uint64_t x = f2_fma(f2_pack(__uint_as_float(rs[2 * i]), __uint_as_float(rs[2 * i + 1])), sl2x2,
-                              f2_pack(-l2_of(2 * i), -l2_of(2 * i + 1)));
-    float x0, x1;
-    f2_unpack(x, x0, x1);
-    float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-    const uint64_t t = f2_sub(f2_pack(__uint_as_float(rp[2 * i]), __uint_as_float(rp[2 * i + 1])),
-                              f2_pack(d_of(2 * i), d_of(2 * i + 1)));
-    float d0, d1;
-    f2_unpack(f2_mul(f2_pack(p0, p1), t), d0, d1);
-    if constexpr (kMasked) {
-      // masked entries may hold arbitrary values: select, never multiply
-      const bool v0 = valid(2 * i), v1 = valid(2 * i + 1);
-      p0 = v0 ? p0 : 0.f;
-      d0 = v0 ? d0 : 0.f;
-      p1 = v1 ? p1 : 0.f;
-      d1 = v1 ? d1 : 0.f;
-    }
-    pp[i] = pack_bf16x2(p0, p1);
-    pd[i] = pack_bf16x2(d0, d1);
+  for (int q = 0; q < 8; ++q) {
+    const float4 lv = l4[q], dv = d4[q];
+    grad_pair(rs[4 * q], rs[4 * q + 1], rp[4 * q], rp[4 * q + 1], sl2x2, lv.x, lv.y, dv.x, dv.y, pp[2 * q], pd[2 * q]);
+    grad_pair(rs[4 * q + 2], rs[4 * q + 3], rp[4 * q + 2], rp[4 * q + 3], sl2x2, lv.z, lv.w, dv.z, dv.w,
+              pp[2 * q + 1], pd[2 * q + 1]);
   }
+  if constexpr (kMasked) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t keep = ((valid >> (2 * i)) & 1u ? 0x0000ffffu : 0u) | ((valid >> (2 * i + 1)) & 1u ? 0xffff0000u : 0u);
+      pp[i] &= keep;
+      pd[i] &= keep;
+    }
+  }
+}
+
+// The same with one L*log2e and D for all 32 elements (a query row).
+template <bool kMasked>
+__device__ __forceinline__ void softmax_grad32_row(const uint32_t (&rs)[32], const uint32_t (&rp)[32], float sl2,
+                                                   float l2, float dd, uint32_t valid, uint32_t (&pp)[16],
+                                                   uint32_t (&pd)[16]) {
+  const uint64_t sl2x2 = f2_pack(sl2, sl2);
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    grad_pair(rs[2 * i], rs[2 * i + 1], rp[2 * i], rp[2 * i + 1], sl2x2, l2, l2, dd, dd, pp[i], pd[i]);
+  if constexpr (kMasked) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t keep = ((valid >> (2 * i)) & 1u ? 0x0000ffffu : 0u) | ((valid >> (2 * i + 1)) & 1u ? 0xffff0000u : 0u);
+      pp[i] &= keep;
+      pd[i] &= keep;
+    }
+  }
+}
+
+// Bits [lo, hi) of a 32-bit mask (lo, hi clipped to [0, 32]).
+__device__ __forceinline__ uint32_t bit_range(int lo, int hi) {
+  lo = lo < 0 ? 0 : (lo > 32 ? 32 : lo);
+  hi = hi < 0 ? 0 : (hi > 32 ? 32 : hi);
+  if (hi <= lo) return 0u;
+  const uint32_t upto_hi = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
+  const uint32_t below_lo = (1u << lo) - 1u;
+  return upto_hi & ~below_lo;
 }
 
 // ================================================================ dK / dV
@@ -403,9 +440,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
              mbar_wait_bounded(s_full, item & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
         tc_fence_after();
-        uint32_t rs0[32], rs1[32], rp0[32], rp1[32];
-        tmem_ld32x4(tA + hf * 64, tA + hf * 64 + 32, tB + hf * 64, tB + hf * 64 + 32, rs0, rs1, rp0, rp1);
-        // dP^T is in registers: the MMA may now compute the next block's dP^T
+        // dP^T (both 32-column halves) and the first half of S^T in one
+        // round trip; dP^T is then in registers and the MMA may compute the
+        // next block's dP^T while this block's arithmetic runs
+        uint32_t rs[32], rp0[32], rp1[32];
+        tmem_ld32x3(tB + hf * 64, tB + hf * 64 + 32, tA + hf * 64, rp0, rp1, rs);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(dp_free);
@@ -413,35 +452,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const float4* D4 = reinterpret_cast<const float4*>(sLD + st * (2 * kTile) + kTile + hf * 64);
         // Blocks away from the diagonal and from ragged chunk ends need no mask.
         const bool full = !dg && q_valid == kTile && U.k_valid == kTile;
+        // query column c (of this warp's 64) is valid for key row jr when the
+        // key is in its chunk, the query is in its chunk, and (on the
+        // diagonal) c >= jr
+        const int cb = hf * 64;
+        const int lo = dg ? jr - cb : 0;
         uint32_t pp0[16], pd0[16], pp1[16], pd1[16];
-        auto l4 = [&](int base) {
-          return [=](int i) {
-            const float4 v = L4[(base + i) >> 2];
-            const int e = (base + i) & 3;
-            return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
-          };
-        };
-        auto d4 = [&](int base) {
-          return [=](int i) {
-            const float4 v = D4[(base + i) >> 2];
-            const int e = (base + i) & 3;
-            return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
-          };
-        };
         if (full) {
-          softmax_grad32<false>(rs0, rp0, sl2, l4(0), d4(0), [](int) { return true; }, pp0, pd0);
-          softmax_grad32<false>(rs1, rp1, sl2, l4(32), d4(32), [](int) { return true; }, pp1, pd1);
+          softmax_grad32<false>(rs, rp0, sl2, L4, D4, 0u, pp0, pd0);
         } else {
-          auto v0 = [&](int i) {
-            const int c = hf * 64 + i;
-            return key_ok && c < q_valid && !(dg && jr > c);
-          };
-          auto v1 = [&](int i) {
-            const int c = hf * 64 + 32 + i;
-            return key_ok && c < q_valid && !(dg && jr > c);
-          };
-          softmax_grad32<true>(rs0, rp0, sl2, l4(0), d4(0), v0, pp0, pd0);
-          softmax_grad32<true>(rs1, rp1, sl2, l4(32), d4(32), v1, pp1, pd1);
+          softmax_grad32<true>(rs, rp0, sl2, L4, D4, key_ok ? bit_range(lo, q_valid - cb) : 0u, pp0, pd0);
+        }
+        tmem_ld32(tA + hf * 64 + 32, rs);  // second half of S^T
+        if (full) {
+          softmax_grad32<false>(rs, rp1, sl2, L4 + 8, D4 + 8, 0u, pp1, pd1);
+        } else {
+          softmax_grad32<true>(rs, rp1, sl2, L4 + 8, D4 + 8, key_ok ? bit_range(lo - 32, q_valid - cb - 32) : 0u,
+                               pp1, pd1);
         }
         // P^T -> [64h, 64h+32), dS^T -> [64h+32, 64h+64) of region A
         tmem_st16x4(tA + hf * 64, tA + hf * 64 + 16, tA + hf * 64 + 32, tA + hf * 64 + 48, pp0, pp1, pd0, pd1);
@@ -453,37 +480,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // ---- dK, dV of the tile: TMEM -> bf16 -> global
       if (!(ok = mbar_wait_bounded(dkv_full, ul & 1, abort_flag, kWaitLimitNs))) break;
       tc_fence_after();
-      uint32_t rv[D / 2], rk[D / 2];
+      // 32 columns at a time: TMEM -> registers -> bf16 -> global
+      const int64_t off = ((int64_t(U.bi) * g.s + U.k_t0 + jr) * g.hkv + U.g) * D + hf * (D / 2);
 #pragma unroll
       for (int c0 = 0; c0 < D / 2; c0 += 32) {
-        uint32_t r0[32], r1[32];
+        uint32_t rv[32], rk[32];
         tmem_ld32x2(tbase + lane_off + C::kColdV + hf * (D / 2) + c0, tbase + lane_off + C::kColdK + hf * (D / 2) + c0,
-                    r0, r1);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          rv[c0 + i] = r0[i];
-          rk[c0 + i] = r1[i];
+                    rv, rk);
+        if (c0 + 32 >= D / 2) {
+          // last chunk read: the MMA may start the next unit's dV/dK
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(dkv_empty);
         }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dkv_empty);
-      if (key_ok) {
-        const int64_t off = ((int64_t(U.bi) * g.s + U.k_t0 + jr) * g.hkv + U.g) * D + hf * (D / 2);
+        if (key_ok) {
 #pragma unroll
-        for (int i = 0; i < D / 2; i += 8) {
-          uint4 pv, pk;
-          pv.x = pack_bf16x2(__uint_as_float(rv[i]), __uint_as_float(rv[i + 1]));
-          pv.y = pack_bf16x2(__uint_as_float(rv[i + 2]), __uint_as_float(rv[i + 3]));
-          pv.z = pack_bf16x2(__uint_as_float(rv[i + 4]), __uint_as_float(rv[i + 5]));
-          pv.w = pack_bf16x2(__uint_as_float(rv[i + 6]), __uint_as_float(rv[i + 7]));
-          // dK accumulated dS^T Q with dS unscaled: apply 1/sqrt(d) here
-          pk.x = pack_bf16x2(__uint_as_float(rk[i]) * scale, __uint_as_float(rk[i + 1]) * scale);
-          pk.y = pack_bf16x2(__uint_as_float(rk[i + 2]) * scale, __uint_as_float(rk[i + 3]) * scale);
-          pk.z = pack_bf16x2(__uint_as_float(rk[i + 4]) * scale, __uint_as_float(rk[i + 5]) * scale);
-          pk.w = pack_bf16x2(__uint_as_float(rk[i + 6]) * scale, __uint_as_float(rk[i + 7]) * scale);
-          *reinterpret_cast<uint4*>(a.dv + off + i) = pv;
-          *reinterpret_cast<uint4*>(a.dk + off + i) = pk;
+          for (int i = 0; i < 32; i += 8) {
+            uint4 pv, pk;
+            pv.x = pack_bf16x2(__uint_as_float(rv[i]), __uint_as_float(rv[i + 1]));
+            pv.y = pack_bf16x2(__uint_as_float(rv[i + 2]), __uint_as_float(rv[i + 3]));
+            pv.z = pack_bf16x2(__uint_as_float(rv[i + 4]), __uint_as_float(rv[i + 5]));
+            pv.w = pack_bf16x2(__uint_as_float(rv[i + 6]), __uint_as_float(rv[i + 7]));
+            // dK accumulated dS^T Q with dS unscaled: apply 1/sqrt(d) here
+            pk.x = pack_bf16x2(__uint_as_float(rk[i]) * scale, __uint_as_float(rk[i + 1]) * scale);
+            pk.y = pack_bf16x2(__uint_as_float(rk[i + 2]) * scale, __uint_as_float(rk[i + 3]) * scale);
+            pk.z = pack_bf16x2(__uint_as_float(rk[i + 4]) * scale, __uint_as_float(rk[i + 5]) * scale);
+            pk.w = pack_bf16x2(__uint_as_float(rk[i + 6]) * scale, __uint_as_float(rk[i + 7]) * scale);
+            *reinterpret_cast<uint4*>(a.dv + off + c0 + i) = pv;
+            *reinterpret_cast<uint4*>(a.dk + off + c0 + i) = pk;
+          }
         }
       }
       ++ul;
@@ -802,22 +827,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (lane == 0) mbar_arrive(dp_free);
         const bool full = !dg && n_valid == kTile;
         uint32_t pp[16], pd0[16], pd1[16];
-        auto lf = [&](int) { return l2; };
-        auto df = [&](int) { return dd; };
         if (full) {
-          softmax_grad32<false>(rs0, rp0, sl2, lf, df, [](int) { return true; }, pp, pd0);
-          softmax_grad32<false>(rs1, rp1, sl2, lf, df, [](int) { return true; }, pp, pd1);
+          softmax_grad32_row<false>(rs0, rp0, sl2, l2, dd, 0u, pp, pd0);
+          softmax_grad32_row<false>(rs1, rp1, sl2, l2, dd, 0u, pp, pd1);
         } else {
-          auto v0 = [&](int i) {
-            const int c = hf * 64 + i;
-            return c < n_valid && !(dg && c > jr);
-          };
-          auto v1 = [&](int i) {
-            const int c = hf * 64 + 32 + i;
-            return c < n_valid && !(dg && c > jr);
-          };
-          softmax_grad32<true>(rs0, rp0, sl2, lf, df, v0, pp, pd0);
-          softmax_grad32<true>(rs1, rp1, sl2, lf, df, v1, pp, pd1);
+          // key column c (of this warp's 64) is valid when it is inside its
+          // chunk and (on the diagonal) c <= jr
+          const int cb = hf * 64;
+          int hi = n_valid - cb;
+          if (dg && jr + 1 - cb < hi) hi = jr + 1 - cb;
+          softmax_grad32_row<true>(rs0, rp0, sl2, l2, dd, bit_range(0, hi), pp, pd0);
+          softmax_grad32_row<true>(rs1, rp1, sl2, l2, dd, bit_range(0, hi - 32), pp, pd1);
         }
         tmem_st16(tS + hf * 64, pd0);
         tmem_st16(tS + hf * 64 + 16, pd1);

@@ -418,4 +418,23 @@ __device__ __forceinline__ void umma_commit_w(uint64_t* bar) {
       : "memory");
 }
 
+
+// Three TMEM loads of 32 columns with a single wait.
+#define CPATTN_RY8(r, i) "=r"(r[i + 0]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
+                         "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
+__device__ __forceinline__ void tmem_ld32x3(uint32_t ta, uint32_t tb, uint32_t tc, uint32_t (&ra)[32],
+                                            uint32_t (&rb)[32], uint32_t (&rc)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%96];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%97];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, [%98];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : CPATTN_RY8(ra, 0), CPATTN_RY8(ra, 8), CPATTN_RY8(ra, 16), CPATTN_RY8(ra, 24), CPATTN_RY8(rb, 0),
+        CPATTN_RY8(rb, 8), CPATTN_RY8(rb, 16), CPATTN_RY8(rb, 24), CPATTN_RY8(rc, 0), CPATTN_RY8(rc, 8),
+        CPATTN_RY8(rc, 16), CPATTN_RY8(rc, 24)
+      : "r"(ta), "r"(tb), "r"(tc)
+      : "memory");
+}
+#undef CPATTN_RY8
+
 }  // namespace cpattn

@@ -99,6 +99,12 @@ int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& 
     if (cudaFuncSetAttribute(cpattn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
       return CPATTN_ERR_CUDA;
+    // The in-kernel register split assumes exactly kFwdLaunchRegs registers
+    // per thread at launch; with fewer, the growing warpgroups would wait
+    // for registers that never come free.
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, cpattn_fwd_kernel<D>) != cudaSuccess) return CPATTN_ERR_CUDA;
+    if (fa.numRegs != kFwdLaunchRegs) return CPATTN_ERR_LAUNCH_FAILED;
     di->fwd_attr[slot] = true;
   }
   const int units = fwd_num_units(args.g);

@@ -1,10 +1,11 @@
 // Forward kernel: all virtual CP ranks in one persistent launch.
 //
-// One CTA per SM, 10 warps:
+// One CTA per SM, 12 warps:
 //   warps 0-3  softmax/correction/epilogue for sub-tile 0 (one row per thread)
 //   warps 4-7  the same for sub-tile 1
 //   warp 8     TMA producer (Q tiles, and the K/V ring)
 //   warp 9     TMEM owner and tcgen05.mma issuer
+//   warps 10-11 idle (complete the third warpgroup for the register split)
 // A work unit is a 128-row query tile for a pair of query heads; the two
 // sub-tiles walk the same key tiles (CP-step order, see cp_schedule.cuh) so
 // the MMA warp can alternate between them:
@@ -31,7 +32,17 @@
 
 namespace cpattn {
 
-constexpr int kFwdThreads = 320;
+// 12 warps: two softmax warpgroups, and a third with the producer and MMA
+// warps (its last two warps only take part in the register split). The
+// block is launched with kFwdLaunchRegs registers per thread; the softmax
+// warpgroups then grow to kFwdSoftmaxRegs and the third shrinks to
+// kFwdOtherRegs: 2*128*200 + 128*96 = 63488 <= 384*168 = 64512.
+constexpr int kFwdThreads = 384;
+constexpr int kFwdLaunchRegs = 168;
+constexpr int kFwdSoftmaxRegs = 200;
+constexpr int kFwdOtherRegs = 96;
+static_assert(2 * 128 * kFwdSoftmaxRegs + 128 * kFwdOtherRegs <= kFwdThreads * kFwdLaunchRegs,
+              "register split exceeds the launch budget");
 // A row's running max is moved (and O, l rescaled) as soon as a key tile
 // raises it. The largest P of the row is then exactly 1, which bf16 holds
 // exactly; with a lagging max (FA4's thresholded rescale) that dominant P
@@ -128,6 +139,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
+  if (warp >= 8) {
+  reg_dealloc<kFwdOtherRegs>();  // this warpgroup: producer, MMA, two idle warps
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -292,7 +305,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       umma_commit_w(drain);
       mbar_wait_warp(drain, 0, abort_flag, kWaitLimitNs);
     }
+  }
   } else {
+    reg_alloc<kFwdSoftmaxRegs>();  // the two softmax warpgroups
     // ------------------------------------------------------------ softmax
     const int sub = warp >> 2;
     const int wq = warp & 3;

@@ -1,8 +1,8 @@
 """Benchmark: context-parallel causal attention forward + backward on GB300.
 
 One step = one pass of the whole hot path over one batch of synthetic input:
-cpattn_fwd (all virtual CP ranks, fused LSE merge) then cpattn_bwd
-(preprocess, main kernel, dQ conversion), through the C-ABI library.
+cpattn_fwd (all virtual CP ranks, fused LSE merge) then the three stages of
+cpattn_bwd (row vectors, dK/dV, dQ), through the C-ABI library.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME]
@@ -214,19 +214,23 @@ def run_ours(args, w):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     wsp = torch.empty(cpattn_bwd_workspace_bytes(w.b, w.s, w.hq, w.hkv, w.d, w.cp), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = 4  # fwd kernel; bwd preprocess, main, dQ conversion
+    launches_per_step = 4  # forward; backward row vectors, dK/dV, dQ
 
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
 
     def step(evs=None):
+        # one event before the forward and after each kernel: the forward,
+        # then the backward's three stages (row vectors, dK/dV, dQ)
         if evs:
             evs[0].record(stream)
         cpattn_fwd(q, k, v, w.cp, causal=w.causal, o=o, lse=lse, stream=stream)
         if evs:
             evs[1].record(stream)
-        cpattn_bwd(q, k, v, o, lse, do, w.cp, causal=w.causal, dq=dq, dk=dk, dv=dv, workspace=wsp, stream=stream)
-        if evs:
-            evs[2].record(stream)
+        for stage in range(3):
+            cpattn_bwd(q, k, v, o, lse, do, w.cp, causal=w.causal, dq=dq, dk=dk, dv=dv, workspace=wsp,
+                       stream=stream, stage=stage)
+            if evs:
+                evs[2 + stage].record(stream)
 
     def barrier():
         if ws > 1:
@@ -240,7 +244,7 @@ def run_ours(args, w):
         raise RuntimeError("a kernel reported a timeout during warm-up")
 
     # ---- device-timed region: inputs resident in HBM
-    evs = [[ev(), ev(), ev()] for _ in range(args.steps)]
+    evs = [[ev() for _ in range(5)] for _ in range(args.steps)]
     with ClockSampler(local) as clk:
         barrier()
         t_start, t_end = ev(), ev()
@@ -250,8 +254,8 @@ def run_ours(args, w):
         t_end.record(stream)
         barrier()
     total_ms = t_start.elapsed_time(t_end)
-    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    kern_ms = {name: sum(e[i].elapsed_time(e[i + 1]) for e in evs) / len(evs)
+               for i, name in enumerate(("fwd", "bwd_pre", "bwd_dkdv", "bwd_dq"))}
     if cpattn_device_status(stream) != 0:
         raise RuntimeError("a kernel reported a timeout in the timed region")
     t = torch.tensor([total_ms], device=dev)
@@ -291,15 +295,24 @@ def run_ours(args, w):
         peaks = _peaks()
         step_flops = w.fwd_flops() + w.bwd_flops()
         value = step_flops * args.steps * ws / (total_ms * 1e-3) / 1e12
-        fwd_avg = sum(fwd_ms) / len(fwd_ms)
-        bwd_avg = sum(bwd_ms) / len(bwd_ms)
+        fwd_avg = kern_ms["fwd"]
+        bwd_avg = kern_ms["bwd_pre"] + kern_ms["bwd_dkdv"] + kern_ms["bwd_dq"]
         fwd_tf = w.fwd_flops() / (fwd_avg * 1e-3) / 1e12
         bwd_tf = w.bwd_flops() / (bwd_avg * 1e-3) / 1e12
-        dominant = "bwd" if bwd_avg >= fwd_avg else "fwd"
-        achieved = bwd_tf if dominant == "bwd" else fwd_tf
+        # per-kernel algorithmic work: the matmuls each tensor-bound kernel
+        # performs (forward 2, dK/dV 4, dQ 3 -- S and dP are formed in both
+        # backward kernels), bytes for the HBM-bound preprocess
+        kern_flops = {"fwd": w.fwd_flops(), "bwd_dkdv": 2.0 * w.fwd_flops(), "bwd_dq": 1.5 * w.fwd_flops()}
+        pre_bytes = 2 * 2 * w.b * w.s * w.hq * w.d + 4 * w.b * w.hq * w.s * 3
+        dominant = max(kern_flops, key=lambda n: kern_ms[n])
+        achieved = kern_flops[dominant] / (kern_ms[dominant] * 1e-3) / 1e12
         peak = peaks["bf16_tflops_sustained"]
-        traffic = (_profile_traffic("bwd_kernel.cuh", f"cpattn_bwd_kernel_{w.name}.md") if dominant == "bwd" else
-                   _profile_traffic("fwd_kernel.cuh", f"cpattn_fwd_kernel_{w.name}.md"))
+        src = {"fwd": ("fwd_kernel.cuh", "cpattn_fwd_kernel"), "bwd_dkdv": ("bwd_kernel.cuh", "cpattn_bwd_dkdv_kernel"),
+               "bwd_dq": ("bwd_kernel.cuh", "cpattn_bwd_dq_kernel")}[dominant]
+        traffic = _profile_traffic(src[0], f"{src[1]}_{w.name}.md")
+        kernels = {n: {"ms": kern_ms[n], "tflops": kern_flops[n] / (kern_ms[n] * 1e-3) / 1e12} for n in kern_flops}
+        kernels["bwd_pre"] = {"ms": kern_ms["bwd_pre"], "gbs": pre_bytes / (kern_ms["bwd_pre"] * 1e-3) / 1e9,
+                              "hbm_frac": pre_bytes / (kern_ms["bwd_pre"] * 1e-3) / 1e9 / peaks["hbm_gbs"]}
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
@@ -311,11 +324,11 @@ def run_ours(args, w):
             "phases": {"fwd_ms": fwd_avg, "fwd_tflops": fwd_tf, "fwd_frac_burst": fwd_tf / peaks["bf16_tflops"],
                        "bwd_ms": bwd_avg, "bwd_tflops": bwd_tf, "bwd_frac_burst": bwd_tf / peaks["bf16_tflops"],
                        "flops": {"fwd": w.fwd_flops(), "bwd": w.bwd_flops(), "convention": "fwd 2*b*hq*s^2*d; bwd 2.5x fwd"}},
-            "roofline": {"kernel": f"cpattn_{dominant}" + ("_kernel (+ preprocess and dQ conversion in the timed span)"
-                                                            if dominant == "bwd" else "_kernel"),
-                         "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "peak_kind": f"bf16 sustained ({peaks['source']})",
-                         "frac_vs_burst": achieved / peaks["bf16_tflops"], "traffic": traffic},
+            "kernels": kernels,
+            "roofline": {"kernel": src[1], "bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "peak_kind": f"bf16 sustained ({peaks['source']})",
+                         "frac_vs_burst": achieved / peaks["bf16_tflops"], "traffic": traffic,
+                         "flops_per_launch": kern_flops[dominant]},
             "e2e": {"value": step_flops * args.steps * ws / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
             "gpu_launches": launches_per_step * args.steps,

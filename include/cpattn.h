@@ -96,6 +96,20 @@ int cpattn_bwd(const void* q, const void* k, const void* v, const void* o, const
                int d, int cp, int causal, void* stream);
 
 /*
+ * One stage of cpattn_bwd, for callers that schedule or time the backward's
+ * kernels themselves. Stage 0 writes the per-row vectors (L*log2(e) and
+ * D = rowsum(dO * O)) into the workspace; stage 1 computes dk and dv
+ * (key-tile-stationary); stage 2 computes dq (query-tile-stationary, key
+ * tiles in CP-step order). Stages 1 and 2 read only the inputs and what
+ * stage 0 wrote, so once stage 0 is complete they may run in either order or
+ * on different streams. cpattn_bwd runs stages 0, 1, 2 on one stream.
+ * Arguments as cpattn_bwd; stage outside 0..2 -> CPATTN_ERR_INVALID_ARG.
+ */
+int cpattn_bwd_stage(int stage, const void* q, const void* k, const void* v, const void* o, const float* lse,
+                     const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int b,
+                     int s, int hq, int hkv, int d, int cp, int causal, void* stream);
+
+/*
  * cpattn_bwd without a workspace argument. The pages describe nothing like
  * it: it exists for callers that cannot allocate device memory when they
  * call the backward -- code that runs under a device-memory budget fixed at

@@ -173,6 +173,7 @@ __device__ __forceinline__ uint32_t bit_range(int lo, int hi) {
 template <int D>
 struct DkdvCfg {
   static constexpr int kTileBytes = kTile * D * 2;  // 128 x D bf16
+  static constexpr int kHalfRows = kTile / 2;       // a block is processed as two 64-query halves
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kTileBytes;
   static constexpr int kOffQ = kOffV + kTileBytes;       // two stages
@@ -180,25 +181,30 @@ struct DkdvCfg {
   static constexpr int kOffLD = kOffdO + 2 * kTileBytes;
   static constexpr int kLDBytes = 2 * kTile * 4;  // L[128], D[128] fp32 per stage
   static constexpr int kOffBar = kOffLD + 2 * kLDBytes;
-  // kv_full kv_empty q_full[2] q_empty[2] s_full p_full dkv_full dkv_empty drain dp_free
-  static constexpr int kNumBars = 12;
+  // kv_full kv_empty q_full[2] q_empty[2] s_full[2] p_full[2] dkv_full dkv_empty drain
+  static constexpr int kNumBars = 13;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
-  static constexpr uint32_t kColA = 0, kColB = 128, kColdV = 256, kColdK = 256 + D;
+  // TMEM: two half-block buffers X0, X1 of [S^T 64 | dP^T 64], then dV, dK
+  static constexpr uint32_t kColX = 0, kColdV = 256, kColdK = 256 + D;
 };
 
 // Key-tile-stationary dK/dV. One CTA per SM, 10 warps:
 //   warps 0-7  element-wise; warp w covers TMEM lanes 32*(w%4).. (key rows)
-//              and column half w/4 (64 query columns of S^T/dP^T, D/2
-//              columns of dK/dV)
+//              and 32-query half w/4 of each 64-query half-block (D/2
+//              columns of dK/dV at the end)
 //   warp 8     TMA producer (K/V per unit; Q, dO, L, D per block, 2 stages)
-//   warp 9     TMEM owner and MMA issuer
-// TMEM: A [0,128) S^T, then P^T and dS^T packed bf16 (the warp of column
-// half h writes P^T of its 64 queries to columns [64h, 64h+32) and dS^T to
-// [64h+32, 64h+64), inside the range it read); B [128,256) dP^T; dV; dK.
-// Because dP^T is only read (never overwritten) by the element-wise warps,
-// dP^T of the next block is issued as soon as they have loaded it and runs
-// under their arithmetic; S^T of the next block follows the dV/dK MMAs.
+//   warp 9     TMEM owner and MMA issuer (whole warp, elect.sync)
+// Each (query tile, head) block is processed as two halves of 64 queries,
+// so that S^T and dP^T of a half take 64 TMEM columns each and two halves fit
+// double-buffered beside the dK/dV accumulators:
+//   X_b = [S^T (64 cols) | dP^T (64 cols)], b = half index & 1.
+// The element-wise warps turn X_b into packed bf16 P^T and dS^T in place (the
+// warp of query quarter q writes P^T to [32q, 32q+16) and dS^T to
+// [32q+16, 32q+32), inside what it read), which feed dV += P^T dO and
+// dK += dS^T Q from TMEM. The MMA warp issues S^T/dP^T of the half after next
+// as soon as those MMAs are issued, so the tensor core computes the next
+// half while the element-wise warps work on the current one.
 // Units walk their query tiles from the end of the sequence down (QWalk), so
 // the CTAs in flight read the same Q/dO tiles from L2.
 template <int D>
@@ -219,12 +225,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* kv_empty = bars + 1;
   uint64_t* q_full = bars + 2;
   uint64_t* q_empty = bars + 4;
-  uint64_t* s_full = bars + 6;
-  uint64_t* p_full = bars + 7;
-  uint64_t* dkv_full = bars + 8;
-  uint64_t* dkv_empty = bars + 9;
-  uint64_t* drain = bars + 10;
-  uint64_t* dp_free = bars + 11;
+  uint64_t* s_full = bars + 6;  // per buffer
+  uint64_t* p_full = bars + 8;  // per buffer
+  uint64_t* dkv_full = bars + 10;
+  uint64_t* dkv_empty = bars + 11;
+  uint64_t* drain = bars + 12;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -242,13 +247,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 8);
     }
-    mbar_init(s_full, 1);
-    mbar_init(p_full, 8);
     mbar_init(dkv_full, 1);
     mbar_init(dkv_empty, 8);
     mbar_init(drain, 1);
-    mbar_init(dp_free, 8);
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -325,85 +329,83 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     // (the whole warp runs this role; elect.sync picks the issuing lane)
     {
-      constexpr uint32_t idS = make_idesc_bf16(kTile, kTile, false, false);  // S^T, dP^T
-      constexpr uint32_t idKV = make_idesc_bf16(kTile, D, false, true);      // dV, dK
+      constexpr uint32_t idS = make_idesc_bf16(kTile, C::kHalfRows, false, false);  // S^T, dP^T of a half
+      constexpr uint32_t idKV = make_idesc_bf16(kTile, D, false, true);             // dV, dK
       const uint64_t dK_km = make_sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dV_km = make_sdesc_sw128(smem_u32(sV), 16, 1024);
       const uint64_t dQ_km = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t ddO_km = make_sdesc_sw128(smem_u32(sdO), 16, 1024);
       const uint64_t dQ_mn = make_sdesc_sw128(smem_u32(sQ), 16384, 1024);
       const uint64_t ddO_mn = make_sdesc_sw128(smem_u32(sdO), 16384, 1024);
-      const uint32_t tA = tbase + C::kColA, tB = tbase + C::kColB;
       const uint32_t tdV = tbase + C::kColdV, tdK = tbase + C::kColdK;
+      // S^T and dP^T of half t (item t/2, rows 64*(t&1).. of its stage) into X_{t&1}
+      auto issue_sdp = [&](uint32_t t) {
+        const uint32_t st = (t >> 1) & 1;
+        const uint64_t ro = (st * C::kTileBytes + (t & 1) * C::kHalfRows * 128) >> 4;
+        const uint32_t tX = tbase + C::kColX + (t & 1) * 128;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;
+          umma_ss_w(tX, dK_km + off, dQ_km + ro + off, idS, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;
+          umma_ss_w(tX + 64, dV_km + off, ddO_km + ro + off, idS, kk > 0);
+        }
+      };
       bool ok = true;
-      uint32_t item = 0;
+      uint32_t t0 = 0;  // half-blocks before this unit (always even)
       int ul = 0;
       for (int rd = 0; ok; ++rd) {
         const int idx = snake_unit(rd, blockIdx.x, grid);
         if (idx >= num_units) break;
         const BwdUnit U = bwd_decode_unit(g, idx);
-        // S^T = K Q^T into A, dP^T = V dO^T into B, for block `blk` (stage st)
-        auto issue_s = [&](uint32_t st) {
-          const uint64_t so = (st * C::kTileBytes) >> 4;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;
-            umma_ss_w(tA, dK_km + off, dQ_km + so + off, idS, kk > 0);
-          }
-        };
-        auto issue_dp = [&](uint32_t st) {
-          const uint64_t so = (st * C::kTileBytes) >> 4;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;
-            umma_ss_w(tB, dV_km + off, ddO_km + so + off, idS, kk > 0);
-          }
-        };
-        for (int it = 0; it < U.items && ok; ++it, ++item) {
-          const uint32_t st = item & 1;
-          const uint64_t so = (st * C::kTileBytes) >> 4;
-          if (it == 0) {
-            // first block of a unit (new K/V): S^T and dP^T issued here
-            ok = mbar_wait_warp(&q_full[st], (item >> 1) & 1, abort_flag, kWaitLimitNs) &&
-                 mbar_wait_warp(kv_full, ul & 1, abort_flag, kWaitLimitNs) &&
-                 (item == 0 || mbar_wait_warp(dp_free, (item - 1) & 1, abort_flag, kWaitLimitNs));
-            if (!ok) break;
-            tc_fence_after();  // dp_free orders the element-wise warps' TMEM reads
-            issue_s(st);  // A is free: the previous dV/dK MMAs were issued first
-            issue_dp(st);
-            umma_commit_w(s_full);
-          }
-          if (it + 1 < U.items) {
-            // dP^T of the next block as soon as this block's dP^T is in registers
-            ok = mbar_wait_warp(dp_free, item & 1, abort_flag, kWaitLimitNs) &&
-                 mbar_wait_warp(&q_full[st ^ 1], ((item + 1) >> 1) & 1, abort_flag, kWaitLimitNs);
-            if (!ok) break;
-            tc_fence_after();
-            issue_dp(st ^ 1);
-          }
-          ok = mbar_wait_warp(p_full, item & 1, abort_flag, kWaitLimitNs) &&
-               (it > 0 || ul == 0 || mbar_wait_warp(dkv_empty, (ul - 1) & 1, abort_flag, kWaitLimitNs));
+        const int nh = 2 * U.items;
+        // prologue: S^T/dP^T of the unit's first two halves (the first block).
+        // The X buffers are free: the previous unit's last dV/dK MMAs, which
+        // read them, were issued first.
+        ok = mbar_wait_warp(&q_full[(t0 >> 1) & 1], (t0 >> 2) & 1, abort_flag, kWaitLimitNs) &&
+             mbar_wait_warp(kv_full, ul & 1, abort_flag, kWaitLimitNs);
+        if (!ok) break;
+        issue_sdp(t0);
+        umma_commit_w(&s_full[0]);
+        issue_sdp(t0 + 1);
+        umma_commit_w(&s_full[1]);
+        for (int j = 0; j < nh && ok; ++j) {
+          const uint32_t t = t0 + j;
+          const uint32_t b = t & 1, st = (t >> 1) & 1;
+          ok = mbar_wait_warp(&p_full[b], (t >> 1) & 1, abort_flag, kWaitLimitNs) &&
+               (j > 0 || ul == 0 || mbar_wait_warp(dkv_empty, (ul - 1) & 1, abort_flag, kWaitLimitNs));
           if (!ok) break;
           tc_fence_after();
-          const uint32_t acc = it > 0 ? 1u : 0u;
-          // dV += P^T dO, dK += dS^T Q   (A operands straight from TMEM region A)
+          const uint64_t ro = (st * C::kTileBytes + b * C::kHalfRows * 128) >> 4;
+          const uint32_t tX = tbase + C::kColX + b * 128;
+          // dV += P^T dO_half, dK += dS^T Q_half  (K = 64 queries, A from TMEM)
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            umma_ts_w(tdV, tA + half_split_col(kk), ddO_mn + so + ((kk * 2048) >> 4), idKV, acc | (kk > 0));
+          for (int kk = 0; kk < C::kHalfRows / 16; ++kk) {
+            const uint32_t pc = (kk >> 1) * 32 + (kk & 1) * 8;
+            umma_ts_w(tdV, tX + pc, ddO_mn + ro + ((kk * 2048) >> 4), idKV, (j > 0 || kk > 0) ? 1u : 0u);
+          }
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            umma_ts_w(tdK, tA + 32 + half_split_col(kk), dQ_mn + so + ((kk * 2048) >> 4), idKV, acc | (kk > 0));
-          umma_commit_w(&q_empty[st]);
-          if (it + 1 < U.items) {
-            // S^T of the next block, after dV/dK have read region A; its
-            // completion also covers the dP^T issued above
-            issue_s(st ^ 1);
-            umma_commit_w(s_full);
-          } else {
+          for (int kk = 0; kk < C::kHalfRows / 16; ++kk) {
+            const uint32_t pc = (kk >> 1) * 32 + (kk & 1) * 8 + 16;
+            umma_ts_w(tdK, tX + pc, dQ_mn + ro + ((kk * 2048) >> 4), idKV, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          if (b == 1) umma_commit_w(&q_empty[st]);  // both halves of the block consumed
+          if (j + 2 < nh) {
+            // the half after next into this buffer (read by the MMAs just issued)
+            if (b == 0 && !(ok = mbar_wait_warp(&q_full[st ^ 1], ((t + 2) >> 2) & 1, abort_flag, kWaitLimitNs)))
+              break;
+            issue_sdp(t + 2);
+            umma_commit_w(&s_full[b]);
+          }
+          if (j == nh - 1) {
             umma_commit_w(kv_empty);
             umma_commit_w(dkv_full);
           }
         }
+        t0 += nh;
         ++ul;
       }
       if (!ok && lane == 0) atomicOr(a.status, kStatusBwdMma);
@@ -413,15 +415,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else {
     // ------------------------------------------------------------ element-wise
     const int wq = warp & 3;
-    const int hf = warp >> 2;
+    const int hf = warp >> 2;       // which 32 of a half's 64 queries
     const int jr = wq * 32 + lane;  // TMEM lane = key row
     const uint32_t lane_off = uint32_t(wq * 32) << 16;
-    const uint32_t tA = tbase + lane_off + C::kColA;
-    const uint32_t tB = tbase + lane_off + C::kColB;
     const float sl2 = a.scale_log2;
     const float scale = a.scale;
     bool ok = true;
-    uint32_t item = 0;
+    uint32_t t = 0;  // half-blocks processed so far
     int ul = 0;
     for (int rd = 0; ok; ++rd) {
       const int idx = snake_unit(rd, blockIdx.x, grid);
@@ -431,56 +431,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int chunk = 0, tile = 0;
       bool dg = false;
       const bool key_ok = jr < U.k_valid;
-      for (int it = 0; it < U.items && ok; ++it, ++item) {
-        if (it % G == 0) w.next(chunk, tile, dg);
+      for (int j = 0; j < 2 * U.items && ok; ++j, ++t) {
+        if (j % (2 * G) == 0) w.next(chunk, tile, dg);
         const int rem = g.c - tile * kTile;
         const int q_valid = rem < kTile ? rem : kTile;
-        const uint32_t st = item & 1;
-        ok = mbar_wait_bounded(&q_full[st], (item >> 1) & 1, abort_flag, kWaitLimitNs) &&
-             mbar_wait_bounded(s_full, item & 1, abort_flag, kWaitLimitNs);
+        const uint32_t b = t & 1, st = (t >> 1) & 1;
+        ok = mbar_wait_bounded(&q_full[st], (t >> 2) & 1, abort_flag, kWaitLimitNs) &&
+             mbar_wait_bounded(&s_full[b], (t >> 1) & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
         tc_fence_after();
-        // dP^T (both 32-column halves) and the first half of S^T in one
-        // round trip; dP^T is then in registers and the MMA may compute the
-        // next block's dP^T while this block's arithmetic runs
-        uint32_t rs[32], rp0[32], rp1[32];
-        tmem_ld32x3(tB + hf * 64, tB + hf * 64 + 32, tA + hf * 64, rp0, rp1, rs);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(dp_free);
-        const float4* L4 = reinterpret_cast<const float4*>(sLD + st * (2 * kTile) + hf * 64);
-        const float4* D4 = reinterpret_cast<const float4*>(sLD + st * (2 * kTile) + kTile + hf * 64);
+        const uint32_t tX = tbase + lane_off + C::kColX + b * 128;
+        uint32_t rs[32], rp[32];
+        tmem_ld32x2(tX + hf * 32, tX + 64 + hf * 32, rs, rp);
+        // this warp's 32 queries: rows cb .. cb+31 of the block
+        const int cb = (t & 1) * C::kHalfRows + hf * 32;
+        const float4* L4 = reinterpret_cast<const float4*>(sLD + st * (2 * kTile) + cb);
+        const float4* D4 = reinterpret_cast<const float4*>(sLD + st * (2 * kTile) + kTile + cb);
         // Blocks away from the diagonal and from ragged chunk ends need no mask.
         const bool full = !dg && q_valid == kTile && U.k_valid == kTile;
-        // query column c (of this warp's 64) is valid for key row jr when the
-        // key is in its chunk, the query is in its chunk, and (on the
-        // diagonal) c >= jr
-        const int cb = hf * 64;
-        const int lo = dg ? jr - cb : 0;
-        uint32_t pp0[16], pd0[16], pp1[16], pd1[16];
+        uint32_t pp[16], pd[16];
         if (full) {
-          softmax_grad32<false>(rs, rp0, sl2, L4, D4, 0u, pp0, pd0);
+          softmax_grad32<false>(rs, rp, sl2, L4, D4, 0u, pp, pd);
         } else {
-          softmax_grad32<true>(rs, rp0, sl2, L4, D4, key_ok ? bit_range(lo, q_valid - cb) : 0u, pp0, pd0);
+          // query c is valid for key row jr when the key is in its chunk, the
+          // query is in its chunk, and (on the diagonal) c >= jr
+          const int lo = dg ? jr - cb : 0;
+          softmax_grad32<true>(rs, rp, sl2, L4, D4, key_ok ? bit_range(lo, q_valid - cb) : 0u, pp, pd);
         }
-        tmem_ld32(tA + hf * 64 + 32, rs);  // second half of S^T
-        if (full) {
-          softmax_grad32<false>(rs, rp1, sl2, L4 + 8, D4 + 8, 0u, pp1, pd1);
-        } else {
-          softmax_grad32<true>(rs, rp1, sl2, L4 + 8, D4 + 8, key_ok ? bit_range(lo - 32, q_valid - cb - 32) : 0u,
-                               pp1, pd1);
-        }
-        // P^T -> [64h, 64h+32), dS^T -> [64h+32, 64h+64) of region A
-        tmem_st16x4(tA + hf * 64, tA + hf * 64 + 16, tA + hf * 64 + 32, tA + hf * 64 + 48, pp0, pp1, pd0, pd1);
+        // P^T -> [32h, 32h+16), dS^T -> [32h+16, 32h+32) of X_b
+        tmem_st16x2(tX + hf * 32, tX + hf * 32 + 16, pp, pd);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_full);
+        if (lane == 0) mbar_arrive(&p_full[b]);
       }
       if (!ok) break;
-      // ---- dK, dV of the tile: TMEM -> bf16 -> global
+      // ---- dK, dV of the tile: TMEM -> bf16 -> global, 32 columns at a time
       if (!(ok = mbar_wait_bounded(dkv_full, ul & 1, abort_flag, kWaitLimitNs))) break;
       tc_fence_after();
-      // 32 columns at a time: TMEM -> registers -> bf16 -> global
       const int64_t off = ((int64_t(U.bi) * g.s + U.k_t0 + jr) * g.hkv + U.g) * D + hf * (D / 2);
 #pragma unroll
       for (int c0 = 0; c0 < D / 2; c0 += 32) {

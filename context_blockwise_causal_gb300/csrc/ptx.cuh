@@ -448,4 +448,15 @@ __device__ __forceinline__ void tmem_ld32x3(uint32_t ta, uint32_t tb, uint32_t t
 }
 #undef CPATTN_RY8
 
+
+// Two TMEM stores of 16 columns (to two addresses) with a single wait.
+__device__ __forceinline__ void tmem_st16x2(uint32_t ta, uint32_t tb, const uint32_t (&ra)[16],
+                                            const uint32_t (&rb)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17};\n\t"
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%1], {%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(ta), "r"(tb), "r"(ra[0]), "r"(ra[1]), "r"(ra[2]), "r"(ra[3]), "r"(ra[4]), "r"(ra[5]), "r"(ra[6]), "r"(ra[7]), "r"(ra[8]), "r"(ra[9]), "r"(ra[10]), "r"(ra[11]), "r"(ra[12]), "r"(ra[13]), "r"(ra[14]), "r"(ra[15]), "r"(rb[0]), "r"(rb[1]), "r"(rb[2]), "r"(rb[3]), "r"(rb[4]), "r"(rb[5]), "r"(rb[6]), "r"(rb[7]), "r"(rb[8]), "r"(rb[9]), "r"(rb[10]), "r"(rb[11]), "r"(rb[12]), "r"(rb[13]), "r"(rb[14]), "r"(rb[15])
+      : "memory");
+}
+
 }  // namespace cpattn

@@ -114,32 +114,6 @@ __device__ __forceinline__ void grad_pair(uint32_t s0, uint32_t s1, uint32_t dp0
   pd = pack_bf16x2(g0, g1);
 }
 
-// P and dS for 32 consecutive elements (raw fp32 bits of S and dP), packed
-// to bf16 pairs. L*log2e and D per element come as 8 float4 (one per 4
-// elements). When `masked`, bit i of `valid` keeps element i; masked entries
-// (which may hold arbitrary values) are selected to zero, never multiplied.
-template <bool kMasked>
-__device__ __forceinline__ void softmax_grad32(const uint32_t (&rs)[32], const uint32_t (&rp)[32], float sl2,
-                                               const float4* l4, const float4* d4, uint32_t valid,
-                                               uint32_t (&pp)[16], uint32_t (&pd)[16]) {
-  const uint64_t sl2x2 = f2_pack(sl2, sl2);
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const float4 lv = l4[q], dv = d4[q];
-    grad_pair(rs[4 * q], rs[4 * q + 1], rp[4 * q], rp[4 * q + 1], sl2x2, lv.x, lv.y, dv.x, dv.y, pp[2 * q], pd[2 * q]);
-    grad_pair(rs[4 * q + 2], rs[4 * q + 3], rp[4 * q + 2], rp[4 * q + 3], sl2x2, lv.z, lv.w, dv.z, dv.w,
-              pp[2 * q + 1], pd[2 * q + 1]);
-  }
-  if constexpr (kMasked) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t keep = ((valid >> (2 * i)) & 1u ? 0x0000ffffu : 0u) | ((valid >> (2 * i + 1)) & 1u ? 0xffff0000u : 0u);
-      pp[i] &= keep;
-      pd[i] &= keep;
-    }
-  }
-}
-
 // The same with one L*log2e and D for all 32 elements (a query row).
 template <bool kMasked>
 __device__ __forceinline__ void softmax_grad32_row(const uint32_t (&rs)[32], const uint32_t (&rp)[32], float sl2,
@@ -170,41 +144,109 @@ __device__ __forceinline__ uint32_t bit_range(int lo, int hi) {
 }
 
 // ================================================================ dK / dV
+// P for one warp's 32 keys x 32 queries held in 16x256b fragments (see
+// tmem_ld16x256b_2x2): element 16u + 4r + 2e + j of rs is key row 16u + 8e +
+// t/4 and query 8r + 2(t%4) + j. The thread needs L*log2e for only its 8
+// queries (lv[r]: queries 8r + 2(t%4) + {0,1} as .x, .y). Output register
+// 8u + 2r + e holds the bf16 pair of queries 8r + 2(t%4) + {0,1} for key row
+// 16u + 8e + t/4: the packed column 4r + t%4 of the 16x128b fragment (see
+// tmem_st16x128b_2x2). When `masked`, bit c of valid[2u + e] keeps query c
+// of that key row; masked entries are selected to zero.
+template <bool kMasked>
+__device__ __forceinline__ void softmax_p_frag(const uint32_t (&rs)[32], float sl2, const float2 (&lv)[4],
+                                               const uint32_t (&valid)[4], int c4, uint32_t (&pp)[16]) {
+  const uint64_t sl2x2 = f2_pack(sl2, sl2);
+#pragma unroll
+  for (int u = 0; u < 2; ++u)
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int i = 16 * u + 4 * r + 2 * e;
+        const int o = 8 * u + 2 * r + e;
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(rs[i]), __uint_as_float(rs[i + 1])), sl2x2,
+                         f2_pack(-lv[r].x, -lv[r].y)),
+                  x0, x1);
+        pp[o] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
+        if constexpr (kMasked) {
+          const uint32_t bits = valid[2 * u + e] >> (8 * r + 2 * c4);
+          pp[o] &= (bits & 1u ? 0x0000ffffu : 0u) | (bits & 2u ? 0xffff0000u : 0u);
+        }
+      }
+}
+
+// dS = P (dP - D) for the same fragment: P as the packed bf16 pairs from
+// softmax_p_frag, dP as raw fp32 bits in the 16x256b layout, D per query as
+// lv above. Output in the packed 16x128b layout; masked entries are selected
+// to zero (their dP - D may be anything).
+template <bool kMasked>
+__device__ __forceinline__ void ds_frag(const uint32_t (&pp)[16], const uint32_t (&rp)[32], const float2 (&dv)[4],
+                                        const uint32_t (&valid)[4], int c4, uint32_t (&pd)[16]) {
+#pragma unroll
+  for (int u = 0; u < 2; ++u)
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int i = 16 * u + 4 * r + 2 * e;
+        const int o = 8 * u + 2 * r + e;
+        const float p0 = __uint_as_float(pp[o] << 16), p1 = __uint_as_float(pp[o] & 0xffff0000u);
+        float g0, g1;
+        f2_unpack(f2_mul(f2_pack(p0, p1),
+                         f2_sub(f2_pack(__uint_as_float(rp[i]), __uint_as_float(rp[i + 1])), f2_pack(dv[r].x, dv[r].y))),
+                  g0, g1);
+        pd[o] = pack_bf16x2(g0, g1);
+        if constexpr (kMasked) {
+          const uint32_t bits = valid[2 * u + e] >> (8 * r + 2 * c4);
+          pd[o] &= (bits & 1u ? 0x0000ffffu : 0u) | (bits & 2u ? 0xffff0000u : 0u);
+        }
+      }
+}
+
 template <int D>
 struct DkdvCfg {
   static constexpr int kTileBytes = kTile * D * 2;  // 128 x D bf16
-  static constexpr int kHalfRows = kTile / 2;       // a block is processed as two 64-query halves
+  static constexpr int kQStages = 3;                // Q tiles in flight
+  static constexpr int kOStages = 2;                // dO tiles (with L, D) in flight
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kTileBytes;
-  static constexpr int kOffQ = kOffV + kTileBytes;       // two stages
-  static constexpr int kOffdO = kOffQ + 2 * kTileBytes;  // two stages
-  static constexpr int kOffLD = kOffdO + 2 * kTileBytes;
-  static constexpr int kLDBytes = 2 * kTile * 4;  // L[128], D[128] fp32 per stage
-  static constexpr int kOffBar = kOffLD + 2 * kLDBytes;
-  // kv_full kv_empty q_full[2] q_empty[2] s_full[2] p_full[2] dkv_full dkv_empty drain
-  static constexpr int kNumBars = 13;
+  static constexpr int kOffQ = kOffV + kTileBytes;
+  static constexpr int kOffdO = kOffQ + kQStages * kTileBytes;
+  static constexpr int kOffLD = kOffdO + kOStages * kTileBytes;
+  static constexpr int kLDBytes = 2 * kTile * 4;  // L[128], D[128] fp32 per dO stage
+  static constexpr int kOffBar = kOffLD + kOStages * kLDBytes;
+  // kv_full kv_empty q_full[3] q_empty[3] o_full[2] o_empty[2]
+  // s_full s_free dp_full p_full dkv_full dkv_empty drain
+  static constexpr int kNumBars = 2 + 2 * kQStages + 2 * kOStages + 7;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
-  // TMEM: two half-block buffers X0, X1 of [S^T 64 | dP^T 64], then dV, dK
-  static constexpr uint32_t kColX = 0, kColdV = 256, kColdK = 256 + D;
+  static constexpr int kLayoutBytes = kOffMisc + 16;
+  // The d=128 layout leaves no room for re-alignment: the dynamic shared
+  // memory base must already be 1024-byte aligned (checked at run time).
+  static constexpr bool kNeedAlignedBase = (kLayoutBytes + 1024 > 232448);
+  static constexpr int kSmemBytes = kNeedAlignedBase ? kLayoutBytes : kLayoutBytes + 1024;
+  static_assert(kLayoutBytes <= 232448, "dK/dV shared memory layout too large");
+  // TMEM: S^T [0,128), dP^T [128,256) (later P^T | dS^T), dV, dK
+  static constexpr uint32_t kColS = 0, kColdP = 128, kColdV = 256, kColdK = 256 + D;
 };
 
 // Key-tile-stationary dK/dV. One CTA per SM, 10 warps:
 //   warps 0-7  element-wise; warp w covers TMEM lanes 32*(w%4).. (key rows)
-//              and 32-query half w/4 of each 64-query half-block (D/2
-//              columns of dK/dV at the end)
-//   warp 8     TMA producer (K/V per unit; Q, dO, L, D per block, 2 stages)
+//              and queries 64*(w/4) .. +63 of each block (D/2 columns of
+//              dK/dV at the end)
+//   warp 8     TMA producer (K/V per unit; Q in 3 stages; dO, L, D in 2)
 //   warp 9     TMEM owner and MMA issuer (whole warp, elect.sync)
-// Each (query tile, head) block is processed as two halves of 64 queries,
-// so that S^T and dP^T of a half take 64 TMEM columns each and two halves fit
-// double-buffered beside the dK/dV accumulators:
-//   X_b = [S^T (64 cols) | dP^T (64 cols)], b = half index & 1.
-// The element-wise warps turn X_b into packed bf16 P^T and dS^T in place (the
-// warp of query quarter q writes P^T to [32q, 32q+16) and dS^T to
-// [32q+16, 32q+32), inside what it read), which feed dV += P^T dO and
-// dK += dS^T Q from TMEM. The MMA warp issues S^T/dP^T of the half after next
-// as soon as those MMAs are issued, so the tensor core computes the next
-// half while the element-wise warps work on the current one.
+// Per (query tile, head) block i, all MMAs have N = 128 (or D):
+//   S^T(i) = K Q^T -> [0,128)       dP^T(i) = V dO^T -> [128,256)
+//   dK += dS^T(i) Q,  dV += P^T(i) dO   (A operands packed in [128,256))
+// The element-wise warps read S^T(i) and release its columns at once
+// (s_free), compute P in registers, then read dP^T(i) and write packed bf16
+// P^T and dS^T over it (each warp inside the columns it read: P^T to
+// [128+64h, +32), dS^T to [128+64h+32, +32)). So the tensor core runs
+// S^T(i+1) while the warps finish block i, and the exponentials of block i
+// overlap dK/dV(i-1) and dP^T(i):
+//   tensor core:  S^T(i+1) | dK(i) dV(i) | dP^T(i+1) | S^T(i+2) | ...
+//   warps:        P(i+1) from S^T(i+1) ..............| dS(i+1)  |
 // Units walk their query tiles from the end of the sequence down (QWalk), so
 // the CTAs in flight read the same Q/dO tiles from L2.
 template <int D>
@@ -213,8 +255,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                            const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
                            const BwdArgs a) {
   using C = DkdvCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
+  if constexpr (!C::kNeedAlignedBase)
+    smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicOr(a.status, kStatusBwdSmemAlign);
+    return;
+  }
   uint8_t* sK = smem + C::kOffK;
   uint8_t* sV = smem + C::kOffV;
   uint8_t* sQ = smem + C::kOffQ;
@@ -224,12 +272,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* kv_full = bars + 0;
   uint64_t* kv_empty = bars + 1;
   uint64_t* q_full = bars + 2;
-  uint64_t* q_empty = bars + 4;
-  uint64_t* s_full = bars + 6;  // per buffer
-  uint64_t* p_full = bars + 8;  // per buffer
-  uint64_t* dkv_full = bars + 10;
-  uint64_t* dkv_empty = bars + 11;
-  uint64_t* drain = bars + 12;
+  uint64_t* q_empty = q_full + C::kQStages;
+  uint64_t* o_full = q_empty + C::kQStages;
+  uint64_t* o_empty = o_full + C::kOStages;
+  uint64_t* s_full = o_empty + C::kOStages;
+  uint64_t* s_free = s_full + 1;
+  uint64_t* dp_full = s_full + 2;
+  uint64_t* p_full = s_full + 3;
+  uint64_t* dkv_full = s_full + 4;
+  uint64_t* dkv_empty = s_full + 5;
+  uint64_t* drain = s_full + 6;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -244,12 +296,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     *abort_flag = 0;
     mbar_init(kv_full, 1);
     mbar_init(kv_empty, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kQStages; ++i) {
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
-      mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 8);
     }
+    for (int i = 0; i < C::kOStages; ++i) {
+      mbar_init(&o_full[i], 1);
+      mbar_init(&o_empty[i], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 8);
+    mbar_init(dp_full, 1);
+    mbar_init(p_full, 8);
     mbar_init(dkv_full, 1);
     mbar_init(dkv_empty, 8);
     mbar_init(drain, 1);
@@ -274,22 +332,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       bool ok = true;
-      uint32_t item = 0;  // blocks loaded so far (stage = item & 1)
+      uint32_t item = 0;  // blocks loaded so far
       int ul = 0;
       auto load_item = [&](const BwdUnit& U, int chunk, int tile, int h) -> bool {
-        const uint32_t st = item & 1;
-        if (item >= 2 && !mbar_wait_bounded(&q_empty[st], ((item >> 1) - 1) & 1, abort_flag, kWaitLimitNs))
-          return false;
-        mbar_arrive_expect_tx(&q_full[st], 2 * C::kTileBytes + C::kLDBytes);
         const int row = U.bi * g.s + chunk * g.c + tile * kTile;
-        for (int x = 0; x < D; x += 64) {
-          tma_load_3d(sQ + st * C::kTileBytes + (x / 64) * (kTile * 128), &tmq, &q_full[st], x, h, row);
-          tma_load_3d(sdO + st * C::kTileBytes + (x / 64) * (kTile * 128), &tmdo, &q_full[st], x, h, row);
-        }
+        const uint32_t qs = item % C::kQStages, os = item % C::kOStages;
+        if (item >= C::kQStages &&
+            !mbar_wait_lean(&q_empty[qs], ((item / C::kQStages) - 1) & 1, abort_flag, kWaitLimitNs))
+          return false;
+        mbar_arrive_expect_tx(&q_full[qs], C::kTileBytes);
+        for (int x = 0; x < D; x += 64)
+          tma_load_3d(sQ + qs * C::kTileBytes + (x / 64) * (kTile * 128), &tmq, &q_full[qs], x, h, row);
+        if (item >= C::kOStages &&
+            !mbar_wait_lean(&o_empty[os], ((item / C::kOStages) - 1) & 1, abort_flag, kWaitLimitNs))
+          return false;
+        mbar_arrive_expect_tx(&o_full[os], C::kTileBytes + C::kLDBytes);
+        for (int x = 0; x < D; x += 64)
+          tma_load_3d(sdO + os * C::kTileBytes + (x / 64) * (kTile * 128), &tmdo, &o_full[os], x, h, row);
         const int64_t pos = ld_pos(g, a.ntp, U.bi, h, chunk, tile, 0);
-        bulk_load(reinterpret_cast<uint8_t*>(sLD) + st * C::kLDBytes, a.lvec + pos, kTile * 4, &q_full[st]);
-        bulk_load(reinterpret_cast<uint8_t*>(sLD) + st * C::kLDBytes + kTile * 4, a.dvec + pos, kTile * 4,
-                  &q_full[st]);
+        bulk_load(reinterpret_cast<uint8_t*>(sLD) + os * C::kLDBytes, a.lvec + pos, kTile * 4, &o_full[os]);
+        bulk_load(reinterpret_cast<uint8_t*>(sLD) + os * C::kLDBytes + kTile * 4, a.dvec + pos, kTile * 4,
+                  &o_full[os]);
         ++item;
         return true;
       };
@@ -307,7 +370,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (ok && first) {
               // K/V of this unit, once its first block is on its way.
               first = false;
-              if (ul > 0 && !(ok = mbar_wait_bounded(kv_empty, (ul - 1) & 1, abort_flag, kWaitLimitNs))) break;
+              if (ul > 0 && !(ok = mbar_wait_lean(kv_empty, (ul - 1) & 1, abort_flag, kWaitLimitNs))) break;
               mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
               const int krow = U.bi * g.s + U.k_t0;
               for (int x = 0; x < D; x += 64) {
@@ -321,107 +384,125 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (!ok) atomicOr(a.status, kStatusBwdProducer);
       // Let every copy still in flight land before the CTA can exit.
-      for (uint32_t i = item > 2 ? item - 2 : 0; i < item; ++i)
-        mbar_wait_bounded(&q_full[i & 1], (i >> 1) & 1, abort_flag, kWaitLimitNs);
-      if (ul > 0) mbar_wait_bounded(kv_full, (ul - 1) & 1, abort_flag, kWaitLimitNs);
+      for (uint32_t i = item > C::kQStages ? item - C::kQStages : 0; i < item; ++i)
+        mbar_wait_lean(&q_full[i % C::kQStages], (i / C::kQStages) & 1, abort_flag, kWaitLimitNs);
+      for (uint32_t i = item > C::kOStages ? item - C::kOStages : 0; i < item; ++i)
+        mbar_wait_lean(&o_full[i % C::kOStages], (i / C::kOStages) & 1, abort_flag, kWaitLimitNs);
+      if (ul > 0) mbar_wait_lean(kv_full, (ul - 1) & 1, abort_flag, kWaitLimitNs);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     // (the whole warp runs this role; elect.sync picks the issuing lane)
     {
-      constexpr uint32_t idS = make_idesc_bf16(kTile, C::kHalfRows, false, false);  // S^T, dP^T of a half
-      constexpr uint32_t idKV = make_idesc_bf16(kTile, D, false, true);             // dV, dK
+      constexpr uint32_t idS = make_idesc_bf16(kTile, kTile, false, false);  // S^T, dP^T
+      constexpr uint32_t idKV = make_idesc_bf16(kTile, D, false, true);      // dV, dK
       const uint64_t dK_km = make_sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dV_km = make_sdesc_sw128(smem_u32(sV), 16, 1024);
       const uint64_t dQ_km = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t ddO_km = make_sdesc_sw128(smem_u32(sdO), 16, 1024);
       const uint64_t dQ_mn = make_sdesc_sw128(smem_u32(sQ), 16384, 1024);
       const uint64_t ddO_mn = make_sdesc_sw128(smem_u32(sdO), 16384, 1024);
+      const uint32_t tS = tbase + C::kColS, tdP = tbase + C::kColdP;
       const uint32_t tdV = tbase + C::kColdV, tdK = tbase + C::kColdK;
-      // S^T and dP^T of half t (item t/2, rows 64*(t&1).. of its stage) into X_{t&1}
-      auto issue_sdp = [&](uint32_t t) {
-        const uint32_t st = (t >> 1) & 1;
-        const uint64_t ro = (st * C::kTileBytes + (t & 1) * C::kHalfRows * 128) >> 4;
-        const uint32_t tX = tbase + C::kColX + (t & 1) * 128;
+      auto issue_s = [&](uint32_t i) {  // S^T(i) = K Q^T
+        const uint64_t ro = ((i % C::kQStages) * C::kTileBytes) >> 4;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;
-          umma_ss_w(tX, dK_km + off, dQ_km + ro + off, idS, kk > 0);
+          umma_ss_w(tS, dK_km + off, dQ_km + ro + off, idS, kk > 0);
         }
+      };
+      auto issue_dp = [&](uint32_t i) {  // dP^T(i) = V dO^T
+        const uint64_t ro = ((i % C::kOStages) * C::kTileBytes) >> 4;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;
-          umma_ss_w(tX + 64, dV_km + off, ddO_km + ro + off, idS, kk > 0);
+          umma_ss_w(tdP, dV_km + off, ddO_km + ro + off, idS, kk > 0);
         }
       };
       bool ok = true;
-      uint32_t t0 = 0;  // half-blocks before this unit (always even)
+      uint32_t i0 = 0;  // blocks before this unit
       int ul = 0;
       for (int rd = 0; ok; ++rd) {
         const int idx = snake_unit(rd, blockIdx.x, grid);
         if (idx >= num_units) break;
         const BwdUnit U = bwd_decode_unit(g, idx);
-        const int nh = 2 * U.items;
-        // prologue: S^T/dP^T of the unit's first two halves (the first block).
-        // The X buffers are free: the previous unit's last dV/dK MMAs, which
-        // read them, were issued first.
-        ok = mbar_wait_warp(&q_full[(t0 >> 1) & 1], (t0 >> 2) & 1, abort_flag, kWaitLimitNs) &&
-             mbar_wait_warp(kv_full, ul & 1, abort_flag, kWaitLimitNs);
+        const int n = U.items;
+        // prologue: S^T and dP^T of the unit's first block. The S^T columns
+        // are free once the element-wise warps have read the previous S^T;
+        // the dP^T columns once the previous dK/dV MMAs (issued) read them.
+        ok = mbar_wait_warp_lean(kv_full, ul & 1, abort_flag, kWaitLimitNs) &&
+             mbar_wait_warp_lean(&q_full[i0 % C::kQStages], (i0 / C::kQStages) & 1, abort_flag, kWaitLimitNs) &&
+             (i0 == 0 || mbar_wait_warp_lean(s_free, (i0 - 1) & 1, abort_flag, kWaitLimitNs));
         if (!ok) break;
-        issue_sdp(t0);
-        umma_commit_w(&s_full[0]);
-        issue_sdp(t0 + 1);
-        umma_commit_w(&s_full[1]);
-        for (int j = 0; j < nh && ok; ++j) {
-          const uint32_t t = t0 + j;
-          const uint32_t b = t & 1, st = (t >> 1) & 1;
-          ok = mbar_wait_warp(&p_full[b], (t >> 1) & 1, abort_flag, kWaitLimitNs) &&
-               (j > 0 || ul == 0 || mbar_wait_warp(dkv_empty, (ul - 1) & 1, abort_flag, kWaitLimitNs));
+        issue_s(i0);
+        umma_commit_w(s_full);
+        if (!(ok = mbar_wait_warp_lean(&o_full[i0 % C::kOStages], (i0 / C::kOStages) & 1, abort_flag, kWaitLimitNs)))
+          break;
+        issue_dp(i0);
+        umma_commit_w(dp_full);
+        for (int j = 0; j < n && ok; ++j) {
+          const uint32_t i = i0 + j;
+          if (j + 1 < n) {
+            // S^T(i+1) as soon as S^T(i) has been read
+            ok = mbar_wait_warp_lean(s_free, i & 1, abort_flag, kWaitLimitNs) &&
+                 mbar_wait_warp_lean(&q_full[(i + 1) % C::kQStages], ((i + 1) / C::kQStages) & 1, abort_flag,
+                                kWaitLimitNs);
+            if (!ok) break;
+            issue_s(i + 1);
+            umma_commit_w(s_full);
+          }
+          ok = mbar_wait_warp_lean(p_full, i & 1, abort_flag, kWaitLimitNs) &&
+               (j > 0 || ul == 0 || mbar_wait_warp_lean(dkv_empty, (ul - 1) & 1, abort_flag, kWaitLimitNs));
           if (!ok) break;
           tc_fence_after();
-          const uint64_t ro = (st * C::kTileBytes + b * C::kHalfRows * 128) >> 4;
-          const uint32_t tX = tbase + C::kColX + b * 128;
-          // dV += P^T dO_half, dK += dS^T Q_half  (K = 64 queries, A from TMEM)
+          // dK += dS^T Q, dV += P^T dO (K = 128 queries, A from TMEM)
+          const uint64_t rq = ((i % C::kQStages) * C::kTileBytes) >> 4;
+          const uint64_t ro = ((i % C::kOStages) * C::kTileBytes) >> 4;
 #pragma unroll
-          for (int kk = 0; kk < C::kHalfRows / 16; ++kk) {
-            const uint32_t pc = (kk >> 1) * 32 + (kk & 1) * 8;
-            umma_ts_w(tdV, tX + pc, ddO_mn + ro + ((kk * 2048) >> 4), idKV, (j > 0 || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            umma_ts_w(tdK, tdP + 32 + half_split_col(kk), dQ_mn + rq + ((kk * 2048) >> 4), idKV,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+          umma_commit_w(&q_empty[i % C::kQStages]);
 #pragma unroll
-          for (int kk = 0; kk < C::kHalfRows / 16; ++kk) {
-            const uint32_t pc = (kk >> 1) * 32 + (kk & 1) * 8 + 16;
-            umma_ts_w(tdK, tX + pc, dQ_mn + ro + ((kk * 2048) >> 4), idKV, (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          if (b == 1) umma_commit_w(&q_empty[st]);  // both halves of the block consumed
-          if (j + 2 < nh) {
-            // the half after next into this buffer (read by the MMAs just issued)
-            if (b == 0 && !(ok = mbar_wait_warp(&q_full[st ^ 1], ((t + 2) >> 2) & 1, abort_flag, kWaitLimitNs)))
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            umma_ts_w(tdV, tdP + half_split_col(kk), ddO_mn + ro + ((kk * 2048) >> 4), idKV,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+          umma_commit_w(&o_empty[i % C::kOStages]);
+          if (j + 1 < n) {
+            // dP^T(i+1) over P^T/dS^T(i), which the MMAs just issued read first
+            if (!(ok = mbar_wait_warp_lean(&o_full[(i + 1) % C::kOStages], ((i + 1) / C::kOStages) & 1, abort_flag,
+                                      kWaitLimitNs)))
               break;
-            issue_sdp(t + 2);
-            umma_commit_w(&s_full[b]);
-          }
-          if (j == nh - 1) {
+            issue_dp(i + 1);
+            umma_commit_w(dp_full);
+          } else {
             umma_commit_w(kv_empty);
             umma_commit_w(dkv_full);
           }
         }
-        t0 += nh;
+        i0 += n;
         ++ul;
       }
       if (!ok && lane == 0) atomicOr(a.status, kStatusBwdMma);
       umma_commit_w(drain);
-      mbar_wait_warp(drain, 0, abort_flag, kWaitLimitNs);
+      mbar_wait_warp_lean(drain, 0, abort_flag, kWaitLimitNs);
     }
   } else {
     // ------------------------------------------------------------ element-wise
     const int wq = warp & 3;
-    const int hf = warp >> 2;       // which 32 of a half's 64 queries
-    const int jr = wq * 32 + lane;  // TMEM lane = key row
+    const int hf = warp >> 2;                 // queries 64*hf .. +63 of each block
+    const int jr = wq * 32 + lane;            // TMEM lane = key row (32x32b accesses)
+    const int g4 = lane >> 2, c4 = lane & 3;  // 16-lane fragments: row t/4 (+8), column pair t%4
     const uint32_t lane_off = uint32_t(wq * 32) << 16;
+    constexpr uint32_t kL16 = 16u << 16;  // lanes +16
+    const uint32_t tS = tbase + lane_off + C::kColS + 64 * hf;
+    const uint32_t tP = tbase + lane_off + C::kColdP + 64 * hf;
     const float sl2 = a.scale_log2;
     const float scale = a.scale;
+    const uint32_t none[4] = {0u, 0u, 0u, 0u};
     bool ok = true;
-    uint32_t t = 0;  // half-blocks processed so far
+    uint32_t i = 0;  // blocks processed so far
     int ul = 0;
     for (int rd = 0; ok; ++rd) {
       const int idx = snake_unit(rd, blockIdx.x, grid);
@@ -431,42 +512,75 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int chunk = 0, tile = 0;
       bool dg = false;
       const bool key_ok = jr < U.k_valid;
-      for (int j = 0; j < 2 * U.items && ok; ++j, ++t) {
-        if (j % (2 * G) == 0) w.next(chunk, tile, dg);
+      for (int j = 0; j < U.items && ok; ++j, ++i) {
+        if (j % G == 0) w.next(chunk, tile, dg);
         const int rem = g.c - tile * kTile;
         const int q_valid = rem < kTile ? rem : kTile;
-        const uint32_t b = t & 1, st = (t >> 1) & 1;
-        ok = mbar_wait_bounded(&q_full[st], (t >> 2) & 1, abort_flag, kWaitLimitNs) &&
-             mbar_wait_bounded(&s_full[b], (t >> 1) & 1, abort_flag, kWaitLimitNs);
+        const uint32_t os = i % C::kOStages;
+        ok = mbar_wait_lean(&o_full[os], (i / C::kOStages) & 1, abort_flag, kWaitLimitNs) &&
+             mbar_wait_lean(s_full, i & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t tX = tbase + lane_off + C::kColX + b * 128;
-        uint32_t rs[32], rp[32];
-        tmem_ld32x2(tX + hf * 32, tX + 64 + hf * 32, rs, rp);
-        // this warp's 32 queries: rows cb .. cb+31 of the block
-        const int cb = (t & 1) * C::kHalfRows + hf * 32;
-        const float4* L4 = reinterpret_cast<const float4*>(sLD + st * (2 * kTile) + cb);
-        const float4* D4 = reinterpret_cast<const float4*>(sLD + st * (2 * kTile) + kTile + cb);
-        // Blocks away from the diagonal and from ragged chunk ends need no mask.
-        const bool full = !dg && q_valid == kTile && U.k_valid == kTile;
-        uint32_t pp[16], pd[16];
-        if (full) {
-          softmax_grad32<false>(rs, rp, sl2, L4, D4, 0u, pp, pd);
-        } else {
-          // query c is valid for key row jr when the key is in its chunk, the
-          // query is in its chunk, and (on the diagonal) c >= jr
-          const int lo = dg ? jr - cb : 0;
-          softmax_grad32<true>(rs, rp, sl2, L4, D4, key_ok ? bit_range(lo, q_valid - cb) : 0u, pp, pd);
-        }
-        // P^T -> [32h, 32h+16), dS^T -> [32h+16, 32h+32) of X_b
-        tmem_st16x2(tX + hf * 32, tX + hf * 32 + 16, pp, pd);
+        // S^T: this warp's 32 keys x 64 queries, then release the columns
+        uint32_t ra[32], rb[32];
+        tmem_ld16x256b_2x2(tS, tS + kL16, tS + 32, tS + kL16 + 32, ra, rb);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[b]);
+        if (lane == 0) mbar_arrive(s_free);
+        // this thread's 16 queries: 64*hf + 32*cb + 8r + 2*c4 + {0, 1}
+        const float* Lq = sLD + os * (2 * kTile) + 64 * hf + 2 * c4;
+        float2 lv[2][4], dv[2][4];
+#pragma unroll
+        for (int cb = 0; cb < 2; ++cb)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) lv[cb][r] = *reinterpret_cast<const float2*>(Lq + 32 * cb + 8 * r);
+        // Blocks away from the diagonal and from ragged chunk ends need no mask.
+        const bool full = !dg && q_valid == kTile && U.k_valid == kTile;
+        uint32_t valid[2][4];
+        uint32_t pp[2][16];
+        if (full) {
+          softmax_p_frag<false>(ra, sl2, lv[0], none, c4, pp[0]);
+          softmax_p_frag<false>(rb, sl2, lv[1], none, c4, pp[1]);
+        } else {
+          // query q (in the block) is valid for key row kr when the key is in
+          // its chunk, the query is in its chunk, and (on the diagonal) q >= kr
+#pragma unroll
+          for (int cb = 0; cb < 2; ++cb)
+#pragma unroll
+            for (int f = 0; f < 4; ++f) {
+              const int kr = wq * 32 + 8 * f + g4;  // key row of fragment row f (16u + 8e = 8f)
+              const int qb = 64 * hf + 32 * cb;
+              valid[cb][f] = kr < U.k_valid ? bit_range(dg ? kr - qb : 0, q_valid - qb) : 0u;
+            }
+          softmax_p_frag<true>(ra, sl2, lv[0], valid[0], c4, pp[0]);
+          softmax_p_frag<true>(rb, sl2, lv[1], valid[1], c4, pp[1]);
+        }
+#pragma unroll
+        for (int cb = 0; cb < 2; ++cb)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) dv[cb][r] = *reinterpret_cast<const float2*>(Lq + kTile + 32 * cb + 8 * r);
+        // dP^T of the same keys and queries
+        if (!(ok = mbar_wait_lean(dp_full, i & 1, abort_flag, kWaitLimitNs))) break;
+        tc_fence_after();
+        tmem_ld16x256b_2x2(tP, tP + kL16, tP + 32, tP + kL16 + 32, ra, rb);
+        uint32_t pd[2][16];
+        if (full) {
+          ds_frag<false>(pp[0], ra, dv[0], none, c4, pd[0]);
+          ds_frag<false>(pp[1], rb, dv[1], none, c4, pd[1]);
+        } else {
+          ds_frag<true>(pp[0], ra, dv[0], valid[0], c4, pd[0]);
+          ds_frag<true>(pp[1], rb, dv[1], valid[1], c4, pd[1]);
+        }
+        // P^T -> [64h, 64h+32), dS^T -> [64h+32, 64h+64) of the dP^T columns
+        tmem_st16x128b_2x2(tP, tP + kL16, tP + 32, tP + kL16 + 32, pp[0], pd[0]);
+        tmem_st16x128b_2x2(tP + 16, tP + kL16 + 16, tP + 48, tP + kL16 + 48, pp[1], pd[1]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
       }
       if (!ok) break;
       // ---- dK, dV of the tile: TMEM -> bf16 -> global, 32 columns at a time
-      if (!(ok = mbar_wait_bounded(dkv_full, ul & 1, abort_flag, kWaitLimitNs))) break;
+      if (!(ok = mbar_wait_lean(dkv_full, ul & 1, abort_flag, kWaitLimitNs))) break;
       tc_fence_after();
       const int64_t off = ((int64_t(U.bi) * g.s + U.k_t0 + jr) * g.hkv + U.g) * D + hf * (D / 2);
 #pragma unroll
@@ -482,19 +596,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         if (key_ok) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 8) {
+          for (int q = 0; q < 32; q += 8) {
             uint4 pv, pk;
-            pv.x = pack_bf16x2(__uint_as_float(rv[i]), __uint_as_float(rv[i + 1]));
-            pv.y = pack_bf16x2(__uint_as_float(rv[i + 2]), __uint_as_float(rv[i + 3]));
-            pv.z = pack_bf16x2(__uint_as_float(rv[i + 4]), __uint_as_float(rv[i + 5]));
-            pv.w = pack_bf16x2(__uint_as_float(rv[i + 6]), __uint_as_float(rv[i + 7]));
+            pv.x = pack_bf16x2(__uint_as_float(rv[q]), __uint_as_float(rv[q + 1]));
+            pv.y = pack_bf16x2(__uint_as_float(rv[q + 2]), __uint_as_float(rv[q + 3]));
+            pv.z = pack_bf16x2(__uint_as_float(rv[q + 4]), __uint_as_float(rv[q + 5]));
+            pv.w = pack_bf16x2(__uint_as_float(rv[q + 6]), __uint_as_float(rv[q + 7]));
             // dK accumulated dS^T Q with dS unscaled: apply 1/sqrt(d) here
-            pk.x = pack_bf16x2(__uint_as_float(rk[i]) * scale, __uint_as_float(rk[i + 1]) * scale);
-            pk.y = pack_bf16x2(__uint_as_float(rk[i + 2]) * scale, __uint_as_float(rk[i + 3]) * scale);
-            pk.z = pack_bf16x2(__uint_as_float(rk[i + 4]) * scale, __uint_as_float(rk[i + 5]) * scale);
-            pk.w = pack_bf16x2(__uint_as_float(rk[i + 6]) * scale, __uint_as_float(rk[i + 7]) * scale);
-            *reinterpret_cast<uint4*>(a.dv + off + c0 + i) = pv;
-            *reinterpret_cast<uint4*>(a.dk + off + c0 + i) = pk;
+            pk.x = pack_bf16x2(__uint_as_float(rk[q]) * scale, __uint_as_float(rk[q + 1]) * scale);
+            pk.y = pack_bf16x2(__uint_as_float(rk[q + 2]) * scale, __uint_as_float(rk[q + 3]) * scale);
+            pk.z = pack_bf16x2(__uint_as_float(rk[q + 4]) * scale, __uint_as_float(rk[q + 5]) * scale);
+            pk.w = pack_bf16x2(__uint_as_float(rk[q + 6]) * scale, __uint_as_float(rk[q + 7]) * scale);
+            *reinterpret_cast<uint4*>(a.dv + off + c0 + q) = pv;
+            *reinterpret_cast<uint4*>(a.dk + off + c0 + q) = pk;
           }
         }
       }

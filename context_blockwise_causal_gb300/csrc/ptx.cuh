@@ -48,13 +48,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Time limit of every wait on a barrier inside the kernels.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
-// Bounded wait on phase `parity` of `bar`. Gives up when `*abort` becomes
-// non-zero (another role already gave up) or after `limit_ns` of wall time;
-// in the latter case it raises `*abort` itself. Returns true when the phase
-// completed.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                                  uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Bounded waits on phase `parity` of `bar`. They give up when `*abort`
+// becomes non-zero (another role already gave up) or after `limit_ns` of wall
+// time; in the latter case they raise `*abort` themselves. They return true
+// when the phase completed.
+//
+// The slow path: poll until the phase completes or the wait gives up.
+__device__ __forceinline__ bool mbar_wait_loop(uint64_t* bar, uint32_t parity, volatile int* abort, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   uint32_t spins = 0;
   while (true) {
@@ -69,13 +69,40 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// Per-thread bounded wait on a barrier phase; false on timeout or abort.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                  uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_loop(bar, parity, abort, limit_ns);
+}
+
 // Warp-uniform bounded wait for roles run by a whole converged warp (the MMA
-// issuers): every lane waits, then the lanes agree, so a lane that timed out
-// can never leave the others at a full-mask elect.sync.
+// issuers): the lanes agree on the outcome, so a lane that timed out can
+// never leave the others at a full-mask elect.sync.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort,
                                                uint64_t limit_ns) {
-  const bool ok = mbar_wait_bounded(bar, parity, abort, limit_ns);
-  return __all_sync(0xffffffffu, ok);
+  bool ok = __all_sync(0xffffffffu, mbar_try_wait(bar, parity));
+  if (!ok) ok = __all_sync(0xffffffffu, mbar_wait_loop(bar, parity, abort, limit_ns));
+  return ok;
+}
+
+// The same waits with the slow path out of line, so that the fast path
+// (phase already complete) is one test and no loop. For kernels without a
+// register split (a call inside a setmaxnreg region does not allocate).
+__device__ __noinline__ bool mbar_wait_loop_ool(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                uint64_t limit_ns) {
+  return mbar_wait_loop(bar, parity, abort, limit_ns);
+}
+__device__ __forceinline__ bool mbar_wait_lean(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                               uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_loop_ool(bar, parity, abort, limit_ns);
+}
+__device__ __forceinline__ bool mbar_wait_warp_lean(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                    uint64_t limit_ns) {
+  bool ok = __all_sync(0xffffffffu, mbar_try_wait(bar, parity));
+  if (!ok) ok = __all_sync(0xffffffffu, mbar_wait_loop_ool(bar, parity, abort, limit_ns));
+  return ok;
 }
 
 // Register reallocation between warpgroups (all four warps of a warpgroup
@@ -325,6 +352,24 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, uint32_t (
       : "r"(ta), "r"(tb)
       : "memory");
 }
+// 16-lane fragments. A 16x256b.x4 access covers 16 TMEM lanes x 32 columns:
+// thread t holds lanes t/4 (registers 4r, 4r+1) and t/4 + 8 (registers
+// 4r+2, 4r+3) at columns 8r + 2(t%4) and 8r + 2(t%4) + 1, r = 0..3.
+// Four such loads (lanes +0 and +16 of two column ranges) with one wait:
+// ra[0..15] from ta0, ra[16..31] from ta1, rb likewise from tb0, tb1.
+__device__ __forceinline__ void tmem_ld16x256b_2x2(uint32_t ta0, uint32_t ta1, uint32_t tb0, uint32_t tb1,
+                                                   uint32_t (&ra)[32], uint32_t (&rb)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%65];\n\t"
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47}, [%66];\n\t"
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%67];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : CPATTN_RA8(0), CPATTN_RA8(8), CPATTN_RA8(16), CPATTN_RA8(24), CPATTN_RB8(0), CPATTN_RB8(8),
+        CPATTN_RB8(16), CPATTN_RB8(24)
+      : "r"(ta0), "r"(ta1), "r"(tb0), "r"(tb1)
+      : "memory");
+}
 #undef CPATTN_RA8
 #undef CPATTN_RB8
 
@@ -456,6 +501,21 @@ __device__ __forceinline__ void tmem_st16x2(uint32_t ta, uint32_t tb, const uint
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17};\n\t"
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%1], {%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33};\n\t"
       "tcgen05.wait::st.sync.aligned;" ::"r"(ta), "r"(tb), "r"(ra[0]), "r"(ra[1]), "r"(ra[2]), "r"(ra[3]), "r"(ra[4]), "r"(ra[5]), "r"(ra[6]), "r"(ra[7]), "r"(ra[8]), "r"(ra[9]), "r"(ra[10]), "r"(ra[11]), "r"(ra[12]), "r"(ra[13]), "r"(ra[14]), "r"(ra[15]), "r"(rb[0]), "r"(rb[1]), "r"(rb[2]), "r"(rb[3]), "r"(rb[4]), "r"(rb[5]), "r"(rb[6]), "r"(rb[7]), "r"(rb[8]), "r"(rb[9]), "r"(rb[10]), "r"(rb[11]), "r"(rb[12]), "r"(rb[13]), "r"(rb[14]), "r"(rb[15])
+      : "memory");
+}
+
+// Four 16x128b.x4 stores with one wait. A 16x128b.x4 access covers 16 lanes
+// x 16 columns: thread t writes lane t/4 (register 2r) and lane t/4 + 8
+// (register 2r+1) at column 4r + t%4, r = 0..3. ra[0..7] go to ta0,
+// ra[8..15] to ta1, rb likewise to tb0, tb1.
+__device__ __forceinline__ void tmem_st16x128b_2x2(uint32_t ta0, uint32_t ta1, uint32_t tb0, uint32_t tb1,
+                                                   const uint32_t (&ra)[16], const uint32_t (&rb)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x128b.x4.b32 [%0], {%4,%5,%6,%7,%8,%9,%10,%11};\n\t"
+      "tcgen05.st.sync.aligned.16x128b.x4.b32 [%1], {%12,%13,%14,%15,%16,%17,%18,%19};\n\t"
+      "tcgen05.st.sync.aligned.16x128b.x4.b32 [%2], {%20,%21,%22,%23,%24,%25,%26,%27};\n\t"
+      "tcgen05.st.sync.aligned.16x128b.x4.b32 [%3], {%28,%29,%30,%31,%32,%33,%34,%35};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(ta0), "r"(ta1), "r"(tb0), "r"(tb1), "r"(ra[0]), "r"(ra[1]), "r"(ra[2]), "r"(ra[3]), "r"(ra[4]), "r"(ra[5]), "r"(ra[6]), "r"(ra[7]), "r"(ra[8]), "r"(ra[9]), "r"(ra[10]), "r"(ra[11]), "r"(ra[12]), "r"(ra[13]), "r"(ra[14]), "r"(ra[15]), "r"(rb[0]), "r"(rb[1]), "r"(rb[2]), "r"(rb[3]), "r"(rb[4]), "r"(rb[5]), "r"(rb[6]), "r"(rb[7]), "r"(rb[8]), "r"(rb[9]), "r"(rb[10]), "r"(rb[11]), "r"(rb[12]), "r"(rb[13]), "r"(rb[14]), "r"(rb[15])
       : "memory");
 }
 

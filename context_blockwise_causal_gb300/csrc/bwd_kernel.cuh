@@ -761,7 +761,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       auto load = [&](const CUtensorMap* map, int head, int row) -> bool {
         const uint32_t slot = nload % C::kSlots;
         if (nload >= (uint32_t)C::kSlots &&
-            !mbar_wait_bounded(&kv_empty[slot], ((nload / C::kSlots) - 1) & 1, abort_flag, kWaitLimitNs))
+            !mbar_wait_lean(&kv_empty[slot], ((nload / C::kSlots) - 1) & 1, abort_flag, kWaitLimitNs))
           return false;
         mbar_arrive_expect_tx(&kv_full[slot], C::kTileBytes);
         uint8_t* dst = sKV + slot * C::kTileBytes;
@@ -774,7 +774,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int idx = snake_unit(rd, blockIdx.x, grid);
         if (idx >= num_units) break;
         const FwdUnit U = dq_decode_unit(g, idx);
-        if (ul > 0 && !(ok = mbar_wait_bounded(q_empty, (ul - 1) & 1, abort_flag, kWaitLimitNs))) break;
+        if (ul > 0 && !(ok = mbar_wait_lean(q_empty, (ul - 1) & 1, abort_flag, kWaitLimitNs))) break;
         mbar_arrive_expect_tx(q_full, 2 * C::kTileBytes);
         const int qrow = U.bi * g.s + U.q_t0;
         for (int x = 0; x < D; x += 64) {
@@ -795,8 +795,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!ok) atomicOr(a.status, kStatusBwdProducer);
       const uint32_t first = nload > (uint32_t)C::kSlots ? nload - C::kSlots : 0;
       for (uint32_t i = first; i < nload; ++i)
-        mbar_wait_bounded(&kv_full[i % C::kSlots], (i / C::kSlots) & 1, abort_flag, kWaitLimitNs);
-      if (ul > 0) mbar_wait_bounded(q_full, (ul - 1) & 1, abort_flag, kWaitLimitNs);
+        mbar_wait_lean(&kv_full[i % C::kSlots], (i / C::kSlots) & 1, abort_flag, kWaitLimitNs);
+      if (ul > 0) mbar_wait_lean(q_full, (ul - 1) & 1, abort_flag, kWaitLimitNs);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
@@ -838,15 +838,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (idx >= num_units) break;
         const FwdUnit U = dq_decode_unit(g, idx);
         const int n = U.n;
-        if (!(ok = mbar_wait_warp(q_full, ul & 1, abort_flag, kWaitLimitNs))) break;
+        if (!(ok = mbar_wait_warp_lean(q_full, ul & 1, abort_flag, kWaitLimitNs))) break;
         // prologue: S(0), dP(0). The dP region is free once the previous
         // tile's element-wise warps have read it.
         uint32_t ks, kp, vs, vp;
         take(vs, vp);
         take(ks, kp);
-        ok = mbar_wait_warp(&kv_full[ks], kp, abort_flag, kWaitLimitNs) &&
-             mbar_wait_warp(&kv_full[vs], vp, abort_flag, kWaitLimitNs) &&
-             (jt == 0 || mbar_wait_warp(dp_free, (jt - 1) & 1, abort_flag, kWaitLimitNs));
+        ok = mbar_wait_warp_lean(&kv_full[ks], kp, abort_flag, kWaitLimitNs) &&
+             mbar_wait_warp_lean(&kv_full[vs], vp, abort_flag, kWaitLimitNs) &&
+             (jt == 0 || mbar_wait_warp_lean(dp_free, (jt - 1) & 1, abort_flag, kWaitLimitNs));
         if (!ok) break;
         tc_fence_after();
         issue_sdp(jt, ks, vs);
@@ -858,9 +858,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (j + 1 < n) {
             take(vs, vp);
             take(ks, kp);
-            ok = mbar_wait_warp(dp_free, jt & 1, abort_flag, kWaitLimitNs) &&
-                 mbar_wait_warp(&kv_full[ks], kp, abort_flag, kWaitLimitNs) &&
-                 mbar_wait_warp(&kv_full[vs], vp, abort_flag, kWaitLimitNs);
+            ok = mbar_wait_warp_lean(dp_free, jt & 1, abort_flag, kWaitLimitNs) &&
+                 mbar_wait_warp_lean(&kv_full[ks], kp, abort_flag, kWaitLimitNs) &&
+                 mbar_wait_warp_lean(&kv_full[vs], vp, abort_flag, kWaitLimitNs);
             if (!ok) break;
             tc_fence_after();
             // the other S buffer held dS(jt-1), read by the dQ MMA issued before
@@ -869,8 +869,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             umma_commit_w(&kv_empty[vs]);
             if (j + 1 == n - 1) umma_commit_w(q_empty);
           }
-          ok = mbar_wait_warp(ds_full, jt & 1, abort_flag, kWaitLimitNs) &&
-               (j > 0 || ul == 0 || mbar_wait_warp(dq_empty, (ul - 1) & 1, abort_flag, kWaitLimitNs));
+          ok = mbar_wait_warp_lean(ds_full, jt & 1, abort_flag, kWaitLimitNs) &&
+               (j > 0 || ul == 0 || mbar_wait_warp_lean(dq_empty, (ul - 1) & 1, abort_flag, kWaitLimitNs));
           if (!ok) break;
           tc_fence_after();
           // dQ += dS(jt) K_j   (dS from TMEM, K MN-major)
@@ -886,7 +886,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (!ok && lane == 0) atomicOr(a.status, kStatusBwdMma);
       umma_commit_w(drain);
-      mbar_wait_warp(drain, 0, abort_flag, kWaitLimitNs);
+      mbar_wait_warp_lean(drain, 0, abort_flag, kWaitLimitNs);
     }
   } else {
     // ------------------------------------------------------------ element-wise
@@ -916,7 +916,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         w.next(chunk, tile, dg);
         const int rem = g.c - tile * kTile;
         const int n_valid = rem < kTile ? rem : kTile;
-        if (!(ok = mbar_wait_bounded(s_full, jt & 1, abort_flag, kWaitLimitNs))) break;
+        if (!(ok = mbar_wait_lean(s_full, jt & 1, abort_flag, kWaitLimitNs))) break;
         tc_fence_after();
         const uint32_t tS = tbase + lane_off + C::kColS + (jt & 1) * kTile;
         uint32_t rs0[32], rs1[32], rp0[32], rp1[32];
@@ -948,7 +948,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (!ok) break;
       // ---- dQ of the tile: TMEM -> scale -> bf16 -> global
-      if (!(ok = mbar_wait_bounded(dq_full, ul & 1, abort_flag, kWaitLimitNs))) break;
+      if (!(ok = mbar_wait_lean(dq_full, ul & 1, abort_flag, kWaitLimitNs))) break;
       tc_fence_after();
       uint32_t rq[D / 2];
       {

@@ -34,5 +34,6 @@ from .context_parallel import (  # noqa: F401
     cp_step_plan,
     block_attention,
     lse_merge,
+    cp_step_partials,
     cp_attention_forward,
 )

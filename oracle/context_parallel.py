@@ -123,6 +123,42 @@ def lse_merge(parts):
     return O, L
 
 
+def cp_step_partials(q, k, v, cp, step, causal=True):
+    """Every virtual rank's partial result of one CP step, in natural order.
+
+    q: [b, s, hq, d]; k, v: [b, s, hkv, d]; float64 CPU. At step ``step``
+    rank r computes the block of ``cp_step_plan(r, cp, causal)[step]``
+    ([MLM-CP] 3.2 steps 2-3, 3.4). Returns (o_i [b, s, hq, d], lse_i
+    [b, hq, s]): for the query rows of those blocks the block's own softmax
+    output and log-sum-exp (before any correction, 3.2 step 4); every other
+    row gets O = 0 and L = -inf, so merging all steps' partials with
+    ``lse_merge`` row by row gives the attention result.
+    """
+    b, s, hq, d = q.shape
+    hkv = k.shape[2]
+    G = hq // hkv
+    c = s // (2 * cp)
+    scale = 1.0 / math.sqrt(d)
+    o = torch.zeros(b, s, hq, d, dtype=_F64)
+    lse = torch.full((b, hq, s), float("-inf"), dtype=_F64)
+
+    def chunk_pos(ch):
+        return torch.arange(ch * c, (ch + 1) * c, dtype=torch.long)
+
+    for bi in range(b):
+        for h in range(hq):
+            g = h // G
+            for r in range(cp):
+                _i, _j, q_ch, kv_ch, masked = cp_step_plan(r, cp, causal)[step]
+                q_pos = torch.cat([chunk_pos(ch) for ch in q_ch])
+                k_pos = torch.cat([chunk_pos(ch) for ch in kv_ch])
+                Oi, Li = block_attention(q[bi, q_pos, h], k[bi, k_pos, g], v[bi, k_pos, g], q_pos, k_pos, masked,
+                                         scale)
+                o[bi, q_pos, h] = Oi
+                lse[bi, h, q_pos] = Li
+    return o, lse
+
+
 def cp_attention_forward(q, k, v, cp, causal=True, merge_order=None):
     """Attention computed the CP way: per virtual rank, per step, then merged.
 

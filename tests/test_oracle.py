@@ -287,3 +287,41 @@ def test_lse_merge_two_halves_closed_form():
     w = 1.0 / (1.0 + math.exp(-3.0))
     assert abs(L[1] - (2.0 + math.log(1 + math.exp(-3.0)))) < 1e-14
     assert abs(O[1, 0] - 4.0 * (1 - w)) < 1e-14
+
+
+@pytest.mark.parametrize("b,s,hq,hkv,d,cp,causal", [(1, 24, 2, 1, 4, 3, True), (2, 32, 4, 2, 8, 4, True),
+                                                    (1, 40, 2, 2, 3, 5, True), (1, 24, 2, 2, 4, 3, False)])
+def test_step_partials_merge_to_uncut(b, s, hq, hkv, d, cp, causal):
+    """Merging the cp per-step partials row by row gives uncut attention."""
+    g = torch.Generator().manual_seed(300 + s + cp)
+    q, k, v = _rand(b, s, hq, d, gen=g), _rand(b, s, hkv, d, gen=g), _rand(b, s, hkv, d, gen=g)
+    o_ref, l_ref = attention_forward(q, k, v, causal=causal)
+    parts = [oracle.cp_step_partials(q, k, v, cp, i, causal=causal) for i in range(cp)]
+    for bi in range(b):
+        for h in range(hq):
+            O, L = oracle.lse_merge([(o_i[bi, :, h], l_i[bi, h]) for o_i, l_i in parts])
+            assert torch.allclose(O, o_ref[bi, :, h], atol=1e-12, rtol=0)
+            assert torch.allclose(L, l_ref[bi, h], atol=1e-12, rtol=0)
+
+
+def test_step_partials_structure():
+    """Which rows take part in each step ([MLM-CP] 3.4), and step 0 of the
+    first chunk being plain causal attention over that chunk's prefix."""
+    b, s, hq, hkv, d, cp = 1, 32, 2, 1, 4, 4
+    c = s // (2 * cp)
+    g = torch.Generator().manual_seed(7)
+    q, k, v = _rand(b, s, hq, d, gen=g), _rand(b, s, hkv, d, gen=g), _rand(b, s, hkv, d, gen=g)
+    o_ref, l_ref = attention_forward(q, k, v)
+    for i in range(cp):
+        o_i, l_i = oracle.cp_step_partials(q, k, v, cp, i)
+        for r in range(cp):
+            lo, hi = range(r * c, (r + 1) * c), range((2 * cp - 1 - r) * c, (2 * cp - r) * c)
+            first_in = i <= r  # the first chunk's rows take part in steps 0..r
+            assert bool(torch.isfinite(l_i[0, :, list(lo)]).all()) == first_in
+            assert torch.isfinite(l_i[0, :, list(hi)]).all()  # the second chunk's rows in every step
+            if not first_in:
+                assert (o_i[0, list(lo)] == 0).all()
+        if i == 0:
+            # chunk 0 (rank 0's first chunk) sees exactly keys 0..t at step 0
+            assert torch.allclose(o_i[0, :c], o_ref[0, :c], atol=1e-12)
+            assert torch.allclose(l_i[0, :, :c], l_ref[0, :, :c], atol=1e-12)

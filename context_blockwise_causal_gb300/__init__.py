@@ -17,6 +17,10 @@ from ._build import LIB_PATH, build  # noqa: F401
 __all__ = [
     "CpattnError",
     "cpattn_fwd",
+    "cpattn_fwd_step",
+    "cpattn_lse_merge",
+    "cpattn_fwd_unfused",
+    "cpattn_fwd_unfused_workspace_bytes",
     "cpattn_bwd",
     "cpattn_bwd_workspace_bytes",
     "cpattn_zigzag_index",
@@ -57,6 +61,14 @@ def library():
         lib = ctypes.CDLL(LIB_PATH)
         lib.cpattn_fwd.argtypes = [_p, _p, _p, _p, _p] + [_i] * 7 + [_p]
         lib.cpattn_fwd.restype = _i
+        lib.cpattn_fwd_step.argtypes = [_p] * 5 + [_i] * 8 + [_p]
+        lib.cpattn_fwd_step.restype = _i
+        lib.cpattn_lse_merge.argtypes = [_p] * 7 + [_i] * 4 + [_p]
+        lib.cpattn_lse_merge.restype = _i
+        lib.cpattn_fwd_unfused_workspace_bytes.argtypes = [_i] * 4
+        lib.cpattn_fwd_unfused_workspace_bytes.restype = _sz
+        lib.cpattn_fwd_unfused.argtypes = [_p] * 6 + [_sz] + [_i] * 7 + [_p]
+        lib.cpattn_fwd_unfused.restype = _i
         lib.cpattn_bwd.argtypes = [_p] * 10 + [_sz] + [_i] * 7 + [_p]
         lib.cpattn_bwd.restype = _i
         lib.cpattn_bwd_stage.argtypes = [_i] + [_p] * 10 + [_sz] + [_i] * 7 + [_p]
@@ -126,6 +138,95 @@ def cpattn_fwd(q, k, v, cp, causal=True, o=None, lse=None, stream=None):
                               d, int(cp), 1 if causal else 0, _stream_handle(stream))
     if rc:
         raise CpattnError(rc, "cpattn_fwd")
+    return o, lse
+
+
+def _check_f32(name, t, shape):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous fp32 CUDA tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def cpattn_fwd_step(q, k, v, cp, step, causal=True, o_part=None, lse_part=None, stream=None):
+    """Every virtual rank's unmerged result of CP step ``step``.
+
+    Returns (o_part [b,s,hq,d] fp32, lse_part [b,hq,s] fp32); rows that take
+    no part in the step get 0 and -inf.
+    """
+    b, s, hq, hkv, d = _dims(q, k, v)
+    if o_part is None:
+        o_part = torch.empty(b, s, hq, d, device=q.device, dtype=torch.float32)
+    if lse_part is None:
+        lse_part = torch.empty(b, hq, s, device=q.device, dtype=torch.float32)
+    _check_f32("o_part", o_part, (b, s, hq, d))
+    _check_f32("lse_part", lse_part, (b, hq, s))
+    rc = library().cpattn_fwd_step(q.data_ptr(), k.data_ptr(), v.data_ptr(), o_part.data_ptr(), lse_part.data_ptr(),
+                                   b, s, hq, hkv, d, int(cp), int(step), 1 if causal else 0, _stream_handle(stream))
+    if rc:
+        raise CpattnError(rc, "cpattn_fwd_step")
+    return o_part, lse_part
+
+
+def cpattn_lse_merge(o_a, lse_a, o_b=None, lse_b=None, o_out=None, lse_out=None, o_bf16=None, stream=None):
+    """Log-sum-exp merge of two partial results (fp32 [b,s,hq,d] / [b,hq,s]).
+
+    Returns (o_out, lse_out, o_bf16); o_out may be ``o_a`` and lse_out
+    ``lse_a`` (in place). With ``o_out=False`` no fp32 output is written
+    (then ``o_bf16`` must be given or is allocated).
+    """
+    if o_a.dim() != 4:
+        raise ValueError("o_a must be [b, s, hq, d]")
+    b, s, hq, d = o_a.shape
+    _check_f32("o_a", o_a, (b, s, hq, d))
+    _check_f32("lse_a", lse_a, (b, hq, s))
+    if (o_b is None) != (lse_b is None):
+        raise ValueError("o_b and lse_b go together")
+    if o_b is not None:
+        _check_f32("o_b", o_b, (b, s, hq, d))
+        _check_f32("lse_b", lse_b, (b, hq, s))
+    if o_out is None:
+        o_out = torch.empty_like(o_a)
+    if o_out is not False:
+        _check_f32("o_out", o_out, (b, s, hq, d))
+    elif o_bf16 is None:
+        o_bf16 = torch.empty(b, s, hq, d, device=o_a.device, dtype=torch.bfloat16)
+    if lse_out is None:
+        lse_out = torch.empty_like(lse_a)
+    _check_f32("lse_out", lse_out, (b, hq, s))
+    if o_bf16 is not None:
+        _check_act("o_bf16", o_bf16, (b, s, hq, d))
+    ptr = lambda t: None if t is None or t is False else t.data_ptr()  # noqa: E731
+    rc = library().cpattn_lse_merge(ptr(o_a), ptr(lse_a), ptr(o_b), ptr(lse_b), ptr(o_out), ptr(lse_out),
+                                    ptr(o_bf16), b, s, hq, d, _stream_handle(stream))
+    if rc:
+        raise CpattnError(rc, "cpattn_lse_merge")
+    return (None if o_out is False else o_out), lse_out, o_bf16
+
+
+def cpattn_fwd_unfused_workspace_bytes(b, s, hq, d):
+    return int(library().cpattn_fwd_unfused_workspace_bytes(b, s, hq, d))
+
+
+def cpattn_fwd_unfused(q, k, v, cp, causal=True, o=None, lse=None, workspace=None, stream=None):
+    """The forward as cp step launches and log-sum-exp merges. Returns (o, lse)."""
+    b, s, hq, hkv, d = _dims(q, k, v)
+    if o is None:
+        o = torch.empty_like(q)
+    _check_act("o", o, q.shape)
+    if lse is None:
+        lse = torch.empty(b, hq, s, device=q.device, dtype=torch.float32)
+    _check_f32("lse", lse, (b, hq, s))
+    need = cpattn_fwd_unfused_workspace_bytes(b, s, hq, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    rc = library().cpattn_fwd_unfused(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                      workspace.data_ptr(), workspace.numel() * workspace.element_size(), b, s, hq,
+                                      hkv, d, int(cp), 1 if causal else 0, _stream_handle(stream))
+    if rc:
+        raise CpattnError(rc, "cpattn_fwd_unfused")
     return o, lse
 
 

@@ -21,6 +21,19 @@ def _nvcc():
     return "nvcc"
 
 
+def is_stale():
+    """True when the library is missing or older than a source or header."""
+    if not os.path.exists(LIB_PATH):
+        return True
+    built = os.path.getmtime(LIB_PATH)
+    inc = os.path.join(os.path.dirname(PKG_DIR), "include")
+    for d in (CSRC, inc):
+        for f in os.listdir(d):
+            if os.path.getmtime(os.path.join(d, f)) > built:
+                return True
+    return False
+
+
 def build(verbose=False):
     """Compile every CUDA source of the library into one shared object."""
     srcs = [os.path.join(CSRC, s) for s in SOURCES]

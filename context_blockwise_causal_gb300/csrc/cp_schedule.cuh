@@ -87,13 +87,30 @@ __host__ __device__ inline int snake_unit(int round, int bid, int grid) {
   return (round & 1) ? round * grid + (grid - 1 - bid) : round * grid + bid;
 }
 
-// Walks a unit's key tiles in CP-step order.
+// Walks a unit's key tiles in CP-step order (all steps, or one step only).
 struct KvWalk {
   int cp, r, half, k, u, tpc, causal;
   int step, seg, v;
+  int last;  // last step walked
 
   __host__ __device__ KvWalk(const CpGeom& g, const FwdUnit& U)
-      : cp(g.cp), r(U.r), half(U.half), k(U.k), u(U.u), tpc(g.tpc), causal(g.causal), step(0), seg(0), v(0) {}
+      : cp(g.cp), r(U.r), half(U.half), k(U.k), u(U.u), tpc(g.tpc), causal(g.causal), step(0), seg(0), v(0),
+        last(g.cp - 1) {}
+
+  // Restrict the walk to the key tiles of CP step `st`.
+  __host__ __device__ void only_step(int st) {
+    step = st;
+    last = st;
+    seg = 0;
+    v = 0;
+  }
+
+  // Number of key tiles the unit visits at CP step `st`.
+  __host__ __device__ int step_tiles(int st) const {
+    int n = 0, ch, nt, dg;
+    for (int sg = 0; segment(st, sg, ch, nt, dg); ++sg) n += nt;
+    return n;
+  }
 
   // Segment `sg` of step `st`: a run of tiles [0, ntiles) of chunk `chunk`;
   // `diag` is the masked tile index in it, or -1.
@@ -145,7 +162,7 @@ struct KvWalk {
   }
 
   __host__ __device__ bool next(int& chunk, int& tile, bool& is_diag) {
-    while (step < cp) {
+    while (step <= last) {
       int ch, nt, dg;
       if (segment(step, seg, ch, nt, dg)) {
         if (v < nt) {

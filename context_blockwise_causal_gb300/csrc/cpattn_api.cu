@@ -11,6 +11,7 @@
 #include "../../include/cpattn.h"
 #include "bwd_kernel.cuh"
 #include "fwd_kernel.cuh"
+#include "merge_kernel.cuh"
 #include "tmap.h"
 
 namespace cpattn {
@@ -33,7 +34,7 @@ struct DeviceInfo {
   bool sm103 = false;
   int num_sms = 0;
   unsigned int* status = nullptr;
-  bool fwd_attr[2] = {false, false};
+  bool fwd_attr[4] = {false, false, false, false};  // [d == 128][step form]
   bool bwd_attr[2] = {false, false};
 };
 DeviceInfo g_devs[kMaxDevices];
@@ -90,26 +91,26 @@ CpGeom make_geom(int b, int s, int hq, int hkv, int cp, int causal) {
   return g;
 }
 
-template <int D>
+template <int D, bool kStep>
 int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& args,
                DeviceInfo* di, cudaStream_t st) {
   using C = FwdCfg<D>;
-  const int slot = D == 128 ? 1 : 0;
+  const int slot = (D == 128 ? 2 : 0) + (kStep ? 1 : 0);
   if (!di->fwd_attr[slot]) {
-    if (cudaFuncSetAttribute(cpattn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(cpattn_fwd_kernel<D, kStep>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes) != cudaSuccess)
       return CPATTN_ERR_CUDA;
     // The in-kernel register split assumes exactly kFwdLaunchRegs registers
     // per thread at launch; with fewer, the growing warpgroups would wait
     // for registers that never come free.
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, cpattn_fwd_kernel<D>) != cudaSuccess) return CPATTN_ERR_CUDA;
+    if (cudaFuncGetAttributes(&fa, cpattn_fwd_kernel<D, kStep>) != cudaSuccess) return CPATTN_ERR_CUDA;
     if (fa.numRegs != kFwdLaunchRegs) return CPATTN_ERR_LAUNCH_FAILED;
     di->fwd_attr[slot] = true;
   }
   const int units = fwd_num_units(args.g);
   const int grid = units < di->num_sms ? units : di->num_sms;
-  cpattn_fwd_kernel<D><<<grid, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, args);
+  cpattn_fwd_kernel<D, kStep><<<grid, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, args);
   return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_LAUNCH_FAILED;
 }
 
@@ -136,10 +137,128 @@ extern "C" int cpattn_fwd(const void* q, const void* k, const void* v, void* o, 
   args.g = make_geom(b, s, hq, hkv, cp, causal);
   args.o = static_cast<__nv_bfloat16*>(o);
   args.lse = lse;
+  args.o_part = nullptr;
+  args.step = -1;
   args.scale_log2 = float(1.4426950408889634 / std::sqrt(double(d)));
   args.status = di->status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return d == 128 ? launch_fwd<128>(tq, tk, tv, args, di, st) : launch_fwd<64>(tq, tk, tv, args, di, st);
+  return d == 128 ? launch_fwd<128, false>(tq, tk, tv, args, di, st) : launch_fwd<64, false>(tq, tk, tv, args, di, st);
+}
+
+extern "C" int cpattn_fwd_step(const void* q, const void* k, const void* v, float* o_part, float* lse_part, int b,
+                               int s, int hq, int hkv, int d, int cp, int step, int causal, void* stream) {
+  if (!q || !k || !v || !o_part || !lse_part) return CPATTN_ERR_NULL_PTR;
+  int rc = check_geometry(b, s, hq, hkv, d, cp);
+  if (rc) return rc;
+  if (step < 0 || step >= cp) return CPATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_part) || !aligned16(lse_part))
+    return CPATTN_ERR_MISALIGNED;
+  DeviceInfo* di = nullptr;
+  if ((rc = device_info(&di))) return rc;
+  CUtensorMap tq, tk, tv;
+  const uint64_t rows = uint64_t(b) * s;
+  if (!encode_bf16_rows_heads_d(&tq, q, rows, hq, d, kTile) || !encode_bf16_rows_heads_d(&tk, k, rows, hkv, d, kTile) ||
+      !encode_bf16_rows_heads_d(&tv, v, rows, hkv, d, kTile))
+    return CPATTN_ERR_CUDA;
+  FwdArgs args;
+  args.g = make_geom(b, s, hq, hkv, cp, causal);
+  args.o = nullptr;
+  args.lse = lse_part;
+  args.o_part = o_part;
+  args.step = step;
+  args.scale_log2 = float(1.4426950408889634 / std::sqrt(double(d)));
+  args.status = di->status;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return d == 128 ? launch_fwd<128, true>(tq, tk, tv, args, di, st) : launch_fwd<64, true>(tq, tk, tv, args, di, st);
+}
+
+extern "C" int cpattn_lse_merge(const float* o_a, const float* lse_a, const float* o_b, const float* lse_b,
+                                float* o_out, float* lse_out, void* o_bf16, int b, int s, int hq, int d,
+                                void* stream) {
+  if (!o_a || !lse_a || !lse_out || (!o_out && !o_bf16) || (!o_b) != (!lse_b)) return CPATTN_ERR_NULL_PTR;
+  if (b < 1 || s < 1 || hq < 1 || (d != 64 && d != 128)) return CPATTN_ERR_INVALID_ARG;
+  if (int64_t(b) * s * hq >= (int64_t(1) << 31)) return CPATTN_ERR_INVALID_ARG;
+  if (!aligned16(o_a) || (o_b && !aligned16(o_b)) || (o_out && !aligned16(o_out)) || (o_bf16 && !aligned16(o_bf16)) ||
+      (reinterpret_cast<uintptr_t>(lse_a) & 3u) || (lse_b && (reinterpret_cast<uintptr_t>(lse_b) & 3u)) ||
+      (reinterpret_cast<uintptr_t>(lse_out) & 3u))
+    return CPATTN_ERR_MISALIGNED;
+  DeviceInfo* di = nullptr;
+  int rc = device_info(&di);
+  if (rc) return rc;
+  MergeArgs m;
+  m.b = b;
+  m.s = s;
+  m.hq = hq;
+  m.o_a = o_a;
+  m.lse_a = lse_a;
+  m.o_b = o_b;
+  m.lse_b = lse_b;
+  m.o_out = o_out;
+  m.lse_out = lse_out;
+  m.o_bf16 = static_cast<__nv_bfloat16*>(o_bf16);
+  const int64_t threads = int64_t(b) * s * hq * (d / 4);
+  int64_t blocks = (threads + 255) / 256;
+  const int64_t cap = int64_t(di->num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (d == 128)
+    cpattn_lse_merge_kernel<128><<<int(blocks), 256, 0, st>>>(m);
+  else
+    cpattn_lse_merge_kernel<64><<<int(blocks), 256, 0, st>>>(m);
+  return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_LAUNCH_FAILED;
+}
+
+namespace cpattn {
+namespace {
+struct UnfusedLayout {
+  size_t o_acc, lse_acc, o_part, lse_part, total;
+};
+UnfusedLayout unfused_layout(int b, int s, int hq, int d) {
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t ob = size_t(b) * s * hq * d * 4, lb = size_t(b) * hq * s * 4;
+  UnfusedLayout L;
+  L.o_acc = 0;
+  L.lse_acc = al(ob);
+  L.o_part = L.lse_acc + al(lb);
+  L.lse_part = L.o_part + al(ob);
+  L.total = L.lse_part + al(lb);
+  return L;
+}
+}  // namespace
+}  // namespace cpattn
+
+extern "C" size_t cpattn_fwd_unfused_workspace_bytes(int b, int s, int hq, int d) {
+  if (b < 1 || s < 1 || hq < 1 || (d != 64 && d != 128)) return 0;
+  return unfused_layout(b, s, hq, d).total;
+}
+
+extern "C" int cpattn_fwd_unfused(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
+                                  size_t ws_bytes, int b, int s, int hq, int hkv, int d, int cp, int causal,
+                                  void* stream) {
+  if (!q || !k || !v || !o || !lse || !workspace) return CPATTN_ERR_NULL_PTR;
+  int rc = check_geometry(b, s, hq, hkv, d, cp);
+  if (rc) return rc;
+  const UnfusedLayout L = unfused_layout(b, s, hq, d);
+  if (ws_bytes < L.total) return CPATTN_ERR_WORKSPACE_TOO_SMALL;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || !aligned16(o) || !aligned16(lse))
+    return CPATTN_ERR_MISALIGNED;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* o_acc = reinterpret_cast<float*>(ws + L.o_acc);
+  float* lse_acc = reinterpret_cast<float*>(ws + L.lse_acc);
+  float* o_part = reinterpret_cast<float*>(ws + L.o_part);
+  float* lse_part = reinterpret_cast<float*>(ws + L.lse_part);
+  // step 0 into the accumulator, then each later step merged into it; the
+  // last merge writes the bf16 output and the final LSE
+  if ((rc = cpattn_fwd_step(q, k, v, o_acc, lse_acc, b, s, hq, hkv, d, cp, 0, causal, stream))) return rc;
+  if (cp == 1) return cpattn_lse_merge(o_acc, lse_acc, nullptr, nullptr, nullptr, lse, o, b, s, hq, d, stream);
+  for (int i = 1; i < cp; ++i) {
+    if ((rc = cpattn_fwd_step(q, k, v, o_part, lse_part, b, s, hq, hkv, d, cp, i, causal, stream))) return rc;
+    const bool last = i == cp - 1;
+    if ((rc = cpattn_lse_merge(o_acc, lse_acc, o_part, lse_part, last ? nullptr : o_acc, last ? lse : lse_acc,
+                               last ? o : nullptr, b, s, hq, d, stream)))
+      return rc;
+  }
+  return CPATTN_OK;
 }
 
 namespace cpattn {

@@ -52,8 +52,10 @@ constexpr float kRescaleThreshold = 0.0f;  // log2 units
 
 struct FwdArgs {
   CpGeom g;
-  __nv_bfloat16* o;
-  float* lse;
+  __nv_bfloat16* o;  // fused form: normalised output, bf16
+  float* lse;        // natural-log LSE [b, hq, s] (of the step, in step form)
+  float* o_part;     // step form: the step's normalised partial output, fp32
+  int step;          // step form: the CP step computed
   float scale_log2;  // log2(e) / sqrt(d)
   unsigned int* status;
 };
@@ -80,7 +82,12 @@ enum FwdStatusBits : unsigned int {
   kStatusSoftmax = 1u << 2,
 };
 
-template <int D>
+// kStep = false: the fused forward (all CP steps, merged on chip, bf16 O).
+// kStep = true: one CP step `a.step` for every rank, unmerged: each query
+// row's softmax over that step's keys only, written as an fp32 partial O and
+// its LSE ("大模型面试宝典 · Megatron-LM 篇", 3.2 step 4, before correction);
+// rows that take no part in the step get O = 0, L = -inf.
+template <int D, bool kStep>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     cpattn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv, const FwdArgs a) {
@@ -151,6 +158,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int idx = snake_unit(rd, blockIdx.x, grid);
         if (idx >= num_units) break;
         const FwdUnit U = fwd_decode_unit(g, idx);
+        KvWalk w(g, U);
+        if constexpr (kStep) {
+          w.only_step(a.step);
+          if (w.step_tiles(a.step) == 0) continue;  // no key tile at this step
+        }
         if (ul > 0) {
           ok = mbar_wait_bounded(&q_empty[0], (ul - 1) & 1, abort_flag, kWaitLimitNs) &&
                mbar_wait_bounded(&q_empty[1], (ul - 1) & 1, abort_flag, kWaitLimitNs);
@@ -164,7 +176,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             tma_load_3d(sQ + sub * C::kQBytes + (x / 64) * (kTile * 128), &tmq, &q_full[sub], x, h, qrow);
         }
         const bool shared_kv = U.g0 == U.g1;
-        KvWalk w(g, U);
         int chunk, tile;
         bool dg;
         auto load = [&](const CUtensorMap* map, int head, int row) -> bool {
@@ -235,7 +246,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (idx >= num_units) break;
         const FwdUnit U = fwd_decode_unit(g, idx);
         const bool shared_kv = U.g0 == U.g1;
-        const int n = U.n;
+        const int n = kStep ? KvWalk(g, U).step_tiles(a.step) : U.n;
+        if (kStep && n == 0) continue;
         ok = mbar_wait_warp(&q_full[0], ul & 1, abort_flag, kWaitLimitNs) &&
              mbar_wait_warp(&q_full[1], ul & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
@@ -324,9 +336,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (idx >= num_units) break;
       const FwdUnit U = fwd_decode_unit(g, idx);
       KvWalk w(g, U);
+      int n = U.n;
+      if constexpr (kStep) {
+        w.only_step(a.step);
+        n = w.step_tiles(a.step);
+        if (n == 0) {
+          // the unit's rows take no part in this step: O = 0, L = -inf
+          if (row < U.q_valid && (sub == 0 || U.store1)) {
+            const int h = sub ? U.h1 : U.h0;
+            const int t = U.q_t0 + row;
+            float4* dst = reinterpret_cast<float4*>(a.o_part + ((int64_t(U.bi) * g.s + t) * g.hq + h) * D);
+#pragma unroll
+            for (int c0 = 0; c0 < D / 4; ++c0) dst[c0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            a.lse[(int64_t(U.bi) * g.hq + h) * g.s + t] = -INFINITY;
+          }
+          continue;
+        }
+      }
       float m_used = -INFINITY;
       float l = 0.f;
-      for (int j = 0; j < U.n; ++j) {
+      for (int j = 0; j < n; ++j) {
         int chunk = 0, tile = 0;
         bool dg = false;
         w.next(chunk, tile, dg);
@@ -433,7 +462,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_empty[sub]);
       const bool store = row < U.q_valid && (sub == 0 || U.store1);
-      if (store) {
+      if (kStep && store) {
+        const int h = sub ? U.h1 : U.h0;
+        const int t = U.q_t0 + row;
+        const float inv = 1.f / l;
+        float4* dst = reinterpret_cast<float4*>(a.o_part + ((int64_t(U.bi) * g.s + t) * g.hq + h) * D);
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 4)
+          dst[c0 / 4] = make_float4(__uint_as_float(ov[c0]) * inv, __uint_as_float(ov[c0 + 1]) * inv,
+                                    __uint_as_float(ov[c0 + 2]) * inv, __uint_as_float(ov[c0 + 3]) * inv);
+        a.lse[(int64_t(U.bi) * g.hq + h) * g.s + t] = (m_used + log2f(l)) * 0.69314718055994530942f;
+      } else if (store) {
         const int h = sub ? U.h1 : U.h0;
         const int t = U.q_t0 + row;
         const float inv = 1.f / l;

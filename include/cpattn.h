@@ -76,6 +76,60 @@ int cpattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                int d, int cp, int causal, void* stream);
 
 /*
+ * The same forward in the unfused form the pages describe: one launch per CP
+ * step, each writing every rank's partial result to device memory, and a
+ * log-sum-exp correction after every step ("大模型面试宝典 · Megatron-LM 篇",
+ * 3.2 steps 4-5; the two-stage L / O correction of "Megatron 面试题（一）",
+ * item M019). Same inputs, outputs and result as cpattn_fwd (up to rounding
+ * order); it exists to run the steps one by one (e.g. to overlap them with a
+ * KV exchange) and as the baseline against which the fused form is measured.
+ * Calls cpattn_fwd_step cp times and cpattn_lse_merge max(cp-1, 1) times.
+ *   workspace: device, 256-byte aligned, at least
+ *              cpattn_fwd_unfused_workspace_bytes(b, s, hq, d) bytes (two fp32
+ *              copies of O and of the LSE); contents need not be initialised
+ *              and are overwritten. Errors as cpattn_fwd, plus
+ *              CPATTN_ERR_WORKSPACE_TOO_SMALL; workspace misaligned ->
+ *              CPATTN_ERR_MISALIGNED.
+ */
+size_t cpattn_fwd_unfused_workspace_bytes(int b, int s, int hq, int d);
+int cpattn_fwd_unfused(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
+                       size_t ws_bytes, int b, int s, int hq, int hkv, int d, int cp, int causal, void* stream);
+
+/*
+ * One CP step for every virtual rank, unmerged ("大模型面试宝典 · Megatron-LM
+ * 篇", 3.2 steps 2-4, 3.4): at step `step` (0 <= step < cp) rank r computes
+ * its block against the KV of rank (r - step) mod cp with the step's mask,
+ * each query row taking the softmax over that block's keys only.
+ *   o_part:   [b, s, hq, d] fp32: the block's normalised output for each query
+ *             row that takes part in the step, 0 for the other rows.
+ *   lse_part: [b, hq, s] fp32, natural log: the block's log-sum-exp, -inf for
+ *             rows that take no part.
+ * Merging the cp steps' results with cpattn_lse_merge gives cpattn_fwd's
+ * result. Errors as cpattn_fwd; step outside [0, cp) -> CPATTN_ERR_INVALID_ARG.
+ */
+int cpattn_fwd_step(const void* q, const void* k, const void* v, float* o_part, float* lse_part, int b, int s,
+                    int hq, int hkv, int d, int cp, int step, int causal, void* stream);
+
+/*
+ * Log-sum-exp merge of two partial results over disjoint key sets, row by
+ * row (the correction of "大模型面试宝典 · Megatron-LM 篇", 3.2 steps 4-5):
+ *   L = log(e^{L_a} + e^{L_b}),  O = e^{L_a - L} O_a + e^{L_b - L} O_b;
+ * rows with L_a = L_b = -inf give L = -inf, O = 0.
+ *   o_a, o_b:     [b, s, hq, d] fp32; lse_a, lse_b: [b, hq, s] fp32 natural log.
+ *                 o_b and lse_b may both be NULL (no second part: O_a, L_a are
+ *                 passed through, e.g. to convert to bf16).
+ *   o_out:        [b, s, hq, d] fp32 merged O, may alias o_a; may be NULL.
+ *   lse_out:      [b, hq, s] fp32 merged L, may alias lse_a.
+ *   o_bf16:       optional [b, s, hq, d] bf16 copy of the merged O (NULL = none);
+ *                 o_out and o_bf16 may not both be NULL.
+ * d in {64, 128}. The fp32/bf16 O pointers must be 16-byte aligned, the LSE
+ * pointers 4-byte aligned. Errors: NULL_PTR, INVALID_ARG, MISALIGNED,
+ * UNSUPPORTED_ARCH, LAUNCH_FAILED.
+ */
+int cpattn_lse_merge(const float* o_a, const float* lse_a, const float* o_b, const float* lse_b, float* o_out,
+                     float* lse_out, void* o_bf16, int b, int s, int hq, int d, void* stream);
+
+/*
  * Bytes of caller-provided device workspace cpattn_bwd needs for these sizes
  * (two fp32 vectors per query row and head: lse * log2(e) and
  * D = rowsum(dO * O), in 128-row tile order). Returns 0 for unsupported sizes.

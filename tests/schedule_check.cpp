@@ -61,6 +61,25 @@ static int check(int b, int s, int hq, int hkv, int cp, int causal, int grid) {
       }
     }
     if (nt != U.n) { printf("unit %d: walk has %d tiles, n = %d\n", idx, nt, U.n); return 1; }
+    // the single-step walks, step after step, give the same tiles in order
+    KvWalk full(g, U);
+    int tot = 0;
+    for (int st = 0; st < cp; ++st) {
+      KvWalk one(g, U);
+      one.only_step(st);
+      int c1, t1, c2, t2, ns = 0;
+      bool d1, d2;
+      while (one.next(c1, t1, d1)) {
+        ++ns;
+        if (!full.next(c2, t2, d2) || c1 != c2 || t1 != t2 || d1 != d2) {
+          printf("unit %d: step %d walk differs from the full walk\n", idx, st);
+          return 1;
+        }
+      }
+      if (ns != one.step_tiles(st)) { printf("unit %d: step %d has %d tiles, step_tiles %d\n", idx, st, ns, one.step_tiles(st)); return 1; }
+      tot += ns;
+    }
+    if (tot != U.n) { printf("unit %d: steps sum to %d tiles, n = %d\n", idx, tot, U.n); return 1; }
   }
   if (verify(g, count, "forward")) return 1;
   // backward: key-tile units walking the query tiles that see them

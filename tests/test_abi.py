@@ -18,7 +18,9 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def lib():
     import context_blockwise_causal_gb300 as pkg
 
-    if not os.path.exists(pkg.LIB_PATH):
+    from context_blockwise_causal_gb300._build import is_stale
+
+    if is_stale():
         pkg.build()
     return pkg.library()
 
@@ -91,3 +93,26 @@ def test_bwd_argument_errors_and_workspace_size(lib):
     assert b(p, p, p, p, p, p, p, p, p, p, n - 1, 1, 512, 4, 2, 64, 2, 1, None) == -5
     assert b(p, p, p, p, p, p, p, p, p, None, n, 1, 512, 4, 2, 64, 2, 1, None) == -2
     assert b(p, p, p, p, p, p, p, p, p, p, n, 1, 512, 4, 3, 64, 2, 1, None) == -1
+
+
+def test_unfused_argument_errors_and_workspace_size(lib):
+    # two fp32 copies of O and of the LSE, each rounded up to 256 bytes
+    o_bytes, l_bytes = 1 * 512 * 4 * 64 * 4, 1 * 4 * 512 * 4
+    assert lib.cpattn_fwd_unfused_workspace_bytes(1, 512, 4, 64) == 2 * o_bytes + 2 * l_bytes
+    assert lib.cpattn_fwd_unfused_workspace_bytes(1, 512, 4, 96) == 0
+    n = lib.cpattn_fwd_unfused_workspace_bytes(1, 512, 4, 64)
+    p = ctypes.c_void_p(4096)
+    u = lib.cpattn_fwd_unfused
+    assert u(p, p, p, p, p, p, n - 1, 1, 512, 4, 4, 64, 2, 1, None) == -5
+    assert u(p, p, p, p, p, None, n, 1, 512, 4, 4, 64, 2, 1, None) == -2
+    assert u(p, p, p, p, p, ctypes.c_void_p(4096 + 16), n, 1, 512, 4, 4, 64, 2, 1, None) == -3
+    assert u(p, p, p, p, p, p, n, 1, 512, 4, 3, 64, 2, 1, None) == -1
+    st = lib.cpattn_fwd_step
+    assert st(p, p, p, p, p, 1, 512, 4, 4, 64, 2, 2, 1, None) == -1   # step >= cp
+    assert st(p, p, p, p, p, 1, 512, 4, 4, 64, 2, -1, 1, None) == -1
+    assert st(p, p, p, None, p, 1, 512, 4, 4, 64, 2, 0, 1, None) == -2
+    m = lib.cpattn_lse_merge
+    assert m(p, p, p, None, p, p, None, 1, 512, 4, 64, None) == -2   # o_b without lse_b
+    assert m(p, p, None, None, None, p, None, 1, 512, 4, 64, None) == -2  # no output
+    assert m(p, p, None, None, p, p, None, 1, 512, 4, 96, None) == -1
+    assert m(ctypes.c_void_p(4096 + 4), p, None, None, p, p, None, 1, 512, 4, 64, None) == -3

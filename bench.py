@@ -92,7 +92,7 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, smax, reasons = [], None, set()
+        sm, smax, reasons, masks = [], None, set(), set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
@@ -103,6 +103,7 @@ class ClockSampler:
                 smax = float(f[2])
             except ValueError:
                 continue
+            masks.add(f[4])
             for nm, v in zip(names, f[5:9]):
                 if v.lower() == "active":
                     reasons.add(nm)
@@ -110,7 +111,7 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         loaded = [x for x in sm if smax is None or x > 0.3 * smax] or sm
         return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "active_reason_masks": sorted(masks), "samples": len(sm)}
 
 
 def _profile_traffic(kernel_file, profile_name):
@@ -291,6 +292,32 @@ def run_ours(args, w):
         dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
     e2e_ms = e2e_ms.item()
 
+    # ---- the unfused forward (cp step launches + cp-1 merges), outside the
+    # timed step: the baseline the fused forward is measured against
+    unfused = None
+    if not args.no_unfused:
+        from context_blockwise_causal_gb300 import cpattn_fwd_unfused, cpattn_fwd_unfused_workspace_bytes
+
+        uws = torch.empty(cpattn_fwd_unfused_workspace_bytes(w.b, w.s, w.hq, w.d), dtype=torch.uint8, device=dev)
+        o_u = torch.empty_like(q)
+        lse_u = torch.empty_like(lse)
+        for _ in range(2):
+            cpattn_fwd_unfused(q, k, v, w.cp, causal=w.causal, o=o_u, lse=lse_u, workspace=uws, stream=stream)
+        barrier()
+        u0, u1 = ev(), ev()
+        u0.record(stream)
+        for _ in range(args.steps):
+            cpattn_fwd_unfused(q, k, v, w.cp, causal=w.causal, o=o_u, lse=lse_u, workspace=uws, stream=stream)
+        u1.record(stream)
+        barrier()
+        if cpattn_device_status(stream) != 0:
+            raise RuntimeError("a kernel reported a timeout in the unfused forward")
+        u_ms = u0.elapsed_time(u1) / args.steps
+        unfused = {"ms": u_ms, "tflops": w.fwd_flops() / (u_ms * 1e-3) / 1e12,
+                   "launches_per_call": 2 * w.cp - 1 if w.cp > 1 else 2,
+                   "fused_fwd_ms": kern_ms["fwd"], "unfused_over_fused": u_ms / kern_ms["fwd"]}
+        del uws
+
     if rank == 0:
         peaks = _peaks()
         step_flops = w.fwd_flops() + w.bwd_flops()
@@ -334,6 +361,8 @@ def run_ours(args, w):
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),
         }
+        if unfused is not None:
+            line["unfused_fwd"] = unfused
         if not args.no_cpu_baseline:
             dt, fl = _oracle_sample(w, args.ref_rows, seed=w.seed + 5)
             line["cpu_baseline"] = {
@@ -348,12 +377,13 @@ def run_ours(args, w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--ref-rows", type=int, default=1024)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-unfused", action="store_true", help="skip timing the unfused forward")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

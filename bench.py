@@ -313,10 +313,32 @@ def run_ours(args, w):
         if cpattn_device_status(stream) != 0:
             raise RuntimeError("a kernel reported a timeout in the unfused forward")
         u_ms = u0.elapsed_time(u1) / args.steps
+        # one merge on its own (HBM-bound): read two fp32 O and LSE, write one
+        from context_blockwise_causal_gb300 import cpattn_lse_merge
+
+        nb = w.b * w.s * w.hq * w.d * 4
+        o_a = uws[:nb].view(torch.float32).view(w.b, w.s, w.hq, w.d)
+        o_b = uws[nb:2 * nb].view(torch.float32).view(w.b, w.s, w.hq, w.d)
+        o_a.zero_()
+        o_b.zero_()
+        l_a = torch.zeros_like(lse)
+        l_b = torch.zeros_like(lse)
+        cpattn_lse_merge(o_a, l_a, o_b, l_b, o_out=o_a, lse_out=l_a, stream=stream)
+        barrier()
+        m0, m1 = ev(), ev()
+        m0.record(stream)
+        for _ in range(args.steps):
+            cpattn_lse_merge(o_a, l_a, o_b, l_b, o_out=o_a, lse_out=l_a, stream=stream)
+        m1.record(stream)
+        barrier()
+        m_ms = m0.elapsed_time(m1) / args.steps
+        m_bytes = 3 * nb + 3 * lse.numel() * 4
         unfused = {"ms": u_ms, "tflops": w.fwd_flops() / (u_ms * 1e-3) / 1e12,
                    "launches_per_call": 2 * w.cp - 1 if w.cp > 1 else 2,
-                   "fused_fwd_ms": kern_ms["fwd"], "unfused_over_fused": u_ms / kern_ms["fwd"]}
-        del uws
+                   "fused_fwd_ms": kern_ms["fwd"], "unfused_over_fused": u_ms / kern_ms["fwd"],
+                   "merge": {"ms": m_ms, "bytes": m_bytes, "gbs": m_bytes / (m_ms * 1e-3) / 1e9,
+                             "hbm_frac": m_bytes / (m_ms * 1e-3) / 1e9 / _peaks()["hbm_gbs"]}}
+        del uws, o_a, o_b
 
     if rank == 0:
         peaks = _peaks()

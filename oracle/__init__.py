@@ -37,3 +37,4 @@ from .context_parallel import (  # noqa: F401
     cp_step_partials,
     cp_attention_forward,
 )
+from .rope import rope_angles, rope_apply, natural_positions, rank_local_positions  # noqa: F401

@@ -325,3 +325,57 @@ def test_step_partials_structure():
             # chunk 0 (rank 0's first chunk) sees exactly keys 0..t at step 0
             assert torch.allclose(o_i[0, :c], o_ref[0, :c], atol=1e-12)
             assert torch.allclose(l_i[0, :, :c], l_ref[0, :, :c], atol=1e-12)
+
+
+# ---------------------------------------------------------------- RoPE
+def test_rope_hand_values():
+    # d = 2, base irrelevant for i = 0: a plain rotation by pos radians
+    x = torch.tensor([[[[1.0, 0.0]], [[1.0, 0.0]], [[0.0, 2.0]]]], dtype=F64)  # [1, 3, 1, 2]
+    out = oracle.rope_apply(x, torch.tensor([0, 1, 3]))
+    assert torch.allclose(out[0, 0, 0], torch.tensor([1.0, 0.0], dtype=F64), atol=0)
+    assert torch.allclose(out[0, 1, 0], torch.tensor([math.cos(1.0), math.sin(1.0)], dtype=F64), atol=1e-15)
+    assert torch.allclose(out[0, 2, 0], torch.tensor([-2 * math.sin(3.0), 2 * math.cos(3.0)], dtype=F64), atol=1e-15)
+    # d = 4: the second pair turns base^(-1/2) as fast
+    th = oracle.rope_angles(torch.tensor([5]), 4, base=100.0)
+    assert abs(th[0, 0] - 5.0) < 1e-15 and abs(th[0, 1] - 0.5) < 1e-15
+
+
+def test_rope_relative_phase_and_inverse():
+    g = torch.Generator().manual_seed(3)
+    d = 16
+    q, k = torch.randn(1, 1, 1, d, generator=g, dtype=F64), torch.randn(1, 1, 1, d, generator=g, dtype=F64)
+    dots = []
+    for m, n in ((7, 3), (104, 100), (4, 0)):  # m - n = 4 each time
+        qm = oracle.rope_apply(q, torch.tensor([m]))
+        kn = oracle.rope_apply(k, torch.tensor([n]))
+        dots.append(float((qm * kn).sum()))
+    assert max(dots) - min(dots) < 1e-12
+    x = torch.randn(2, 5, 3, d, generator=g, dtype=F64)
+    pos = torch.tensor([0, 9, 33, 1000, 131071])
+    y = oracle.rope_apply(x, pos)
+    # pair norms are kept, the inverse undoes the rotation
+    assert torch.allclose(y[..., :d // 2] ** 2 + y[..., d // 2:] ** 2, x[..., :d // 2] ** 2 + x[..., d // 2:] ** 2,
+                          atol=1e-12)
+    assert torch.allclose(oracle.rope_apply(y, pos, inverse=True), x, atol=1e-12)
+
+
+def test_rope_positions_for_cp_shards_and_packing():
+    s, cp = 48, 3
+    c = s // (2 * cp)
+    # rank-local positions are the zigzag global positions, not 0..2c-1
+    for r in range(cp):
+        pos = oracle.rank_local_positions(s, cp, r)
+        assert pos.tolist() == list(range(r * c, (r + 1) * c)) + list(range((2 * cp - 1 - r) * c, (2 * cp - r) * c))
+    # packing: the position restarts at each sample
+    cu = [0, 10, 30, 48]
+    pos = oracle.natural_positions(s, cu)
+    assert pos.tolist() == list(range(10)) + list(range(20)) + list(range(18))
+    # rotating a rank's shard with its local positions = rotating the whole
+    # sequence and taking the shard
+    g = torch.Generator().manual_seed(4)
+    x = torch.randn(1, s, 2, 8, generator=g, dtype=F64)
+    full = oracle.rope_apply(x, oracle.natural_positions(s, cu))
+    for r in range(cp):
+        idx = oracle.zigzag_global_index(s, cp)[r]
+        shard = oracle.rope_apply(x[:, idx], oracle.rank_local_positions(s, cp, r, cu))
+        assert torch.allclose(shard, full[:, idx], atol=1e-15)

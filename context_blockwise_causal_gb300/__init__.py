@@ -21,6 +21,7 @@ __all__ = [
     "cpattn_lse_merge",
     "cpattn_fwd_unfused",
     "cpattn_fwd_unfused_workspace_bytes",
+    "cpattn_rope",
     "cpattn_bwd",
     "cpattn_bwd_workspace_bytes",
     "cpattn_zigzag_index",
@@ -69,6 +70,8 @@ def library():
         lib.cpattn_fwd_unfused_workspace_bytes.restype = _sz
         lib.cpattn_fwd_unfused.argtypes = [_p] * 6 + [_sz] + [_i] * 7 + [_p]
         lib.cpattn_fwd_unfused.restype = _i
+        lib.cpattn_rope.argtypes = [_p] + [_i] * 7 + [_p, _i, ctypes.c_float, _i, _p]
+        lib.cpattn_rope.restype = _i
         lib.cpattn_bwd.argtypes = [_p] * 10 + [_sz] + [_i] * 7 + [_p]
         lib.cpattn_bwd.restype = _i
         lib.cpattn_bwd_stage.argtypes = [_i] + [_p] * 10 + [_sz] + [_i] * 7 + [_p]
@@ -228,6 +231,31 @@ def cpattn_fwd_unfused(q, k, v, cp, causal=True, o=None, lse=None, workspace=Non
     if rc:
         raise CpattnError(rc, "cpattn_fwd_unfused")
     return o, lse
+
+
+def cpattn_rope(x, base=10000.0, cp=1, rank=None, s=None, cu_seqlens=None, inverse=False, stream=None):
+    """Rotary position embedding of x [b, n, h, d] bf16, in place; returns x.
+
+    rank None: natural order (position = token index). rank r: x is virtual
+    rank r's zigzag shard of a sequence of s tokens (n = s / cp).
+    cu_seqlens: optional int32 CUDA tensor of packed-sample offsets (b == 1).
+    """
+    _check_act("x", x)
+    if x.dim() != 4:
+        raise ValueError("x must be [b, n, h, d]")
+    b, n, h, d = x.shape
+    if s is None:
+        s = n if rank is None else n * cp
+    cu_ptr, nseq = None, 0
+    if cu_seqlens is not None:
+        if not cu_seqlens.is_cuda or cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_contiguous():
+            raise TypeError("cu_seqlens must be a contiguous int32 CUDA tensor")
+        cu_ptr, nseq = cu_seqlens.data_ptr(), cu_seqlens.numel() - 1
+    rc = library().cpattn_rope(x.data_ptr(), b, n, h, d, int(s), int(cp), -1 if rank is None else int(rank), cu_ptr,
+                               nseq, float(base), 1 if inverse else 0, _stream_handle(stream))
+    if rc:
+        raise CpattnError(rc, "cpattn_rope")
+    return x
 
 
 def cpattn_bwd_workspace_bytes(b, s, hq, hkv, d, cp):

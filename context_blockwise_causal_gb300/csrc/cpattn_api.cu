@@ -12,6 +12,7 @@
 #include "bwd_kernel.cuh"
 #include "fwd_kernel.cuh"
 #include "merge_kernel.cuh"
+#include "rope_kernel.cuh"
 #include "tmap.h"
 
 namespace cpattn {
@@ -205,6 +206,48 @@ extern "C" int cpattn_lse_merge(const float* o_a, const float* lse_a, const floa
     cpattn_lse_merge_kernel<128><<<int(blocks), 256, 0, st>>>(m);
   else
     cpattn_lse_merge_kernel<64><<<int(blocks), 256, 0, st>>>(m);
+  return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_LAUNCH_FAILED;
+}
+
+extern "C" int cpattn_rope(void* x, int b, int n, int h, int d, int s, int cp, int rank, const int* cu_seqlens,
+                           int nseq, float base, int inverse, void* stream) {
+  if (!x) return CPATTN_ERR_NULL_PTR;
+  if (b < 1 || n < 1 || h < 1 || s < 1 || cp < 1 || (d != 64 && d != 128) || !(base > 1.0f))
+    return CPATTN_ERR_INVALID_ARG;
+  if (rank < 0) {
+    if (n != s) return CPATTN_ERR_INVALID_ARG;
+  } else {
+    if (rank >= cp || s % (2 * cp) != 0 || n != s / cp) return CPATTN_ERR_INVALID_ARG;
+  }
+  if (cu_seqlens && (b != 1 || nseq < 1)) return CPATTN_ERR_INVALID_ARG;
+  if (int64_t(b) * n * h * d >= (int64_t(1) << 40)) return CPATTN_ERR_INVALID_ARG;
+  if (!aligned16(x) || (cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u))) return CPATTN_ERR_MISALIGNED;
+  DeviceInfo* di = nullptr;
+  int rc = device_info(&di);
+  if (rc) return rc;
+  RopeArgs a;
+  a.x = static_cast<__nv_bfloat16*>(x);
+  a.b = b;
+  a.n = n;
+  a.h = h;
+  a.s = s;
+  a.cp = cp;
+  a.rank = rank < 0 ? -1 : rank;
+  a.cu_seqlens = cu_seqlens;
+  a.nseq = cu_seqlens ? nseq : 0;
+  a.inverse = inverse ? 1 : 0;
+  const double two_pi = 6.283185307179586476925;
+  for (int i = 0; i < kRopeMaxHalf; ++i)
+    a.turns_per_pos[i] = i < d / 2 ? std::pow(double(base), -2.0 * i / d) / two_pi : 0.0;
+  const int64_t threads = int64_t(b) * n * (d / 4);
+  int64_t blocks = (threads + 255) / 256;
+  const int64_t cap = int64_t(di->num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (d == 128)
+    cpattn_rope_kernel<128><<<int(blocks), 256, 0, st>>>(a);
+  else
+    cpattn_rope_kernel<64><<<int(blocks), 256, 0, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_LAUNCH_FAILED;
 }
 

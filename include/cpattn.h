@@ -130,6 +130,33 @@ int cpattn_lse_merge(const float* o_a, const float* lse_a, const float* o_b, con
                      float* lse_out, void* o_bf16, int b, int s, int hq, int d, void* stream);
 
 /*
+ * Rotary position embedding, in place, with the positions context
+ * parallelism needs ("Megatron 面试题（一）：模型抽象与训练数据流", item M016):
+ * each token turns by its position in the full sequence, not by its index in
+ * a rank's shard, and packed samples restart the position at their start.
+ * Pair (x_i, x_{i+d/2}), i < d/2, turns by theta = pos * base^(-2i/d):
+ *   x_i' = x_i cos(theta) - x_{i+d/2} sin(theta),
+ *   x_{i+d/2}' = x_i sin(theta) + x_{i+d/2} cos(theta).
+ *   x:          [b, n, h, d] bf16, rotated in place (q or k; h heads).
+ *   rank < 0:   natural token order, n == s, position of token t = t.
+ *   rank >= 0:  x is virtual rank `rank`'s zigzag shard (chunk rank, then
+ *               chunk 2cp-1-rank; n == s / cp, s divisible by 2cp): local
+ *               token u has the zigzag map's global position.
+ *   cu_seqlens: optional device int32 [nseq + 1] sample offsets in the full
+ *               sequence (0 = cu[0] < ... < cu[nseq] = s); requires b == 1;
+ *               the position becomes the token's offset within its sample.
+ *               NULL = one sample.
+ *   base:       frequency base (> 1), e.g. 10000.
+ *   inverse:    non-zero rotates by -theta (the gradient: dx = R^T dy).
+ * The angle is formed in fp64 and reduced to one turn before fp32 sin/cos,
+ * so long positions keep full accuracy. d in {64, 128}. Errors: NULL_PTR,
+ * INVALID_ARG, MISALIGNED (x not 16-byte aligned), UNSUPPORTED_ARCH,
+ * LAUNCH_FAILED.
+ */
+int cpattn_rope(void* x, int b, int n, int h, int d, int s, int cp, int rank, const int* cu_seqlens, int nseq,
+                float base, int inverse, void* stream);
+
+/*
  * Bytes of caller-provided device workspace cpattn_bwd needs for these sizes
  * (two fp32 vectors per query row and head: lse * log2(e) and
  * D = rowsum(dO * O), in 128-row tile order). Returns 0 for unsupported sizes.

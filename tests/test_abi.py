@@ -116,3 +116,16 @@ def test_unfused_argument_errors_and_workspace_size(lib):
     assert m(p, p, None, None, None, p, None, 1, 512, 4, 64, None) == -2  # no output
     assert m(p, p, None, None, p, p, None, 1, 512, 4, 96, None) == -1
     assert m(ctypes.c_void_p(4096 + 4), p, None, None, p, p, None, 1, 512, 4, 64, None) == -3
+
+
+def test_rope_argument_errors(lib):
+    p = ctypes.c_void_p(4096)
+    r = lib.cpattn_rope
+    assert r(None, 1, 512, 4, 64, 512, 2, -1, None, 0, 10000.0, 0, None) == -2
+    assert r(p, 1, 512, 4, 96, 512, 2, -1, None, 0, 10000.0, 0, None) == -1   # d
+    assert r(p, 1, 500, 4, 64, 512, 2, -1, None, 0, 10000.0, 0, None) == -1   # natural order: n == s
+    assert r(p, 1, 512, 4, 64, 512, 2, 0, None, 0, 10000.0, 0, None) == -1    # shard: n == s / cp
+    assert r(p, 1, 256, 4, 64, 512, 2, 2, None, 0, 10000.0, 0, None) == -1    # rank >= cp
+    assert r(p, 2, 512, 4, 64, 512, 2, -1, p, 3, 10000.0, 0, None) == -1      # packing needs b == 1
+    assert r(p, 1, 512, 4, 64, 512, 2, -1, None, 0, 1.0, 0, None) == -1      # base > 1
+    assert r(ctypes.c_void_p(4096 + 4), 1, 512, 4, 64, 512, 2, -1, None, 0, 10000.0, 0, None) == -3

@@ -59,8 +59,10 @@ def _scores(qrows, kk, t, causal, scale):
     return S
 
 
-def attention_forward(q, k, v, causal=True, rows=None, row_block=1024):
+def attention_forward(q, k, v, causal=True, rows=None, row_block=1024, scale=None):
     """O and LSE of softmax attention for the query positions ``rows``.
+
+    Scores are ``scale * q.k`` (default scale 1/sqrt(d)).
 
     q: [b, s, hq, d]; k, v: [b, s_kv, hkv, d]; CPU tensors of a float type
     that upcasts exactly (bf16, fp16, fp32, fp64); arithmetic is float64.
@@ -70,7 +72,7 @@ def attention_forward(q, k, v, causal=True, rows=None, row_block=1024):
     """
     b, s, hq, d, skv, hkv = _check(q, k, v)
     G = hq // hkv
-    scale = softmax_scale(d)
+    scale = softmax_scale(d) if scale is None else float(scale)
     t_all = _rows_tensor(rows, s)
     n = t_all.numel()
     o = torch.zeros(b, n, hq, d, dtype=_F64)
@@ -94,7 +96,7 @@ def attention_forward(q, k, v, causal=True, rows=None, row_block=1024):
     return o, lse
 
 
-def attention_backward(q, k, v, do, causal=True, dq_rows=None, dkv_heads=None, row_block=512):
+def attention_backward(q, k, v, do, causal=True, dq_rows=None, dkv_heads=None, row_block=512, scale=None):
     """Gradients of sum(dO * O) with respect to q, k and v.
 
     With P = softmax(S) row-wise and O = P V (the forward above):
@@ -105,6 +107,7 @@ def attention_backward(q, k, v, do, causal=True, dq_rows=None, dkv_heads=None, r
         dK[j] = scale * sum_t dS[t, j] q[t]
     dK and dV of KV head g sum over every query head of g's group.
 
+    ``scale``: the forward's score scale (default 1/sqrt(d)).
     ``dq_rows``: query positions whose dQ is wanted (default: all).
     ``dkv_heads``: KV heads whose dK/dV are wanted (default: all); these need
     every row of every query head in the group.
@@ -115,7 +118,7 @@ def attention_backward(q, k, v, do, causal=True, dq_rows=None, dkv_heads=None, r
     if do.shape != q.shape or do.dtype not in _EXACT:
         raise ValueError("do must match q")
     G = hq // hkv
-    scale = softmax_scale(d)
+    scale = softmax_scale(d) if scale is None else float(scale)
     t_dq = _rows_tensor(dq_rows, s)
     heads = list(range(hkv)) if dkv_heads is None else [int(g) for g in dkv_heads]
     dq = torch.zeros(b, t_dq.numel(), hq, d, dtype=_F64)

@@ -379,3 +379,34 @@ def test_rope_positions_for_cp_shards_and_packing():
         idx = oracle.zigzag_global_index(s, cp)[r]
         shard = oracle.rope_apply(x[:, idx], oracle.rank_local_positions(s, cp, r, cu))
         assert torch.allclose(shard, full[:, idx], atol=1e-15)
+
+
+# ---------------------------------------------------------------- user scale
+def test_scale_zero_gives_uniform_weights():
+    # scale 0: every visible key weighs the same: O = running mean of v, L = log(t+1)
+    g = torch.Generator().manual_seed(12)
+    q, k, v = _rand(1, 6, 1, 4, gen=g), _rand(1, 6, 1, 4, gen=g), _rand(1, 6, 1, 4, gen=g)
+    o, lse = attention_forward(q, k, v, scale=0.0)
+    for t in range(6):
+        assert torch.allclose(o[0, t, 0], v[0, :t + 1, 0].mean(dim=0), atol=1e-14)
+        assert abs(lse[0, 0, t] - math.log(t + 1)) < 1e-14
+
+
+def test_scale_moves_into_the_queries():
+    # scale * (q . k) = (alpha q) . k * (scale / alpha): forward and gradients
+    g = torch.Generator().manual_seed(13)
+    b, s, hq, hkv, d = 1, 12, 2, 1, 8
+    q, k, v, do = (_rand(b, s, hq, d, gen=g), _rand(b, s, hkv, d, gen=g), _rand(b, s, hkv, d, gen=g),
+                   _rand(b, s, hq, d, gen=g))
+    alpha, sc = 3.0, 0.7
+    o1, l1 = attention_forward(q, k, v, scale=sc)
+    o2, l2 = attention_forward(q * alpha, k, v, scale=sc / alpha)
+    assert torch.allclose(o1, o2, atol=1e-12) and torch.allclose(l1, l2, atol=1e-12)
+    dq1, dk1, dv1 = attention_backward(q, k, v, do, scale=sc)
+    dq2, dk2, dv2 = attention_backward(q * alpha, k, v, do, scale=sc / alpha)
+    assert torch.allclose(dq1, dq2 * alpha, atol=1e-12)
+    assert torch.allclose(dk1, dk2, atol=1e-12) and torch.allclose(dv1, dv2, atol=1e-12)
+    # default is 1/sqrt(d)
+    o3, _ = attention_forward(q, k, v, scale=1 / math.sqrt(d))
+    o4, _ = attention_forward(q, k, v)
+    assert torch.equal(o3, o4)

@@ -340,6 +340,25 @@ def run_ours(args, w):
                              "hbm_frac": m_bytes / (m_ms * 1e-3) / 1e9 / _peaks()["hbm_gbs"]}}
         del uws, o_a, o_b
 
+    # ---- RoPE of q and k in place (HBM-bound), forward then inverse
+    from context_blockwise_causal_gb300 import cpattn_rope
+
+    for inv in (False, True):
+        cpattn_rope(q, inverse=inv, stream=stream)
+        cpattn_rope(k, inverse=inv, stream=stream)
+    barrier()
+    r0, r1 = ev(), ev()
+    r0.record(stream)
+    for i in range(2 * args.steps):
+        cpattn_rope(q, inverse=bool(i & 1), stream=stream)
+        cpattn_rope(k, inverse=bool(i & 1), stream=stream)
+    r1.record(stream)
+    barrier()
+    rope_ms = r0.elapsed_time(r1) / (2 * args.steps)
+    rope_bytes = 2 * (q.numel() + k.numel()) * 2  # read and write q and k, bf16
+    rope = {"ms": rope_ms, "bytes": rope_bytes, "gbs": rope_bytes / (rope_ms * 1e-3) / 1e9,
+            "what": "cpattn_rope on q and k (two launches)"}
+
     if rank == 0:
         peaks = _peaks()
         step_flops = w.fwd_flops() + w.bwd_flops()
@@ -385,6 +404,8 @@ def run_ours(args, w):
         }
         if unfused is not None:
             line["unfused_fwd"] = unfused
+        rope["hbm_frac"] = rope["gbs"] / peaks["hbm_gbs"]
+        line["rope"] = rope
         if not args.no_cpu_baseline:
             dt, fl = _oracle_sample(w, args.ref_rows, seed=w.seed + 5)
             line["cpu_baseline"] = {

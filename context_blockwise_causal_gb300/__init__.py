@@ -62,6 +62,10 @@ def library():
         lib = ctypes.CDLL(LIB_PATH)
         lib.cpattn_fwd.argtypes = [_p, _p, _p, _p, _p] + [_i] * 7 + [_p]
         lib.cpattn_fwd.restype = _i
+        lib.cpattn_fwd_ex.argtypes = [_p, _p, _p, _p, _p] + [_i] * 7 + [ctypes.c_float, _p]
+        lib.cpattn_fwd_ex.restype = _i
+        lib.cpattn_bwd_ex.argtypes = [_p] * 10 + [_sz] + [_i] * 7 + [ctypes.c_float, _p]
+        lib.cpattn_bwd_ex.restype = _i
         lib.cpattn_fwd_step.argtypes = [_p] * 5 + [_i] * 8 + [_p]
         lib.cpattn_fwd_step.restype = _i
         lib.cpattn_lse_merge.argtypes = [_p] * 7 + [_i] * 4 + [_p]
@@ -123,11 +127,12 @@ def _dims(q, k, v):
     return b, s, hq, k.shape[2], d
 
 
-def cpattn_fwd(q, k, v, cp, causal=True, o=None, lse=None, stream=None):
+def cpattn_fwd(q, k, v, cp, causal=True, o=None, lse=None, stream=None, scale=None):
     """Context-parallel causal attention forward. Returns (o, lse).
 
     q [b,s,hq,d], k/v [b,s,hkv,d] bf16 CUDA tensors; o like q (bf16) and lse
-    [b,hq,s] fp32 are allocated when not given.
+    [b,hq,s] fp32 are allocated when not given. ``scale`` (default 1/sqrt(d))
+    multiplies the scores (cpattn_fwd_ex).
     """
     b, s, hq, hkv, d = _dims(q, k, v)
     if o is None:
@@ -137,10 +142,14 @@ def cpattn_fwd(q, k, v, cp, causal=True, o=None, lse=None, stream=None):
         lse = torch.empty(b, hq, s, device=q.device, dtype=torch.float32)
     if lse.dtype != torch.float32 or tuple(lse.shape) != (b, hq, s) or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous fp32 [b, hq, s] tensor")
-    rc = library().cpattn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), b, s, hq, hkv,
-                              d, int(cp), 1 if causal else 0, _stream_handle(stream))
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), b, s, hq, hkv, d, int(cp),
+            1 if causal else 0)
+    if scale is None:
+        rc = library().cpattn_fwd(*args, _stream_handle(stream))
+    else:
+        rc = library().cpattn_fwd_ex(*args, float(scale), _stream_handle(stream))
     if rc:
-        raise CpattnError(rc, "cpattn_fwd")
+        raise CpattnError(rc, "cpattn_fwd" if scale is None else "cpattn_fwd_ex")
     return o, lse
 
 
@@ -263,11 +272,13 @@ def cpattn_bwd_workspace_bytes(b, s, hq, hkv, d, cp):
 
 
 def cpattn_bwd(q, k, v, o, lse, do, cp, causal=True, dq=None, dk=None, dv=None, workspace=None, stream=None,
-               stage=None):
+               stage=None, scale=None):
     """Backward from the forward's saved o and lse. Returns (dq, dk, dv).
 
     ``stage`` (0, 1 or 2) runs only that stage of the backward (see
-    cpattn_bwd_stage in include/cpattn.h); None runs all three.
+    cpattn_bwd_stage in include/cpattn.h); None runs all three. ``scale``:
+    the forward's softmax scale when it was not 1/sqrt(d) (cpattn_bwd_ex;
+    whole backward only).
     """
     b, s, hq, hkv, d = _dims(q, k, v)
     _check_act("o", o, q.shape)
@@ -289,7 +300,11 @@ def cpattn_bwd(q, k, v, o, lse, do, cp, causal=True, dq=None, dk=None, dv=None, 
     ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(), dq.data_ptr(),
             dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(), ws_bytes, b, s, hq, hkv, d, int(cp),
             1 if causal else 0, _stream_handle(stream))
-    if stage is None:
+    if scale is not None:
+        if stage is not None:
+            raise ValueError("a custom scale runs the whole backward (stage must be None)")
+        rc = library().cpattn_bwd_ex(*ptrs[:-1], float(scale), ptrs[-1])
+    elif stage is None:
         rc = library().cpattn_bwd(*ptrs)
     else:
         rc = library().cpattn_bwd_stage(int(stage), *ptrs)

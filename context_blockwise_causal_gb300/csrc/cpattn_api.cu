@@ -120,8 +120,14 @@ int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& 
 
 using namespace cpattn;
 
-extern "C" int cpattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int b, int s, int hq,
-                          int hkv, int d, int cp, int causal, void* stream) {
+namespace {
+bool valid_scale(float scale) { return scale > 0.f && scale <= 3.0e38f; }
+double default_scale(int d) { return 1.0 / std::sqrt(double(d)); }
+}  // namespace
+
+namespace {
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int b, int s, int hq, int hkv, int d,
+             int cp, int causal, double scale, void* stream) {
   if (!q || !k || !v || !o || !lse) return CPATTN_ERR_NULL_PTR;
   int rc = check_geometry(b, s, hq, hkv, d, cp);
   if (rc) return rc;
@@ -140,10 +146,22 @@ extern "C" int cpattn_fwd(const void* q, const void* k, const void* v, void* o, 
   args.lse = lse;
   args.o_part = nullptr;
   args.step = -1;
-  args.scale_log2 = float(1.4426950408889634 / std::sqrt(double(d)));
+  args.scale_log2 = float(1.4426950408889634 * scale);
   args.status = di->status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return d == 128 ? launch_fwd<128, false>(tq, tk, tv, args, di, st) : launch_fwd<64, false>(tq, tk, tv, args, di, st);
+}
+}  // namespace
+
+extern "C" int cpattn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int b, int s, int hq,
+                             int hkv, int d, int cp, int causal, float scale, void* stream) {
+  if (!valid_scale(scale)) return CPATTN_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, o, lse, b, s, hq, hkv, d, cp, causal, double(scale), stream);
+}
+
+extern "C" int cpattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int b, int s, int hq,
+                          int hkv, int d, int cp, int causal, void* stream) {
+  return fwd_impl(q, k, v, o, lse, b, s, hq, hkv, d, cp, causal, default_scale(d), stream);
 }
 
 extern "C" int cpattn_fwd_step(const void* q, const void* k, const void* v, float* o_part, float* lse_part, int b,
@@ -379,7 +397,7 @@ namespace {
 // Argument checks and tensor maps shared by cpattn_bwd and cpattn_bwd_stage.
 int prepare_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int b, int s, int hq, int hkv,
-                int d, int cp, int causal, CUtensorMap* maps, BwdArgs* args, DeviceInfo** di) {
+                int d, int cp, int causal, double scale, CUtensorMap* maps, BwdArgs* args, DeviceInfo** di) {
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return CPATTN_ERR_NULL_PTR;
   int rc = check_geometry(b, s, hq, hkv, d, cp);
   if (rc) return rc;
@@ -407,8 +425,8 @@ int prepare_bwd(const void* q, const void* k, const void* v, const void* o, cons
   args->dq = static_cast<__nv_bfloat16*>(dq);
   args->dk = static_cast<__nv_bfloat16*>(dk);
   args->dv = static_cast<__nv_bfloat16*>(dv);
-  args->scale = float(1.0 / std::sqrt(double(d)));
-  args->scale_log2 = float(1.4426950408889634 / std::sqrt(double(d)));
+  args->scale = float(scale);
+  args->scale_log2 = float(1.4426950408889634 * scale);
   args->status = (*di)->status;
   return CPATTN_OK;
 }
@@ -416,18 +434,36 @@ int prepare_bwd(const void* q, const void* k, const void* v, const void* o, cons
 }  // namespace
 }  // namespace cpattn
 
-extern "C" int cpattn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                          const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
-                          int b, int s, int hq, int hkv, int d, int cp, int causal, void* stream) {
+namespace {
+int bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout, void* dq,
+             void* dk, void* dv, void* workspace, size_t workspace_bytes, int b, int s, int hq, int hkv, int d, int cp,
+             int causal, double scale, void* stream) {
   CUtensorMap maps[4];
   BwdArgs args;
   DeviceInfo* di = nullptr;
   const int rc = prepare_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, b, s, hq, hkv, d, cp,
-                             causal, maps, &args, &di);
+                             causal, double(scale), maps, &args, &di);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return d == 128 ? launch_bwd<128>(maps[0], maps[1], maps[2], maps[3], args, di, st)
                   : launch_bwd<64>(maps[0], maps[1], maps[2], maps[3], args, di, st);
+}
+
+}  // namespace
+
+extern "C" int cpattn_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                             const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                             int b, int s, int hq, int hkv, int d, int cp, int causal, float scale, void* stream) {
+  if (!valid_scale(scale)) return CPATTN_ERR_INVALID_ARG;
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, b, s, hq, hkv, d, cp, causal,
+                  double(scale), stream);
+}
+
+extern "C" int cpattn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                          const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                          int b, int s, int hq, int hkv, int d, int cp, int causal, void* stream) {
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, b, s, hq, hkv, d, cp, causal,
+                  default_scale(d), stream);
 }
 
 extern "C" int cpattn_bwd_stage(int stage, const void* q, const void* k, const void* v, const void* o,
@@ -439,7 +475,7 @@ extern "C" int cpattn_bwd_stage(int stage, const void* q, const void* k, const v
   BwdArgs args;
   DeviceInfo* di = nullptr;
   const int rc = prepare_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, b, s, hq, hkv, d, cp,
-                             causal, maps, &args, &di);
+                             causal, default_scale(d), maps, &args, &di);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return d == 128 ? launch_bwd_stage<128>(stage, maps[0], maps[1], maps[2], maps[3], args, di, st)
@@ -493,9 +529,8 @@ extern "C" int cpattn_bwd_noalloc(const void* q, const void* k, const void* v, c
       !encode_bf16_rows_heads_d(&tv, v, rows, hkv, d, kTile) ||
       !encode_bf16_rows_heads_d(&tdo, dout, rows, hq, d, kTile))
     return CPATTN_ERR_CUDA;
-  // The preprocess kernel zeroes the dQ accumulator part and rewrites the
-  // L/D vectors on every call, so stale contents of the shared array from an
-  // earlier call do not matter.
+  // The preprocess kernel rewrites the L/D vectors on every call, so stale
+  // contents of the shared array from an earlier call do not matter.
   uint8_t* ws = static_cast<uint8_t*>(scratch);
   BwdArgs args;
   args.g = make_geom(b, s, hq, hkv, cp, causal);

@@ -76,6 +76,15 @@ int cpattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                int d, int cp, int causal, void* stream);
 
 /*
+ * cpattn_fwd with a caller-chosen softmax scale (scores = scale * q.k instead
+ * of q.k / sqrt(d)); lse is then log sum_j exp(scale * q_t.k_j). scale must be
+ * positive and finite, else CPATTN_ERR_INVALID_ARG. cpattn_fwd(...) equals
+ * cpattn_fwd_ex(..., 1/sqrt(d), stream).
+ */
+int cpattn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int b, int s, int hq, int hkv,
+                  int d, int cp, int causal, float scale, void* stream);
+
+/*
  * The same forward in the unfused form the pages describe: one launch per CP
  * step, each writing every rank's partial result to device memory, and a
  * log-sum-exp correction after every step ("大模型面试宝典 · Megatron-LM 篇",
@@ -175,6 +184,15 @@ size_t cpattn_bwd_workspace_bytes(int b, int s, int hq, int hkv, int d, int cp);
 int cpattn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int b, int s, int hq, int hkv,
                int d, int cp, int causal, void* stream);
+
+/*
+ * cpattn_bwd for a forward run with cpattn_fwd_ex's `scale` (the same value
+ * must be passed; lse is that forward's). Errors as cpattn_bwd, plus
+ * CPATTN_ERR_INVALID_ARG for a scale that is not positive and finite.
+ */
+int cpattn_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                  void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int b, int s, int hq, int hkv,
+                  int d, int cp, int causal, float scale, void* stream);
 
 /*
  * One stage of cpattn_bwd, for callers that schedule or time the backward's

@@ -129,3 +129,10 @@ def test_rope_argument_errors(lib):
     assert r(p, 2, 512, 4, 64, 512, 2, -1, p, 3, 10000.0, 0, None) == -1      # packing needs b == 1
     assert r(p, 1, 512, 4, 64, 512, 2, -1, None, 0, 1.0, 0, None) == -1      # base > 1
     assert r(ctypes.c_void_p(4096 + 4), 1, 512, 4, 64, 512, 2, -1, None, 0, 10000.0, 0, None) == -3
+
+
+def test_scaled_entry_points_reject_bad_scales(lib):
+    p = ctypes.c_void_p(4096)
+    for bad in (0.0, -1.0, float("nan"), float("inf")):
+        assert lib.cpattn_fwd_ex(p, p, p, p, p, 1, 512, 4, 4, 64, 2, 1, bad, None) == -1
+        assert lib.cpattn_bwd_ex(p, p, p, p, p, p, p, p, p, p, 1 << 20, 1, 512, 4, 2, 64, 2, 1, bad, None) == -1

@@ -38,3 +38,4 @@ from .context_parallel import (  # noqa: F401
     cp_attention_forward,
 )
 from .rope import rope_angles, rope_apply, natural_positions, rank_local_positions  # noqa: F401
+from .varlen import varlen_attention_forward, varlen_attention_backward  # noqa: F401

@@ -410,3 +410,38 @@ def test_scale_moves_into_the_queries():
     o3, _ = attention_forward(q, k, v, scale=1 / math.sqrt(d))
     o4, _ = attention_forward(q, k, v)
     assert torch.equal(o3, o4)
+
+
+# ---------------------------------------------------------------- packed samples
+def test_varlen_uniform_lengths_equal_a_batch():
+    g = torch.Generator().manual_seed(14)
+    b, L, hq, hkv, d = 3, 10, 2, 1, 4
+    q, k, v, do = (_rand(b, L, hq, d, gen=g), _rand(b, L, hkv, d, gen=g), _rand(b, L, hkv, d, gen=g),
+                   _rand(b, L, hq, d, gen=g))
+    o, lse = attention_forward(q, k, v)
+    cu = [0, L, 2 * L, 3 * L]
+    flat = lambda t: t.reshape(b * L, t.shape[2], t.shape[3])  # noqa: E731
+    ov, lv = oracle.varlen_attention_forward(flat(q), flat(k), flat(v), cu)
+    assert torch.allclose(ov, flat(o), atol=1e-14)
+    assert torch.allclose(lv, lse.permute(1, 0, 2).reshape(hq, b * L), atol=1e-14)
+    dq, dk, dv = attention_backward(q, k, v, do)
+    gq, gk, gv = oracle.varlen_attention_backward(flat(q), flat(k), flat(v), flat(do), cu)
+    assert torch.allclose(gq, flat(dq), atol=1e-13) and torch.allclose(gk, flat(dk), atol=1e-13)
+    assert torch.allclose(gv, flat(dv), atol=1e-13)
+
+
+def test_varlen_samples_do_not_see_each_other():
+    g = torch.Generator().manual_seed(15)
+    total, hq, hkv, d = 20, 2, 2, 4
+    cu = [0, 6, 6, 20]  # an empty sample in the middle
+    q, k, v = _rand(1, total, hq, d, gen=g)[0], _rand(1, total, hkv, d, gen=g)[0], _rand(1, total, hkv, d, gen=g)[0]
+    o1, l1 = oracle.varlen_attention_forward(q, k, v, cu)
+    k2, v2 = k.clone(), v.clone()
+    k2[6:] += 1.0
+    v2[6:] -= 2.0
+    o2, l2 = oracle.varlen_attention_forward(q, k2, v2, cu)
+    assert torch.equal(o1[:6], o2[:6]) and torch.equal(l1[:, :6], l2[:, :6])
+    # the first token of the second sample attends only to itself: O = v, L = scale q.k
+    assert torch.allclose(o1[6], v[6].to(F64).repeat_interleave(hq // hkv, dim=0), atol=1e-14)
+    sc = 1 / math.sqrt(d)
+    assert torch.allclose(l1[:, 6], (q[6].to(F64) * k[6].to(F64)).sum(-1) * sc, atol=1e-14)

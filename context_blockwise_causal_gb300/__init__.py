@@ -22,6 +22,8 @@ __all__ = [
     "cpattn_fwd_unfused",
     "cpattn_fwd_unfused_workspace_bytes",
     "cpattn_rope",
+    "cpattn_fwd_varlen",
+    "cpattn_bwd_varlen",
     "cpattn_bwd",
     "cpattn_bwd_workspace_bytes",
     "cpattn_zigzag_index",
@@ -76,6 +78,12 @@ def library():
         lib.cpattn_fwd_unfused.restype = _i
         lib.cpattn_rope.argtypes = [_p] + [_i] * 7 + [_p, _i, ctypes.c_float, _i, _p]
         lib.cpattn_rope.restype = _i
+        lib.cpattn_fwd_varlen.argtypes = [_p] * 6 + [_i] * 6 + [ctypes.c_float, _p]
+        lib.cpattn_fwd_varlen.restype = _i
+        lib.cpattn_bwd_varlen_workspace_bytes.argtypes = [_p] + [_i] * 5
+        lib.cpattn_bwd_varlen_workspace_bytes.restype = _sz
+        lib.cpattn_bwd_varlen.argtypes = [_p] * 10 + [_sz, _p] + [_i] * 6 + [ctypes.c_float, _p]
+        lib.cpattn_bwd_varlen.restype = _i
         lib.cpattn_bwd.argtypes = [_p] * 10 + [_sz] + [_i] * 7 + [_p]
         lib.cpattn_bwd.restype = _i
         lib.cpattn_bwd_stage.argtypes = [_i] + [_p] * 10 + [_sz] + [_i] * 7 + [_p]
@@ -265,6 +273,68 @@ def cpattn_rope(x, base=10000.0, cp=1, rank=None, s=None, cu_seqlens=None, inver
     if rc:
         raise CpattnError(rc, "cpattn_rope")
     return x
+
+
+def _cu_host(cu_seqlens):
+    cu = torch.as_tensor(cu_seqlens, dtype=torch.int32).cpu().contiguous()
+    return cu, ctypes.c_void_p(cu.data_ptr()), cu.numel() - 1
+
+
+def _packed_dims(q, k, v):
+    if q.dim() != 3 or k.dim() != 3:
+        raise ValueError("packed q must be [total, hq, d] and k, v [total, hkv, d]")
+    _check_act("q", q)
+    _check_act("k", k)
+    _check_act("v", v, k.shape)
+    if k.shape[0] != q.shape[0] or k.shape[2] != q.shape[2]:
+        raise ValueError("q and k disagree")
+    return q.shape[0], q.shape[1], k.shape[1], q.shape[2]
+
+
+def cpattn_fwd_varlen(q, k, v, cu_seqlens, cp, causal=True, scale=None, o=None, lse=None, stream=None):
+    """Forward over packed samples (attention within each sample).
+
+    q [total, hq, d], k/v [total, hkv, d]; cu_seqlens: sample offsets (host
+    list/tensor). Returns (o [total, hq, d], lse [hq, total]).
+    """
+    total, hq, hkv, d = _packed_dims(q, k, v)
+    cu, cu_p, nseq = _cu_host(cu_seqlens)
+    if int(cu[-1]) != total:
+        raise ValueError("cu_seqlens must end at the packed length")
+    o = torch.empty_like(q) if o is None else o
+    _check_act("o", o, q.shape)
+    lse = torch.empty(hq, total, device=q.device, dtype=torch.float32) if lse is None else lse
+    _check_f32("lse", lse, (hq, total))
+    rc = library().cpattn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), cu_p,
+                                     nseq, hq, hkv, d, int(cp), 1 if causal else 0,
+                                     0.0 if scale is None else float(scale), _stream_handle(stream))
+    if rc:
+        raise CpattnError(rc, "cpattn_fwd_varlen")
+    return o, lse
+
+
+def cpattn_bwd_varlen(q, k, v, o, lse, do, cu_seqlens, cp, causal=True, scale=None, dq=None, dk=None, dv=None,
+                      workspace=None, stream=None):
+    """Backward over packed samples. Returns (dq, dk, dv)."""
+    total, hq, hkv, d = _packed_dims(q, k, v)
+    cu, cu_p, nseq = _cu_host(cu_seqlens)
+    _check_act("o", o, q.shape)
+    _check_act("do", do, q.shape)
+    _check_f32("lse", lse, (hq, total))
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = int(library().cpattn_bwd_varlen_workspace_bytes(cu_p, nseq, hq, hkv, d, int(cp)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    rc = library().cpattn_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                     do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+                                     workspace.numel() * workspace.element_size(), cu_p, nseq, hq, hkv, d, int(cp),
+                                     1 if causal else 0, 0.0 if scale is None else float(scale),
+                                     _stream_handle(stream))
+    if rc:
+        raise CpattnError(rc, "cpattn_bwd_varlen")
+    return dq, dk, dv
 
 
 def cpattn_bwd_workspace_bytes(b, s, hq, hkv, d, cp):

@@ -41,6 +41,7 @@ struct BwdArgs {
   const __nv_bfloat16* o;
   const __nv_bfloat16* dout;
   const float* lse;
+  int64_t lse_stride;  // row stride of lse per (batch, head): s, or a packed tensor's total
   float* lvec;  // [b, hq, ntp]: lse * log2(e)
   float* dvec;  // [b, hq, ntp]: rowsum(dO * O)
   __nv_bfloat16* dq;
@@ -92,7 +93,7 @@ __global__ void __launch_bounds__(256) cpattn_bwd_pre_kernel(const BwdArgs a) {
     const int in = t - chunk * g.c;
     const int64_t pos = ld_pos(g, a.ntp, bi, h, chunk, in / kTile, in % kTile);
     a.dvec[pos] = acc;
-    a.lvec[pos] = a.lse[(int64_t(bi) * g.hq + h) * g.s + t] * 1.4426950408889634f;
+    a.lvec[pos] = a.lse[(int64_t(bi) * g.hq + h) * a.lse_stride + t] * 1.4426950408889634f;
   }
 }
 

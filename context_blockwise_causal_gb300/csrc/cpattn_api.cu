@@ -127,11 +127,11 @@ double default_scale(int d) { return 1.0 / std::sqrt(double(d)); }
 
 namespace {
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int b, int s, int hq, int hkv, int d,
-             int cp, int causal, double scale, void* stream) {
+             int cp, int causal, double scale, void* stream, int64_t lse_stride = -1) {
   if (!q || !k || !v || !o || !lse) return CPATTN_ERR_NULL_PTR;
   int rc = check_geometry(b, s, hq, hkv, d, cp);
   if (rc) return rc;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u))
     return CPATTN_ERR_MISALIGNED;
   DeviceInfo* di = nullptr;
   if ((rc = device_info(&di))) return rc;
@@ -144,6 +144,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   args.g = make_geom(b, s, hq, hkv, cp, causal);
   args.o = static_cast<__nv_bfloat16*>(o);
   args.lse = lse;
+  args.lse_stride = lse_stride < 0 ? s : lse_stride;
   args.o_part = nullptr;
   args.step = -1;
   args.scale_log2 = float(1.4426950408889634 * scale);
@@ -156,11 +157,13 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
 extern "C" int cpattn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int b, int s, int hq,
                              int hkv, int d, int cp, int causal, float scale, void* stream) {
   if (!valid_scale(scale)) return CPATTN_ERR_INVALID_ARG;
+  if (lse && !aligned16(lse)) return CPATTN_ERR_MISALIGNED;
   return fwd_impl(q, k, v, o, lse, b, s, hq, hkv, d, cp, causal, double(scale), stream);
 }
 
 extern "C" int cpattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int b, int s, int hq,
                           int hkv, int d, int cp, int causal, void* stream) {
+  if (lse && !aligned16(lse)) return CPATTN_ERR_MISALIGNED;
   return fwd_impl(q, k, v, o, lse, b, s, hq, hkv, d, cp, causal, default_scale(d), stream);
 }
 
@@ -183,6 +186,7 @@ extern "C" int cpattn_fwd_step(const void* q, const void* k, const void* v, floa
   args.g = make_geom(b, s, hq, hkv, cp, causal);
   args.o = nullptr;
   args.lse = lse_part;
+  args.lse_stride = s;
   args.o_part = o_part;
   args.step = step;
   args.scale_log2 = float(1.4426950408889634 / std::sqrt(double(d)));
@@ -397,14 +401,15 @@ namespace {
 // Argument checks and tensor maps shared by cpattn_bwd and cpattn_bwd_stage.
 int prepare_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int b, int s, int hq, int hkv,
-                int d, int cp, int causal, double scale, CUtensorMap* maps, BwdArgs* args, DeviceInfo** di) {
+                int d, int cp, int causal, double scale, CUtensorMap* maps, BwdArgs* args, DeviceInfo** di,
+                int64_t lse_stride = -1) {
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return CPATTN_ERR_NULL_PTR;
   int rc = check_geometry(b, s, hq, hkv, d, cp);
   if (rc) return rc;
-  for (const void* p : {q, k, v, o, static_cast<const void*>(lse), dout, static_cast<const void*>(dq),
-                        static_cast<const void*>(dk), static_cast<const void*>(dv),
-                        static_cast<const void*>(workspace)})
+  for (const void* p : {q, k, v, o, dout, static_cast<const void*>(dq), static_cast<const void*>(dk),
+                        static_cast<const void*>(dv), static_cast<const void*>(workspace)})
     if (!aligned16(p)) return CPATTN_ERR_MISALIGNED;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return CPATTN_ERR_MISALIGNED;
   const BwdLayout L = bwd_layout(b, s, hq, d, cp);
   if (workspace_bytes < L.total) return CPATTN_ERR_WORKSPACE_TOO_SMALL;
   if ((rc = device_info(di))) return rc;
@@ -420,6 +425,7 @@ int prepare_bwd(const void* q, const void* k, const void* v, const void* o, cons
   args->o = static_cast<const __nv_bfloat16*>(o);
   args->dout = static_cast<const __nv_bfloat16*>(dout);
   args->lse = lse;
+  args->lse_stride = lse_stride < 0 ? s : lse_stride;
   args->lvec = reinterpret_cast<float*>(ws + L.lvec);
   args->dvec = reinterpret_cast<float*>(ws + L.dvec);
   args->dq = static_cast<__nv_bfloat16*>(dq);
@@ -437,12 +443,12 @@ int prepare_bwd(const void* q, const void* k, const void* v, const void* o, cons
 namespace {
 int bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout, void* dq,
              void* dk, void* dv, void* workspace, size_t workspace_bytes, int b, int s, int hq, int hkv, int d, int cp,
-             int causal, double scale, void* stream) {
+             int causal, double scale, void* stream, int64_t lse_stride = -1) {
   CUtensorMap maps[4];
   BwdArgs args;
   DeviceInfo* di = nullptr;
   const int rc = prepare_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, b, s, hq, hkv, d, cp,
-                             causal, double(scale), maps, &args, &di);
+                             causal, double(scale), maps, &args, &di, lse_stride);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return d == 128 ? launch_bwd<128>(maps[0], maps[1], maps[2], maps[3], args, di, st)
@@ -455,6 +461,7 @@ extern "C" int cpattn_bwd_ex(const void* q, const void* k, const void* v, const 
                              const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                              int b, int s, int hq, int hkv, int d, int cp, int causal, float scale, void* stream) {
   if (!valid_scale(scale)) return CPATTN_ERR_INVALID_ARG;
+  if (lse && !aligned16(lse)) return CPATTN_ERR_MISALIGNED;
   return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, b, s, hq, hkv, d, cp, causal,
                   double(scale), stream);
 }
@@ -462,8 +469,85 @@ extern "C" int cpattn_bwd_ex(const void* q, const void* k, const void* v, const 
 extern "C" int cpattn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                           const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                           int b, int s, int hq, int hkv, int d, int cp, int causal, void* stream) {
+  if (lse && !aligned16(lse)) return CPATTN_ERR_MISALIGNED;
   return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, b, s, hq, hkv, d, cp, causal,
                   default_scale(d), stream);
+}
+
+// ---------------------------------------------------------------- packed samples
+namespace {
+// Checks the host sample offsets; returns the total token count or a
+// negative error code.
+int64_t check_cu(const int* cu, int nseq, int cp) {
+  if (!cu) return CPATTN_ERR_NULL_PTR;
+  if (nseq < 1 || cp < 1 || cu[0] != 0) return CPATTN_ERR_INVALID_ARG;
+  for (int i = 0; i < nseq; ++i) {
+    const int64_t len = int64_t(cu[i + 1]) - cu[i];
+    if (len < 0 || len % (2 * cp) != 0) return CPATTN_ERR_INVALID_ARG;
+  }
+  return cu[nseq];
+}
+}  // namespace
+
+extern "C" int cpattn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 const int* cu_seqlens, int nseq, int hq, int hkv, int d, int cp, int causal,
+                                 float scale, void* stream) {
+  const int64_t total = check_cu(cu_seqlens, nseq, cp);
+  if (total < 0) return int(total);
+  if (!q || !k || !v || !o || !lse) return CPATTN_ERR_NULL_PTR;
+  if (!(scale == 0.f || valid_scale(scale))) return CPATTN_ERR_INVALID_ARG;
+  if (!aligned16(lse)) return CPATTN_ERR_MISALIGNED;
+  if (d != 64 && d != 128) return CPATTN_ERR_INVALID_ARG;
+  const double sc = scale == 0.f ? default_scale(d) : double(scale);
+  for (int i = 0; i < nseq; ++i) {
+    const int start = cu_seqlens[i], len = cu_seqlens[i + 1] - cu_seqlens[i];
+    if (len == 0) continue;
+    const size_t qo = size_t(start) * hq * d * 2, ko = size_t(start) * hkv * d * 2;
+    const int rc = fwd_impl(static_cast<const uint8_t*>(q) + qo, static_cast<const uint8_t*>(k) + ko,
+                            static_cast<const uint8_t*>(v) + ko, static_cast<uint8_t*>(o) + qo, lse + start, 1, len,
+                            hq, hkv, d, cp, causal, sc, stream, total);
+    if (rc) return rc;
+  }
+  return CPATTN_OK;
+}
+
+extern "C" size_t cpattn_bwd_varlen_workspace_bytes(const int* cu_seqlens, int nseq, int hq, int hkv, int d, int cp) {
+  if (check_cu(cu_seqlens, nseq, cp) < 0 || hq < 1 || hkv < 1 || hq % hkv || (d != 64 && d != 128)) return 0;
+  size_t need = 0;
+  for (int i = 0; i < nseq; ++i) {
+    const int len = cu_seqlens[i + 1] - cu_seqlens[i];
+    if (len == 0) continue;
+    const size_t n = bwd_layout(1, len, hq, d, cp).total;
+    need = n > need ? n : need;
+  }
+  return need;
+}
+
+extern "C" int cpattn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                 const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                                 size_t workspace_bytes, const int* cu_seqlens, int nseq, int hq, int hkv, int d,
+                                 int cp, int causal, float scale, void* stream) {
+  const int64_t total = check_cu(cu_seqlens, nseq, cp);
+  if (total < 0) return int(total);
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return CPATTN_ERR_NULL_PTR;
+  if (!(scale == 0.f || valid_scale(scale))) return CPATTN_ERR_INVALID_ARG;
+  if (!aligned16(lse)) return CPATTN_ERR_MISALIGNED;
+  if (d != 64 && d != 128) return CPATTN_ERR_INVALID_ARG;
+  const double sc = scale == 0.f ? default_scale(d) : double(scale);
+  // The samples run one after another on the stream, so they share the
+  // workspace (sized for the longest).
+  for (int i = 0; i < nseq; ++i) {
+    const int start = cu_seqlens[i], len = cu_seqlens[i + 1] - cu_seqlens[i];
+    if (len == 0) continue;
+    const size_t qo = size_t(start) * hq * d * 2, ko = size_t(start) * hkv * d * 2;
+    const int rc = bwd_impl(static_cast<const uint8_t*>(q) + qo, static_cast<const uint8_t*>(k) + ko,
+                            static_cast<const uint8_t*>(v) + ko, static_cast<const uint8_t*>(o) + qo, lse + start,
+                            static_cast<const uint8_t*>(dout) + qo, static_cast<uint8_t*>(dq) + qo,
+                            static_cast<uint8_t*>(dk) + ko, static_cast<uint8_t*>(dv) + ko, workspace,
+                            workspace_bytes, 1, len, hq, hkv, d, cp, causal, sc, stream, total);
+    if (rc) return rc;
+  }
+  return CPATTN_OK;
 }
 
 extern "C" int cpattn_bwd_stage(int stage, const void* q, const void* k, const void* v, const void* o,
@@ -538,6 +622,7 @@ extern "C" int cpattn_bwd_noalloc(const void* q, const void* k, const void* v, c
   args.o = static_cast<const __nv_bfloat16*>(o);
   args.dout = static_cast<const __nv_bfloat16*>(dout);
   args.lse = lse;
+  args.lse_stride = s;
   args.lvec = reinterpret_cast<float*>(ws + L.lvec);
   args.dvec = reinterpret_cast<float*>(ws + L.dvec);
   args.dq = static_cast<__nv_bfloat16*>(dq);

@@ -53,7 +53,8 @@ constexpr float kRescaleThreshold = 0.0f;  // log2 units
 struct FwdArgs {
   CpGeom g;
   __nv_bfloat16* o;  // fused form: normalised output, bf16
-  float* lse;        // natural-log LSE [b, hq, s] (of the step, in step form)
+  float* lse;        // natural-log LSE [b, hq, lse_stride] (of the step, in step form)
+  int64_t lse_stride;  // row stride of lse per (batch, head): s, or a packed tensor's total
   float* o_part;     // step form: the step's normalised partial output, fp32
   int step;          // step form: the CP step computed
   float scale_log2;  // log2(e) / sqrt(d)
@@ -348,7 +349,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             float4* dst = reinterpret_cast<float4*>(a.o_part + ((int64_t(U.bi) * g.s + t) * g.hq + h) * D);
 #pragma unroll
             for (int c0 = 0; c0 < D / 4; ++c0) dst[c0] = make_float4(0.f, 0.f, 0.f, 0.f);
-            a.lse[(int64_t(U.bi) * g.hq + h) * g.s + t] = -INFINITY;
+            a.lse[(int64_t(U.bi) * g.hq + h) * a.lse_stride + t] = -INFINITY;
           }
           continue;
         }
@@ -471,7 +472,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int c0 = 0; c0 < D; c0 += 4)
           dst[c0 / 4] = make_float4(__uint_as_float(ov[c0]) * inv, __uint_as_float(ov[c0 + 1]) * inv,
                                     __uint_as_float(ov[c0 + 2]) * inv, __uint_as_float(ov[c0 + 3]) * inv);
-        a.lse[(int64_t(U.bi) * g.hq + h) * g.s + t] = (m_used + log2f(l)) * 0.69314718055994530942f;
+        a.lse[(int64_t(U.bi) * g.hq + h) * a.lse_stride + t] = (m_used + log2f(l)) * 0.69314718055994530942f;
       } else if (store) {
         const int h = sub ? U.h1 : U.h0;
         const int t = U.q_t0 + row;
@@ -486,7 +487,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           pkv.w = pack_bf16x2(__uint_as_float(ov[c0 + 6]) * inv, __uint_as_float(ov[c0 + 7]) * inv);
           *reinterpret_cast<uint4*>(dst + c0) = pkv;
         }
-        a.lse[(int64_t(U.bi) * g.hq + h) * g.s + t] = (m_used + log2f(l)) * 0.69314718055994530942f;
+        a.lse[(int64_t(U.bi) * g.hq + h) * a.lse_stride + t] = (m_used + log2f(l)) * 0.69314718055994530942f;
       }
       ++ul;
     }

@@ -139,6 +139,29 @@ int cpattn_lse_merge(const float* o_a, const float* lse_a, const float* o_b, con
                      float* lse_out, void* o_bf16, int b, int s, int hq, int d, void* stream);
 
 /*
+ * Packed samples (variable lengths): tensors hold several samples back to
+ * back -- q, o, dout, dq: [total, hq, d]; k, v, dk, dv: [total, hkv, d];
+ * lse: [hq, total] -- and attention stays within each sample. Each sample is
+ * split by the zigzag into 2*cp chunks of its own (its length must be
+ * divisible by 2*cp; 0 is allowed and skipped) and computed exactly as
+ * cpattn_fwd / cpattn_bwd compute a b = 1 sequence.
+ *   cu_seqlens: HOST int32 [nseq + 1] sample offsets, 0 = cu[0] <= ... <=
+ *               cu[nseq] = total (read during the call only).
+ *   scale:      0 selects 1/sqrt(d); otherwise as cpattn_fwd_ex.
+ * The samples are launched one after another on `stream` (one forward
+ * launch, or four backward launches, per sample). cpattn_bwd_varlen needs a
+ * workspace of cpattn_bwd_varlen_workspace_bytes(...) bytes (the largest
+ * sample's), shared by the samples. Errors as cpattn_fwd / cpattn_bwd;
+ * malformed offsets -> CPATTN_ERR_INVALID_ARG.
+ */
+int cpattn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
+                      int nseq, int hq, int hkv, int d, int cp, int causal, float scale, void* stream);
+size_t cpattn_bwd_varlen_workspace_bytes(const int* cu_seqlens, int nseq, int hq, int hkv, int d, int cp);
+int cpattn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                      void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, const int* cu_seqlens,
+                      int nseq, int hq, int hkv, int d, int cp, int causal, float scale, void* stream);
+
+/*
  * Rotary position embedding, in place, with the positions context
  * parallelism needs ("Megatron 面试题（一）：模型抽象与训练数据流", item M016):
  * each token turns by its position in the full sequence, not by its index in

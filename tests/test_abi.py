@@ -136,3 +136,21 @@ def test_scaled_entry_points_reject_bad_scales(lib):
     for bad in (0.0, -1.0, float("nan"), float("inf")):
         assert lib.cpattn_fwd_ex(p, p, p, p, p, 1, 512, 4, 4, 64, 2, 1, bad, None) == -1
         assert lib.cpattn_bwd_ex(p, p, p, p, p, p, p, p, p, p, 1 << 20, 1, 512, 4, 2, 64, 2, 1, bad, None) == -1
+
+
+def test_varlen_offsets_are_checked(lib):
+    p = ctypes.c_void_p(4096)
+    f = lib.cpattn_fwd_varlen
+
+    def cu(*xs):
+        return (ctypes.c_int * len(xs))(*xs)
+
+    assert f(p, p, p, p, p, None, 1, 4, 4, 64, 2, 1, 0.0, None) == -2
+    assert f(p, p, p, p, p, cu(0, 510), 1, 4, 4, 64, 2, 1, 0.0, None) == -1      # 510 % 4
+    assert f(p, p, p, p, p, cu(4, 512), 1, 4, 4, 64, 2, 1, 0.0, None) == -1      # cu[0] != 0
+    assert f(p, p, p, p, p, cu(0, 512, 256), 2, 4, 4, 64, 2, 1, 0.0, None) == -1  # decreasing
+    assert f(p, p, p, p, p, cu(0, 512), 1, 4, 4, 64, 2, 1, -1.0, None) == -1     # scale
+    w = lib.cpattn_bwd_varlen_workspace_bytes
+    # the largest sample's workspace: two fp32 vectors per query row and head, tile-padded
+    assert w(cu(0, 512, 1536, 1792), 3, 4, 2, 64, 2) == lib.cpattn_bwd_workspace_bytes(1, 1024, 4, 2, 64, 2)
+    assert w(cu(0, 510), 1, 4, 2, 64, 2) == 0

@@ -1,0 +1,56 @@
+"""Packed samples (cpattn_fwd_varlen / cpattn_bwd_varlen) through the C ABI
+against the CPU fp64 oracle (oracle.varlen_attention_*): mixed lengths,
+empty samples, ragged tiles, GQA, d = 64 and 128, a custom scale.
+Tolerances as for one sequence: max |O err| <= 1e-2 beyond the bf16
+output's half ulp, max |LSE err| <= 1e-3, relative L2 <= 2e-2 per gradient."""
+import pytest
+import torch
+
+import oracle
+from context_blockwise_causal_gb300 import cpattn_bwd_varlen, cpattn_device_status, cpattn_fwd_varlen
+
+pytestmark = pytest.mark.gpu
+
+
+def _half_ulp_bf16(x):
+    e = torch.floor(torch.log2(x.abs().clamp_min(2.0 ** -126)))
+    return 2.0 ** (e - 8)
+
+
+def _rel(x, ref):
+    x = x.double()
+    return ((x - ref).norm() / ref.norm().clamp_min(1e-30)).item()
+
+
+CASES = [
+    # lengths, hq, hkv, d, cp, scale
+    ([512, 1024, 256], 4, 2, 128, 2, None),
+    ([960, 0, 192, 384], 6, 2, 64, 3, None),     # empty sample, ragged chunks
+    ([2048, 128], 8, 1, 128, 4, 0.05),          # MQA, custom scale
+    ([96], 2, 2, 128, 3, None),                 # one sample, c = 16
+]
+
+
+@pytest.mark.parametrize("lengths,hq,hkv,d,cp,scale", CASES)
+def test_varlen_forward_backward(lengths, hq, hkv, d, cp, scale):
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + n)
+    total = cu[-1]
+    g = torch.Generator(device="cpu").manual_seed(100 + total + cp)
+    q = torch.randn(total, hq, d, generator=g).to(torch.bfloat16)
+    k = torch.randn(total, hkv, d, generator=g).to(torch.bfloat16)
+    v = torch.randn(total, hkv, d, generator=g).to(torch.bfloat16)
+    do = torch.randn(total, hq, d, generator=g).to(torch.bfloat16)
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = cpattn_fwd_varlen(qd, kd, vd, cu, cp, scale=scale)
+    dq, dk, dv = cpattn_bwd_varlen(qd, kd, vd, o, lse, dod, cu, cp, scale=scale)
+    torch.cuda.synchronize()
+    assert cpattn_device_status() == 0
+    o_r, l_r = oracle.varlen_attention_forward(q, k, v, cu, scale=scale)
+    err = (o.double().cpu() - o_r).abs()
+    assert (err <= 1e-2 + _half_ulp_bf16(o_r)).all(), err.max().item()
+    assert (lse.double().cpu() - l_r).abs().max().item() <= 1e-3
+    dq_r, dk_r, dv_r = oracle.varlen_attention_backward(q, k, v, do, cu, scale=scale)
+    for name, got, ref in (("dq", dq, dq_r), ("dk", dk, dk_r), ("dv", dv, dv_r)):
+        assert _rel(got.float().cpu(), ref) <= 2e-2, name

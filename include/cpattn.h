@@ -149,7 +149,7 @@ int cpattn_lse_merge(const float* o_a, const float* lse_a, const float* o_b, con
  *               cu[nseq] = total (read during the call only).
  *   scale:      0 selects 1/sqrt(d); otherwise as cpattn_fwd_ex.
  * The samples are launched one after another on `stream` (one forward
- * launch, or four backward launches, per sample). cpattn_bwd_varlen needs a
+ * launch, or three backward launches, per sample). cpattn_bwd_varlen needs a
  * workspace of cpattn_bwd_varlen_workspace_bytes(...) bytes (the largest
  * sample's), shared by the samples. Errors as cpattn_fwd / cpattn_bwd;
  * malformed offsets -> CPATTN_ERR_INVALID_ARG.

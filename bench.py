@@ -44,6 +44,18 @@ def _peaks():
     return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
+def _max_over_ranks(value, device, ws):
+    """The largest of `value` over the ranks of the default process group
+    (the slowest rank sets the job's time); `value` itself when alone."""
+    if ws <= 1:
+        return float(value)
+    import torch.distributed as dist
+
+    t = torch.tensor([float(value)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.item()
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -259,10 +271,7 @@ def run_ours(args, w):
                for i, name in enumerate(("fwd", "bwd_pre", "bwd_dkdv", "bwd_dq"))}
     if cpattn_device_status(stream) != 0:
         raise RuntimeError("a kernel reported a timeout in the timed region")
-    t = torch.tensor([total_ms], device=dev)
-    if ws > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = t.item()
+    total_ms = _max_over_ranks(total_ms, dev, ws)
 
     # ---- end to end through the public API with host buffers: every step
     # copies its inputs in from pinned host memory and its gradients out to
@@ -328,10 +337,7 @@ def run_ours(args, w):
     barrier()
     e0, e1 = e2e_run(args.steps)
     barrier()
-    e2e_ms = torch.tensor([e0.elapsed_time(e1)], device=dev)
-    if ws > 1:
-        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
-    e2e_ms = e2e_ms.item()
+    e2e_ms = _max_over_ranks(e0.elapsed_time(e1), dev, ws)
     del bufs[1]
 
     # ---- the unfused forward (cp step launches + cp-1 merges), outside the

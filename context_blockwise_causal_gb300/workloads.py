@@ -52,7 +52,7 @@ class Workload:
 WORKLOADS = {
     w.name: w
     for w in [
-        Workload("small_b1_s512_h4_d64_cp2", b=1, s=512, hq=4, hkv=4, d=64, cp=2, seed=1000),
+        Workload("small_b1_s512_h4_d64_cp2", b=1, s=512, hq=4, hkv=4, d=64, cp=2, backward=True, seed=1000),
         Workload("mha_b2_s4096_h32_d128_cp4", b=2, s=4096, hq=32, hkv=32, d=128, cp=4, seed=1001),
         Workload("gqa_b1_s16384_h64kv8_d128_cp8", b=1, s=16384, hq=64, hkv=8, d=128, cp=8, seed=1002,
                  check_rows=1024),

@@ -102,38 +102,6 @@ __global__ void __launch_bounds__(256) cpattn_bwd_pre_kernel(const BwdArgs a) {
 // region, each written by the warp that read the fp32 values there.
 __device__ __forceinline__ uint32_t half_split_col(int kk) { return kk < 4 ? kk * 8 : 64 + (kk - 4) * 8; }
 
-// One element pair: P = 2^(s*sl2 - l), dS = P (dp - d), packed to bf16x2.
-__device__ __forceinline__ void grad_pair(uint32_t s0, uint32_t s1, uint32_t dp0, uint32_t dp1, uint64_t sl2x2,
-                                          float l0, float l1, float d0, float d1, uint32_t& pp, uint32_t& pd) {
-  float x0, x1;
-  f2_unpack(f2_fma(f2_pack(__uint_as_float(s0), __uint_as_float(s1)), sl2x2, f2_pack(-l0, -l1)), x0, x1);
-  const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-  float g0, g1;
-  f2_unpack(f2_mul(f2_pack(p0, p1), f2_sub(f2_pack(__uint_as_float(dp0), __uint_as_float(dp1)), f2_pack(d0, d1))),
-            g0, g1);
-  pp = pack_bf16x2(p0, p1);
-  pd = pack_bf16x2(g0, g1);
-}
-
-// The same with one L*log2e and D for all 32 elements (a query row).
-template <bool kMasked>
-__device__ __forceinline__ void softmax_grad32_row(const uint32_t (&rs)[32], const uint32_t (&rp)[32], float sl2,
-                                                   float l2, float dd, uint32_t valid, uint32_t (&pp)[16],
-                                                   uint32_t (&pd)[16]) {
-  const uint64_t sl2x2 = f2_pack(sl2, sl2);
-#pragma unroll
-  for (int i = 0; i < 16; ++i)
-    grad_pair(rs[2 * i], rs[2 * i + 1], rp[2 * i], rp[2 * i + 1], sl2x2, l2, l2, dd, dd, pp[i], pd[i]);
-  if constexpr (kMasked) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t keep = ((valid >> (2 * i)) & 1u ? 0x0000ffffu : 0u) | ((valid >> (2 * i + 1)) & 1u ? 0xffff0000u : 0u);
-      pp[i] &= keep;
-      pd[i] &= keep;
-    }
-  }
-}
-
 // Bits [lo, hi) of a 32-bit mask (lo, hi clipped to [0, 32]).
 __device__ __forceinline__ uint32_t bit_range(int lo, int hi) {
   lo = lo < 0 ? 0 : (lo > 32 ? 32 : lo);
@@ -627,6 +595,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ================================================================ dQ
+// P for one query row's 32 keys (raw fp32 bits of S), packed to bf16 pairs:
+// P = 2^(S*sl2 - l2); when `masked`, bit i of `valid` keeps key i (masked
+// entries are selected to zero).
+template <bool kMasked>
+__device__ __forceinline__ void p_row32(const uint32_t (&rs)[32], float sl2, float l2, uint32_t valid,
+                                        uint32_t (&pp)[16]) {
+  const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2 = f2_pack(-l2, -l2);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float x0, x1;
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(rs[2 * i]), __uint_as_float(rs[2 * i + 1])), sl2x2, nl2), x0, x1);
+    pp[i] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
+    if constexpr (kMasked)
+      pp[i] &= ((valid >> (2 * i)) & 1u ? 0x0000ffffu : 0u) | ((valid >> (2 * i + 1)) & 1u ? 0xffff0000u : 0u);
+  }
+}
+
+// dS = P (dP - D) for the same 32 keys, P as packed bf16 pairs, D per row;
+// masked entries are selected to zero (their dP - D may be anything).
+template <bool kMasked>
+__device__ __forceinline__ void ds_row32(const uint32_t (&pp)[16], const uint32_t (&rp)[32], float dd,
+                                         uint32_t valid, uint32_t (&pd)[16]) {
+  const uint64_t ddx2 = f2_pack(dd, dd);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float g0, g1;
+    f2_unpack(f2_mul(f2_pack(__uint_as_float(pp[i] << 16), __uint_as_float(pp[i] & 0xffff0000u)),
+                     f2_sub(f2_pack(__uint_as_float(rp[2 * i]), __uint_as_float(rp[2 * i + 1])), ddx2)),
+              g0, g1);
+    pd[i] = pack_bf16x2(g0, g1);
+    if constexpr (kMasked)
+      pd[i] &= ((valid >> (2 * i)) & 1u ? 0x0000ffffu : 0u) | ((valid >> (2 * i + 1)) & 1u ? 0xffff0000u : 0u);
+  }
+}
+
 template <int D>
 struct DqCfg {
   static constexpr int kTileBytes = kTile * D * 2;
@@ -635,15 +638,19 @@ struct DqCfg {
   static constexpr int kOffdO = kOffQ + kTileBytes;
   static constexpr int kOffKV = kOffdO + kTileBytes;
   static constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
-  // q_full q_empty s_full dp_free ds_full dq_full dq_empty drain kv_full[] kv_empty[]
-  static constexpr int kNumBars = 8 + 2 * kSlots;
+  // q_full q_empty qa_full qa_empty s_full s_free dp_full p_full dq_full
+  // dq_empty drain, kv_full[] kv_empty[]
+  static constexpr int kNumBars = 11 + 2 * kSlots;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kLayoutBytes = kOffMisc + 16;
   // The d=128 layout leaves no room for re-alignment: the dynamic shared
   // memory base must already be 1024-byte aligned (checked at run time).
   static constexpr bool kNeedAlignedBase = (kLayoutBytes + 1024 > 232448);
   static constexpr int kSmemBytes = kNeedAlignedBase ? kLayoutBytes : kLayoutBytes + 1024;
-  static constexpr uint32_t kColS = 0, kColdP = 256, kColdQ = 384;
+  static_assert(kLayoutBytes <= 232448, "dQ shared memory layout too large");
+  // TMEM: S [0,128), dP [128,256) (later dS, packed), dQ [256,256+D), then Q
+  // and dO as bf16 A operands (D/2 columns each).
+  static constexpr uint32_t kColS = 0, kColdP = 128, kColdQ = 256, kColQA = 256 + D, kColdOA = 256 + D + D / 2;
 };
 
 // dQ work units: one 128-row query tile of one head, longest first.
@@ -677,14 +684,21 @@ __host__ __device__ inline FwdUnit dq_decode_unit(const CpGeom& g, int idx) {
 
 // Query-tile-stationary dQ. One CTA per SM, 10 warps:
 //   warps 0-7  element-wise; warp w covers TMEM lanes 32*(w%4).. (query rows)
-//              and column half w/4 (64 key columns of S/dP, D/2 columns of dQ)
+//              and keys 64*(w/4) .. +63 of each key tile (D/2 columns of Q,
+//              dO and dQ)
 //   warp 8     TMA producer (Q, dO per unit; K/V ring in CP-step order)
-//   warp 9     TMEM owner and MMA issuer
-// TMEM: S0 [0,128), S1 [128,256) (double-buffered; dS overwrites the first
-// 32 columns of each 64-column half, packed bf16), dP [256,384), dQ.
-// MMA order per key tile j: S(j+1), dP(j+1) as soon as the element-wise
-// warps have read S(j), dP(j) (so they overlap the arithmetic of tile j),
-// then dQ += dS(j) K_j.
+//   warp 9     TMEM owner and MMA issuer (whole warp, elect.sync)
+// At the start of a unit the element-wise warps copy its Q and dO tiles from
+// shared memory into TMEM as packed bf16, so every MMA takes its A operand
+// from TMEM and reads only B (a K or V tile) from shared memory:
+//   S(j) = Q K_j^T -> [0,128)     dP(j) = dO V_j^T -> [128,256)
+//   dQ += dS(j) K_j               (dS packed over dP(j))
+// The element-wise warps load S(j) and at once release its columns (s_free),
+// compute P in registers, then load dP(j) and write packed bf16 dS over it,
+// each warp inside the columns it read. Tensor-core order per key tile:
+//   S(j+1) | dQ(j) | dP(j+1) | S(j+2) | ...
+// so the exponentials of tile j overlap dQ(j-1) and dP(j), and only the dS
+// step is on the tensor core's critical path.
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     cpattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -705,14 +719,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* s_full = bars + 2;
-  uint64_t* dp_free = bars + 3;
-  uint64_t* ds_full = bars + 4;
-  uint64_t* dq_full = bars + 5;
-  uint64_t* dq_empty = bars + 6;
-  uint64_t* drain = bars + 7;
-  uint64_t* kv_full = bars + 8;
-  uint64_t* kv_empty = bars + 8 + C::kSlots;
+  uint64_t* qa_full = bars + 2;
+  uint64_t* qa_empty = bars + 3;
+  uint64_t* s_full = bars + 4;
+  uint64_t* s_free = bars + 5;
+  uint64_t* dp_full = bars + 6;
+  uint64_t* p_full = bars + 7;
+  uint64_t* dq_full = bars + 8;
+  uint64_t* dq_empty = bars + 9;
+  uint64_t* drain = bars + 10;
+  uint64_t* kv_full = bars + 11;
+  uint64_t* kv_empty = bars + 11 + C::kSlots;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -725,10 +742,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    mbar_init(q_empty, 8);
+    mbar_init(qa_full, 8);
+    mbar_init(qa_empty, 1);
     mbar_init(s_full, 1);
-    mbar_init(dp_free, 8);
-    mbar_init(ds_full, 8);
+    mbar_init(s_free, 8);
+    mbar_init(dp_full, 1);
+    mbar_init(p_full, 8);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 8);
     mbar_init(drain, 1);
@@ -775,6 +795,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int idx = snake_unit(rd, blockIdx.x, grid);
         if (idx >= num_units) break;
         const FwdUnit U = dq_decode_unit(g, idx);
+        // the Q/dO stage is free once the element-wise warps copied the
+        // previous unit's tiles into TMEM
         if (ul > 0 && !(ok = mbar_wait_lean(q_empty, (ul - 1) & 1, abort_flag, kWaitLimitNs))) break;
         mbar_arrive_expect_tx(q_full, 2 * C::kTileBytes);
         const int qrow = U.bi * g.s + U.q_t0;
@@ -787,8 +809,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bool dg;
         while (ok && w.next(chunk, tile, dg)) {
           const int row = U.bi * g.s + chunk * g.c + tile * kTile;
-          // V before K: V is released by the dP MMA, K only after dQ, so
-          // this order lets the ring run further ahead
+          // V before K: V is released by the dP MMA, K only after dQ
           ok = load(&tmv, U.g0, row) && load(&tmk, U.g0, row);
         }
         ++ul;
@@ -805,83 +826,92 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     {
       constexpr uint32_t idS = make_idesc_bf16(kTile, kTile, false, false);  // S, dP
       constexpr uint32_t idQ = make_idesc_bf16(kTile, D, false, true);       // dQ += dS K
-      const uint64_t dQ_km = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
-      const uint64_t ddO_km = make_sdesc_sw128(smem_u32(sdO), 16, 1024);
       const uint64_t dKV_km = make_sdesc_sw128(smem_u32(sKV), 16, 1024);
       const uint64_t dKV_mn = make_sdesc_sw128(smem_u32(sKV), 16384, 1024);
-      const uint32_t tdP = tbase + C::kColdP, tdQ = tbase + C::kColdQ;
+      const uint32_t tS = tbase + C::kColS, tdP = tbase + C::kColdP, tdQ = tbase + C::kColdQ;
+      const uint32_t tQA = tbase + C::kColQA, tdOA = tbase + C::kColdOA;
       uint32_t ncons = 0;
       auto take = [&](uint32_t& slot, uint32_t& par) {
         slot = ncons % C::kSlots;
         par = (ncons / C::kSlots) & 1;
         ++ncons;
       };
-      auto issue_sdp = [&](uint32_t jt, uint32_t ks, uint32_t vs) {
+      // S = Q K^T and dP = dO V^T, A (Q, dO) from TMEM, B from the ring
+      auto issue_s = [&](uint32_t ks) {
         const uint64_t kb = dKV_km + ((ks * C::kTileBytes) >> 4);
-        const uint64_t vb = dKV_km + ((vs * C::kTileBytes) >> 4);
-        const uint32_t tS = tbase + C::kColS + (jt & 1) * kTile;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;
-          umma_ss_w(tS, dQ_km + off, kb + off, idS, kk > 0);
+          umma_ts_w(tS, tQA + kk * 8, kb + off, idS, kk > 0);
         }
+      };
+      auto issue_dp = [&](uint32_t vs) {
+        const uint64_t vb = dKV_km + ((vs * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk / 4) * (kTile * 128) + (kk % 4) * 32) >> 4;
-          umma_ss_w(tdP, ddO_km + off, vb + off, idS, kk > 0);
+          umma_ts_w(tdP, tdOA + kk * 8, vb + off, idS, kk > 0);
         }
       };
       bool ok = true;
-      uint32_t jt = 0;  // key tiles processed so far (S buffer = jt & 1)
+      uint32_t jt = 0;  // key tiles processed so far
       int ul = 0;
       for (int rd = 0; ok; ++rd) {
         const int idx = snake_unit(rd, blockIdx.x, grid);
         if (idx >= num_units) break;
         const FwdUnit U = dq_decode_unit(g, idx);
         const int n = U.n;
-        if (!(ok = mbar_wait_warp_lean(q_full, ul & 1, abort_flag, kWaitLimitNs))) break;
-        // prologue: S(0), dP(0). The dP region is free once the previous
-        // tile's element-wise warps have read it.
+        // prologue: S and dP of the unit's first key tile, once Q/dO are in
+        // TMEM. The S columns are free once the previous S was read; the dP
+        // columns once the previous dQ MMAs (issued) read the dS there.
         uint32_t ks, kp, vs, vp;
         take(vs, vp);
         take(ks, kp);
-        ok = mbar_wait_warp_lean(&kv_full[ks], kp, abort_flag, kWaitLimitNs) &&
-             mbar_wait_warp_lean(&kv_full[vs], vp, abort_flag, kWaitLimitNs) &&
-             (jt == 0 || mbar_wait_warp_lean(dp_free, (jt - 1) & 1, abort_flag, kWaitLimitNs));
+        ok = mbar_wait_warp_lean(qa_full, ul & 1, abort_flag, kWaitLimitNs) &&
+             mbar_wait_warp_lean(&kv_full[ks], kp, abort_flag, kWaitLimitNs) &&
+             (jt == 0 || mbar_wait_warp_lean(s_free, (jt - 1) & 1, abort_flag, kWaitLimitNs));
         if (!ok) break;
         tc_fence_after();
-        issue_sdp(jt, ks, vs);
+        issue_s(ks);
         umma_commit_w(s_full);
+        if (!(ok = mbar_wait_warp_lean(&kv_full[vs], vp, abort_flag, kWaitLimitNs))) break;
+        issue_dp(vs);
+        umma_commit_w(dp_full);
         umma_commit_w(&kv_empty[vs]);
-        if (n == 1) umma_commit_w(q_empty);
+        if (n == 1) umma_commit_w(qa_empty);
         for (int j = 0; j < n && ok; ++j, ++jt) {
           const uint32_t cur_ks = ks;
+          uint32_t nvs = 0, nvp = 0;
           if (j + 1 < n) {
-            take(vs, vp);
+            // S(jt+1) as soon as S(jt) has been read
+            take(nvs, nvp);
             take(ks, kp);
-            ok = mbar_wait_warp_lean(dp_free, jt & 1, abort_flag, kWaitLimitNs) &&
-                 mbar_wait_warp_lean(&kv_full[ks], kp, abort_flag, kWaitLimitNs) &&
-                 mbar_wait_warp_lean(&kv_full[vs], vp, abort_flag, kWaitLimitNs);
+            ok = mbar_wait_warp_lean(s_free, jt & 1, abort_flag, kWaitLimitNs) &&
+                 mbar_wait_warp_lean(&kv_full[ks], kp, abort_flag, kWaitLimitNs);
             if (!ok) break;
             tc_fence_after();
-            // the other S buffer held dS(jt-1), read by the dQ MMA issued before
-            issue_sdp(jt + 1, ks, vs);
+            issue_s(ks);
             umma_commit_w(s_full);
-            umma_commit_w(&kv_empty[vs]);
-            if (j + 1 == n - 1) umma_commit_w(q_empty);
           }
-          ok = mbar_wait_warp_lean(ds_full, jt & 1, abort_flag, kWaitLimitNs) &&
+          ok = mbar_wait_warp_lean(p_full, jt & 1, abort_flag, kWaitLimitNs) &&
                (j > 0 || ul == 0 || mbar_wait_warp_lean(dq_empty, (ul - 1) & 1, abort_flag, kWaitLimitNs));
           if (!ok) break;
           tc_fence_after();
           // dQ += dS(jt) K_j   (dS from TMEM, K MN-major)
-          const uint32_t tS = tbase + C::kColS + (jt & 1) * kTile;
           const uint64_t kmn = dKV_mn + ((cur_ks * C::kTileBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            umma_ts_w(tdQ, tS + half_split_col(kk), kmn + ((kk * 2048) >> 4), idQ, (j > 0 || kk > 0) ? 1u : 0u);
+            umma_ts_w(tdQ, tdP + half_split_col(kk), kmn + ((kk * 2048) >> 4), idQ, (j > 0 || kk > 0) ? 1u : 0u);
           umma_commit_w(&kv_empty[cur_ks]);
           if (j == n - 1) umma_commit_w(dq_full);
+          if (j + 1 < n) {
+            // dP(jt+1) over dS(jt), which the dQ MMAs just issued read first
+            if (!(ok = mbar_wait_warp_lean(&kv_full[nvs], nvp, abort_flag, kWaitLimitNs))) break;
+            issue_dp(nvs);
+            umma_commit_w(dp_full);
+            umma_commit_w(&kv_empty[nvs]);
+            if (j + 1 == n - 1) umma_commit_w(qa_empty);  // the unit's last reads of Q/dO in TMEM
+          }
         }
         ++ul;
       }
@@ -895,7 +925,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int hf = warp >> 2;
     const int jr = wq * 32 + lane;  // TMEM lane = query row
     const uint32_t lane_off = uint32_t(wq * 32) << 16;
-    const uint32_t tdP = tbase + lane_off + C::kColdP;
+    const uint32_t tS = tbase + lane_off + C::kColS + hf * 64;
+    const uint32_t tdP = tbase + lane_off + C::kColdP + hf * 64;
     const float sl2 = a.scale_log2;
     const float scale = a.scale;
     bool ok = true;
@@ -905,6 +936,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int idx = snake_unit(rd, blockIdx.x, grid);
       if (idx >= num_units) break;
       const FwdUnit U = dq_decode_unit(g, idx);
+      // ---- this row's Q and dO (columns hf*D/2 ..) into TMEM as packed bf16
+      ok = mbar_wait_lean(q_full, ul & 1, abort_flag, kWaitLimitNs) &&
+           (ul == 0 || mbar_wait_lean(qa_empty, (ul - 1) & 1, abort_flag, kWaitLimitNs));
+      if (!ok) break;
+      tc_fence_after();  // the previous unit's MMAs have finished reading these columns
+      {
+        // swizzled rows of the TMA tile: 16-byte chunk c of row jr sits at
+        // chunk c ^ (jr & 7) of the row's 128 bytes, d-block x at x * 16 KB
+        constexpr int kChunks = D / 16;  // 16-byte chunks of this warp's D/2 elements
+        uint32_t rq[D / 4], ro[D / 4];
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) {
+          const int e0 = hf * (D / 2) + c * 8;  // first element of the chunk
+          const int x = e0 / 64, cc = (e0 % 64) / 8;
+          const uint32_t off = x * (kTile * 128) + jr * 128 + ((cc ^ (jr & 7)) * 16);
+          const uint4 vq = *reinterpret_cast<const uint4*>(sQ + off);
+          const uint4 vo = *reinterpret_cast<const uint4*>(sdO + off);
+          rq[4 * c] = vq.x; rq[4 * c + 1] = vq.y; rq[4 * c + 2] = vq.z; rq[4 * c + 3] = vq.w;
+          ro[4 * c] = vo.x; ro[4 * c + 1] = vo.y; ro[4 * c + 2] = vo.z; ro[4 * c + 3] = vo.w;
+        }
+        const uint32_t tq = tbase + lane_off + C::kColQA + hf * (D / 4);
+        const uint32_t to = tbase + lane_off + C::kColdOA + hf * (D / 4);
+        if constexpr (D == 128) {
+          tmem_st32(tq, rq);
+          tmem_st32(to, ro);
+        } else {
+          tmem_st16(tq, rq);
+          tmem_st16(to, ro);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(qa_full);
+        mbar_arrive(q_empty);
+      }
       // this row's L*log2e and D (padded rows of a ragged tile read arbitrary
       // values; their dQ is never stored)
       const int64_t pos = ld_pos(g, a.ntp, U.bi, U.h0, U.k, U.u, jr);
@@ -919,33 +986,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int n_valid = rem < kTile ? rem : kTile;
         if (!(ok = mbar_wait_lean(s_full, jt & 1, abort_flag, kWaitLimitNs))) break;
         tc_fence_after();
-        const uint32_t tS = tbase + lane_off + C::kColS + (jt & 1) * kTile;
-        uint32_t rs0[32], rs1[32], rp0[32], rp1[32];
-        tmem_ld32x4(tS + hf * 64, tS + hf * 64 + 32, tdP + hf * 64, tdP + hf * 64 + 32, rs0, rs1, rp0, rp1);
-        // S(jt) and dP(jt) are in registers: the MMA may refill dP (and the
-        // other S buffer) while this tile's arithmetic runs.
+        uint32_t r0[32], r1[32];
+        tmem_ld32x2(tS, tS + 32, r0, r1);
+        // S(jt) is in registers: the MMA may compute S(jt+1) meanwhile
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(dp_free);
+        if (lane == 0) mbar_arrive(s_free);
         const bool full = !dg && n_valid == kTile;
-        uint32_t pp[16], pd0[16], pd1[16];
+        // key column c (of this warp's 64) is valid when it is inside its
+        // chunk and (on the diagonal) c <= jr
+        const int cb = hf * 64;
+        int hi = n_valid - cb;
+        if (dg && jr + 1 - cb < hi) hi = jr + 1 - cb;
+        const uint32_t v0 = full ? 0u : bit_range(0, hi), v1 = full ? 0u : bit_range(0, hi - 32);
+        uint32_t pp0[16], pp1[16];
         if (full) {
-          softmax_grad32_row<false>(rs0, rp0, sl2, l2, dd, 0u, pp, pd0);
-          softmax_grad32_row<false>(rs1, rp1, sl2, l2, dd, 0u, pp, pd1);
+          p_row32<false>(r0, sl2, l2, 0u, pp0);
+          p_row32<false>(r1, sl2, l2, 0u, pp1);
         } else {
-          // key column c (of this warp's 64) is valid when it is inside its
-          // chunk and (on the diagonal) c <= jr
-          const int cb = hf * 64;
-          int hi = n_valid - cb;
-          if (dg && jr + 1 - cb < hi) hi = jr + 1 - cb;
-          softmax_grad32_row<true>(rs0, rp0, sl2, l2, dd, bit_range(0, hi), pp, pd0);
-          softmax_grad32_row<true>(rs1, rp1, sl2, l2, dd, bit_range(0, hi - 32), pp, pd1);
+          p_row32<true>(r0, sl2, l2, v0, pp0);
+          p_row32<true>(r1, sl2, l2, v1, pp1);
         }
-        tmem_st16(tS + hf * 64, pd0);
-        tmem_st16(tS + hf * 64 + 16, pd1);
+        if (!(ok = mbar_wait_lean(dp_full, jt & 1, abort_flag, kWaitLimitNs))) break;
+        tc_fence_after();
+        tmem_ld32x2(tdP, tdP + 32, r0, r1);
+        uint32_t pd0[16], pd1[16];
+        if (full) {
+          ds_row32<false>(pp0, r0, dd, 0u, pd0);
+          ds_row32<false>(pp1, r1, dd, 0u, pd1);
+        } else {
+          ds_row32<true>(pp0, r0, dd, v0, pd0);
+          ds_row32<true>(pp1, r1, dd, v1, pd1);
+        }
+        // dS packed into [64h, 64h+32) of the dP columns (read above)
+        tmem_st16x2(tdP, tdP + 16, pd0, pd1);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(ds_full);
+        if (lane == 0) mbar_arrive(p_full);
       }
       if (!ok) break;
       // ---- dQ of the tile: TMEM -> scale -> bf16 -> global
@@ -953,13 +1030,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       uint32_t rq[D / 2];
       {
-        uint32_t r0[32], r1[32];
+        uint32_t q0[32], q1[32];
         tmem_ld32x2(tbase + lane_off + C::kColdQ + hf * (D / 2),
-                    tbase + lane_off + C::kColdQ + hf * (D / 2) + (D == 128 ? 32 : 0), r0, r1);
+                    tbase + lane_off + C::kColdQ + hf * (D / 2) + (D == 128 ? 32 : 0), q0, q1);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          rq[i] = r0[i];
-          if constexpr (D == 128) rq[32 + i] = r1[i];
+          rq[i] = q0[i];
+          if constexpr (D == 128) rq[32 + i] = q1[i];
         }
       }
       tc_fence_before();

@@ -154,3 +154,11 @@ def test_varlen_offsets_are_checked(lib):
     # the largest sample's workspace: two fp32 vectors per query row and head, tile-padded
     assert w(cu(0, 512, 1536, 1792), 3, 4, 2, 64, 2) == lib.cpattn_bwd_workspace_bytes(1, 1024, 4, 2, 64, 2)
     assert w(cu(0, 510), 1, 4, 2, 64, 2) == 0
+
+
+def test_sizes_beyond_the_index_range_are_rejected(lib):
+    p = ctypes.c_void_p(4096)
+    # b * s >= 2^31 tokens: 32-bit token indices would overflow
+    assert lib.cpattn_fwd(p, p, p, p, p, 2, 1 << 30, 1, 1, 64, 1, 1, None) == -1
+    assert lib.cpattn_bwd_workspace_bytes(2, 1 << 30, 1, 1, 64, 1) == 0
+    assert lib.cpattn_fwd_unfused(p, p, p, p, p, p, 1 << 40, 2, 1 << 30, 1, 1, 64, 1, 1, None) == -1

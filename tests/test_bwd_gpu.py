@@ -104,3 +104,27 @@ def test_bwd_stages_in_any_order_match_the_whole():
     assert cpattn_device_status() == 0
     for got, want in zip((dq, dk, dv), ref):
         assert torch.equal(got, want)
+
+
+def test_bwd_long_context_properties_and_sampled_rows():
+    """128K tokens, cp = 16 (Q, K ~ N(0, 4)): dQ at seeded rows against the
+    oracle, and two identities over the full gradients that hold at any size:
+    sum_j dV_j = sum_t dO_t over a KV group's query heads (softmax rows sum to
+    one) and sum_j dK_j = 0 (each row of dS sums to zero)."""
+    base = WORKLOADS["long_b1_s131072_h32kv8_d128_cp16"]
+    w = Workload("long_bwd", b=1, s=base.s, hq=base.hq, hkv=base.hkv, d=base.d, cp=base.cp, q_std=base.q_std,
+                 k_std=base.k_std, backward=True, seed=base.seed + 50)
+    x = make_inputs(w, device="cuda")
+    dq, dk, dv = _run(w, x)
+    G = w.hq // w.hkv
+    do_sum = x["do"].double().sum(dim=1).reshape(w.b, w.hkv, G, w.d).sum(dim=2)  # [b, hkv, d]
+    dv_sum = dv.double().sum(dim=1)                                            # [b, hkv, d]
+    assert ((dv_sum - do_sum).norm() / do_sum.norm()).item() <= 1e-2
+    dk_sum = dk.double().sum(dim=1)
+    assert (dk_sum.abs() <= 1e-2 * dk.double().abs().sum(dim=1) + 1e-6).all()
+    rows = sample_rows(w, 128, seed=w.seed + 3)
+    cpu = {k: t.cpu() for k, t in x.items()}
+    del x
+    dq_r, _, _ = oracle.attention_backward(cpu["q"], cpu["k"], cpu["v"], cpu["do"], causal=True, dq_rows=rows,
+                                           dkv_heads=[], row_block=64)
+    assert rel_l2(dq.float().cpu()[:, rows], dq_r) <= REL_L2

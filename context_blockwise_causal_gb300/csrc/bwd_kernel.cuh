@@ -61,8 +61,11 @@ enum BwdStatusBits : unsigned int {
 
 // Position of query row `row` of (chunk, tile) of head `h` in the
 // tile-padded L/D vectors.
-__device__ __forceinline__ int64_t ld_pos(const CpGeom& g, int ntp, int bi, int h, int chunk, int tile, int row) {
-  return int64_t(bi * g.hq + h) * ntp + (chunk * g.tpc + tile) * kTile + row;
+// Row `row` of tile `tile` of chunk `chunk` of sequence `seq` (tpc tiles per
+// chunk) in the tile-padded L/D vectors [sequences, hq, ntp].
+__device__ __forceinline__ int64_t ld_pos(const CpGeom& g, int ntp, int seq, int h, int chunk, int tile, int tpc,
+                                          int row) {
+  return int64_t(seq * g.hq + h) * ntp + (chunk * tpc + tile) * kTile + row;
 }
 
 // ---------------------------------------------------------------- preprocess
@@ -89,9 +92,21 @@ __global__ void __launch_bounds__(256) cpattn_bwd_pre_kernel(const BwdArgs a) {
         acc = fmaf(__uint_as_float(xs[k] & 0xffff0000u), __uint_as_float(ys[k] & 0xffff0000u), acc);
       }
     }
-    const int chunk = t / g.c;
-    const int in = t - chunk * g.c;
-    const int64_t pos = ld_pos(g, a.ntp, bi, h, chunk, in / kTile, in % kTile);
+    // the row's sequence (batch element, or the packed sample holding t)
+    int seq = bi, tl = t;
+    if (g.nseq > 0) {
+      int lo = 0, hi = g.nseq;  // cu[lo] <= t < cu[hi]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (g.cu[mid] <= t) lo = mid; else hi = mid;
+      }
+      seq = lo;
+      tl = t - g.cu[lo];
+    }
+    const SeqGeom q = seq_geom(g, seq);
+    const int chunk = tl / q.c;
+    const int in = tl - chunk * q.c;
+    const int64_t pos = ld_pos(g, a.ntp, seq, h, chunk, in / kTile, q.tpc, in % kTile);
     a.dvec[pos] = acc;
     a.lvec[pos] = a.lse[(int64_t(bi) * g.hq + h) * a.lse_stride + t] * 1.4426950408889634f;
   }
@@ -304,7 +319,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t item = 0;  // blocks loaded so far
       int ul = 0;
       auto load_item = [&](const BwdUnit& U, int chunk, int tile, int h) -> bool {
-        const int row = U.bi * g.s + chunk * g.c + tile * kTile;
+        const int row = U.tok0 + chunk * U.c + tile * kTile;
         const uint32_t qs = item % C::kQStages, os = item % C::kOStages;
         if (item >= C::kQStages &&
             !mbar_wait_lean(&q_empty[qs], ((item / C::kQStages) - 1) & 1, abort_flag, kWaitLimitNs))
@@ -318,7 +333,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive_expect_tx(&o_full[os], C::kTileBytes + C::kLDBytes);
         for (int x = 0; x < D; x += 64)
           tma_load_3d(sdO + os * C::kTileBytes + (x / 64) * (kTile * 128), &tmdo, &o_full[os], x, h, row);
-        const int64_t pos = ld_pos(g, a.ntp, U.bi, h, chunk, tile, 0);
+        const int64_t pos = ld_pos(g, a.ntp, U.seq, h, chunk, tile, U.tpc, 0);
         bulk_load(reinterpret_cast<uint8_t*>(sLD) + os * C::kLDBytes, a.lvec + pos, kTile * 4, &o_full[os]);
         bulk_load(reinterpret_cast<uint8_t*>(sLD) + os * C::kLDBytes + kTile * 4, a.dvec + pos, kTile * 4,
                   &o_full[os]);
@@ -329,6 +344,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int idx = snake_unit(rd, blockIdx.x, grid);
         if (idx >= num_units) break;
         const BwdUnit U = bwd_decode_unit(g, idx);
+        if (U.items == 0) continue;  // a tile a shorter packed sample does not have
         QWalk w(g, U);
         int chunk, tile;
         bool dg;
@@ -341,7 +357,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               first = false;
               if (ul > 0 && !(ok = mbar_wait_lean(kv_empty, (ul - 1) & 1, abort_flag, kWaitLimitNs))) break;
               mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
-              const int krow = U.bi * g.s + U.k_t0;
+              const int krow = U.tok0 + U.k_t0;
               for (int x = 0; x < D; x += 64) {
                 tma_load_3d(sK + (x / 64) * (kTile * 128), &tmk, kv_full, x, U.g, krow);
                 tma_load_3d(sV + (x / 64) * (kTile * 128), &tmv, kv_full, x, U.g, krow);
@@ -396,6 +412,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int idx = snake_unit(rd, blockIdx.x, grid);
         if (idx >= num_units) break;
         const BwdUnit U = bwd_decode_unit(g, idx);
+        if (U.items == 0) continue;  // a tile a shorter packed sample does not have
         const int n = U.items;
         // prologue: S^T and dP^T of the unit's first block. The S^T columns
         // are free once the element-wise warps have read the previous S^T;
@@ -477,13 +494,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int idx = snake_unit(rd, blockIdx.x, grid);
       if (idx >= num_units) break;
       const BwdUnit U = bwd_decode_unit(g, idx);
+      if (U.items == 0) continue;  // a tile a shorter packed sample does not have
       QWalk w(g, U);
       int chunk = 0, tile = 0;
       bool dg = false;
       const bool key_ok = jr < U.k_valid;
       for (int j = 0; j < U.items && ok; ++j, ++i) {
         if (j % G == 0) w.next(chunk, tile, dg);
-        const int rem = g.c - tile * kTile;
+        const int rem = U.c - tile * kTile;
         const int q_valid = rem < kTile ? rem : kTile;
         const uint32_t os = i % C::kOStages;
         ok = mbar_wait_lean(&o_full[os], (i / C::kOStages) & 1, abort_flag, kWaitLimitNs) &&
@@ -551,7 +569,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // ---- dK, dV of the tile: TMEM -> bf16 -> global, 32 columns at a time
       if (!(ok = mbar_wait_lean(dkv_full, ul & 1, abort_flag, kWaitLimitNs))) break;
       tc_fence_after();
-      const int64_t off = ((int64_t(U.bi) * g.s + U.k_t0 + jr) * g.hkv + U.g) * D + hf * (D / 2);
+      const int64_t off = ((int64_t(U.tok0) + U.k_t0 + jr) * g.hkv + U.g) * D + hf * (D / 2);
 #pragma unroll
       for (int c0 = 0; c0 < D / 2; c0 += 32) {
         uint32_t rv[32], rk[32];
@@ -652,35 +670,6 @@ struct DqCfg {
   // and dO as bf16 A operands (D/2 columns each).
   static constexpr uint32_t kColS = 0, kColdP = 128, kColdQ = 256, kColQA = 256 + D, kColdOA = 256 + D + D / 2;
 };
-
-// dQ work units: one 128-row query tile of one head, longest first.
-__host__ __device__ inline int dq_num_units(const CpGeom& g) { return g.b * g.hq * 2 * g.cp * g.tpc; }
-
-__host__ __device__ inline FwdUnit dq_decode_unit(const CpGeom& g, int idx) {
-  // The forward's decomposition with one head per unit (h0 == h1), so the
-  // forward's CP-step key walk (KvWalk) applies as is.
-  FwdUnit U;
-  const int per = g.b * g.hq;
-  const int ntile = 2 * g.cp * g.tpc;
-  const int gt = (ntile - 1) - idx / per;
-  const int rest = idx % per;
-  U.bi = rest / g.hq;
-  U.h0 = U.h1 = rest % g.hq;
-  U.g0 = U.g1 = U.h0 / (g.hq / g.hkv);
-  U.store1 = false;
-  U.k = gt / g.tpc;
-  U.u = gt % g.tpc;
-  U.half = U.k >= g.cp ? 1 : 0;
-  U.r = U.half ? 2 * g.cp - 1 - U.k : U.k;
-  U.q_t0 = U.k * g.c + U.u * kTile;
-  const int rem = g.c - U.u * kTile;
-  U.q_valid = rem < kTile ? rem : kTile;
-  if (g.causal)
-    U.n = (U.half ? (2 * g.cp - 1 - U.r) * g.tpc : U.r * g.tpc) + U.u + 1;
-  else
-    U.n = 2 * g.cp * g.tpc;
-  return U;
-}
 
 // Query-tile-stationary dQ. One CTA per SM, 10 warps:
 //   warps 0-7  element-wise; warp w covers TMEM lanes 32*(w%4).. (query rows)
@@ -795,11 +784,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int idx = snake_unit(rd, blockIdx.x, grid);
         if (idx >= num_units) break;
         const FwdUnit U = dq_decode_unit(g, idx);
+        if (U.n == 0) continue;  // a tile a shorter packed sample does not have
         // the Q/dO stage is free once the element-wise warps copied the
         // previous unit's tiles into TMEM
         if (ul > 0 && !(ok = mbar_wait_lean(q_empty, (ul - 1) & 1, abort_flag, kWaitLimitNs))) break;
         mbar_arrive_expect_tx(q_full, 2 * C::kTileBytes);
-        const int qrow = U.bi * g.s + U.q_t0;
+        const int qrow = U.tok0 + U.q_t0;
         for (int x = 0; x < D; x += 64) {
           tma_load_3d(sQ + (x / 64) * (kTile * 128), &tmq, q_full, x, U.h0, qrow);
           tma_load_3d(sdO + (x / 64) * (kTile * 128), &tmdo, q_full, x, U.h0, qrow);
@@ -808,7 +798,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         int chunk, tile;
         bool dg;
         while (ok && w.next(chunk, tile, dg)) {
-          const int row = U.bi * g.s + chunk * g.c + tile * kTile;
+          const int row = U.tok0 + chunk * U.c + tile * kTile;
           // V before K: V is released by the dP MMA, K only after dQ
           ok = load(&tmv, U.g0, row) && load(&tmk, U.g0, row);
         }
@@ -860,6 +850,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int idx = snake_unit(rd, blockIdx.x, grid);
         if (idx >= num_units) break;
         const FwdUnit U = dq_decode_unit(g, idx);
+        if (U.n == 0) continue;  // a tile a shorter packed sample does not have
         const int n = U.n;
         // prologue: S and dP of the unit's first key tile, once Q/dO are in
         // TMEM. The S columns are free once the previous S was read; the dP
@@ -936,6 +927,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int idx = snake_unit(rd, blockIdx.x, grid);
       if (idx >= num_units) break;
       const FwdUnit U = dq_decode_unit(g, idx);
+      if (U.n == 0) continue;  // a tile a shorter packed sample does not have
       // ---- this row's Q and dO (columns hf*D/2 ..) into TMEM as packed bf16
       ok = mbar_wait_lean(q_full, ul & 1, abort_flag, kWaitLimitNs) &&
            (ul == 0 || mbar_wait_lean(qa_empty, (ul - 1) & 1, abort_flag, kWaitLimitNs));
@@ -974,7 +966,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       // this row's L*log2e and D (padded rows of a ragged tile read arbitrary
       // values; their dQ is never stored)
-      const int64_t pos = ld_pos(g, a.ntp, U.bi, U.h0, U.k, U.u, jr);
+      const int64_t pos = ld_pos(g, a.ntp, U.seq, U.h0, U.k, U.u, U.tpc, jr);
       const float l2 = a.lvec[pos];
       const float dd = a.dvec[pos];
       KvWalk w(g, U);
@@ -982,7 +974,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         int chunk = 0, tile = 0;
         bool dg = false;
         w.next(chunk, tile, dg);
-        const int rem = g.c - tile * kTile;
+        const int rem = U.c - tile * kTile;
         const int n_valid = rem < kTile ? rem : kTile;
         if (!(ok = mbar_wait_lean(s_full, jt & 1, abort_flag, kWaitLimitNs))) break;
         tc_fence_after();
@@ -1043,7 +1035,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(dq_empty);
       if (jr < U.q_valid) {
-        __nv_bfloat16* dst = a.dq + ((int64_t(U.bi) * g.s + U.q_t0 + jr) * g.hq + U.h0) * D + hf * (D / 2);
+        __nv_bfloat16* dst = a.dq + ((int64_t(U.tok0) + U.q_t0 + jr) * g.hq + U.h0) * D + hf * (D / 2);
 #pragma unroll
         for (int i = 0; i < D / 2; i += 8) {
           uint4 pk;

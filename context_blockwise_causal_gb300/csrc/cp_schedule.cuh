@@ -26,16 +26,49 @@
 namespace cpattn {
 
 constexpr int kTile = 128;
+constexpr int kMaxSeqs = 512;  // packed samples per call (their offsets travel as kernel parameters)
 
+// Geometry of a call. Either a uniform batch (nseq == 0: b sequences of s
+// tokens, chunk length c, tpc tiles per chunk) or packed samples (nseq > 0:
+// b == 1, s == total tokens, sample i is tokens [cu[i], cu[i+1]) with its own
+// chunk length; tpc is the largest sample's tile count).
 struct CpGeom {
   int b, s, hq, hkv, cp, causal;
-  int c;       // chunk length
-  int tpc;     // tiles per chunk
+  int c;       // chunk length (uniform batch)
+  int tpc;     // tiles per chunk (the largest sample's when packed)
   int npairs;  // query-head pairs per batch element: ceil(hq / 2)
+  int nseq = 0;
+  int cu[kMaxSeqs + 1];
 };
 
+// A sequence's placement: its first token in the token rows, its chunk
+// length and tiles per chunk (0 tiles for an empty sample).
+struct SeqGeom {
+  int tok0, c, tpc;
+};
+
+__host__ __device__ inline int num_seqs(const CpGeom& g) { return g.nseq > 0 ? g.nseq : g.b; }
+
+__host__ __device__ inline SeqGeom seq_geom(const CpGeom& g, int i) {
+  SeqGeom q;
+  if (g.nseq == 0) {
+    q.tok0 = i * g.s;
+    q.c = g.c;
+    q.tpc = g.tpc;
+  } else {
+    q.tok0 = g.cu[i];
+    q.c = (g.cu[i + 1] - g.cu[i]) / (2 * g.cp);
+    q.tpc = (q.c + kTile - 1) / kTile;
+  }
+  return q;
+}
+
 struct FwdUnit {
-  int bi;        // batch element
+  int bi;        // batch element (0 for packed samples)
+  int seq;       // batch element or packed sample
+  int tok0;      // its first token row
+  int lse_t0;    // offset of its positions in an LSE row (the sample's start when packed)
+  int c, tpc;    // its chunk length and tiles per chunk
   int h0, h1;    // query heads of the two sub-tiles (h1 == h0 for an odd tail)
   int g0, g1;    // their KV heads
   bool store1;   // sub-tile 1 is a distinct head (its output is stored)
@@ -44,21 +77,49 @@ struct FwdUnit {
   int r, half;   // owning virtual rank and which of its two chunks
   int q_t0;      // first token of the query tile (within the sequence)
   int q_valid;   // rows of the tile inside the chunk
-  int n;         // number of key tiles the unit visits
+  int n;         // number of key tiles the unit visits (0: no such tile in a shorter packed sample)
 };
 
-__host__ __device__ inline int fwd_num_units(const CpGeom& g) { return g.b * g.npairs * 2 * g.cp * g.tpc; }
+__host__ __device__ inline int fwd_num_units(const CpGeom& g) {
+  return num_seqs(g) * g.npairs * 2 * g.cp * g.tpc;
+}
+
+// The query tile with global tile index gt of unit U's sequence (U.seq set).
+__host__ __device__ inline void fill_query_tile(const CpGeom& g, FwdUnit& U, int gt) {
+  const SeqGeom q = seq_geom(g, U.seq);
+  U.bi = g.nseq > 0 ? 0 : U.seq;
+  U.tok0 = q.tok0;
+  U.lse_t0 = g.nseq > 0 ? q.tok0 : 0;
+  U.c = q.c;
+  U.tpc = q.tpc;
+  if (gt >= 2 * g.cp * U.tpc) {  // beyond this packed sample's tiles
+    U.k = U.u = U.half = U.r = U.q_t0 = U.q_valid = 0;
+    U.n = 0;
+    return;
+  }
+  U.k = gt / U.tpc;
+  U.u = gt % U.tpc;
+  U.half = U.k >= g.cp ? 1 : 0;
+  U.r = U.half ? 2 * g.cp - 1 - U.k : U.k;
+  U.q_t0 = U.k * U.c + U.u * kTile;
+  const int rem = U.c - U.u * kTile;
+  U.q_valid = rem < kTile ? rem : kTile;
+  if (g.causal)
+    U.n = (U.half ? (2 * g.cp - 1 - U.r) * U.tpc : U.r * U.tpc) + U.u + 1;
+  else
+    U.n = 2 * g.cp * U.tpc;
+}
 
 // Units are numbered in longest-first order: the causal cost of the query
 // tile with global tile index gt is gt+1 key tiles, so index 0 is the last
-// tile of the sequence.
+// tile of the sequence (of the longest samples when packed; tile indices a
+// shorter sample does not have decode as empty units, n == 0).
 __host__ __device__ inline FwdUnit fwd_decode_unit(const CpGeom& g, int idx) {
   FwdUnit U;
-  const int per = g.b * g.npairs;
-  const int ntile = 2 * g.cp * g.tpc;
-  const int gt = (ntile - 1) - idx / per;
+  const int per = num_seqs(g) * g.npairs;
+  const int gt = (2 * g.cp * g.tpc - 1) - idx / per;
   const int rest = idx % per;
-  U.bi = rest / g.npairs;
+  U.seq = rest / g.npairs;
   const int pr = rest % g.npairs;
   const int G = g.hq / g.hkv;
   U.h0 = 2 * pr;
@@ -66,17 +127,25 @@ __host__ __device__ inline FwdUnit fwd_decode_unit(const CpGeom& g, int idx) {
   U.h1 = U.store1 ? 2 * pr + 1 : 2 * pr;
   U.g0 = U.h0 / G;
   U.g1 = U.h1 / G;
-  U.k = gt / g.tpc;
-  U.u = gt % g.tpc;
-  U.half = U.k >= g.cp ? 1 : 0;
-  U.r = U.half ? 2 * g.cp - 1 - U.k : U.k;
-  U.q_t0 = U.k * g.c + U.u * kTile;
-  const int rem = g.c - U.u * kTile;
-  U.q_valid = rem < kTile ? rem : kTile;
-  if (g.causal)
-    U.n = (U.half ? (2 * g.cp - 1 - U.r) * g.tpc : U.r * g.tpc) + U.u + 1;
-  else
-    U.n = 2 * g.cp * g.tpc;
+  fill_query_tile(g, U, gt);
+  return U;
+}
+
+// dQ work units: one 128-row query tile of one head, longest first: the
+// forward's decomposition with one head per unit (h0 == h1), so the
+// forward's CP-step key walk (KvWalk) applies as is.
+__host__ __device__ inline int dq_num_units(const CpGeom& g) { return num_seqs(g) * g.hq * 2 * g.cp * g.tpc; }
+
+__host__ __device__ inline FwdUnit dq_decode_unit(const CpGeom& g, int idx) {
+  FwdUnit U;
+  const int per = num_seqs(g) * g.hq;
+  const int gt = (2 * g.cp * g.tpc - 1) - idx / per;
+  const int rest = idx % per;
+  U.seq = rest / g.hq;
+  U.h0 = U.h1 = rest % g.hq;
+  U.g0 = U.g1 = U.h0 / (g.hq / g.hkv);
+  U.store1 = false;
+  fill_query_tile(g, U, gt);
   return U;
 }
 
@@ -94,7 +163,7 @@ struct KvWalk {
   int last;  // last step walked
 
   __host__ __device__ KvWalk(const CpGeom& g, const FwdUnit& U)
-      : cp(g.cp), r(U.r), half(U.half), k(U.k), u(U.u), tpc(g.tpc), causal(g.causal), step(0), seg(0), v(0),
+      : cp(g.cp), r(U.r), half(U.half), k(U.k), u(U.u), tpc(U.tpc), causal(g.causal), step(0), seg(0), v(0),
         last(g.cp - 1) {}
 
   // Restrict the walk to the key tiles of CP step `st`.
@@ -198,32 +267,44 @@ struct KvWalk {
 // by the CTAs in flight and stay in L2. dK/dV of the tile accumulate on chip
 // over all its blocks.
 struct BwdUnit {
-  int bi, g;      // batch element, KV head
+  int bi, g;      // batch element (0 for packed samples), KV head
+  int seq;        // batch element or packed sample
+  int tok0;       // its first token row
+  int c, tpc;     // its chunk length and tiles per chunk
   int kc, v;      // key chunk and tile within it
   int gt;         // global tile index of the key tile: kc * tpc + v
   int k_t0;       // first key token
   int k_valid;    // keys of the tile inside the chunk
   int nq;         // number of query tiles that see the tile
-  int items;      // nq * (hq / hkv)
+  int items;      // nq * (hq / hkv); 0 for a tile a shorter packed sample does not have
 };
 
-__host__ __device__ inline int bwd_num_units(const CpGeom& g) { return g.b * g.hkv * 2 * g.cp * g.tpc; }
+__host__ __device__ inline int bwd_num_units(const CpGeom& g) { return num_seqs(g) * g.hkv * 2 * g.cp * g.tpc; }
 
 // Longest-first: the key tile with global tile index gt is seen by ntile-gt
 // query tiles (causal), so unit 0 is the first tile of the sequence.
 __host__ __device__ inline BwdUnit bwd_decode_unit(const CpGeom& g, int idx) {
   BwdUnit U;
-  const int per = g.b * g.hkv;
-  const int ntile = 2 * g.cp * g.tpc;
+  const int per = num_seqs(g) * g.hkv;
   const int gt = idx / per;
   const int rest = idx % per;
-  U.bi = rest / g.hkv;
+  U.seq = rest / g.hkv;
+  U.bi = g.nseq > 0 ? 0 : U.seq;
   U.g = rest % g.hkv;
+  const SeqGeom q = seq_geom(g, U.seq);
+  U.tok0 = q.tok0;
+  U.c = q.c;
+  U.tpc = q.tpc;
   U.gt = gt;
-  U.kc = gt / g.tpc;
-  U.v = gt % g.tpc;
-  U.k_t0 = U.kc * g.c + U.v * kTile;
-  const int rem = g.c - U.v * kTile;
+  const int ntile = 2 * g.cp * U.tpc;
+  if (gt >= ntile) {  // beyond this packed sample's tiles
+    U.kc = U.v = U.k_t0 = U.k_valid = U.nq = U.items = 0;
+    return U;
+  }
+  U.kc = gt / U.tpc;
+  U.v = gt % U.tpc;
+  U.k_t0 = U.kc * U.c + U.v * kTile;
+  const int rem = U.c - U.v * kTile;
   U.k_valid = rem < kTile ? rem : kTile;
   U.nq = g.causal ? ntile - gt : ntile;
   U.items = U.nq * (g.hq / g.hkv);
@@ -235,7 +316,7 @@ struct QWalk {
   int tpc, lo, gt_k, causal, gt;
 
   __host__ __device__ QWalk(const CpGeom& g, const BwdUnit& U)
-      : tpc(g.tpc), lo(g.causal ? U.gt : 0), gt_k(U.gt), causal(g.causal), gt(2 * g.cp * g.tpc - 1) {}
+      : tpc(U.tpc), lo(g.causal ? U.gt : 0), gt_k(U.gt), causal(g.causal), gt(2 * g.cp * U.tpc - 1) {}
 
   __host__ __device__ bool next(int& chunk, int& tile, bool& is_diag) {
     if (gt < lo) return false;

@@ -127,7 +127,7 @@ double default_scale(int d) { return 1.0 / std::sqrt(double(d)); }
 
 namespace {
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int b, int s, int hq, int hkv, int d,
-             int cp, int causal, double scale, void* stream, int64_t lse_stride = -1) {
+             int cp, int causal, double scale, void* stream, int64_t lse_stride = -1, const CpGeom* packed = nullptr) {
   if (!q || !k || !v || !o || !lse) return CPATTN_ERR_NULL_PTR;
   int rc = check_geometry(b, s, hq, hkv, d, cp);
   if (rc) return rc;
@@ -141,7 +141,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
       !encode_bf16_rows_heads_d(&tv, v, rows, hkv, d, kTile))
     return CPATTN_ERR_CUDA;
   FwdArgs args;
-  args.g = make_geom(b, s, hq, hkv, cp, causal);
+  args.g = packed ? *packed : make_geom(b, s, hq, hkv, cp, causal);
   args.o = static_cast<__nv_bfloat16*>(o);
   args.lse = lse;
   args.lse_stride = lse_stride < 0 ? s : lse_stride;
@@ -336,16 +336,20 @@ struct BwdLayout {
   int ntp;
 };
 
-BwdLayout bwd_layout(int b, int s, int hq, int d, int cp) {
-  (void)d;
+// nseq sequences of up to tpc tiles per chunk
+BwdLayout bwd_layout_tiles(int nseq, int tpc, int hq, int cp) {
   BwdLayout L;
-  const int c = s / (2 * cp);
-  const int tpc = (c + kTile - 1) / kTile;
   L.ntp = 2 * cp * tpc * kTile;
   L.lvec = 0;
-  L.dvec = align256(size_t(b) * hq * L.ntp * 4);
-  L.total = L.dvec + align256(size_t(b) * hq * L.ntp * 4);
+  L.dvec = align256(size_t(nseq) * hq * L.ntp * 4);
+  L.total = L.dvec + align256(size_t(nseq) * hq * L.ntp * 4);
   return L;
+}
+
+BwdLayout bwd_layout(int b, int s, int hq, int d, int cp) {
+  (void)d;
+  const int c = s / (2 * cp);
+  return bwd_layout_tiles(b, (c + kTile - 1) / kTile, hq, cp);
 }
 
 template <int D>
@@ -402,7 +406,7 @@ namespace {
 int prepare_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int b, int s, int hq, int hkv,
                 int d, int cp, int causal, double scale, CUtensorMap* maps, BwdArgs* args, DeviceInfo** di,
-                int64_t lse_stride = -1) {
+                int64_t lse_stride = -1, const CpGeom* packed = nullptr) {
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return CPATTN_ERR_NULL_PTR;
   int rc = check_geometry(b, s, hq, hkv, d, cp);
   if (rc) return rc;
@@ -410,7 +414,7 @@ int prepare_bwd(const void* q, const void* k, const void* v, const void* o, cons
                         static_cast<const void*>(dv), static_cast<const void*>(workspace)})
     if (!aligned16(p)) return CPATTN_ERR_MISALIGNED;
   if (reinterpret_cast<uintptr_t>(lse) & 3u) return CPATTN_ERR_MISALIGNED;
-  const BwdLayout L = bwd_layout(b, s, hq, d, cp);
+  const BwdLayout L = packed ? bwd_layout_tiles(packed->nseq, packed->tpc, hq, cp) : bwd_layout(b, s, hq, d, cp);
   if (workspace_bytes < L.total) return CPATTN_ERR_WORKSPACE_TOO_SMALL;
   if ((rc = device_info(di))) return rc;
   const uint64_t rows = uint64_t(b) * s;
@@ -420,7 +424,7 @@ int prepare_bwd(const void* q, const void* k, const void* v, const void* o, cons
       !encode_bf16_rows_heads_d(&maps[3], dout, rows, hq, d, kTile))
     return CPATTN_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  args->g = make_geom(b, s, hq, hkv, cp, causal);
+  args->g = packed ? *packed : make_geom(b, s, hq, hkv, cp, causal);
   args->ntp = L.ntp;
   args->o = static_cast<const __nv_bfloat16*>(o);
   args->dout = static_cast<const __nv_bfloat16*>(dout);
@@ -443,12 +447,12 @@ int prepare_bwd(const void* q, const void* k, const void* v, const void* o, cons
 namespace {
 int bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout, void* dq,
              void* dk, void* dv, void* workspace, size_t workspace_bytes, int b, int s, int hq, int hkv, int d, int cp,
-             int causal, double scale, void* stream, int64_t lse_stride = -1) {
+             int causal, double scale, void* stream, int64_t lse_stride = -1, const CpGeom* packed = nullptr) {
   CUtensorMap maps[4];
   BwdArgs args;
   DeviceInfo* di = nullptr;
   const int rc = prepare_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, b, s, hq, hkv, d, cp,
-                             causal, double(scale), maps, &args, &di, lse_stride);
+                             causal, double(scale), maps, &args, &di, lse_stride, packed);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return d == 128 ? launch_bwd<128>(maps[0], maps[1], maps[2], maps[3], args, di, st)
@@ -478,6 +482,27 @@ extern "C" int cpattn_bwd(const void* q, const void* k, const void* v, const voi
 namespace {
 // Checks the host sample offsets; returns the total token count or a
 // negative error code.
+// Packed-sample geometry (nseq <= kMaxSeqs): one launch covers every sample.
+CpGeom packed_geom(const int* cu, int nseq, int hq, int hkv, int cp, int causal) {
+  CpGeom g = make_geom(1, cu[nseq], hq, hkv, cp, causal);
+  g.nseq = nseq;
+  g.c = 0;  // per sample
+  int tpc = 0;
+  for (int i = 0; i <= nseq; ++i) g.cu[i] = cu[i];
+  for (int i = 0; i < nseq; ++i) {
+    const int c = (cu[i + 1] - cu[i]) / (2 * cp);
+    const int t = (c + kTile - 1) / kTile;
+    tpc = t > tpc ? t : tpc;
+  }
+  g.tpc = tpc;
+  return g;
+}
+
+bool packed_units_fit(const CpGeom& g) {
+  const int64_t per = int64_t(g.nseq) * 2 * g.cp * g.tpc;
+  return per * (g.npairs > g.hq ? g.npairs : g.hq) < (int64_t(1) << 31);
+}
+
 int64_t check_cu(const int* cu, int nseq, int cp) {
   if (!cu) return CPATTN_ERR_NULL_PTR;
   if (nseq < 1 || cp < 1 || cu[0] != 0) return CPATTN_ERR_INVALID_ARG;
@@ -499,6 +524,14 @@ extern "C" int cpattn_fwd_varlen(const void* q, const void* k, const void* v, vo
   if (!aligned16(lse)) return CPATTN_ERR_MISALIGNED;
   if (d != 64 && d != 128) return CPATTN_ERR_INVALID_ARG;
   const double sc = scale == 0.f ? default_scale(d) : double(scale);
+  if (total == 0) return CPATTN_OK;
+  if (nseq <= kMaxSeqs) {
+    if (hq < 1 || hkv < 1) return CPATTN_ERR_INVALID_ARG;
+    const CpGeom g = packed_geom(cu_seqlens, nseq, hq, hkv, cp, causal);
+    if (!packed_units_fit(g)) return CPATTN_ERR_INVALID_ARG;
+    return fwd_impl(q, k, v, o, lse, 1, int(total), hq, hkv, d, cp, causal, sc, stream, total, &g);
+  }
+  // more samples than one launch's parameters hold: a launch per sample
   for (int i = 0; i < nseq; ++i) {
     const int start = cu_seqlens[i], len = cu_seqlens[i + 1] - cu_seqlens[i];
     if (len == 0) continue;
@@ -513,6 +546,10 @@ extern "C" int cpattn_fwd_varlen(const void* q, const void* k, const void* v, vo
 
 extern "C" size_t cpattn_bwd_varlen_workspace_bytes(const int* cu_seqlens, int nseq, int hq, int hkv, int d, int cp) {
   if (check_cu(cu_seqlens, nseq, cp) < 0 || hq < 1 || hkv < 1 || hq % hkv || (d != 64 && d != 128)) return 0;
+  if (nseq <= kMaxSeqs) {
+    const CpGeom g = packed_geom(cu_seqlens, nseq, hq, hkv, cp, 1);
+    return g.tpc > 0 ? bwd_layout_tiles(nseq, g.tpc, hq, cp).total : 16;
+  }
   size_t need = 0;
   for (int i = 0; i < nseq; ++i) {
     const int len = cu_seqlens[i + 1] - cu_seqlens[i];
@@ -534,8 +571,16 @@ extern "C" int cpattn_bwd_varlen(const void* q, const void* k, const void* v, co
   if (!aligned16(lse)) return CPATTN_ERR_MISALIGNED;
   if (d != 64 && d != 128) return CPATTN_ERR_INVALID_ARG;
   const double sc = scale == 0.f ? default_scale(d) : double(scale);
-  // The samples run one after another on the stream, so they share the
-  // workspace (sized for the longest).
+  if (total == 0) return CPATTN_OK;
+  if (nseq <= kMaxSeqs) {
+    if (hq < 1 || hkv < 1) return CPATTN_ERR_INVALID_ARG;
+    const CpGeom g = packed_geom(cu_seqlens, nseq, hq, hkv, cp, causal);
+    if (!packed_units_fit(g)) return CPATTN_ERR_INVALID_ARG;
+    return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, 1, int(total), hq, hkv, d, cp,
+                    causal, sc, stream, total, &g);
+  }
+  // More samples than one launch's parameters hold: a launch per sample,
+  // one after another on the stream, sharing the workspace.
   for (int i = 0; i < nseq; ++i) {
     const int start = cu_seqlens[i], len = cu_seqlens[i + 1] - cu_seqlens[i];
     if (len == 0) continue;

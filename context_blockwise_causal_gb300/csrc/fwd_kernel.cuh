@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int idx = snake_unit(rd, blockIdx.x, grid);
         if (idx >= num_units) break;
         const FwdUnit U = fwd_decode_unit(g, idx);
+        if (U.n == 0) continue;  // a tile a shorter packed sample does not have
         KvWalk w(g, U);
         if constexpr (kStep) {
           w.only_step(a.step);
@@ -169,7 +170,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                mbar_wait_bounded(&q_empty[1], (ul - 1) & 1, abort_flag, kWaitLimitNs);
           if (!ok) break;
         }
-        const int qrow = U.bi * g.s + U.q_t0;
+        const int qrow = U.tok0 + U.q_t0;
         for (int sub = 0; sub < 2; ++sub) {
           mbar_arrive_expect_tx(&q_full[sub], C::kQBytes);
           const int h = sub ? U.h1 : U.h0;
@@ -192,7 +193,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           return true;
         };
         while (ok && w.next(chunk, tile, dg)) {
-          const int row = U.bi * g.s + chunk * g.c + tile * kTile;
+          const int row = U.tok0 + chunk * U.c + tile * kTile;
           ok = load(&tmk, U.g0, row) && (shared_kv || load(&tmk, U.g1, row)) && load(&tmv, U.g0, row) &&
                (shared_kv || load(&tmv, U.g1, row));
         }
@@ -246,6 +247,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int idx = snake_unit(rd, blockIdx.x, grid);
         if (idx >= num_units) break;
         const FwdUnit U = fwd_decode_unit(g, idx);
+        if (U.n == 0) continue;
         const bool shared_kv = U.g0 == U.g1;
         const int n = kStep ? KvWalk(g, U).step_tiles(a.step) : U.n;
         if (kStep && n == 0) continue;
@@ -336,6 +338,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int idx = snake_unit(rd, blockIdx.x, grid);
       if (idx >= num_units) break;
       const FwdUnit U = fwd_decode_unit(g, idx);
+      if (U.n == 0) continue;
       KvWalk w(g, U);
       int n = U.n;
       if constexpr (kStep) {
@@ -346,10 +349,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (row < U.q_valid && (sub == 0 || U.store1)) {
             const int h = sub ? U.h1 : U.h0;
             const int t = U.q_t0 + row;
-            float4* dst = reinterpret_cast<float4*>(a.o_part + ((int64_t(U.bi) * g.s + t) * g.hq + h) * D);
+            float4* dst = reinterpret_cast<float4*>(a.o_part + ((int64_t(U.tok0) + t) * g.hq + h) * D);
 #pragma unroll
             for (int c0 = 0; c0 < D / 4; ++c0) dst[c0] = make_float4(0.f, 0.f, 0.f, 0.f);
-            a.lse[(int64_t(U.bi) * g.hq + h) * a.lse_stride + t] = -INFINITY;
+            a.lse[(int64_t(U.bi) * g.hq + h) * a.lse_stride + U.lse_t0 + t] = -INFINITY;
           }
           continue;
         }
@@ -360,7 +363,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         int chunk = 0, tile = 0;
         bool dg = false;
         w.next(chunk, tile, dg);
-        const int rem = g.c - tile * kTile;
+        const int rem = U.c - tile * kTile;
         const int n_valid = rem < kTile ? rem : kTile;
         if (!(ok = mbar_wait_bounded(&s_full[sub], scnt & 1, abort_flag, kWaitLimitNs))) break;
         ++scnt;
@@ -467,17 +470,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int h = sub ? U.h1 : U.h0;
         const int t = U.q_t0 + row;
         const float inv = 1.f / l;
-        float4* dst = reinterpret_cast<float4*>(a.o_part + ((int64_t(U.bi) * g.s + t) * g.hq + h) * D);
+        float4* dst = reinterpret_cast<float4*>(a.o_part + ((int64_t(U.tok0) + t) * g.hq + h) * D);
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 4)
           dst[c0 / 4] = make_float4(__uint_as_float(ov[c0]) * inv, __uint_as_float(ov[c0 + 1]) * inv,
                                     __uint_as_float(ov[c0 + 2]) * inv, __uint_as_float(ov[c0 + 3]) * inv);
-        a.lse[(int64_t(U.bi) * g.hq + h) * a.lse_stride + t] = (m_used + log2f(l)) * 0.69314718055994530942f;
+        a.lse[(int64_t(U.bi) * g.hq + h) * a.lse_stride + U.lse_t0 + t] = (m_used + log2f(l)) * 0.69314718055994530942f;
       } else if (store) {
         const int h = sub ? U.h1 : U.h0;
         const int t = U.q_t0 + row;
         const float inv = 1.f / l;
-        __nv_bfloat16* dst = a.o + ((int64_t(U.bi) * g.s + t) * g.hq + h) * D;
+        __nv_bfloat16* dst = a.o + ((int64_t(U.tok0) + t) * g.hq + h) * D;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 8) {
           uint4 pkv;
@@ -487,7 +490,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           pkv.w = pack_bf16x2(__uint_as_float(ov[c0 + 6]) * inv, __uint_as_float(ov[c0 + 7]) * inv);
           *reinterpret_cast<uint4*>(dst + c0) = pkv;
         }
-        a.lse[(int64_t(U.bi) * g.hq + h) * a.lse_stride + t] = (m_used + log2f(l)) * 0.69314718055994530942f;
+        a.lse[(int64_t(U.bi) * g.hq + h) * a.lse_stride + U.lse_t0 + t] = (m_used + log2f(l)) * 0.69314718055994530942f;
       }
       ++ul;
     }

@@ -148,11 +148,14 @@ int cpattn_lse_merge(const float* o_a, const float* lse_a, const float* o_b, con
  *   cu_seqlens: HOST int32 [nseq + 1] sample offsets, 0 = cu[0] <= ... <=
  *               cu[nseq] = total (read during the call only).
  *   scale:      0 selects 1/sqrt(d); otherwise as cpattn_fwd_ex.
- * The samples are launched one after another on `stream` (one forward
- * launch, or three backward launches, per sample). cpattn_bwd_varlen needs a
- * workspace of cpattn_bwd_varlen_workspace_bytes(...) bytes (the largest
- * sample's), shared by the samples. Errors as cpattn_fwd / cpattn_bwd;
- * malformed offsets -> CPATTN_ERR_INVALID_ARG.
+ * Up to 512 samples run in one launch per kernel (the offsets travel as
+ * kernel parameters; work units are dealt longest tile first across all
+ * samples); with more samples each sample is launched on its own, one after
+ * another on `stream`. cpattn_bwd_varlen needs a workspace of
+ * cpattn_bwd_varlen_workspace_bytes(...) bytes (per sample two fp32 vectors
+ * padded to the longest sample's tiles; for more than 512 samples, the
+ * longest sample's alone). Errors as cpattn_fwd / cpattn_bwd; malformed
+ * offsets -> CPATTN_ERR_INVALID_ARG.
  */
 int cpattn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
                       int nseq, int hq, int hkv, int d, int cp, int causal, float scale, void* stream);

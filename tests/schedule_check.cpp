@@ -1,12 +1,18 @@
-// Brute-force check of the forward work decomposition (host build).
+// Brute-force check of the kernels' work decomposition (host build).
 // For each geometry given on the command line it verifies that
 //   * the snake assignment gives every unit to exactly one CTA,
-//   * each unit's key walk has exactly n tiles, in CP-step order,
-//   * over all units, every (batch, head, query, key) pair the mask allows is
-//     computed exactly once and no other pair is.
+//   * units come longest-first, each key walk has exactly n tiles in CP-step
+//     order, and the single-step walks, step after step, give the same tiles,
+//   * over all forward units, over all dQ units, and over all backward
+//     (key-tile) units, every (head, query, key) pair the mask allows is
+//     computed exactly once and no other pair is -- in particular no pair
+//     crosses a packed-sample boundary.
+// Geometries: "U b s hq hkv cp causal grid" (a uniform batch) or
+// "P nseq len_1 .. len_nseq hq hkv cp causal grid" (packed samples).
 // Prints "ok" per geometry or the first violation, exit code 1 on failure.
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <algorithm>
 #include <vector>
 
@@ -14,14 +20,78 @@
 
 using namespace cpattn;
 
-static int verify(const CpGeom& g, const std::vector<unsigned char>& count, const char* what);
+struct Rows {
+  int total;                 // token rows
+  std::vector<int> seq_of;   // sequence of each row
+  std::vector<int> pos_of;   // position of each row within its sequence
+};
 
-static int check(int b, int s, int hq, int hkv, int cp, int causal, int grid) {
-  CpGeom g;
-  g.b = b; g.s = s; g.hq = hq; g.hkv = hkv; g.cp = cp; g.causal = causal;
-  g.c = s / (2 * cp);
-  g.tpc = (g.c + kTile - 1) / kTile;
-  g.npairs = (hq + 1) / 2;
+static Rows rows_of(const CpGeom& g) {
+  Rows R;
+  R.total = g.b * g.s;
+  R.seq_of.assign(R.total, 0);
+  R.pos_of.assign(R.total, 0);
+  for (int i = 0; i < num_seqs(g); ++i) {
+    const int t0 = g.nseq > 0 ? g.cu[i] : i * g.s;
+    const int len = g.nseq > 0 ? g.cu[i + 1] - g.cu[i] : g.s;
+    for (int t = 0; t < len; ++t) {
+      R.seq_of[t0 + t] = i;
+      R.pos_of[t0 + t] = t;
+    }
+  }
+  return R;
+}
+
+static int verify(const CpGeom& g, const Rows& R, const std::vector<unsigned char>& count, const char* what) {
+  const size_t T = R.total;
+  for (int h = 0; h < g.hq; ++h)
+    for (int qa = 0; qa < R.total; ++qa)
+      for (int ka = 0; ka < R.total; ++ka) {
+        const bool same = R.seq_of[qa] == R.seq_of[ka];
+        const int want = same && (!g.causal || R.pos_of[ka] <= R.pos_of[qa]) ? 1 : 0;
+        const int got = count[size_t(h) * T * T + size_t(qa) * T + ka];
+        if (got != want) {
+          printf("%s pair (%d,%d) head %d: count %d want %d\n", what, qa, ka, h, got, want);
+          return 1;
+        }
+      }
+  return 0;
+}
+
+static int mark(std::vector<unsigned char>& count, const Rows& R, int h, int qa, int ka, const char* what) {
+  unsigned char& c = count[size_t(h) * R.total * R.total + size_t(qa) * R.total + ka];
+  if (c) {
+    printf("%s pair (%d,%d) head %d computed twice\n", what, qa, ka, h);
+    return 1;
+  }
+  c = 1;
+  return 0;
+}
+
+// Walk one query-tile unit (forward sub-tile or dQ unit) and mark its pairs.
+static int walk_query_unit(const CpGeom& g, const Rows& R, const FwdUnit& U, int h, std::vector<unsigned char>& count,
+                           const char* what) {
+  KvWalk w(g, U);
+  int chunk, tile, nt = 0;
+  bool dg;
+  while (w.next(chunk, tile, dg)) {
+    ++nt;
+    const int rem = U.c - tile * kTile;
+    const int nv = rem < kTile ? rem : kTile;
+    for (int row = 0; row < U.q_valid; ++row)
+      for (int col = 0; col < nv; ++col) {
+        if (dg && col > row) continue;
+        const int qa = U.tok0 + U.q_t0 + row, ka = U.tok0 + chunk * U.c + tile * kTile + col;
+        if (mark(count, R, h, qa, ka, what)) return -1;
+      }
+  }
+  return nt;
+}
+
+static int check(const CpGeom& g, int grid) {
+  const Rows R = rows_of(g);
+  std::vector<unsigned char> count(size_t(g.hq) * R.total * R.total, 0);
+  // ---- forward
   const int nu = fwd_num_units(g);
   std::vector<int> seen(nu, 0);
   for (int bid = 0; bid < grid; ++bid)
@@ -32,39 +102,24 @@ static int check(int b, int s, int hq, int hkv, int cp, int causal, int grid) {
     }
   for (int i = 0; i < nu; ++i)
     if (seen[i] != 1) { printf("unit %d assigned %d times\n", i, seen[i]); return 1; }
-  // count[(b*hq + h) * s * s + t * s + j]
-  std::vector<unsigned char> count(size_t(b) * hq * s * s, 0);
   int prev_n = 1 << 30;
   for (int idx = 0; idx < nu; ++idx) {
-    FwdUnit U = fwd_decode_unit(g, idx);
-    if (causal && U.n > prev_n) { printf("units not in longest-first order at %d\n", idx); return 1; }
+    const FwdUnit U = fwd_decode_unit(g, idx);
+    if (U.n == 0) continue;  // a tile a shorter packed sample does not have
+    if (g.causal && g.nseq == 0 && U.n > prev_n) { printf("units not in longest-first order at %d\n", idx); return 1; }
     prev_n = U.n;
-    KvWalk w(g, U);
-    int chunk, tile, nt = 0;
-    bool dg;
-    while (w.next(chunk, tile, dg)) {
-      ++nt;
-      const int rem = g.c - tile * kTile;
-      const int nv = rem < kTile ? rem : kTile;
-      for (int sub = 0; sub < 2; ++sub) {
-        if (sub == 1 && !U.store1) continue;
-        const int h = sub ? U.h1 : U.h0;
-        if (h / (hq / hkv) != (sub ? U.g1 : U.g0)) { printf("bad kv head\n"); return 1; }
-        for (int row = 0; row < U.q_valid; ++row)
-          for (int col = 0; col < nv; ++col) {
-            if (dg && col > row) continue;
-            const int t = U.q_t0 + row, j = chunk * g.c + tile * kTile + col;
-            unsigned char& c = count[(size_t(U.bi) * hq + h) * s * s + size_t(t) * s + j];
-            if (c) { printf("pair (%d,%d) head %d computed twice\n", t, j, h); return 1; }
-            c = 1;
-          }
-      }
+    for (int sub = 0; sub < 2; ++sub) {
+      if (sub == 1 && !U.store1) continue;
+      const int h = sub ? U.h1 : U.h0;
+      if (h / (g.hq / g.hkv) != (sub ? U.g1 : U.g0)) { printf("bad kv head\n"); return 1; }
+      const int nt = walk_query_unit(g, R, U, h, count, "forward");
+      if (nt < 0) return 1;
+      if (nt != U.n) { printf("unit %d: walk has %d tiles, n = %d\n", idx, nt, U.n); return 1; }
     }
-    if (nt != U.n) { printf("unit %d: walk has %d tiles, n = %d\n", idx, nt, U.n); return 1; }
     // the single-step walks, step after step, give the same tiles in order
     KvWalk full(g, U);
     int tot = 0;
-    for (int st = 0; st < cp; ++st) {
+    for (int st = 0; st < g.cp; ++st) {
       KvWalk one(g, U);
       one.only_step(st);
       int c1, t1, c2, t2, ns = 0;
@@ -76,69 +131,107 @@ static int check(int b, int s, int hq, int hkv, int cp, int causal, int grid) {
           return 1;
         }
       }
-      if (ns != one.step_tiles(st)) { printf("unit %d: step %d has %d tiles, step_tiles %d\n", idx, st, ns, one.step_tiles(st)); return 1; }
+      if (ns != one.step_tiles(st)) {
+        printf("unit %d: step %d has %d tiles, step_tiles %d\n", idx, st, ns, one.step_tiles(st));
+        return 1;
+      }
       tot += ns;
     }
     if (tot != U.n) { printf("unit %d: steps sum to %d tiles, n = %d\n", idx, tot, U.n); return 1; }
   }
-  if (verify(g, count, "forward")) return 1;
-  // backward: key-tile units walking the query tiles that see them
+  if (verify(g, R, count, "forward")) return 1;
+  // ---- dQ units: one query tile of one head
+  std::fill(count.begin(), count.end(), 0);
+  const int nd = dq_num_units(g);
+  for (int idx = 0; idx < nd; ++idx) {
+    const FwdUnit U = dq_decode_unit(g, idx);
+    if (U.n == 0) continue;
+    const int nt = walk_query_unit(g, R, U, U.h0, count, "dq");
+    if (nt < 0) return 1;
+    if (nt != U.n) { printf("dq unit %d: walk has %d tiles, n = %d\n", idx, nt, U.n); return 1; }
+  }
+  if (verify(g, R, count, "dq")) return 1;
+  // ---- backward: key-tile units walking the query tiles that see them
   std::fill(count.begin(), count.end(), 0);
   const int nb = bwd_num_units(g);
-  const int G = hq / hkv;
+  const int G = g.hq / g.hkv;
   int prev_items = 1 << 30;
   for (int idx = 0; idx < nb; ++idx) {
-    BwdUnit U = bwd_decode_unit(g, idx);
-    if (causal && U.items > prev_items) { printf("bwd units not longest-first at %d\n", idx); return 1; }
+    const BwdUnit U = bwd_decode_unit(g, idx);
+    if (U.items == 0) continue;
+    if (g.causal && g.nseq == 0 && U.items > prev_items) { printf("bwd units not longest-first at %d\n", idx); return 1; }
     prev_items = U.items;
     QWalk w(g, U);
     int chunk, tile, nt = 0;
     bool dg;
     while (w.next(chunk, tile, dg)) {
       ++nt;
-      const int rem = g.c - tile * kTile;
+      const int rem = U.c - tile * kTile;
       const int qv = rem < kTile ? rem : kTile;
       for (int h = U.g * G; h < (U.g + 1) * G; ++h)
         for (int row = 0; row < qv; ++row)
           for (int col = 0; col < U.k_valid; ++col) {
             if (dg && col > row) continue;
-            const int t = chunk * g.c + tile * kTile + row, j = U.k_t0 + col;
-            unsigned char& c = count[(size_t(U.bi) * hq + h) * s * s + size_t(t) * s + j];
-            if (c) { printf("bwd pair (%d,%d) head %d computed twice\n", t, j, h); return 1; }
-            c = 1;
+            const int qa = U.tok0 + chunk * U.c + tile * kTile + row, ka = U.tok0 + U.k_t0 + col;
+            if (mark(count, R, h, qa, ka, "bwd")) return 1;
           }
     }
     if (nt != U.nq) { printf("bwd unit %d: walk has %d tiles, nq = %d\n", idx, nt, U.nq); return 1; }
     if (U.items != nt * G) { printf("bwd unit %d: items mismatch\n", idx); return 1; }
   }
-  return verify(g, count, "backward");
-}
-
-static int verify(const CpGeom& g, const std::vector<unsigned char>& count, const char* what) {
-  const int b = g.b, hq = g.hq, s = g.s, causal = g.causal;
-  for (int bi = 0; bi < b; ++bi)
-    for (int h = 0; h < hq; ++h)
-      for (int t = 0; t < s; ++t)
-        for (int j = 0; j < s; ++j) {
-          const int want = (!causal || j <= t) ? 1 : 0;
-          if (count[(size_t(bi) * hq + h) * s * s + size_t(t) * s + j] != want) {
-            printf("%s pair (%d,%d) batch %d head %d: count %d want %d\n", what, t, j, bi, h,
-                   count[(size_t(bi) * hq + h) * s * s + size_t(t) * s + j], want);
-            return 1;
-          }
-        }
-  return 0;
+  return verify(g, R, count, "backward");
 }
 
 int main(int argc, char** argv) {
-  // args: groups of 7 ints: b s hq hkv cp causal grid
-  int fails = 0;
-  for (int i = 1; i + 6 < argc; i += 7) {
-    int v[7];
-    for (int k = 0; k < 7; ++k) v[k] = atoi(argv[i + k]);
-    int rc = check(v[0], v[1], v[2], v[3], v[4], v[5], v[6]);
-    printf("%s b=%d s=%d hq=%d hkv=%d cp=%d causal=%d grid=%d\n", rc ? "FAIL" : "ok", v[0], v[1], v[2], v[3], v[4],
-           v[5], v[6]);
+  int fails = 0, i = 1;
+  while (i < argc) {
+    CpGeom g;
+    char desc[256];
+    int grid;
+    if (!strcmp(argv[i], "U") && i + 7 < argc) {
+      g.b = atoi(argv[i + 1]);
+      g.s = atoi(argv[i + 2]);
+      g.hq = atoi(argv[i + 3]);
+      g.hkv = atoi(argv[i + 4]);
+      g.cp = atoi(argv[i + 5]);
+      g.causal = atoi(argv[i + 6]);
+      grid = atoi(argv[i + 7]);
+      g.c = g.s / (2 * g.cp);
+      g.tpc = (g.c + kTile - 1) / kTile;
+      g.nseq = 0;
+      snprintf(desc, sizeof desc, "b=%d s=%d hq=%d hkv=%d cp=%d causal=%d grid=%d", g.b, g.s, g.hq, g.hkv, g.cp,
+               g.causal, grid);
+      i += 8;
+    } else if (!strcmp(argv[i], "P") && i + 1 < argc) {
+      const int n = atoi(argv[i + 1]);
+      if (n < 1 || n > kMaxSeqs || i + 2 + n + 4 >= argc) { printf("bad packed spec\n"); return 1; }
+      g.nseq = n;
+      g.cu[0] = 0;
+      for (int k = 0; k < n; ++k) g.cu[k + 1] = g.cu[k] + atoi(argv[i + 2 + k]);
+      int j = i + 2 + n;
+      g.hq = atoi(argv[j]);
+      g.hkv = atoi(argv[j + 1]);
+      g.cp = atoi(argv[j + 2]);
+      g.causal = atoi(argv[j + 3]);
+      grid = atoi(argv[j + 4]);
+      g.b = 1;
+      g.s = g.cu[n];
+      g.c = 0;
+      g.tpc = 0;
+      for (int k = 0; k < n; ++k) {
+        const int c = (g.cu[k + 1] - g.cu[k]) / (2 * g.cp);
+        g.tpc = std::max(g.tpc, (c + kTile - 1) / kTile);
+      }
+      snprintf(desc, sizeof desc, "packed nseq=%d total=%d hq=%d hkv=%d cp=%d causal=%d grid=%d", n, g.s, g.hq,
+               g.hkv, g.cp, g.causal, grid);
+      i = j + 5;
+    } else {
+      printf("bad arguments at %s\n", argv[i]);
+      return 1;
+    }
+    g.npairs = (g.hq + 1) / 2;
+    const int rc = check(g, grid);
+    printf("%s %s\n", rc ? "FAIL" : "ok", desc);
     fails += rc;
   }
   return fails ? 1 : 0;

@@ -151,8 +151,10 @@ def test_varlen_offsets_are_checked(lib):
     assert f(p, p, p, p, p, cu(0, 512, 256), 2, 4, 4, 64, 2, 1, 0.0, None) == -1  # decreasing
     assert f(p, p, p, p, p, cu(0, 512), 1, 4, 4, 64, 2, 1, -1.0, None) == -1     # scale
     w = lib.cpattn_bwd_varlen_workspace_bytes
-    # the largest sample's workspace: two fp32 vectors per query row and head, tile-padded
-    assert w(cu(0, 512, 1536, 1792), 3, 4, 2, 64, 2) == lib.cpattn_bwd_workspace_bytes(1, 1024, 4, 2, 64, 2)
+    # one launch for all samples: two fp32 vectors per (sample, head), each
+    # sample's rows padded to the longest sample's tiles (here 2 per chunk:
+    # 2cp * 2 * 128 = 1024 rows)
+    assert w(cu(0, 512, 1536, 1792), 3, 4, 2, 64, 2) == 2 * 3 * 4 * 1024 * 4
     assert w(cu(0, 510), 1, 4, 2, 64, 2) == 0
 
 

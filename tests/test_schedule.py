@@ -38,8 +38,28 @@ def checker(tmp_path_factory):
     return exe
 
 
+# packed samples: lengths (each divisible by 2cp, 0 allowed), hq, hkv, cp, causal, grid
+PACKED = [
+    ([512, 256, 1024], 4, 2, 2, 1, 7),
+    ([960, 0, 192, 384], 6, 2, 3, 1, 5),
+    ([2048, 128], 8, 1, 4, 1, 152),
+    ([96], 2, 2, 3, 1, 2),
+    ([768, 1536], 2, 2, 3, 0, 4),
+    ([16, 16, 16, 16, 16, 16], 3, 1, 1, 1, 3),
+]
+
+
 def test_every_allowed_pair_once(checker):
-    args = [str(x) for g in GEOMS for x in g]
+    args = [str(x) for g in GEOMS for x in ("U", *g)]
     out = subprocess.run([checker, *args], capture_output=True, text=True)
     assert out.returncode == 0, out.stdout + out.stderr
     assert out.stdout.count("ok") == len(GEOMS)
+
+
+def test_packed_samples_never_cross_a_boundary(checker):
+    args = []
+    for lens, hq, hkv, cp, causal, grid in PACKED:
+        args += ["P", str(len(lens)), *map(str, lens), str(hq), str(hkv), str(cp), str(causal), str(grid)]
+    out = subprocess.run([checker, *args], capture_output=True, text=True)
+    assert out.returncode == 0, out.stdout + out.stderr
+    assert out.stdout.count("ok") == len(PACKED)

@@ -54,3 +54,29 @@ def test_varlen_forward_backward(lengths, hq, hkv, d, cp, scale):
     dq_r, dk_r, dv_r = oracle.varlen_attention_backward(q, k, v, do, cu, scale=scale)
     for name, got, ref in (("dq", dq, dq_r), ("dk", dk, dk_r), ("dv", dv, dv_r)):
         assert _rel(got.float().cpu(), ref) <= 2e-2, name
+
+
+def test_many_short_samples_in_one_launch():
+    # 40 samples of 64..1024 tokens (cp = 2): one launch per kernel
+    g = torch.Generator(device="cpu").manual_seed(5)
+    lens = [int(x) * 64 for x in torch.randint(1, 17, (40,), generator=g)]
+    cu = [0]
+    for n in lens:
+        cu.append(cu[-1] + n)
+    total, hq, hkv, d, cp = cu[-1], 4, 2, 128, 2
+    q = torch.randn(total, hq, d, generator=g).to(torch.bfloat16)
+    k = torch.randn(total, hkv, d, generator=g).to(torch.bfloat16)
+    v = torch.randn(total, hkv, d, generator=g).to(torch.bfloat16)
+    do = torch.randn(total, hq, d, generator=g).to(torch.bfloat16)
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = cpattn_fwd_varlen(qd, kd, vd, cu, cp)
+    dq, dk, dv = cpattn_bwd_varlen(qd, kd, vd, o, lse, dod, cu, cp)
+    torch.cuda.synchronize()
+    assert cpattn_device_status() == 0
+    o_r, l_r = oracle.varlen_attention_forward(q, k, v, cu)
+    err = (o.double().cpu() - o_r).abs()
+    assert (err <= 1e-2 + _half_ulp_bf16(o_r)).all(), err.max().item()
+    assert (lse.double().cpu() - l_r).abs().max().item() <= 1e-3
+    dq_r, dk_r, dv_r = oracle.varlen_attention_backward(q, k, v, do, cu)
+    for name, got, ref in (("dq", dq, dq_r), ("dk", dk, dk_r), ("dv", dv, dv_r)):
+        assert _rel(got.float().cpu(), ref) <= 2e-2, name

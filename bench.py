@@ -407,34 +407,38 @@ def run_ours(args, w):
     rope = {"ms": rope_ms, "bytes": rope_bytes, "gbs": rope_bytes / (rope_ms * 1e-3) / 1e9,
             "what": "cpattn_rope on q and k (two launches)"}
 
-    # ---- packed samples of the same total length (attention within samples)
+    # ---- packed samples of the same total length (attention within samples):
+    # a mix of long samples, and many short ones; one launch per kernel
     from context_blockwise_causal_gb300 import cpattn_bwd_varlen, cpattn_fwd_varlen
 
-    lens = [w.s // 2, w.s // 4, w.s // 8, w.s // 16, w.s // 16]
-    cu = [0]
-    for n_ in lens:
-        cu.append(cu[-1] + n_)
     qp, kp, vp, dop = (t[0].reshape(w.s, t.shape[2], w.d) for t in (q, k, v, do))
-    o_p, lse_p = cpattn_fwd_varlen(qp, kp, vp, cu, w.cp, stream=stream)
-    g_p = cpattn_bwd_varlen(qp, kp, vp, o_p, lse_p, dop, cu, w.cp, stream=stream)
-    barrier()
-    va, vb, vc = ev(), ev(), ev()
-    va.record(stream)
-    for _ in range(args.steps):
-        cpattn_fwd_varlen(qp, kp, vp, cu, w.cp, o=o_p, lse=lse_p, stream=stream)
-    vb.record(stream)
-    for _ in range(args.steps):
-        cpattn_bwd_varlen(qp, kp, vp, o_p, lse_p, dop, cu, w.cp, dq=g_p[0], dk=g_p[1], dv=g_p[2], stream=stream)
-    vc.record(stream)
-    barrier()
-    if cpattn_device_status(stream) != 0:
-        raise RuntimeError("a kernel reported a timeout in the packed-sample run")
-    vf_ms, vbw_ms = va.elapsed_time(vb) / args.steps, vb.elapsed_time(vc) / args.steps
-    v_fwd_flops = sum(2.0 * w.hq * n_ * n_ * w.d for n_ in lens)
-    varlen = {"samples": lens, "fwd_ms": vf_ms, "bwd_ms": vbw_ms,
-              "fwd_tflops": v_fwd_flops / (vf_ms * 1e-3) / 1e12,
-              "bwd_tflops": 2.5 * v_fwd_flops / (vbw_ms * 1e-3) / 1e12,
-              "launches": {"fwd": len(lens), "bwd": 3 * len(lens)}}
+
+    def packed(lens):
+        cu = [0]
+        for n_ in lens:
+            cu.append(cu[-1] + n_)
+        o_p, lse_p = cpattn_fwd_varlen(qp, kp, vp, cu, w.cp, stream=stream)
+        g_p = cpattn_bwd_varlen(qp, kp, vp, o_p, lse_p, dop, cu, w.cp, stream=stream)
+        barrier()
+        va, vb, vc = ev(), ev(), ev()
+        va.record(stream)
+        for _ in range(args.steps):
+            cpattn_fwd_varlen(qp, kp, vp, cu, w.cp, o=o_p, lse=lse_p, stream=stream)
+        vb.record(stream)
+        for _ in range(args.steps):
+            cpattn_bwd_varlen(qp, kp, vp, o_p, lse_p, dop, cu, w.cp, dq=g_p[0], dk=g_p[1], dv=g_p[2], stream=stream)
+        vc.record(stream)
+        barrier()
+        if cpattn_device_status(stream) != 0:
+            raise RuntimeError("a kernel reported a timeout in the packed-sample run")
+        vf_ms, vbw_ms = va.elapsed_time(vb) / args.steps, vb.elapsed_time(vc) / args.steps
+        fl = sum(2.0 * w.hq * n_ * n_ * w.d for n_ in lens)
+        return {"samples": lens if len(lens) <= 8 else f"{len(lens)} x {lens[0]}", "fwd_ms": vf_ms, "bwd_ms": vbw_ms,
+                "fwd_tflops": fl / (vf_ms * 1e-3) / 1e12, "bwd_tflops": 2.5 * fl / (vbw_ms * 1e-3) / 1e12,
+                "launches": {"fwd": 1, "bwd": 3}}
+
+    varlen = {"mixed": packed([w.s // 2, w.s // 4, w.s // 8, w.s // 16, w.s // 16]),
+              "short": packed([2048] * (w.s // 2048))}
 
     if rank == 0:
         peaks = _peaks()

@@ -38,8 +38,37 @@ struct CpGeom {
   int tpc;     // tiles per chunk (the largest sample's when packed)
   int npairs;  // query-head pairs per batch element: ceil(hq / 2)
   int nseq = 0;
-  int cu[kMaxSeqs + 1];
+  int cu[kMaxSeqs + 1];     // packed: sample offsets
+  int tile0[kMaxSeqs + 1];  // packed: query tiles (2cp * tpc_i) of the samples before sample i
 };
+
+// Packed geometry from the sample offsets (cu[0..nseq] set): the largest
+// sample's tiles per chunk and the tile prefix sums.
+__host__ __device__ inline void finish_packed(CpGeom& g) {
+  g.b = 1;
+  g.s = g.cu[g.nseq];
+  g.c = 0;
+  g.tpc = 0;
+  g.tile0[0] = 0;
+  for (int i = 0; i < g.nseq; ++i) {
+    const int c = (g.cu[i + 1] - g.cu[i]) / (2 * g.cp);
+    const int tpc = (c + kTile - 1) / kTile;
+    g.tpc = tpc > g.tpc ? tpc : g.tpc;
+    g.tile0[i + 1] = g.tile0[i] + 2 * g.cp * tpc;
+  }
+}
+
+// Packed samples: the sample holding global tile position p (a binary
+// search over tile0), and p's offset within that sample's tiles.
+__host__ __device__ inline int packed_sample_of(const CpGeom& g, int p, int& local) {
+  int lo = 0, hi = g.nseq;  // tile0[lo] <= p < tile0[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (g.tile0[mid] <= p) lo = mid; else hi = mid;
+  }
+  local = p - g.tile0[lo];
+  return lo;
+}
 
 // A sequence's placement: its first token in the token rows, its chunk
 // length and tiles per chunk (0 tiles for an empty sample).
@@ -80,9 +109,12 @@ struct FwdUnit {
   int n;         // number of key tiles the unit visits (0: no such tile in a shorter packed sample)
 };
 
-__host__ __device__ inline int fwd_num_units(const CpGeom& g) {
-  return num_seqs(g) * g.npairs * 2 * g.cp * g.tpc;
+// Units per head group of a call: every sequence's query (or key) tiles.
+__host__ __device__ inline int all_tiles(const CpGeom& g) {
+  return g.nseq > 0 ? g.tile0[g.nseq] : g.b * 2 * g.cp * g.tpc;
 }
+
+__host__ __device__ inline int fwd_num_units(const CpGeom& g) { return g.npairs * all_tiles(g); }
 
 // The query tile with global tile index gt of unit U's sequence (U.seq set).
 __host__ __device__ inline void fill_query_tile(const CpGeom& g, FwdUnit& U, int gt) {
@@ -112,15 +144,23 @@ __host__ __device__ inline void fill_query_tile(const CpGeom& g, FwdUnit& U, int
 
 // Units are numbered in longest-first order: the causal cost of the query
 // tile with global tile index gt is gt+1 key tiles, so index 0 is the last
-// tile of the sequence (of the longest samples when packed; tile indices a
-// shorter sample does not have decode as empty units, n == 0).
+// tile of the sequence. Packed samples come one after another (units of one
+// sample share their K/V tiles in L2), each longest tile first.
 __host__ __device__ inline FwdUnit fwd_decode_unit(const CpGeom& g, int idx) {
   FwdUnit U;
-  const int per = num_seqs(g) * g.npairs;
-  const int gt = (2 * g.cp * g.tpc - 1) - idx / per;
-  const int rest = idx % per;
-  U.seq = rest / g.npairs;
-  const int pr = rest % g.npairs;
+  int gt, pr;
+  if (g.nseq > 0) {
+    int local;
+    U.seq = packed_sample_of(g, idx / g.npairs, local);
+    gt = (g.tile0[U.seq + 1] - g.tile0[U.seq]) - 1 - local;
+    pr = idx % g.npairs;
+  } else {
+    const int per = g.b * g.npairs;
+    gt = (2 * g.cp * g.tpc - 1) - idx / per;
+    const int rest = idx % per;
+    U.seq = rest / g.npairs;
+    pr = rest % g.npairs;
+  }
   const int G = g.hq / g.hkv;
   U.h0 = 2 * pr;
   U.store1 = (2 * pr + 1) < g.hq;
@@ -134,15 +174,23 @@ __host__ __device__ inline FwdUnit fwd_decode_unit(const CpGeom& g, int idx) {
 // dQ work units: one 128-row query tile of one head, longest first: the
 // forward's decomposition with one head per unit (h0 == h1), so the
 // forward's CP-step key walk (KvWalk) applies as is.
-__host__ __device__ inline int dq_num_units(const CpGeom& g) { return num_seqs(g) * g.hq * 2 * g.cp * g.tpc; }
+__host__ __device__ inline int dq_num_units(const CpGeom& g) { return g.hq * all_tiles(g); }
 
 __host__ __device__ inline FwdUnit dq_decode_unit(const CpGeom& g, int idx) {
   FwdUnit U;
-  const int per = num_seqs(g) * g.hq;
-  const int gt = (2 * g.cp * g.tpc - 1) - idx / per;
-  const int rest = idx % per;
-  U.seq = rest / g.hq;
-  U.h0 = U.h1 = rest % g.hq;
+  int gt;
+  if (g.nseq > 0) {
+    int local;
+    U.seq = packed_sample_of(g, idx / g.hq, local);
+    gt = (g.tile0[U.seq + 1] - g.tile0[U.seq]) - 1 - local;
+    U.h0 = U.h1 = idx % g.hq;
+  } else {
+    const int per = g.b * g.hq;
+    gt = (2 * g.cp * g.tpc - 1) - idx / per;
+    const int rest = idx % per;
+    U.seq = rest / g.hq;
+    U.h0 = U.h1 = rest % g.hq;
+  }
   U.g0 = U.g1 = U.h0 / (g.hq / g.hkv);
   U.store1 = false;
   fill_query_tile(g, U, gt);
@@ -279,18 +327,24 @@ struct BwdUnit {
   int items;      // nq * (hq / hkv); 0 for a tile a shorter packed sample does not have
 };
 
-__host__ __device__ inline int bwd_num_units(const CpGeom& g) { return num_seqs(g) * g.hkv * 2 * g.cp * g.tpc; }
+__host__ __device__ inline int bwd_num_units(const CpGeom& g) { return g.hkv * all_tiles(g); }
 
 // Longest-first: the key tile with global tile index gt is seen by ntile-gt
 // query tiles (causal), so unit 0 is the first tile of the sequence.
 __host__ __device__ inline BwdUnit bwd_decode_unit(const CpGeom& g, int idx) {
   BwdUnit U;
-  const int per = num_seqs(g) * g.hkv;
-  const int gt = idx / per;
-  const int rest = idx % per;
-  U.seq = rest / g.hkv;
+  int gt;
+  if (g.nseq > 0) {
+    U.seq = packed_sample_of(g, idx / g.hkv, gt);
+    U.g = idx % g.hkv;
+  } else {
+    const int per = g.b * g.hkv;
+    gt = idx / per;
+    const int rest = idx % per;
+    U.seq = rest / g.hkv;
+    U.g = rest % g.hkv;
+  }
   U.bi = g.nseq > 0 ? 0 : U.seq;
-  U.g = rest % g.hkv;
   const SeqGeom q = seq_geom(g, U.seq);
   U.tok0 = q.tok0;
   U.c = q.c;

@@ -486,21 +486,13 @@ namespace {
 CpGeom packed_geom(const int* cu, int nseq, int hq, int hkv, int cp, int causal) {
   CpGeom g = make_geom(1, cu[nseq], hq, hkv, cp, causal);
   g.nseq = nseq;
-  g.c = 0;  // per sample
-  int tpc = 0;
   for (int i = 0; i <= nseq; ++i) g.cu[i] = cu[i];
-  for (int i = 0; i < nseq; ++i) {
-    const int c = (cu[i + 1] - cu[i]) / (2 * cp);
-    const int t = (c + kTile - 1) / kTile;
-    tpc = t > tpc ? t : tpc;
-  }
-  g.tpc = tpc;
+  finish_packed(g);
   return g;
 }
 
 bool packed_units_fit(const CpGeom& g) {
-  const int64_t per = int64_t(g.nseq) * 2 * g.cp * g.tpc;
-  return per * (g.npairs > g.hq ? g.npairs : g.hq) < (int64_t(1) << 31);
+  return int64_t(g.tile0[g.nseq]) * (g.npairs > g.hq ? g.npairs : g.hq) < (int64_t(1) << 31);
 }
 
 int64_t check_cu(const int* cu, int nseq, int cp) {

@@ -102,11 +102,13 @@ static int check(const CpGeom& g, int grid) {
     }
   for (int i = 0; i < nu; ++i)
     if (seen[i] != 1) { printf("unit %d assigned %d times\n", i, seen[i]); return 1; }
-  int prev_n = 1 << 30;
+  int prev_n = 1 << 30, prev_seq = -1;
   for (int idx = 0; idx < nu; ++idx) {
     const FwdUnit U = fwd_decode_unit(g, idx);
-    if (U.n == 0) continue;  // a tile a shorter packed sample does not have
-    if (g.causal && g.nseq == 0 && U.n > prev_n) { printf("units not in longest-first order at %d\n", idx); return 1; }
+    if (U.n == 0) continue;  // an empty packed sample
+    if (g.nseq > 0 && U.seq != prev_seq) prev_n = 1 << 30;  // packed samples come one after another
+    prev_seq = U.seq;
+    if (g.causal && U.n > prev_n) { printf("units not in longest-first order at %d\n", idx); return 1; }
     prev_n = U.n;
     for (int sub = 0; sub < 2; ++sub) {
       if (sub == 1 && !U.store1) continue;
@@ -156,10 +158,13 @@ static int check(const CpGeom& g, int grid) {
   const int nb = bwd_num_units(g);
   const int G = g.hq / g.hkv;
   int prev_items = 1 << 30;
+  prev_seq = -1;
   for (int idx = 0; idx < nb; ++idx) {
     const BwdUnit U = bwd_decode_unit(g, idx);
     if (U.items == 0) continue;
-    if (g.causal && g.nseq == 0 && U.items > prev_items) { printf("bwd units not longest-first at %d\n", idx); return 1; }
+    if (g.nseq > 0 && U.seq != prev_seq) prev_items = 1 << 30;
+    prev_seq = U.seq;
+    if (g.causal && U.items > prev_items) { printf("bwd units not longest-first at %d\n", idx); return 1; }
     prev_items = U.items;
     QWalk w(g, U);
     int chunk, tile, nt = 0;
@@ -214,14 +219,7 @@ int main(int argc, char** argv) {
       g.cp = atoi(argv[j + 2]);
       g.causal = atoi(argv[j + 3]);
       grid = atoi(argv[j + 4]);
-      g.b = 1;
-      g.s = g.cu[n];
-      g.c = 0;
-      g.tpc = 0;
-      for (int k = 0; k < n; ++k) {
-        const int c = (g.cu[k + 1] - g.cu[k]) / (2 * g.cp);
-        g.tpc = std::max(g.tpc, (c + kTile - 1) / kTile);
-      }
+      finish_packed(g);
       snprintf(desc, sizeof desc, "packed nseq=%d total=%d hq=%d hkv=%d cp=%d causal=%d grid=%d", n, g.s, g.hq,
                g.hkv, g.cp, g.causal, grid);
       i = j + 5;

@@ -10,14 +10,14 @@
 //                             dS^T = P^T (dP^T - D)                (TMEM)
 //                             dV += P^T dO, dK += dS^T Q           (TMEM)
 //                           dK/dV stay on chip across all blocks and are
-//                           written once (dK scaled by 1/sqrt(d)).
+//                           written once (dK scaled by the softmax scale).
 //   cpattn_bwd_dq_kernel    query-tile-stationary: per 128-query tile of one
 //                           head, over the key tiles it sees in the order of
 //                           its rank's CP steps (the forward's walk):
 //                             S = Q K^T, dP = dO V^T               (TMEM)
 //                             dS = P (dP - D)                      (TMEM)
 //                             dQ += dS K                           (TMEM)
-//                           dq written once (scaled by 1/sqrt(d)).
+//                           dq written once (scaled by the softmax scale).
 // Splitting dQ from dK/dV costs two extra matmuls per block (S and dP are
 // formed twice) but needs no atomics and no fp32 accumulator in device
 // memory, and lets each kernel keep its TMEM within 512 columns.
@@ -47,8 +47,8 @@ struct BwdArgs {
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  float scale_log2;  // log2(e) / sqrt(d)
-  float scale;       // 1 / sqrt(d)
+  float scale_log2;  // log2(e) * the softmax scale
+  float scale;       // the softmax scale (1 / sqrt(d) by default)
   unsigned int* status;
 };
 
@@ -589,7 +589,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             pv.y = pack_bf16x2(__uint_as_float(rv[q + 2]), __uint_as_float(rv[q + 3]));
             pv.z = pack_bf16x2(__uint_as_float(rv[q + 4]), __uint_as_float(rv[q + 5]));
             pv.w = pack_bf16x2(__uint_as_float(rv[q + 6]), __uint_as_float(rv[q + 7]));
-            // dK accumulated dS^T Q with dS unscaled: apply 1/sqrt(d) here
+            // dK accumulated dS^T Q with dS unscaled: apply the softmax scale here
             pk.x = pack_bf16x2(__uint_as_float(rk[q]) * scale, __uint_as_float(rk[q + 1]) * scale);
             pk.y = pack_bf16x2(__uint_as_float(rk[q + 2]) * scale, __uint_as_float(rk[q + 3]) * scale);
             pk.z = pack_bf16x2(__uint_as_float(rk[q + 4]) * scale, __uint_as_float(rk[q + 5]) * scale);

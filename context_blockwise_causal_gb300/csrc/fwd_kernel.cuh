@@ -6,7 +6,8 @@
 //   warp 8     TMA producer (Q tiles, and the K/V ring)
 //   warp 9     TMEM owner and tcgen05.mma issuer
 //   warps 10-11 idle (complete the third warpgroup for the register split)
-// A work unit is a 128-row query tile for a pair of query heads; the two
+// A work unit is a 128-row query tile (of a batch element or a packed
+// sample) for a pair of query heads; the two
 // sub-tiles walk the same key tiles (CP-step order, see cp_schedule.cuh) so
 // the MMA warp can alternate between them:
 //     S0(j)=Q0 K_j^T  S1(j)=Q1 K_j^T  O0+=P0(j) V_j  S0(j+1)  O1+=P1(j) V_j  S1(j+1) ...
@@ -57,7 +58,7 @@ struct FwdArgs {
   int64_t lse_stride;  // row stride of lse per (batch, head): s, or a packed tensor's total
   float* o_part;     // step form: the step's normalised partial output, fp32
   int step;          // step form: the CP step computed
-  float scale_log2;  // log2(e) / sqrt(d)
+  float scale_log2;  // log2(e) * the softmax scale
   unsigned int* status;
 };
 

@@ -24,7 +24,8 @@
  *     bf16, contiguous, head_dim fastest. lse: [b, hq, s] fp32, natural log.
  *   - Grouped-query attention: query head h uses KV head h / (hq / hkv)
  *     (page "Megatron 面试题（一）：模型抽象与训练数据流", item M014).
- *   - Softmax scale is 1/sqrt(d). causal != 0 selects the causal mask
+ *   - Softmax scale is 1/sqrt(d) (any positive scale through cpattn_fwd_ex /
+ *     cpattn_bwd_ex). causal != 0 selects the causal mask
  *     (key position <= query position); causal == 0 is full attention with
  *     the same CP chunking (every step unmasked).
  *   - Supported: d in {64, 128}; s divisible by 2*cp; hq divisible by hkv;

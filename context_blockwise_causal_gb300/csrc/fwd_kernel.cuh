@@ -71,8 +71,8 @@ struct FwdCfg {
   static constexpr int kOffKV = 2 * kQBytes;
   static constexpr int kOffBar = kOffKV + kSlots * kKVBytes;
   // barriers: q_full[2] q_empty[2] s_full[2] p_full[2] o_full[2] o_empty[2]
-  //           drain, kv_full[kSlots] kv_empty[kSlots]
-  static constexpr int kNumBars = 13 + 2 * kSlots;
+  //           drain, kv_full[kSlots] kv_empty[kSlots], p_half[2]
+  static constexpr int kNumBars = 15 + 2 * kSlots;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
   static constexpr uint32_t kColO = 256;
@@ -108,6 +108,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   uint64_t* drain = bars + 12;
   uint64_t* kv_full = bars + 13;
   uint64_t* kv_empty = bars + 13 + C::kSlots;
+  uint64_t* p_half = bars + 13 + 2 * C::kSlots;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -124,6 +125,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(&q_empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 4);
+      mbar_init(&p_half[i], 4);
       mbar_init(&o_full[i], 1);
       mbar_init(&o_empty[i], 4);
     }
@@ -228,12 +230,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           umma_ss_w(tbase + sub * kTile, dQ[sub] + off, kb + off, idS, kk > 0);
         }
       };
-      auto issue_PV = [&](int sub, uint32_t slot, bool acc) {
+      // O += P V over keys [64*half, 64*half + 64) (K-steps 4*half .. +3)
+      auto issue_PV = [&](int sub, uint32_t slot, bool acc, int half) {
         const uint64_t vb = dV0 + ((slot * C::kKVBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
+        for (int q = 0; q < kTile / 32; ++q) {
+          const int kk = half * (kTile / 32) + q;
           umma_ts_w(tbase + C::kColO + sub * D, tbase + sub * kTile + kk * 8, vb + ((kk * 2048) >> 4), idO,
-                  (acc || kk > 0) ? 1u : 0u);
+                    (acc || kk > 0) ? 1u : 0u);
+        }
       };
       uint32_t ncons = 0;
       auto take = [&](uint32_t& slot, uint32_t& par) {
@@ -276,14 +281,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           uint32_t v0, v0p, v1, v1p;
           take(v0, v0p);
           if (shared_kv) { v1 = v0; v1p = v0p; } else take(v1, v1p);
-          // ---- sub-tile 0: O0 += P0(j) V_j, then S0(j+1)
+          // ---- sub-tile 0: O0 += P0(j) V_j (first half of the keys as soon
+          // as their P is in TMEM), then S0(j+1)
           ok = mbar_wait_warp(&kv_full[v0], v0p, abort_flag, kWaitLimitNs) &&
-               mbar_wait_warp(&p_full[0], pcnt[0] & 1, abort_flag, kWaitLimitNs) &&
+               mbar_wait_warp(&p_half[0], pcnt[0] & 1, abort_flag, kWaitLimitNs) &&
                (j > 0 || ul == 0 || mbar_wait_warp(&o_empty[0], (ul - 1) & 1, abort_flag, kWaitLimitNs));
           if (!ok) break;
+          tc_fence_after();
+          issue_PV(0, v0, j > 0, 0);
+          if (!(ok = mbar_wait_warp(&p_full[0], pcnt[0] & 1, abort_flag, kWaitLimitNs))) break;
           ++pcnt[0];
           tc_fence_after();
-          issue_PV(0, v0, j > 0);
+          issue_PV(0, v0, j > 0, 1);
           if (!shared_kv) umma_commit_w(&kv_empty[v0]);
           if (j == n - 1) umma_commit_w(&o_full[0]);
           uint32_t nk0 = 0, nk0p = 0, nk1 = 0, nk1p = 0;
@@ -298,12 +307,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
           // ---- sub-tile 1: O1 += P1(j) V_j, then S1(j+1)
           ok = (shared_kv || mbar_wait_warp(&kv_full[v1], v1p, abort_flag, kWaitLimitNs)) &&
-               mbar_wait_warp(&p_full[1], pcnt[1] & 1, abort_flag, kWaitLimitNs) &&
+               mbar_wait_warp(&p_half[1], pcnt[1] & 1, abort_flag, kWaitLimitNs) &&
                (j > 0 || ul == 0 || mbar_wait_warp(&o_empty[1], (ul - 1) & 1, abort_flag, kWaitLimitNs));
           if (!ok) break;
+          tc_fence_after();
+          issue_PV(1, v1, j > 0, 0);
+          if (!(ok = mbar_wait_warp(&p_full[1], pcnt[1] & 1, abort_flag, kWaitLimitNs))) break;
           ++pcnt[1];
           tc_fence_after();
-          issue_PV(1, v1, j > 0);
+          issue_PV(1, v1, j > 0, 1);
           umma_commit_w(&kv_empty[v1]);
           if (j == n - 1) umma_commit_w(&o_full[1]);
           if (j + 1 < n) {
@@ -403,45 +415,52 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           m_used = m_new;
         }
         const float neg = (m_used == -INFINITY) ? 0.f : -m_used;
+        const bool rescale = j > 0 && __any_sync(0xffffffffu, upd);
         // P = 2^(S*scale*log2e - m), packed to bf16 pairs as it is formed so
-        // the fp32 scores die early; the row sum uses the fp32 values.
-        uint32_t pk0[32], pk1[32];
+        // the fp32 scores die early; the row sum uses the fp32 values. The
+        // first 64 keys' P goes to TMEM (and to the MMA warp) before the
+        // second half is formed, so P.V starts while the warps still work.
+        uint32_t pk[32];
         const uint64_t sl2x2 = f2_pack(sl2, sl2), negx2 = f2_pack(neg, neg);
         uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0, acc2 = acc0, acc3 = acc0;
 #pragma unroll
-        for (int i = 0; i < kTile / 2; ++i) {
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(s[2 * i], s[2 * i + 1]), sl2x2, negx2), x0, x1);
-          const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
-          const uint64_t e = f2_pack(e0, e1);
-          if ((i & 3) == 0) acc0 = f2_add(acc0, e);
-          else if ((i & 3) == 1) acc1 = f2_add(acc1, e);
-          else if ((i & 3) == 2) acc2 = f2_add(acc2, e);
-          else acc3 = f2_add(acc3, e);
-          if (i < 32) pk0[i] = pack_bf16x2(e0, e1);
-          else pk1[i - 32] = pack_bf16x2(e0, e1);
-        }
-        if (j > 0 && __any_sync(0xffffffffu, upd)) {
-          // This row's O accumulator is idle: P.V of step j-1 completed
-          // before S(j) was signalled, and P.V of step j waits for p_full.
+        for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t r[32];
-            tmem_ld32(tO + c0, r);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_st32(tO + c0, r);
+          for (int q = 0; q < kTile / 4; ++q) {
+            const int i = hh * (kTile / 4) + q;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(s[2 * i], s[2 * i + 1]), sl2x2, negx2), x0, x1);
+            const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+            const uint64_t e = f2_pack(e0, e1);
+            if ((i & 3) == 0) acc0 = f2_add(acc0, e);
+            else if ((i & 3) == 1) acc1 = f2_add(acc1, e);
+            else if ((i & 3) == 2) acc2 = f2_add(acc2, e);
+            else acc3 = f2_add(acc3, e);
+            pk[q] = pack_bf16x2(e0, e1);
           }
+          if (hh == 0 && rescale) {
+            // Rescale O before any P.V of this tile (the MMA warp waits for
+            // p_half). This row's O accumulator is idle: P.V of step j-1
+            // completed before S(j) was signalled.
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t r[32];
+              tmem_ld32(tO + c0, r);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+              tmem_st32(tO + c0, r);
+            }
+          }
+          tmem_st32(tS + hh * 32, pk);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(hh == 0 ? &p_half[sub] : &p_full[sub]);
         }
         float a0, a1, b0, b1;
         f2_unpack(f2_add(f2_add(acc0, acc1), f2_add(acc2, acc3)), a0, a1);
         (void)b0;
         (void)b1;
         l = l * alpha + (a0 + a1);
-        tmem_st32x2(tS, tS + 32, pk0, pk1);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[sub]);
       }
       if (!ok) break;
       // ---- epilogue: O / l -> bf16, L = (m + log2 l) ln 2

@@ -399,15 +399,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int i = 0; i < kTile; ++i)
             if (i > lim) s[i] = -INFINITY;
         }
-        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+        // row max: eight independent chains of 3-input maxima, chain k over
+        // the scores k, k+8, ..., k+120
+        float mx[8];
 #pragma unroll
-        for (int i = 4; i < kTile; i += 8) {
-          mx0 = fmax3(mx0, s[i], s[i + 1]);
-          mx1 = fmax3(mx1, s[i + 2], s[i + 3]);
-          mx2 = fmax3(mx2, s[i + 4], s[i + 5]);
-          mx3 = fmax3(mx3, s[i + 6], s[i + 7]);
+        for (int k = 0; k < 8; ++k) {
+          float m = fmax3(s[k], s[k + 8], s[k + 16]);
+#pragma unroll
+          for (int i = 24; i + 8 < kTile; i += 16) m = fmax3(m, s[i + k], s[i + 8 + k]);
+          mx[k] = fmaxf(m, s[kTile - 8 + k]);
         }
-        const float m_new = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        const float m_new = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7]))) * sl2;
         const bool upd = m_new > m_used + kRescaleThreshold;
         float alpha = 1.f;
         if (upd) {

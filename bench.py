@@ -496,6 +496,16 @@ def run_ours(args, w):
                 "value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": torch.get_num_threads(), "kind": "oracle",
                 "sample": f"{args.ref_rows} seeded query rows x {w.hq} heads of {w.name}: forward O/LSE + backward "
                           f"dQ (CPU fp64 oracle), {dt:.1f} s"}
+            # the same oracle on one thread, on a smaller sample of the same rows' kind
+            nthr = torch.get_num_threads()
+            torch.set_num_threads(1)
+            try:
+                rows1 = max(1, args.ref_rows // 16)
+                dt1, fl1 = _oracle_sample(w, rows1, seed=w.seed + 6)
+            finally:
+                torch.set_num_threads(nthr)
+            line["cpu_baseline"]["single_thread"] = {"value": fl1 / dt1 / 1e12, "unit": "TFLOP/s", "cores": 1,
+                                                     "sample": f"{rows1} seeded query rows, {dt1:.1f} s"}
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()

@@ -334,9 +334,10 @@ def run_ours(args, w):
         return start, end
 
     e2e_run(2)
-    barrier()
-    e0, e1 = e2e_run(args.steps)
-    barrier()
+    with ClockSampler(local) as clk_e2e:
+        barrier()
+        e0, e1 = e2e_run(args.steps)
+        barrier()
     e2e_ms = _max_over_ranks(e0.elapsed_time(e1), dev, ws)
     del bufs[1]
 
@@ -440,6 +441,35 @@ def run_ours(args, w):
     varlen = {"mixed": packed([w.s // 2, w.s // 4, w.s // 8, w.s // 16, w.s // 16]),
               "short": packed([2048] * (w.s // 2048))}
 
+    # ---- the forward on the other configurations (each: warm-up, then the
+    # median of several launches, L2 flushed before each)
+    sweep = {}
+    if not args.no_sweep and rank == 0:
+        from context_blockwise_causal_gb300.workloads import WORKLOADS, make_inputs as _mk
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        for name, cw in WORKLOADS.items():
+            if name == w.name or name.startswith("train_"):
+                continue
+            xi = _mk(cw, device=dev, with_grad=False)
+            o_c, lse_c = cpattn_fwd(xi["q"], xi["k"], xi["v"], cw.cp, causal=cw.causal, stream=stream)
+            reps = 3 if cw.fwd_flops() > 5e13 else 10
+            tms = []
+            for _ in range(reps):
+                with torch.cuda.stream(stream):
+                    flush.zero_()
+                e0c, e1c = ev(), ev()
+                e0c.record(stream)
+                cpattn_fwd(xi["q"], xi["k"], xi["v"], cw.cp, causal=cw.causal, o=o_c, lse=lse_c, stream=stream)
+                e1c.record(stream)
+                e1c.synchronize()
+                tms.append(e0c.elapsed_time(e1c))
+            if cpattn_device_status(stream) != 0:
+                raise RuntimeError(f"a kernel reported a timeout in the {name} forward")
+            ms = statistics.median(tms)
+            sweep[name] = {"fwd_ms": ms, "fwd_tflops": cw.fwd_flops() / (ms * 1e-3) / 1e12, "reps": reps}
+            del xi, o_c, lse_c
+        del flush
+
     if rank == 0:
         peaks = _peaks()
         step_flops = w.fwd_flops() + w.bwd_flops()
@@ -481,7 +511,7 @@ def run_ours(args, w):
             "e2e": {"value": step_flops * args.steps * ws / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps,
                     "copies": "pinned host <-> device every step, on two copy streams overlapping the kernels "
-                              "(two device buffer sets)"},
+                              "(two device buffer sets)", "clocks": clk_e2e.summary()},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),
         }
@@ -490,6 +520,11 @@ def run_ours(args, w):
         rope["hbm_frac"] = rope["gbs"] / peaks["hbm_gbs"]
         line["rope"] = rope
         line["varlen"] = varlen
+        if sweep:
+            for v_ in sweep.values():
+                v_["frac_burst"] = v_["fwd_tflops"] / peaks["bf16_tflops"]
+                v_["frac_sustained"] = v_["fwd_tflops"] / peaks["bf16_tflops_sustained"]
+            line["fwd_other_configs"] = sweep
         if not args.no_cpu_baseline:
             dt, fl = _oracle_sample(w, args.ref_rows, seed=w.seed + 5)
             line["cpu_baseline"] = {
@@ -521,6 +556,7 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=1024)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-unfused", action="store_true", help="skip timing the unfused forward")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the forward on the other configurations")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

@@ -106,9 +106,19 @@ def library():
     return _LIB
 
 
-def _stream_handle(stream):
+def _stream_handle(stream, *tensors):
+    """The stream to launch on (the current one by default). The library
+    launches on the current CUDA device, so every tensor given must be on it,
+    and so must the stream."""
+    cur = torch.cuda.current_device()
+    for t in tensors:
+        if isinstance(t, torch.Tensor) and t.is_cuda and t.device.index != cur:
+            raise ValueError(f"a tensor is on {t.device} but the current CUDA device is cuda:{cur}; "
+                             f"call under torch.cuda.device({t.device})")
     if stream is None:
         stream = torch.cuda.current_stream()
+    elif stream.device.index != cur:
+        raise ValueError(f"the stream belongs to {stream.device}, the current CUDA device is cuda:{cur}")
     return ctypes.c_void_p(stream.cuda_stream)
 
 
@@ -153,9 +163,9 @@ def cpattn_fwd(q, k, v, cp, causal=True, o=None, lse=None, stream=None, scale=No
     args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), b, s, hq, hkv, d, int(cp),
             1 if causal else 0)
     if scale is None:
-        rc = library().cpattn_fwd(*args, _stream_handle(stream))
+        rc = library().cpattn_fwd(*args, _stream_handle(stream, q, k, v, o, lse))
     else:
-        rc = library().cpattn_fwd_ex(*args, float(scale), _stream_handle(stream))
+        rc = library().cpattn_fwd_ex(*args, float(scale), _stream_handle(stream, q, k, v, o, lse))
     if rc:
         raise CpattnError(rc, "cpattn_fwd" if scale is None else "cpattn_fwd_ex")
     return o, lse
@@ -182,7 +192,8 @@ def cpattn_fwd_step(q, k, v, cp, step, causal=True, o_part=None, lse_part=None, 
     _check_f32("o_part", o_part, (b, s, hq, d))
     _check_f32("lse_part", lse_part, (b, hq, s))
     rc = library().cpattn_fwd_step(q.data_ptr(), k.data_ptr(), v.data_ptr(), o_part.data_ptr(), lse_part.data_ptr(),
-                                   b, s, hq, hkv, d, int(cp), int(step), 1 if causal else 0, _stream_handle(stream))
+                                   b, s, hq, hkv, d, int(cp), int(step), 1 if causal else 0,
+                                   _stream_handle(stream, q, k, v, o_part, lse_part))
     if rc:
         raise CpattnError(rc, "cpattn_fwd_step")
     return o_part, lse_part
@@ -218,7 +229,8 @@ def cpattn_lse_merge(o_a, lse_a, o_b=None, lse_b=None, o_out=None, lse_out=None,
         _check_act("o_bf16", o_bf16, (b, s, hq, d))
     ptr = lambda t: None if t is None or t is False else t.data_ptr()  # noqa: E731
     rc = library().cpattn_lse_merge(ptr(o_a), ptr(lse_a), ptr(o_b), ptr(lse_b), ptr(o_out), ptr(lse_out),
-                                    ptr(o_bf16), b, s, hq, d, _stream_handle(stream))
+                                    ptr(o_bf16), b, s, hq, d,
+                                    _stream_handle(stream, o_a, lse_a, o_b, lse_b, o_out, lse_out, o_bf16))
     if rc:
         raise CpattnError(rc, "cpattn_lse_merge")
     return (None if o_out is False else o_out), lse_out, o_bf16
@@ -244,7 +256,8 @@ def cpattn_fwd_unfused(q, k, v, cp, causal=True, o=None, lse=None, workspace=Non
         raise ValueError("workspace must be a contiguous CUDA tensor")
     rc = library().cpattn_fwd_unfused(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                                       workspace.data_ptr(), workspace.numel() * workspace.element_size(), b, s, hq,
-                                      hkv, d, int(cp), 1 if causal else 0, _stream_handle(stream))
+                                      hkv, d, int(cp), 1 if causal else 0,
+                                      _stream_handle(stream, q, k, v, o, lse, workspace))
     if rc:
         raise CpattnError(rc, "cpattn_fwd_unfused")
     return o, lse
@@ -269,7 +282,7 @@ def cpattn_rope(x, base=10000.0, cp=1, rank=None, s=None, cu_seqlens=None, inver
             raise TypeError("cu_seqlens must be a contiguous int32 CUDA tensor")
         cu_ptr, nseq = cu_seqlens.data_ptr(), cu_seqlens.numel() - 1
     rc = library().cpattn_rope(x.data_ptr(), b, n, h, d, int(s), int(cp), -1 if rank is None else int(rank), cu_ptr,
-                               nseq, float(base), 1 if inverse else 0, _stream_handle(stream))
+                               nseq, float(base), 1 if inverse else 0, _stream_handle(stream, x, cu_seqlens))
     if rc:
         raise CpattnError(rc, "cpattn_rope")
     return x
@@ -307,7 +320,7 @@ def cpattn_fwd_varlen(q, k, v, cu_seqlens, cp, causal=True, scale=None, o=None, 
     _check_f32("lse", lse, (hq, total))
     rc = library().cpattn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), cu_p,
                                      nseq, hq, hkv, d, int(cp), 1 if causal else 0,
-                                     0.0 if scale is None else float(scale), _stream_handle(stream))
+                                     0.0 if scale is None else float(scale), _stream_handle(stream, q, k, v, o, lse))
     if rc:
         raise CpattnError(rc, "cpattn_fwd_varlen")
     return o, lse
@@ -331,7 +344,7 @@ def cpattn_bwd_varlen(q, k, v, o, lse, do, cu_seqlens, cp, causal=True, scale=No
                                      do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
                                      workspace.numel() * workspace.element_size(), cu_p, nseq, hq, hkv, d, int(cp),
                                      1 if causal else 0, 0.0 if scale is None else float(scale),
-                                     _stream_handle(stream))
+                                     _stream_handle(stream, q, k, v, o, lse, do, dq, dk, dv, workspace))
     if rc:
         raise CpattnError(rc, "cpattn_bwd_varlen")
     return dq, dk, dv
@@ -369,7 +382,7 @@ def cpattn_bwd(q, k, v, o, lse, do, cp, causal=True, dq=None, dk=None, dv=None, 
     ws_bytes = workspace.numel() * workspace.element_size()
     ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(), dq.data_ptr(),
             dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(), ws_bytes, b, s, hq, hkv, d, int(cp),
-            1 if causal else 0, _stream_handle(stream))
+            1 if causal else 0, _stream_handle(stream, q, k, v, o, lse, do, dq, dk, dv, workspace))
     if scale is not None:
         if stage is not None:
             raise ValueError("a custom scale runs the whole backward (stage must be None)")

@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/cpattn.h"
@@ -35,8 +36,9 @@ struct DeviceInfo {
   bool sm103 = false;
   int num_sms = 0;
   unsigned int* status = nullptr;
-  bool fwd_attr[4] = {false, false, false, false};  // [d == 128][step form]
-  bool bwd_attr[2] = {false, false};
+  // kernel attributes already set, per kernel; set once, read by any thread
+  std::atomic<bool> fwd_attr[4] = {};  // [d == 128][step form]
+  std::atomic<bool> bwd_attr[2] = {};
 };
 DeviceInfo g_devs[kMaxDevices];
 std::mutex g_mu;
@@ -97,7 +99,7 @@ int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& 
                DeviceInfo* di, cudaStream_t st) {
   using C = FwdCfg<D>;
   const int slot = (D == 128 ? 2 : 0) + (kStep ? 1 : 0);
-  if (!di->fwd_attr[slot]) {
+  if (!di->fwd_attr[slot].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(cpattn_fwd_kernel<D, kStep>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes) != cudaSuccess)
       return CPATTN_ERR_CUDA;
@@ -107,7 +109,7 @@ int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& 
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, cpattn_fwd_kernel<D, kStep>) != cudaSuccess) return CPATTN_ERR_CUDA;
     if (fa.numRegs != kFwdLaunchRegs) return CPATTN_ERR_LAUNCH_FAILED;
-    di->fwd_attr[slot] = true;
+    di->fwd_attr[slot].store(true, std::memory_order_release);
   }
   const int units = fwd_num_units(args.g);
   const int grid = units < di->num_sms ? units : di->num_sms;
@@ -356,13 +358,13 @@ template <int D>
 int launch_bwd_stage(int stage, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      const CUtensorMap& tdo, const BwdArgs& args, DeviceInfo* di, cudaStream_t st) {
   const int slot = D == 128 ? 1 : 0;
-  if (!di->bwd_attr[slot]) {
+  if (!di->bwd_attr[slot].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(cpattn_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DkdvCfg<D>::kSmemBytes) != cudaSuccess ||
         cudaFuncSetAttribute(cpattn_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DqCfg<D>::kSmemBytes) != cudaSuccess)
       return CPATTN_ERR_CUDA;
-    di->bwd_attr[slot] = true;
+    di->bwd_attr[slot].store(true, std::memory_order_release);
   }
   if (stage == 0) {
     const int64_t rows = int64_t(args.g.b) * args.g.s * args.g.hq;

@@ -35,6 +35,10 @@
  *     buffer. Device buffers must be 16-byte aligned. No call allocates
  *     device memory and none keeps per-call state (the one fixed scratch
  *     array, used only by cpattn_bwd_noalloc, is part of the loaded module).
+ *   - Device: calls launch on the calling thread's current CUDA device; the
+ *     device buffers and the stream must belong to it. Library state (kernel
+ *     attributes, the status word) is kept per device and may be used from
+ *     several host threads at once.
  *   - stream: a cudaStream_t passed as void* (NULL = legacy default stream).
  *     Calls only enqueue work and return; results are ready when the stream
  *     is synchronised.

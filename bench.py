@@ -12,7 +12,7 @@ independent replica of the workload on its own GPU: the method needs no
 exchange on one GPU, so there is no collective on the data path; value is the
 work of all ranks divided by the slowest rank's time ("scaling": "weak").
 --impl reference times the CPU fp64 oracle on a bounded sample of the same
-workload on the host cores (the baseline this tier compares against).
+workload on the host cores (the reference arm of the comparison).
 """
 import argparse
 import hashlib

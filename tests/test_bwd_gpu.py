@@ -42,6 +42,9 @@ SMALL = [
     (1, 1536, 8, 1, 128, 4, True),    # MQA, c = 192
     (1, 96, 2, 2, 128, 3, True),      # c = 16
     (1, 768, 4, 4, 128, 3, False),    # no mask
+    (3, 8, 2, 1, 128, 4, True),       # c = 1: one token per half-chunk, batch 3
+    (1, 2, 1, 1, 64, 1, True),        # the smallest case: s = 2, one head
+    (1, 6, 3, 3, 64, 3, False),       # c = 1, no mask, odd hq
 ]
 
 

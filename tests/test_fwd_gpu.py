@@ -57,6 +57,9 @@ SMALL = [
     (1, 2048, 4, 4, 128, 8, True),    # many ranks, c = 128
     (1, 768, 4, 4, 128, 3, False),    # no mask
     (2, 384, 2, 1, 64, 1, False),     # no mask, cp = 1, c = 192
+    (3, 8, 2, 1, 128, 4, True),       # c = 1: one token per half-chunk, batch 3
+    (1, 2, 1, 1, 64, 1, True),        # the smallest case: s = 2, one head
+    (1, 6, 3, 3, 64, 3, False),       # c = 1, no mask, odd hq
 ]
 
 

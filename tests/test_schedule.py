@@ -25,6 +25,11 @@ GEOMS = [
     (1, 768, 4, 4, 3, 0, 6),
     (2, 384, 2, 1, 1, 0, 3),
     (1, 1280, 2, 1, 5, 1, 9),
+    # degenerate chunks: one token per half-chunk (s = 2cp), and two
+    (1, 2, 1, 1, 1, 1, 1),
+    (3, 8, 2, 1, 4, 1, 5),
+    (1, 6, 3, 3, 3, 0, 2),
+    (2, 16, 4, 2, 4, 1, 3),
 ]
 
 
@@ -46,6 +51,7 @@ PACKED = [
     ([96], 2, 2, 3, 1, 2),
     ([768, 1536], 2, 2, 3, 0, 4),
     ([16, 16, 16, 16, 16, 16], 3, 1, 1, 1, 3),
+    ([4, 8, 0, 4], 2, 1, 2, 1, 3),                  # one- and two-token chunks
 ]
 
 

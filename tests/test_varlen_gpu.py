@@ -28,6 +28,7 @@ CASES = [
     ([960, 0, 192, 384], 6, 2, 64, 3, None),     # empty sample, ragged chunks
     ([2048, 128], 8, 1, 128, 4, 0.05),          # MQA, custom scale
     ([96], 2, 2, 128, 3, None),                 # one sample, c = 16
+    ([4, 8, 0, 4], 2, 1, 128, 2, None),         # one- and two-token chunks
 ]
 
 

@@ -69,29 +69,64 @@ __device__ __forceinline__ int64_t ld_pos(const CpGeom& g, int ntp, int seq, int
 }
 
 // ---------------------------------------------------------------- preprocess
+// A warp takes 32 consecutive rows, one per lane for the index arithmetic and
+// the writes. The loads are cooperative: each load instruction reads whole
+// rows (D/8 lanes x 16 bytes per row, so 32*16/(2D) rows per instruction),
+// the partial dot products are summed by xor shuffles inside each row's lane
+// group, and the lane that owns the row keeps its sum.
 template <int D>
 __global__ void __launch_bounds__(256) cpattn_bwd_pre_kernel(const BwdArgs a) {
+  constexpr int kLanesPerRow = D / 8;              // 16 (d = 128) or 8 (d = 64)
+  constexpr int kRowsPerLoad = 32 / kLanesPerRow;  // rows one warp-wide load covers
+  constexpr int kLoads = 32 / kRowsPerLoad;        // loads for the warp's 32 rows
+  constexpr int kBatch = 4;                        // loads in flight per lane
   const CpGeom& g = a.g;
   const int64_t nrows = int64_t(g.b) * g.s * g.hq;
-  for (int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; idx < nrows;
-       idx += int64_t(gridDim.x) * blockDim.x) {
+  const int lane = threadIdx.x & 31;
+  const int li = lane % kLanesPerRow;
+  const int lr = lane / kLanesPerRow;  // which of a load's rows this lane reads
+  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t r0 = ((int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * 32; r0 < nrows; r0 += nwarps * 32) {
+    float mine = 0.f;
+#pragma unroll
+    for (int l0 = 0; l0 < kLoads; l0 += kBatch) {
+      uint4 x[kBatch], y[kBatch];
+#pragma unroll
+      for (int l = 0; l < kBatch; ++l) {
+        const int64_t row = r0 + (l0 + l) * kRowsPerLoad + lr;
+        if (row < nrows) {
+          x[l] = reinterpret_cast<const uint4*>(a.o + row * D)[li];
+          y[l] = reinterpret_cast<const uint4*>(a.dout + row * D)[li];
+        } else {
+          x[l] = make_uint4(0u, 0u, 0u, 0u);
+          y[l] = x[l];
+        }
+      }
+#pragma unroll
+      for (int l = 0; l < kBatch; ++l) {
+        const uint32_t xs[4] = {x[l].x, x[l].y, x[l].z, x[l].w}, ys[4] = {y[l].x, y[l].y, y[l].z, y[l].w};
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          acc = fmaf(__uint_as_float(xs[k] << 16), __uint_as_float(ys[k] << 16), acc);
+          acc = fmaf(__uint_as_float(xs[k] & 0xffff0000u), __uint_as_float(ys[k] & 0xffff0000u), acc);
+        }
+#pragma unroll
+        for (int off = kLanesPerRow / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        // rows (l0 + l) * kRowsPerLoad + j, j < kRowsPerLoad: lane owning row
+        // (l0 + l) * kRowsPerLoad + j takes group j's sum
+        const int first = (l0 + l) * kRowsPerLoad;
+        const float v = __shfl_sync(0xffffffffu, acc, ((lane - first) & (kRowsPerLoad - 1)) * kLanesPerRow);
+        if (lane >= first && lane < first + kRowsPerLoad) mine = v;
+      }
+    }
+    const int64_t idx = r0 + lane;
+    if (idx >= nrows) continue;
+    const float acc = mine;
     const int h = int(idx % g.hq);
     const int64_t bt = idx / g.hq;
     const int t = int(bt % g.s);
     const int bi = int(bt / g.s);
-    const uint4* po = reinterpret_cast<const uint4*>(a.o + idx * D);
-    const uint4* pd = reinterpret_cast<const uint4*>(a.dout + idx * D);
-    float acc = 0.f;
-#pragma unroll 4
-    for (int i = 0; i < D / 8; ++i) {
-      const uint4 x = po[i], y = pd[i];
-      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        acc = fmaf(__uint_as_float(xs[k] << 16), __uint_as_float(ys[k] << 16), acc);
-        acc = fmaf(__uint_as_float(xs[k] & 0xffff0000u), __uint_as_float(ys[k] & 0xffff0000u), acc);
-      }
-    }
     // the row's sequence (batch element, or the packed sample holding t)
     int seq = bi, tl = t;
     if (g.nseq > 0) {

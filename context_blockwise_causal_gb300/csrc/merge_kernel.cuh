@@ -26,46 +26,73 @@ struct MergeArgs {
   __nv_bfloat16* o_bf16;  // optional bf16 copy of the merged O
 };
 
+// A warp takes a contiguous run of rows (one row per D/4 lanes: the whole
+// warp at d = 128, a half-warp at d = 64) and decodes its first row once;
+// the (batch, token, head) of the following rows are stepped, so the loop
+// does no integer division.
 template <int D>
 __global__ void __launch_bounds__(256) cpattn_lse_merge_kernel(const MergeArgs m) {
-  constexpr int kV = D / 4;  // float4 per row; a row lies within one warp
+  constexpr int kV = D / 4;               // float4 per row
+  constexpr int kRowsPerStep = 32 / kV;   // rows a warp handles at once
   const int64_t rows = int64_t(m.b) * m.s * m.hq;
-  const int64_t total = rows * kV;  // a multiple of 32: whole warps per iteration
-  for (int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-       idx += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t row = idx / kV;  // [b, s, hq] order, as o
-    const int c = int(idx % kV);
-    const int h = int(row % m.hq);
-    const int64_t bt = row / m.hq;
-    const int t = int(bt % m.s);
-    const int bi = int(bt / m.s);
-    const int64_t lpos = (int64_t(bi) * m.hq + h) * m.s + t;
-    const float la = m.lse_a[lpos];
-    const float lb = m.lse_b ? m.lse_b[lpos] : -INFINITY;
-    const float4 oa = reinterpret_cast<const float4*>(m.o_a)[idx];
-    const float4 ob = m.o_b ? reinterpret_cast<const float4*>(m.o_b)[idx] : make_float4(0.f, 0.f, 0.f, 0.f);
-    const float mx = fmaxf(la, lb);
-    float wa = 0.f, wb = 0.f, L = -INFINITY;
-    if (mx > -INFINITY) {
-      const float ea = expf(la - mx), eb = expf(lb - mx);
-      const float sum = ea + eb;
-      L = mx + logf(sum);
-      wa = ea / sum;
-      wb = eb / sum;
+  const int lane = threadIdx.x & 31;
+  const int c = lane % kV;
+  const int sub = lane / kV;
+  const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  // rows per warp, a multiple of kRowsPerStep
+  const int64_t per = ((rows + nwarps - 1) / nwarps + kRowsPerStep - 1) / kRowsPerStep * kRowsPerStep;
+  const int64_t r_begin = warp * per;
+  const int64_t r_end = r_begin + per < rows ? r_begin + per : rows;
+  if (r_begin >= r_end) return;
+  // this lane's first row, decoded once
+  int64_t row = r_begin + sub;
+  int h = int(row % m.hq);
+  int64_t bt = row / m.hq;
+  int t = int(bt % m.s);
+  int bi = int(bt / m.s);
+  for (; row - sub < r_end; row += kRowsPerStep) {
+    if (row < r_end) {
+      const int64_t lpos = (int64_t(bi) * m.hq + h) * m.s + t;
+      const int64_t idx = row * kV + c;
+      const float la = m.lse_a[lpos];
+      const float lb = m.lse_b ? m.lse_b[lpos] : -INFINITY;
+      const float4 oa = reinterpret_cast<const float4*>(m.o_a)[idx];
+      const float4 ob = m.o_b ? reinterpret_cast<const float4*>(m.o_b)[idx] : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float mx = fmaxf(la, lb);
+      float wa = 0.f, wb = 0.f, L = -INFINITY;
+      if (mx > -INFINITY) {
+        const float ea = expf(la - mx), eb = expf(lb - mx);
+        const float sum = ea + eb;
+        L = mx + logf(sum);
+        wa = ea / sum;
+        wb = eb / sum;
+      }
+      const float4 r = make_float4(wa * oa.x + wb * ob.x, wa * oa.y + wb * ob.y, wa * oa.z + wb * ob.z,
+                                   wa * oa.w + wb * ob.w);
+      // every lane of the row has read lse_a / o_a before any lane writes
+      // (the outputs may alias the first input)
+      __syncwarp(kV == 32 ? 0xffffffffu : (0xffffu << (16 * sub)));
+      if (m.o_out) reinterpret_cast<float4*>(m.o_out)[idx] = r;
+      if (m.o_bf16) {
+        uint2 pk;
+        pk.x = pack_bf16x2(r.x, r.y);
+        pk.y = pack_bf16x2(r.z, r.w);
+        reinterpret_cast<uint2*>(m.o_bf16)[idx] = pk;
+      }
+      if (c == 0) m.lse_out[lpos] = L;
     }
-    const float4 r = make_float4(wa * oa.x + wb * ob.x, wa * oa.y + wb * ob.y, wa * oa.z + wb * ob.z,
-                                 wa * oa.w + wb * ob.w);
-    // every lane of the row has read lse_a / o_a before any lane writes
-    // (the outputs may alias the first input)
-    __syncwarp();
-    if (m.o_out) reinterpret_cast<float4*>(m.o_out)[idx] = r;
-    if (m.o_bf16) {
-      uint2 pk;
-      pk.x = pack_bf16x2(r.x, r.y);
-      pk.y = pack_bf16x2(r.z, r.w);
-      reinterpret_cast<uint2*>(m.o_bf16)[idx] = pk;
+    // step (bi, t, h) by kRowsPerStep rows ([b, s, hq] order)
+#pragma unroll
+    for (int k = 0; k < kRowsPerStep; ++k) {
+      if (++h == m.hq) {
+        h = 0;
+        if (++t == m.s) {
+          t = 0;
+          ++bi;
+        }
+      }
     }
-    if (c == 0) m.lse_out[lpos] = L;
   }
 }
 

@@ -174,7 +174,9 @@ def run_reference(args, w):
     if rank != 0:
         return
     cores = torch.get_num_threads()
-    rows_n = args.ref_rows
+    # about 4096 sampled rows over the whole run (32..1024 per step), so the
+    # run stays within a few minutes whatever --steps is, unless given
+    rows_n = args.ref_rows or max(32, min(1024, 4096 // (args.steps + args.warmup)))
     for _ in range(args.warmup):
         _oracle_sample(w, rows_n, seed=w.seed + 5)
     times, flops = [], 0.0
@@ -526,16 +528,17 @@ def run_ours(args, w):
                 v_["frac_sustained"] = v_["fwd_tflops"] / peaks["bf16_tflops_sustained"]
             line["fwd_other_configs"] = sweep
         if not args.no_cpu_baseline:
-            dt, fl = _oracle_sample(w, args.ref_rows, seed=w.seed + 5)
+            ref_rows = args.ref_rows or 1024
+            dt, fl = _oracle_sample(w, ref_rows, seed=w.seed + 5)
             line["cpu_baseline"] = {
                 "value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": torch.get_num_threads(), "kind": "oracle",
-                "sample": f"{args.ref_rows} seeded query rows x {w.hq} heads of {w.name}: forward O/LSE + backward "
+                "sample": f"{ref_rows} seeded query rows x {w.hq} heads of {w.name}: forward O/LSE + backward "
                           f"dQ (CPU fp64 oracle), {dt:.1f} s"}
             # the same oracle on one thread, on a smaller sample of the same rows' kind
             nthr = torch.get_num_threads()
             torch.set_num_threads(1)
             try:
-                rows1 = max(1, args.ref_rows // 16)
+                rows1 = max(1, ref_rows // 16)
                 dt1, fl1 = _oracle_sample(w, rows1, seed=w.seed + 6)
             finally:
                 torch.set_num_threads(nthr)
@@ -553,7 +556,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--ref-rows", type=int, default=1024)
+    ap.add_argument("--ref-rows", type=int, default=None,
+                    help="oracle rows per sample (default: 1024 for the CPU baseline; the reference arm spreads "
+                         "about 4096 rows over its steps)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-unfused", action="store_true", help="skip timing the unfused forward")
     ap.add_argument("--no-sweep", action="store_true", help="skip the forward on the other configurations")

@@ -458,10 +458,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(hh == 0 ? &p_half[sub] : &p_full[sub]);
         }
-        float a0, a1, b0, b1;
+        float a0, a1;
         f2_unpack(f2_add(f2_add(acc0, acc1), f2_add(acc2, acc3)), a0, a1);
-        (void)b0;
-        (void)b1;
         l = l * alpha + (a0 + a1);
       }
       if (!ok) break;

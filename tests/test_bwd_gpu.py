@@ -131,3 +131,21 @@ def test_bwd_long_context_properties_and_sampled_rows():
     dq_r, _, _ = oracle.attention_backward(cpu["q"], cpu["k"], cpu["v"], cpu["do"], causal=True, dq_rows=rows,
                                            dkv_heads=[], row_block=64)
     assert rel_l2(dq.float().cpu()[:, rows], dq_r) <= REL_L2
+
+
+@pytest.mark.parametrize("std", [4.0, 8.0])
+def test_bwd_peaky_scores_all_elements(std):
+    """Q, K ~ N(0, std^2): near one-hot probabilities; all gradients against
+    the oracle."""
+    w = Workload("peaky_bwd", b=1, s=1024, hq=4, hkv=2, d=128, cp=4, q_std=std, k_std=std, backward=True,
+                 seed=41 + int(std))
+    x = make_inputs(w, device="cuda")
+    o, lse = cpattn_fwd(x["q"], x["k"], x["v"], w.cp)
+    dq, dk, dv = cpattn_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], w.cp)
+    torch.cuda.synchronize()
+    assert cpattn_device_status() == 0
+    cpu = {n: t.cpu() for n, t in x.items()}
+    refs = oracle.attention_backward(cpu["q"], cpu["k"], cpu["v"], cpu["do"], causal=True)
+    for name, got, ref in (("dq", dq, refs[0]), ("dk", dk, refs[1]), ("dv", dv, refs[2])):
+        err = rel_l2(got.float().cpu(), ref)
+        assert err <= REL_L2, f"{name} rel L2 {err:.3e}"

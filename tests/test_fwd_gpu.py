@@ -109,3 +109,17 @@ def test_fwd_full_size_workloads(name):
     o_ref, l_ref = oracle.attention_forward(q_c, k_c, v_c, causal=w.causal, rows=rows,
                                             row_block=128 if w.s > 32768 else 512)
     _check(o, lse, o_ref, l_ref, rows=rows)
+
+
+@pytest.mark.parametrize("std,cp,d", [(8.0, 4, 128), (16.0, 2, 64)])
+def test_fwd_peaky_scores_all_elements(std, cp, d):
+    """Q, K ~ N(0, std^2): scores of several hundred, a row's maximum moves
+    often and most probabilities underflow; every element against the
+    oracle."""
+    w = Workload("peaky", b=1, s=1024, hq=4, hkv=2, d=d, cp=cp, q_std=std, k_std=std, seed=31 + cp)
+    x = make_inputs(w, device="cuda")
+    o, lse = cpattn_fwd(x["q"], x["k"], x["v"], cp)
+    torch.cuda.synchronize()
+    assert cpattn_device_status() == 0
+    o_ref, l_ref = oracle.attention_forward(x["q"].cpu(), x["k"].cpu(), x["v"].cpu(), causal=True)
+    _check(o, lse, o_ref, l_ref)

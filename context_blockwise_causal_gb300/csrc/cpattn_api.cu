@@ -37,7 +37,7 @@ struct DeviceInfo {
   int num_sms = 0;
   unsigned int* status = nullptr;
   // kernel attributes already set, per kernel; set once, read by any thread
-  std::atomic<bool> fwd_attr[4] = {};  // [d == 128][step form]
+  std::atomic<bool> fwd_attr[8] = {};  // [d == 128][step form][five-slot ring]
   std::atomic<bool> bwd_attr[2] = {};
 };
 DeviceInfo g_devs[kMaxDevices];
@@ -94,27 +94,37 @@ CpGeom make_geom(int b, int s, int hq, int hkv, int cp, int causal) {
   return g;
 }
 
-template <int D, bool kStep>
-int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& args,
-               DeviceInfo* di, cudaStream_t st) {
-  using C = FwdCfg<D>;
-  const int slot = (D == 128 ? 2 : 0) + (kStep ? 1 : 0);
+template <int D, bool kStep, int kRing>
+int launch_fwd_ring(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& args,
+                    DeviceInfo* di, cudaStream_t st) {
+  using C = FwdCfg<D, kRing>;
+  const int slot = (D == 128 ? 4 : 0) + (kStep ? 2 : 0) + (kRing == fwd_ring<D>(false) ? 0 : 1);
   if (!di->fwd_attr[slot].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(cpattn_fwd_kernel<D, kStep>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(cpattn_fwd_kernel<D, kStep, kRing>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes) != cudaSuccess)
       return CPATTN_ERR_CUDA;
     // The in-kernel register split assumes exactly kFwdLaunchRegs registers
     // per thread at launch; with fewer, the growing warpgroups would wait
     // for registers that never come free.
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, cpattn_fwd_kernel<D, kStep>) != cudaSuccess) return CPATTN_ERR_CUDA;
+    if (cudaFuncGetAttributes(&fa, cpattn_fwd_kernel<D, kStep, kRing>) != cudaSuccess) return CPATTN_ERR_CUDA;
     if (fa.numRegs != kFwdLaunchRegs) return CPATTN_ERR_LAUNCH_FAILED;
     di->fwd_attr[slot].store(true, std::memory_order_release);
   }
   const int units = fwd_num_units(args.g);
   const int grid = units < di->num_sms ? units : di->num_sms;
-  cpattn_fwd_kernel<D, kStep><<<grid, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, args);
+  cpattn_fwd_kernel<D, kStep, kRing><<<grid, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, args);
   return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_LAUNCH_FAILED;
+}
+
+// The K/V ring follows the head grouping (see fwd_ring).
+template <int D, bool kStep>
+int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& args,
+               DeviceInfo* di, cudaStream_t st) {
+  const bool odd_group = (args.g.hq / args.g.hkv) % 2 != 0;
+  if (fwd_ring<D>(odd_group) != fwd_ring<D>(false))
+    return launch_fwd_ring<D, kStep, fwd_ring<D>(true)>(tq, tk, tv, args, di, st);
+  return launch_fwd_ring<D, kStep, fwd_ring<D>(false)>(tq, tk, tv, args, di, st);
 }
 
 }  // namespace

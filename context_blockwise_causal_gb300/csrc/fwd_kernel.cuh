@@ -62,11 +62,21 @@ struct FwdArgs {
   unsigned int* status;
 };
 
+// K/V ring of kRing slots. When the two sub-tiles share K/V a key tile takes
+// two slots (K, V); when they do not (odd GQA groups, including MHA) it
+// takes four (K0, K1, V0, V1), so at d = 128 four slots would hold a single
+// tile with nothing prefetched: those launches use five (the shared-memory
+// budget holds five 32 KB slots beside the two Q tiles).
 template <int D>
+constexpr int fwd_ring(bool odd_group) {
+  return D == 128 ? (odd_group ? 5 : 4) : 8;
+}
+
+template <int D, int kRing = fwd_ring<D>(false)>
 struct FwdCfg {
   static constexpr int kQBytes = kTile * D * 2;  // one 128 x D bf16 tile
   static constexpr int kKVBytes = kTile * D * 2;
-  static constexpr int kSlots = D == 128 ? 4 : 8;
+  static constexpr int kSlots = kRing;
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = 2 * kQBytes;
   static constexpr int kOffBar = kOffKV + kSlots * kKVBytes;
@@ -89,11 +99,11 @@ enum FwdStatusBits : unsigned int {
 // row's softmax over that step's keys only, written as an fp32 partial O and
 // its LSE ("大模型面试宝典 · Megatron-LM 篇", 3.2 step 4, before correction);
 // rows that take no part in the step get O = 0, L = -inf.
-template <int D, bool kStep>
+template <int D, bool kStep, int kRing>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     cpattn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv, const FwdArgs a) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, kRing>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + C::kOffQ;

@@ -172,15 +172,31 @@ def pin_varlen(M):
     total = sum(lens)
     q, k, v = _rand(total, hq, d, gen=g), _rand(total, hkv, d, gen=g), _rand(total, hkv, d, gen=g)
     cu = [0, 5, 14, 20]
-    o, lse = M.varlen_attention_forward(q, k, v, cu, causal=True)
-    for i in range(len(lens)):
-        sl = slice(cu[i], cu[i + 1])
-        _close(o[sl], _sdpa(q[None, sl], k[None, sl], v[None, sl], True)[0], 1e-11)
-        _close(lse[:, sl], _lse(q[None, sl], k[None, sl], True)[0], 1e-11)
+    for causal in (True, False):
+        o, lse = M.varlen_attention_forward(q, k, v, cu, causal=causal)
+        for i in range(len(lens)):
+            sl = slice(cu[i], cu[i + 1])
+            _close(o[sl], _sdpa(q[None, sl], k[None, sl], v[None, sl], causal)[0], 1e-11)
+            _close(lse[:, sl], _lse(q[None, sl], k[None, sl], causal)[0], 1e-11)
+
+
+def pin_varlen_backward(M):
+    g = torch.Generator().manual_seed(96)
+    hq, hkv, d, cu = 2, 1, 4, [0, 6, 6, 13]
+    total = cu[-1]
+    q, k, v, do = (_rand(total, hq, d, gen=g), _rand(total, hkv, d, gen=g), _rand(total, hkv, d, gen=g),
+                   _rand(total, hq, d, gen=g))
+    dq, dk, dv = M.varlen_attention_backward(q, k, v, do, cu, causal=True)
+    for a, b in ((0, 6), (6, 13)):
+        qa, ka, va = (x[None, a:b].clone().requires_grad_(True) for x in (q, k, v))
+        (_sdpa(qa, ka, va, True) * do[None, a:b]).sum().backward()
+        _close(dq[a:b], qa.grad[0], 1e-10)
+        _close(dk[a:b], ka.grad[0], 1e-10)
+        _close(dv[a:b], va.grad[0], 1e-10)
 
 
 PINS = [pin_golden_forward, pin_golden_backward, pin_forward_library, pin_backward_autograd, pin_cp_route,
-        pin_step_partials, pin_merge_closed_form, pin_zigzag, pin_rope, pin_varlen]
+        pin_step_partials, pin_merge_closed_form, pin_zigzag, pin_rope, pin_varlen, pin_varlen_backward]
 
 
 # ---------------------------------------------------------------- mutants
@@ -212,6 +228,11 @@ MUTANTS = [
     ("rope_rotation_sign", "rope.py", "out[bi, :, :, :half] = x1 * c - x2 * s", "out[bi, :, :, :half] = x1 * c + x2 * s"),
     ("rope_frequency_exponent", "rope.py", "inv_freq = base ** (-2.0 * i / d)", "inv_freq = base ** (-1.0 * i / d)"),
     ("rope_shard_local_positions", "rope.py", "return natural_positions(s, cu_seqlens)[g]", "return natural_positions(s, cu_seqlens)[: g.numel()]"),
+    ("varlen_samples_from_zero", "varlen.py", "return [(cu[i], cu[i + 1]) for i in range(len(cu) - 1)]",
+     "return [(cu[0], cu[i + 1]) for i in range(len(cu) - 1)]"),
+    ("varlen_always_causal", "varlen.py", "oi, li = attention_forward(q[None, a:b], k[None, a:b], v[None, a:b], causal=causal, scale=scale)",
+     "oi, li = attention_forward(q[None, a:b], k[None, a:b], v[None, a:b], causal=True, scale=scale)"),
+    ("varlen_dk_dv_swapped", "varlen.py", "dq[a:b], dk[a:b], dv[a:b] = gq[0], gk[0], gv[0]", "dq[a:b], dk[a:b], dv[a:b] = gq[0], gv[0], gk[0]"),
 ]
 
 

@@ -5,6 +5,7 @@ the host compiler and checks, by brute force, that every allowed (query, key)
 pair is computed exactly once.
 """
 import os
+import random
 import shutil
 import subprocess
 
@@ -69,3 +70,46 @@ def test_packed_samples_never_cross_a_boundary(checker):
     out = subprocess.run([checker, *args], capture_output=True, text=True)
     assert out.returncode == 0, out.stdout + out.stderr
     assert out.stdout.count("ok") == len(PACKED)
+
+
+def _fuzz_geometries(n, seed):
+    """Seeded random geometries: batch 1-3, cp 1-6, chunk 1-300 tokens, GQA
+    groups 1-4, either mask, grids from 1 to 160 CTAs (sizes kept small for
+    the checker's per-pair table)."""
+    rng = random.Random(seed)
+    out = []
+    while len(out) < n:
+        b, cp, c = rng.randint(1, 3), rng.randint(1, 6), rng.randint(1, 300)
+        s = 2 * cp * c
+        hkv = rng.randint(1, 2)
+        hq = hkv * rng.randint(1, 4)
+        if b * s > 2400:
+            continue
+        out.append((b, s, hq, hkv, cp, rng.randint(0, 1), rng.randint(1, 160)))
+    return out
+
+
+def test_random_geometries(checker):
+    geoms = _fuzz_geometries(24, seed=2026)
+    args = [str(x) for g in geoms for x in ("U", *g)]
+    out = subprocess.run([checker, *args], capture_output=True, text=True)
+    assert out.returncode == 0, out.stdout + out.stderr
+    assert out.stdout.count("ok") == len(geoms)
+
+
+def test_random_packed_geometries(checker):
+    rng = random.Random(7)
+    args, n = [], 0
+    while n < 12:
+        cp = rng.randint(1, 4)
+        lens = [2 * cp * rng.randint(0, 60) for _ in range(rng.randint(1, 6))]
+        if sum(lens) == 0 or sum(lens) > 2000:
+            continue
+        hkv = rng.randint(1, 2)
+        hq = hkv * rng.randint(1, 3)
+        args += ["P", str(len(lens)), *map(str, lens), str(hq), str(hkv), str(cp), str(rng.randint(0, 1)),
+                 str(rng.randint(1, 40))]
+        n += 1
+    out = subprocess.run([checker, *args], capture_output=True, text=True)
+    assert out.returncode == 0, out.stdout + out.stderr
+    assert out.stdout.count("ok") == n

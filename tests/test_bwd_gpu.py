@@ -149,3 +149,44 @@ def test_bwd_peaky_scores_all_elements(std):
     for name, got, ref in (("dq", dq, refs[0]), ("dk", dk, refs[1]), ("dv", dv, refs[2])):
         err = rel_l2(got.float().cpu(), ref)
         assert err <= REL_L2, f"{name} rel L2 {err:.3e}"
+
+
+def _random_geometries(n, seed):
+    import random
+    rng = random.Random(seed)
+    out = []
+    while len(out) < n:
+        cp = rng.randint(1, 4)
+        c = rng.randint(1, 200)
+        b = rng.randint(1, 2)
+        s = 2 * cp * c
+        hkv = rng.randint(1, 2)
+        hq = hkv * rng.randint(1, 4)
+        if b * s * hq > 4096:
+            continue
+        out.append((b, s, hq, hkv, rng.choice([64, 128]), cp, rng.random() < 0.75))
+    return out
+
+
+@pytest.mark.parametrize("b,s,hq,hkv,d,cp,causal", _random_geometries(8, seed=11))
+def test_random_geometries_forward_and_backward(b, s, hq, hkv, d, cp, causal):
+    """Seeded random geometries (ragged chunks, GQA groups 1-4, d 64/128,
+    either mask): every forward element and every gradient against the
+    oracle."""
+    w = Workload("rand", b=b, s=s, hq=hq, hkv=hkv, d=d, cp=cp, causal=causal, backward=True, seed=s + 97 * hq)
+    x = make_inputs(w, device="cuda")
+    o, lse = cpattn_fwd(x["q"], x["k"], x["v"], cp, causal=causal)
+    dq, dk, dv = cpattn_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], cp, causal=causal)
+    torch.cuda.synchronize()
+    assert cpattn_device_status() == 0
+    cpu = {n: t.cpu() for n, t in x.items()}
+    o_ref, l_ref = oracle.attention_forward(cpu["q"], cpu["k"], cpu["v"], causal=causal)
+    ax = o_ref.abs()
+    half = torch.where(ax > 0, torch.exp2(torch.floor(torch.log2(torch.where(ax > 0, ax, torch.ones_like(ax)))) - 8),
+                       torch.zeros_like(ax))
+    assert ((o.double().cpu() - o_ref).abs() - half).max().item() <= 1e-2
+    assert (lse.double().cpu() - l_ref).abs().max().item() <= 1e-3
+    refs = oracle.attention_backward(cpu["q"], cpu["k"], cpu["v"], cpu["do"], causal=causal)
+    for name, got, ref in (("dq", dq, refs[0]), ("dk", dk, refs[1]), ("dv", dv, refs[2])):
+        err = rel_l2(got.float().cpu(), ref)
+        assert err <= REL_L2, f"{name} rel L2 {err:.3e}"

@@ -28,6 +28,7 @@ __all__ = [
     "cpattn_bwd_workspace_bytes",
     "cpattn_zigzag_index",
     "cpattn_device_status",
+    "cpattn_selftest_wait_timeout",
     "library",
 ]
 
@@ -98,6 +99,8 @@ def library():
         lib.cpattn_zigzag_index.restype = _i
         lib.cpattn_device_status.argtypes = [_p, ctypes.POINTER(_i)]
         lib.cpattn_device_status.restype = _i
+        lib.cpattn_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, _p]
+        lib.cpattn_selftest_wait_timeout.restype = _i
         lib.cpattn_strerror.argtypes = [_i]
         lib.cpattn_strerror.restype = ctypes.c_char_p
         lib.cpattn_version.argtypes = []
@@ -404,6 +407,15 @@ def cpattn_zigzag_index(s, cp):
     if rc:
         raise CpattnError(rc, "cpattn_zigzag_index")
     return out
+
+
+def cpattn_selftest_wait_timeout(limit_ns=10_000_000, stream=None):
+    """Enqueue the self-test of the bounded waits: one wait that nothing
+    completes gives up after ``limit_ns`` and sets bit 16 of the device status
+    word (read it with cpattn_device_status)."""
+    rc = library().cpattn_selftest_wait_timeout(int(limit_ns), _stream_handle(stream))
+    if rc:
+        raise CpattnError(rc, "cpattn_selftest_wait_timeout")
 
 
 def cpattn_device_status(stream=None):

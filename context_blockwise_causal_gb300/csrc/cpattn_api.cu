@@ -698,6 +698,32 @@ extern "C" int cpattn_zigzag_index(int s, int cp, int64_t* global_of_local) {
   return CPATTN_OK;
 }
 
+// Self-test of the bounded waits: one thread waits on a barrier phase that
+// nothing completes. The wait gives up after limit_ns of %globaltimer, the
+// kernel records kSelfTestTimeoutBit in the status word and returns; no
+// fault, no hang, and the context stays usable.
+constexpr unsigned int kSelfTestTimeoutBit = 1u << 16;
+__global__ void cpattn_selftest_wait_kernel(unsigned int* status, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait_bounded(&bar, 0, &abort_flag, limit_ns)) atomicOr(status, kSelfTestTimeoutBit);
+}
+
+extern "C" int cpattn_selftest_wait_timeout(unsigned long long limit_ns, void* stream) {
+  if (limit_ns == 0 || limit_ns > kWaitLimitNs) return CPATTN_ERR_INVALID_ARG;
+  DeviceInfo* di = nullptr;
+  int rc = device_info(&di);
+  if (rc) return rc;
+  cpattn_selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(di->status, limit_ns);
+  return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_LAUNCH_FAILED;
+}
+
 extern "C" int cpattn_device_status(void* stream, int* status) {
   if (!status) return CPATTN_ERR_NULL_PTR;
   DeviceInfo* di = nullptr;

@@ -284,6 +284,17 @@ int cpattn_zigzag_index(int s, int cp, int64_t* global_of_local);
  */
 int cpattn_device_status(void* stream, int* status);
 
+/*
+ * Self-test of the timeout path: launches one block whose single waiting
+ * thread waits on a barrier phase that nothing completes, giving up after
+ * limit_ns nanoseconds (1 .. 2e9) exactly as the kernels' waits do. It then
+ * sets bit 16 (0x10000) of the device status word and returns, without a
+ * fault or a hang; cpattn_device_status() reports it afterwards. Returns
+ * CPATTN_ERR_INVALID_ARG for a limit outside the range (before any device
+ * work), else as a launch.
+ */
+int cpattn_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
+
 /* Static description of an error code. */
 const char* cpattn_strerror(int code);
 

@@ -60,6 +60,12 @@ def test_zigzag_index_errors(lib):
     assert lib.cpattn_zigzag_index(12, 3, None) == -2
 
 
+def test_selftest_rejects_limits_out_of_range(lib):
+    lib.cpattn_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, ctypes.c_void_p]
+    assert lib.cpattn_selftest_wait_timeout(0, None) == -1
+    assert lib.cpattn_selftest_wait_timeout(3_000_000_000, None) == -1
+
+
 def test_strerror_and_version(lib):
     assert lib.cpattn_strerror(0) == b"ok"
     for code in range(-8, 0):

@@ -77,6 +77,8 @@ int check_geometry(int b, int s, int hq, int hkv, int d, int cp) {
   if (int64_t(b) * s >= (int64_t(1) << 31)) return CPATTN_ERR_INVALID_ARG;
   const int64_t units = int64_t(b) * ((hq + 1) / 2) * 2 * cp * ((s / (2 * cp) + kTile - 1) / kTile);
   if (units >= (int64_t(1) << 31)) return CPATTN_ERR_INVALID_ARG;
+  // the tile-padded row count of the backward's L/D vectors is an int
+  if (int64_t(2) * cp * ((s / (2 * cp) + kTile - 1) / kTile) * kTile >= (int64_t(1) << 31)) return CPATTN_ERR_INVALID_ARG;
   return CPATTN_OK;
 }
 

@@ -170,3 +170,7 @@ def test_sizes_beyond_the_index_range_are_rejected(lib):
     assert lib.cpattn_fwd(p, p, p, p, p, 2, 1 << 30, 1, 1, 64, 1, 1, None) == -1
     assert lib.cpattn_bwd_workspace_bytes(2, 1 << 30, 1, 1, 64, 1) == 0
     assert lib.cpattn_fwd_unfused(p, p, p, p, p, p, 1 << 40, 2, 1 << 30, 1, 1, 64, 1, 1, None) == -1
+    # a sequence just below 2^31 tokens whose tile padding would not fit an int
+    s = (1 << 31) - 2
+    assert lib.cpattn_fwd(p, p, p, p, p, 1, s, 1, 1, 64, 1, 1, None) == -1
+    assert lib.cpattn_bwd_workspace_bytes(1, s, 1, 1, 64, 1) == 0

@@ -57,6 +57,7 @@ enum BwdStatusBits : unsigned int {
   kStatusBwdMma = 1u << 9,
   kStatusBwdSoftmax = 1u << 10,
   kStatusBwdSmemAlign = 1u << 11,
+  kStatusBwdDrain = 1u << 12,  // copies or MMAs still in flight after the time limit
 };
 
 // Position of query row `row` of (chunk, tile) of head `h` in the
@@ -351,7 +352,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       bool ok = true;
-      uint32_t item = 0;  // blocks loaded so far
+      uint32_t item = 0;  // blocks loaded so far (their dO tiles issued)
+      uint32_t nq = 0;    // Q tiles issued: item, or item + 1 when a dO wait gave up
+      uint32_t nkv = 0;   // K/V tile pairs issued
       int ul = 0;
       auto load_item = [&](const BwdUnit& U, int chunk, int tile, int h) -> bool {
         const int row = U.tok0 + chunk * U.c + tile * kTile;
@@ -362,6 +365,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive_expect_tx(&q_full[qs], C::kTileBytes);
         for (int x = 0; x < D; x += 64)
           tma_load_3d(sQ + qs * C::kTileBytes + (x / 64) * (kTile * 128), &tmq, &q_full[qs], x, h, row);
+        ++nq;
         if (item >= C::kOStages &&
             !mbar_wait_lean(&o_empty[os], ((item / C::kOStages) - 1) & 1, abort_flag, kWaitLimitNs))
           return false;
@@ -397,18 +401,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tma_load_3d(sK + (x / 64) * (kTile * 128), &tmk, kv_full, x, U.g, krow);
                 tma_load_3d(sV + (x / 64) * (kTile * 128), &tmv, kv_full, x, U.g, krow);
               }
+              ++nkv;
             }
           }
         }
         ++ul;
       }
       if (!ok) atomicOr(a.status, kStatusBwdProducer);
-      // Let every copy still in flight land before the CTA can exit.
-      for (uint32_t i = item > C::kQStages ? item - C::kQStages : 0; i < item; ++i)
-        mbar_wait_lean(&q_full[i % C::kQStages], (i / C::kQStages) & 1, abort_flag, kWaitLimitNs);
+      // Let every copy still in flight land before the CTA can exit (older
+      // ones landed before their stage was handed back). These waits do not
+      // stop on the abort flag: the copies complete regardless.
+      bool drained = true;
+      for (uint32_t i = nq > C::kQStages ? nq - C::kQStages : 0; i < nq; ++i)
+        drained &= mbar_wait_drain(&q_full[i % C::kQStages], (i / C::kQStages) & 1, kWaitLimitNs);
       for (uint32_t i = item > C::kOStages ? item - C::kOStages : 0; i < item; ++i)
-        mbar_wait_lean(&o_full[i % C::kOStages], (i / C::kOStages) & 1, abort_flag, kWaitLimitNs);
-      if (ul > 0) mbar_wait_lean(kv_full, (ul - 1) & 1, abort_flag, kWaitLimitNs);
+        drained &= mbar_wait_drain(&o_full[i % C::kOStages], (i / C::kOStages) & 1, kWaitLimitNs);
+      if (nkv > 0) drained &= mbar_wait_drain(kv_full, (nkv - 1) & 1, kWaitLimitNs);
+      if (!drained) atomicOr(a.status, kStatusBwdDrain);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
@@ -506,8 +515,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ++ul;
       }
       if (!ok && lane == 0) atomicOr(a.status, kStatusBwdMma);
+      // no MMA in flight when TMEM and shared memory are released
       umma_commit_w(drain);
-      mbar_wait_warp_lean(drain, 0, abort_flag, kWaitLimitNs);
+      if (!mbar_wait_drain_warp(drain, 0, kWaitLimitNs) && lane == 0) atomicOr(a.status, kStatusBwdDrain);
     }
   } else {
     // ------------------------------------------------------------ element-wise
@@ -840,10 +850,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ++ul;
       }
       if (!ok) atomicOr(a.status, kStatusBwdProducer);
+      // copies still in flight land before the CTA can exit (see above)
+      bool drained = true;
       const uint32_t first = nload > (uint32_t)C::kSlots ? nload - C::kSlots : 0;
       for (uint32_t i = first; i < nload; ++i)
-        mbar_wait_lean(&kv_full[i % C::kSlots], (i / C::kSlots) & 1, abort_flag, kWaitLimitNs);
-      if (ul > 0) mbar_wait_lean(q_full, (ul - 1) & 1, abort_flag, kWaitLimitNs);
+        drained &= mbar_wait_drain(&kv_full[i % C::kSlots], (i / C::kSlots) & 1, kWaitLimitNs);
+      if (ul > 0) drained &= mbar_wait_drain(q_full, (ul - 1) & 1, kWaitLimitNs);
+      if (!drained) atomicOr(a.status, kStatusBwdDrain);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
@@ -942,8 +955,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ++ul;
       }
       if (!ok && lane == 0) atomicOr(a.status, kStatusBwdMma);
+      // no MMA in flight when TMEM and shared memory are released
       umma_commit_w(drain);
-      mbar_wait_warp_lean(drain, 0, abort_flag, kWaitLimitNs);
+      if (!mbar_wait_drain_warp(drain, 0, kWaitLimitNs) && lane == 0) atomicOr(a.status, kStatusBwdDrain);
     }
   } else {
     // ------------------------------------------------------------ element-wise

@@ -98,6 +98,7 @@ enum FwdStatusBits : unsigned int {
   kStatusProducer = 1u << 0,
   kStatusMma = 1u << 1,
   kStatusSoftmax = 1u << 2,
+  kStatusDrain = 1u << 3,  // copies or MMAs still in flight after the time limit
 };
 
 // kStep = false: the fused forward (all CP steps, merged on chip, bf16 O).
@@ -219,14 +220,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ++ul;
       }
       if (!ok) atomicOr(a.status, kStatusProducer);
-      // Let every copy still in flight land before the CTA can exit.
+      // Let every copy still in flight land before the CTA can exit (older
+      // ones landed before their slot was handed back). These waits do not
+      // stop on the abort flag: the copies complete regardless.
+      bool drained = true;
       const uint32_t first = nload > (uint32_t)C::kSlots ? nload - C::kSlots : 0;
       for (uint32_t i = first; i < nload; ++i)
-        mbar_wait_bounded(&kv_full[i % C::kSlots], (i / C::kSlots) & 1, abort_flag, kWaitLimitNs);
+        drained &= mbar_wait_drain(&kv_full[i % C::kSlots], (i / C::kSlots) & 1, kWaitLimitNs);
       if (ul > 0) {
-        mbar_wait_bounded(&q_full[0], (ul - 1) & 1, abort_flag, kWaitLimitNs);
-        mbar_wait_bounded(&q_full[1], (ul - 1) & 1, abort_flag, kWaitLimitNs);
+        drained &= mbar_wait_drain(&q_full[0], (ul - 1) & 1, kWaitLimitNs);
+        drained &= mbar_wait_drain(&q_full[1], (ul - 1) & 1, kWaitLimitNs);
       }
+      if (!drained) atomicOr(a.status, kStatusDrain);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
@@ -345,9 +350,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ++ul;
       }
       if (!ok && lane == 0) atomicOr(a.status, kStatusMma);
-      // No MMA may be in flight when TMEM is released.
+      // No MMA may be in flight when TMEM is released (nor when the shared
+      // memory they read is), whether or not a role gave up.
       umma_commit_w(drain);
-      mbar_wait_warp(drain, 0, abort_flag, kWaitLimitNs);
+      if (!mbar_wait_drain_warp(drain, 0, kWaitLimitNs) && lane == 0) atomicOr(a.status, kStatusDrain);
     }
   }
   } else {

@@ -105,6 +105,24 @@ __device__ __forceinline__ bool mbar_wait_warp_lean(uint64_t* bar, uint32_t pari
   return ok;
 }
 
+// Waits for work that completes by itself -- TMA copies already issued, MMAs
+// already committed to a barrier -- before a CTA releases the shared memory
+// or TMEM that work writes. Unlike the waits above it ignores the abort
+// flag: that work finishes whether or not another role gave up, and leaving
+// before it does would let it write memory the CTA no longer owns. Only the
+// time limit ends it (false: the caller records it in the status word).
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  return true;
+}
+// The same for a whole converged warp (the MMA issuers' final commit).
+__device__ __forceinline__ bool mbar_wait_drain_warp(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, mbar_wait_drain(bar, parity, limit_ns));
+}
+
 // Register reallocation between warpgroups (all four warps of a warpgroup
 // execute the same instruction). The counts must be multiples of 8.
 template <int N>

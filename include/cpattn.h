@@ -280,7 +280,18 @@ int cpattn_zigzag_index(int s, int cp, int64_t* global_of_local);
  * Reads the sticky device status word of the current device into *status
  * (0 = no kernel gave up waiting) and clears it. Synchronises `stream`.
  * Returns CPATTN_ERR_TIMEOUT when the word was non-zero, else 0 or a CUDA
- * error code.
+ * error code. Bits: forward producer / MMA / softmax role gave up (0, 1, 2);
+ * forward copies or MMAs still in flight at the end after the time limit (3);
+ * the same for the backward kernels (8, 9, 10; 12); a backward kernel's
+ * shared memory base not 1024-byte aligned (11); the timeout self-test (16).
+ * A role that gives up makes the others leave too, but every role first waits
+ * for the copies and MMAs it already issued, so no kernel frees memory that
+ * asynchronous work still writes.
+ *
+ * The per-device state behind this word (and the scratch address of
+ * cpattn_bwd_noalloc) is looked up once per device ordinal and kept for the
+ * life of the process: the library does not survive cudaDeviceReset() of a
+ * device it has used (reload the process instead).
  */
 int cpattn_device_status(void* stream, int* status);
 

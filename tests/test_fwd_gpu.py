@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import oracle
-from context_blockwise_causal_gb300 import cpattn_device_status, cpattn_fwd
+from context_blockwise_causal_gb300 import cpattn_device_status, cpattn_fwd, cpattn_fwd_step, cpattn_lse_merge
 from context_blockwise_causal_gb300.workloads import WORKLOADS, Workload, make_inputs, sample_rows
 
 pytestmark = pytest.mark.gpu
@@ -29,7 +29,7 @@ def _bf16_half_ulp(x):
     return torch.where(ax > 0, torch.exp2(e - 8), torch.zeros_like(ax))
 
 
-def _check(o, lse, o_ref, lse_ref, rows=None):
+def _check(o, lse, o_ref, lse_ref, rows=None, name="case"):
     o_gpu = o.float().cpu().double()
     l_gpu = lse.cpu().double()
     if rows is not None:
@@ -40,9 +40,30 @@ def _check(o, lse, o_ref, lse_ref, rows=None):
     half_ulp = _bf16_half_ulp(o_ref)
     o_err = (err - half_ulp).max().item()
     l_err = (l_gpu - lse_ref).abs().max().item()
+    # the raw error and the largest half ulp are printed (pytest -s) so the
+    # share of the allowance a case uses can be read off
+    print(f"PARITY {name}: max|O err| raw {err.max().item():.3e}, beyond half ulp {o_err:.3e}, "
+          f"max half ulp {half_ulp.max().item():.3e}, max|O_ref| {o_ref.abs().max().item():.3f}, "
+          f"max|LSE err| {l_err:.3e}")
     assert o_err <= O_TOL, f"max |O err| beyond output rounding {o_err:.3e} (raw {err.max().item():.3e})"
     assert l_err <= LSE_TOL, f"max |LSE err| {l_err:.3e}"
     return o_err, l_err
+
+
+def _fp32_o_by_steps(q, k, v, cp, causal):
+    """The forward's O in fp32, before any bf16 rounding: the same kernel in
+    its step form (one launch per CP step, normalised fp32 partials) merged
+    step after step by the log-sum-exp kernel into an fp32 result."""
+    b, s, hq, d = q.shape
+    o_acc, l_acc = cpattn_fwd_step(q, k, v, cp, 0, causal=causal)
+    if cp > 1:
+        o_part = torch.empty_like(o_acc)
+        l_part = torch.empty_like(l_acc)
+        for i in range(1, cp):
+            cpattn_fwd_step(q, k, v, cp, i, causal=causal, o_part=o_part, lse_part=l_part)
+            cpattn_lse_merge(o_acc, l_acc, o_part, l_part, o_out=o_acc, lse_out=l_acc)
+        del o_part, l_part
+    return o_acc, l_acc
 
 
 SMALL = [
@@ -104,11 +125,25 @@ def test_fwd_full_size_workloads(name):
     torch.cuda.synchronize()
     assert cpattn_device_status() == 0
     rows = None if w.check_rows == 0 else sample_rows(w, w.check_rows, seed=w.seed + 77)
+    o_c, lse_c = o.cpu(), lse.cpu()
+    del o, lse
+    # the computation's own error, without the bf16 output rounding: fp32 O
+    # through the CP steps must meet the bar with no allowance
+    o32, l32 = _fp32_o_by_steps(x["q"], x["k"], x["v"], w.cp, w.causal)
+    torch.cuda.synchronize()
+    assert cpattn_device_status() == 0
+    o32_c = (o32 if rows is None else o32[:, rows.to(o32.device)]).double().cpu()
+    l32_c = (l32 if rows is None else l32[:, :, rows.to(l32.device)]).double().cpu()
+    del o32, l32
     q_c, k_c, v_c = x["q"].cpu(), x["k"].cpu(), x["v"].cpu()
     del x
     o_ref, l_ref = oracle.attention_forward(q_c, k_c, v_c, causal=w.causal, rows=rows,
                                             row_block=128 if w.s > 32768 else 512)
-    _check(o, lse, o_ref, l_ref, rows=rows)
+    _check(o_c, lse_c, o_ref, l_ref, rows=rows, name=name)
+    raw32 = (o32_c - o_ref).abs().max().item()
+    l32_err = (l32_c - l_ref).abs().max().item()
+    print(f"PARITY {name} fp32 O through the CP steps: max|O err| raw {raw32:.3e}, max|LSE err| {l32_err:.3e}")
+    assert raw32 <= O_TOL and l32_err <= LSE_TOL
 
 
 @pytest.mark.parametrize("std,cp,d", [(8.0, 4, 128), (16.0, 2, 64)])

@@ -81,3 +81,46 @@ def test_many_short_samples_in_one_launch():
     dq_r, dk_r, dv_r = oracle.varlen_attention_backward(q, k, v, do, cu)
     for name, got, ref in (("dq", dq, dq_r), ("dk", dk, dk_r), ("dv", dv, dv_r)):
         assert _rel(got.float().cpu(), ref) <= 2e-2, name
+
+
+def _packed_case(lens, hq, hkv, d, seed):
+    cu = [0]
+    for n in lens:
+        cu.append(cu[-1] + n)
+    total = cu[-1]
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    q = torch.randn(total, hq, d, generator=g).to(torch.bfloat16)
+    k = torch.randn(total, hkv, d, generator=g).to(torch.bfloat16)
+    v = torch.randn(total, hkv, d, generator=g).to(torch.bfloat16)
+    do = torch.randn(total, hq, d, generator=g).to(torch.bfloat16)
+    return cu, q, k, v, do
+
+
+@pytest.mark.parametrize("cp,hq,hkv,d", [(1, 4, 2, 64), (2, 2, 1, 128)])
+def test_more_samples_than_one_launch_holds(cp, hq, hkv, d):
+    """More than 512 samples: the library falls back to one launch per sample,
+    each addressing its rows, its LSE columns (lse + start, row stride the
+    packed total) and the shared workspace itself. 600 samples of 0..64
+    tokens; with cp = 1 the lengths are even but not all multiples of 4, so
+    many samples start at an LSE column that is not 16-byte aligned. Every
+    element against the oracle."""
+    g = torch.Generator(device="cpu").manual_seed(600 + cp)
+    unit = 2 * cp
+    lens = [int(x) * unit for x in torch.randint(0, 64 // unit + 1, (600,), generator=g)]
+    lens[0], lens[1], lens[7] = 0, unit, 64  # an empty sample first, a shortest one, a longest one
+    cu, q, k, v, do = _packed_case(lens, hq, hkv, d, seed=700 + cp)
+    assert len(lens) > 512 and (cp != 1 or any(c % 4 for c in cu))
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = cpattn_fwd_varlen(qd, kd, vd, cu, cp)
+    dq, dk, dv = cpattn_bwd_varlen(qd, kd, vd, o, lse, dod, cu, cp)
+    torch.cuda.synchronize()
+    assert cpattn_device_status() == 0
+    o_r, l_r = oracle.varlen_attention_forward(q, k, v, cu)
+    err = (o.double().cpu() - o_r).abs()
+    assert (err <= 1e-2 + _half_ulp_bf16(o_r)).all(), err.max().item()
+    nonempty = torch.isfinite(l_r)
+    assert torch.equal(torch.isfinite(lse.cpu()), nonempty)
+    assert (lse.double().cpu()[nonempty] - l_r[nonempty]).abs().max().item() <= 1e-3
+    dq_r, dk_r, dv_r = oracle.varlen_attention_backward(q, k, v, do, cu)
+    for name, got, ref in (("dq", dq, dq_r), ("dk", dk, dk_r), ("dv", dv, dv_r)):
+        assert _rel(got.float().cpu(), ref) <= 2e-2, name

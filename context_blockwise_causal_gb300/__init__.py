@@ -27,6 +27,10 @@ __all__ = [
     "cpattn_bwd",
     "cpattn_bwd_workspace_bytes",
     "cpattn_zigzag_index",
+    "cpattn_fwd_rank",
+    "cpattn_fwd_rank_step",
+    "cpattn_bwd_rank",
+    "cpattn_bwd_rank_workspace_bytes",
     "cpattn_device_status",
     "cpattn_selftest_wait_timeout",
     "library",
@@ -95,6 +99,14 @@ def library():
         lib.cpattn_bwd_noalloc_max_scratch_bytes.restype = _sz
         lib.cpattn_bwd_workspace_bytes.argtypes = [_i] * 6
         lib.cpattn_bwd_workspace_bytes.restype = _sz
+        lib.cpattn_fwd_rank.argtypes = [_p] * 5 + [_i] * 8 + [ctypes.c_float, _p]
+        lib.cpattn_fwd_rank.restype = _i
+        lib.cpattn_fwd_rank_step.argtypes = [_p] * 5 + [_i] * 9 + [ctypes.c_float, _p]
+        lib.cpattn_fwd_rank_step.restype = _i
+        lib.cpattn_bwd_rank_workspace_bytes.argtypes = [_i] * 6
+        lib.cpattn_bwd_rank_workspace_bytes.restype = _sz
+        lib.cpattn_bwd_rank.argtypes = [_p] * 10 + [_sz] + [_i] * 9 + [ctypes.c_float, _p]
+        lib.cpattn_bwd_rank.restype = _i
         lib.cpattn_zigzag_index.argtypes = [_i, _i, _p]
         lib.cpattn_zigzag_index.restype = _i
         lib.cpattn_device_status.argtypes = [_p, ctypes.POINTER(_i)]
@@ -397,6 +409,117 @@ def cpattn_bwd(q, k, v, o, lse, do, cp, causal=True, dq=None, dk=None, dv=None, 
     if rc:
         raise CpattnError(rc, "cpattn_bwd" if stage is None else "cpattn_bwd_stage")
     return dq, dk, dv
+
+
+def _rank_dims(q, k, v, cp):
+    """Shapes of a rank-local call: q [b, 2c, hq, d] (the rank's shard) and
+    k, v [cp, b, 2c, hkv, d] (every rank's shard, rank-major) or [b, 2c, hkv, d]
+    (one rank's shard). Returns b, s (the full sequence), hq, hkv, d."""
+    _check_act("q", q)
+    if q.dim() != 4:
+        raise ValueError("q must be the rank's shard [b, 2c, hq, d]")
+    b, local, hq, d = q.shape
+    _check_act("k", k)
+    _check_act("v", v, k.shape)
+    shard = tuple(k.shape[-4:]) if k.dim() in (4, 5) else None
+    if shard is None or shard[0] != b or shard[1] != local or shard[3] != d:
+        raise ValueError("k and v must be [cp, b, 2c, hkv, d] or [b, 2c, hkv, d] matching q")
+    if k.dim() == 5 and k.shape[0] != cp:
+        raise ValueError(f"k and v hold {k.shape[0]} shards, expected cp = {cp}")
+    return b, local * int(cp), hq, shard[2], d
+
+
+def cpattn_fwd_rank(q, k_all, v_all, cp, rank, causal=True, scale=None, o=None, lse=None, stream=None):
+    """One rank's forward in a CP group spread over GPUs (all-gather form).
+
+    q: this rank's zigzag shard [b, 2c, hq, d] (chunk ``rank`` then chunk
+    2cp-1-rank); k_all, v_all: every rank's shard [cp, b, 2c, hkv, d], as an
+    all-gather leaves them. Runs every CP step of the rank in one launch with
+    the merge on chip. Returns (o [b, 2c, hq, d] bf16, lse [b, hq, 2c] fp32).
+    """
+    if k_all.dim() != 5:
+        raise ValueError("k_all and v_all must be [cp, b, 2c, hkv, d]")
+    b, s, hq, hkv, d = _rank_dims(q, k_all, v_all, cp)
+    local = q.shape[1]
+    o = torch.empty_like(q) if o is None else o
+    _check_act("o", o, q.shape)
+    lse = torch.empty(b, hq, local, device=q.device, dtype=torch.float32) if lse is None else lse
+    _check_f32("lse", lse, (b, hq, local))
+    rc = library().cpattn_fwd_rank(q.data_ptr(), k_all.data_ptr(), v_all.data_ptr(), o.data_ptr(), lse.data_ptr(), b,
+                                   s, hq, hkv, d, int(cp), int(rank), 1 if causal else 0,
+                                   0.0 if scale is None else float(scale),
+                                   _stream_handle(stream, q, k_all, v_all, o, lse))
+    if rc:
+        raise CpattnError(rc, "cpattn_fwd_rank")
+    return o, lse
+
+
+def cpattn_fwd_rank_step(q, k_blk, v_blk, cp, rank, step, causal=True, scale=None, o_part=None, lse_part=None,
+                         stream=None):
+    """One CP step of one rank (ring form): q is the rank's shard
+    [b, 2c, hq, d], k_blk/v_blk the shard [b, 2c, hkv, d] of rank
+    (rank - step) mod cp. Returns the step's unmerged result (o_part
+    [b, 2c, hq, d] fp32, lse_part [b, hq, 2c]); rows outside the step get 0
+    and -inf."""
+    if k_blk.dim() != 4:
+        raise ValueError("k_blk and v_blk must be one rank's shard [b, 2c, hkv, d]")
+    b, s, hq, hkv, d = _rank_dims(q, k_blk, v_blk, cp)
+    local = q.shape[1]
+    if o_part is None:
+        o_part = torch.empty(b, local, hq, d, device=q.device, dtype=torch.float32)
+    if lse_part is None:
+        lse_part = torch.empty(b, hq, local, device=q.device, dtype=torch.float32)
+    _check_f32("o_part", o_part, (b, local, hq, d))
+    _check_f32("lse_part", lse_part, (b, hq, local))
+    rc = library().cpattn_fwd_rank_step(q.data_ptr(), k_blk.data_ptr(), v_blk.data_ptr(), o_part.data_ptr(),
+                                        lse_part.data_ptr(), b, s, hq, hkv, d, int(cp), int(rank), int(step),
+                                        1 if causal else 0, 0.0 if scale is None else float(scale),
+                                        _stream_handle(stream, q, k_blk, v_blk, o_part, lse_part))
+    if rc:
+        raise CpattnError(rc, "cpattn_fwd_rank_step")
+    return o_part, lse_part
+
+
+def cpattn_bwd_rank_workspace_bytes(b, s, hq, hkv, d, cp):
+    return int(library().cpattn_bwd_rank_workspace_bytes(b, s, hq, hkv, d, int(cp)))
+
+
+def cpattn_bwd_rank(q, k_all, v_all, o, lse, do, cp, rank, causal=True, scale=None, dq=None, dk_part=None,
+                    dv_part=None, workspace=None, stream=None):
+    """One rank's backward in a CP group spread over GPUs (all-gather form).
+
+    q, o, do: the rank's shard [b, 2c, hq, d]; lse [b, hq, 2c]; k_all, v_all
+    every rank's shard [cp, b, 2c, hkv, d]. Returns (dq [b, 2c, hq, d],
+    dk_part, dv_part [cp, b, 2c, hkv, d]): the rank's own dQ, and its share
+    of every rank's dK/dV, which a reduce-scatter over the group sums.
+    """
+    if k_all.dim() != 5:
+        raise ValueError("k_all and v_all must be [cp, b, 2c, hkv, d]")
+    b, s, hq, hkv, d = _rank_dims(q, k_all, v_all, cp)
+    local = q.shape[1]
+    _check_act("o", o, q.shape)
+    _check_act("do", do, q.shape)
+    _check_f32("lse", lse, (b, hq, local))
+    dq = torch.empty_like(q) if dq is None else dq
+    dk_part = torch.empty_like(k_all) if dk_part is None else dk_part
+    dv_part = torch.empty_like(v_all) if dv_part is None else dv_part
+    _check_act("dq", dq, q.shape)
+    _check_act("dk_part", dk_part, k_all.shape)
+    _check_act("dv_part", dv_part, v_all.shape)
+    need = cpattn_bwd_rank_workspace_bytes(b, s, hq, hkv, d, cp)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    rc = library().cpattn_bwd_rank(q.data_ptr(), k_all.data_ptr(), v_all.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                   do.data_ptr(), dq.data_ptr(), dk_part.data_ptr(), dv_part.data_ptr(),
+                                   workspace.data_ptr(), workspace.numel() * workspace.element_size(), b, s, hq, hkv,
+                                   d, int(cp), int(rank), 1 if causal else 0, 0.0 if scale is None else float(scale),
+                                   _stream_handle(stream, q, k_all, v_all, o, lse, do, dq, dk_part, dv_part,
+                                                  workspace))
+    if rc:
+        raise CpattnError(rc, "cpattn_bwd_rank")
+    return dq, dk_part, dv_part
 
 
 def cpattn_zigzag_index(s, cp):

@@ -1,0 +1,206 @@
+"""Context parallelism over several GPUs: the exchange between CP ranks.
+
+The pages run CP with one rank per device. Rank r of a group of cp ranks
+holds its zigzag shard of q, k, v, dO: chunks r and 2cp-1-r of the
+sequence's 2*cp chunks, concatenated ("大模型面试宝典 · Megatron-LM 篇", 3.2
+step 1 and 3.4). Two ways of moving K/V between the ranks appear there, and
+both are here:
+
+* ring ("大模型面试宝典 · Megatron-LM 篇", 3.1 point 2, 3.2 steps 2-5): at step
+  i every rank passes the K/V shard it holds to the next rank and receives
+  the previous rank's, so that it holds rank (r - i) mod cp's shard at step
+  i. Step i's attention runs while the next shard is in flight (3.2: steps
+  2 and 3 run at the same time); each step's partial output is merged into
+  the running result through its log-sum-exp (3.2 steps 4-5).
+* all-gather ("超大规模集群下大语言模型训练实操指南", section "超长文本场景解决方案"):
+  the forward all-gathers K/V and runs every step of the rank in one fused
+  launch; the backward all-gathers K/V again and reduce-scatters each rank's
+  share of dK/dV.
+
+This module only moves data: sends, receives and collectives of the
+process group (NCCL between GPUs). Every piece of arithmetic -- each step's
+attention, the merges, the backward -- runs in the library's kernels
+through the rank-local entry points (cpattn_fwd_rank, cpattn_fwd_rank_step,
+cpattn_lse_merge, cpattn_bwd_rank). Buffers handed to those kernels are
+always local to the calling GPU; nothing reads another GPU's memory
+directly.
+
+The ``kernels`` and ``exchange`` arguments exist so that the exchange logic
+can be checked on its own: tests pass recording or CPU stand-ins. The
+default kernels are the CUDA library's, and it fails loudly when that
+library is missing.
+"""
+import torch
+import torch.distributed as dist
+
+from . import cpattn_bwd_rank, cpattn_fwd_rank, cpattn_fwd_rank_step, cpattn_lse_merge
+
+__all__ = ["CudaKernels", "GroupExchange", "zigzag_shard", "zigzag_unshard", "cp_forward", "cp_backward"]
+
+
+class CudaKernels:
+    """The device work of one rank: the library's rank-local entry points."""
+
+    @staticmethod
+    def fwd_rank(q, k_all, v_all, cp, rank, causal, scale):
+        return cpattn_fwd_rank(q, k_all, v_all, cp, rank, causal=causal, scale=scale)
+
+    @staticmethod
+    def fwd_rank_step(q, k_blk, v_blk, cp, rank, step, causal, scale, o_part=None, lse_part=None):
+        return cpattn_fwd_rank_step(q, k_blk, v_blk, cp, rank, step, causal=causal, scale=scale, o_part=o_part,
+                                    lse_part=lse_part)
+
+    @staticmethod
+    def lse_merge(o_a, lse_a, o_b, lse_b, o_out, lse_out, o_final):
+        """Merge (o_b, lse_b) into (o_a, lse_a); o_out=False writes the final
+        bf16 output into o_final instead of an fp32 result."""
+        cpattn_lse_merge(o_a, lse_a, o_b, lse_b, o_out=o_out, lse_out=lse_out, o_bf16=o_final)
+
+    @staticmethod
+    def new_output(q):
+        return torch.empty_like(q)
+
+    @staticmethod
+    def bwd_rank(q, k_all, v_all, o, lse, do, cp, rank, causal, scale):
+        return cpattn_bwd_rank(q, k_all, v_all, o, lse, do, cp, rank, causal=causal, scale=scale)
+
+
+class GroupExchange:
+    """K/V movement between the ranks of a torch.distributed process group."""
+
+    def __init__(self, group=None):
+        self.group = group
+        self.rank = dist.get_rank(group)
+        self.cp = dist.get_world_size(group)
+        # the ring: receive from the previous rank, send to the next
+        self.next = self._global((self.rank + 1) % self.cp)
+        self.prev = self._global((self.rank - 1) % self.cp)
+
+    def _global(self, r):
+        return r if self.group is None else dist.get_global_rank(self.group, r)
+
+    def all_gather(self, x):
+        """Every rank's x stacked rank-major: [cp, *x.shape]."""
+        x = x.contiguous()
+        # gathered as the concatenation along dimension 0 (the form every
+        # backend takes), then viewed rank-major
+        out = torch.empty((self.cp * x.shape[0],) + tuple(x.shape[1:]), dtype=x.dtype, device=x.device)
+        dist.all_gather_into_tensor(out, x, group=self.group)
+        return out.view((self.cp,) + tuple(x.shape))
+
+    def reduce_scatter(self, parts):
+        """parts [cp, *shape] on every rank: this rank gets the sum over the
+        ranks of their parts[rank]."""
+        out = torch.empty(tuple(parts.shape[1:]), dtype=parts.dtype, device=parts.device)
+        flat = parts.contiguous().view((parts.shape[0] * parts.shape[1],) + tuple(parts.shape[2:]))
+        dist.reduce_scatter_tensor(out, flat, op=dist.ReduceOp.SUM, group=self.group)
+        return out
+
+    def ring_start(self, send, recv):
+        """Post one ring hop: each tensor of ``send`` goes to the next rank,
+        each of ``recv`` is filled from the previous one. Returns the
+        requests; the send and receive pairs are issued together, so no
+        rank blocks on a send before its own receive is posted."""
+        ops = [dist.P2POp(dist.isend, t, self.next, group=self.group) for t in send]
+        ops += [dist.P2POp(dist.irecv, t, self.prev, group=self.group) for t in recv]
+        return dist.batch_isend_irecv(ops)
+
+    @staticmethod
+    def ring_wait(reqs):
+        for r in reqs or ():
+            r.wait()
+
+
+def zigzag_shard(x, cp, rank, dim=1):
+    """Rank ``rank``'s zigzag shard of a natural-order tensor: chunks rank and
+    2cp-1-rank of dimension ``dim`` (length s, cut into 2cp chunks),
+    concatenated. Data preparation for callers that start from whole
+    sequences (a data loader normally hands each rank its shard)."""
+    s = x.shape[dim]
+    if s % (2 * cp):
+        raise ValueError(f"length {s} is not divisible by 2*cp = {2 * cp}")
+    c = s // (2 * cp)
+    lo = x.narrow(dim, rank * c, c)
+    hi = x.narrow(dim, (2 * cp - 1 - rank) * c, c)
+    return torch.cat((lo, hi), dim=dim)
+
+
+def zigzag_unshard(shards, dim=1):
+    """Inverse of zigzag_shard: the natural-order tensor from every rank's
+    shard (a list in rank order)."""
+    cp = len(shards)
+    c = shards[0].shape[dim] // 2
+    chunks = [None] * (2 * cp)
+    for r, sh in enumerate(shards):
+        chunks[r] = sh.narrow(dim, 0, c)
+        chunks[2 * cp - 1 - r] = sh.narrow(dim, c, c)
+    return torch.cat(chunks, dim=dim)
+
+
+def _ring_forward(q, k, v, rank, cp, causal, scale, kernels, exchange):
+    # Two receive buffers alternate; the caller's own k, v serve step 0 and
+    # are never written. A buffer is refilled only after the step that read
+    # it was issued and its outgoing copy completed.
+    recv = [(torch.empty_like(k), torch.empty_like(v)) for _ in range(min(cp - 1, 2))]
+    kv = (k, v)
+    o = kernels.new_output(q)
+    o_acc = l_acc = o_part = l_part = lse = None
+    for i in range(cp):
+        nxt = recv[i % 2] if i + 1 < cp else None
+        reqs = exchange.ring_start(kv, nxt) if nxt is not None else None  # in flight during step i
+        if i == 0:
+            o_acc, l_acc = kernels.fwd_rank_step(q, kv[0], kv[1], cp, rank, 0, causal, scale)
+        else:
+            o_part, l_part = kernels.fwd_rank_step(q, kv[0], kv[1], cp, rank, i, causal, scale, o_part, l_part)
+        if i == cp - 1:
+            # the last correction writes the bf16 output and the final lse
+            lse = torch.empty_like(l_acc)
+            kernels.lse_merge(o_acc, l_acc, o_part, l_part, False, lse, o)
+        elif i > 0:
+            kernels.lse_merge(o_acc, l_acc, o_part, l_part, o_acc, l_acc, None)
+        exchange.ring_wait(reqs)
+        if nxt is not None:
+            kv = nxt
+    return o, lse
+
+
+def cp_forward(q, k, v, group=None, causal=True, scale=None, form="allgather", kernels=None, exchange=None,
+               keep_kv=False):
+    """CP attention forward of this rank. q [b, 2c, hq, d], k, v [b, 2c, hkv, d]:
+    the rank's zigzag shards. Returns (o [b, 2c, hq, d], lse [b, hq, 2c]) for
+    the rank's rows, equal to those rows of attention over the whole
+    sequence; with ``keep_kv`` (all-gather form) also the gathered
+    (k_all, v_all), which cp_backward can reuse instead of gathering again.
+
+    form="allgather": one all-gather of K and of V, then every CP step in one
+    fused launch (the merge on chip). form="ring": cp steps, each computed
+    while the next shard travels one hop, merged step by step.
+    """
+    exchange = exchange or GroupExchange(group)
+    kernels = kernels or CudaKernels
+    rank, cp = exchange.rank, exchange.cp
+    if form == "ring":
+        if keep_kv:
+            raise ValueError("keep_kv applies to the all-gather form")
+        return _ring_forward(q, k, v, rank, cp, causal, scale, kernels, exchange)
+    if form != "allgather":
+        raise ValueError("form must be 'allgather' or 'ring'")
+    k_all = exchange.all_gather(k)
+    v_all = exchange.all_gather(v)
+    o, lse = kernels.fwd_rank(q, k_all, v_all, cp, rank, causal, scale)
+    return (o, lse, k_all, v_all) if keep_kv else (o, lse)
+
+
+def cp_backward(q, k, v, o, lse, do, group=None, causal=True, scale=None, kv_all=None, kernels=None,
+                exchange=None):
+    """CP attention backward of this rank from its saved o and lse: all-gather
+    K and V (unless ``kv_all`` = (k_all, v_all) from cp_forward is given),
+    the rank's kernels, then a reduce-scatter that sums every rank's share of
+    each shard's dK/dV. Returns (dq, dk, dv) of the rank's shards."""
+    exchange = exchange or GroupExchange(group)
+    kernels = kernels or CudaKernels
+    rank, cp = exchange.rank, exchange.cp
+    if kv_all is None:
+        kv_all = (exchange.all_gather(k), exchange.all_gather(v))
+    dq, dk_part, dv_part = kernels.bwd_rank(q, kv_all[0], kv_all[1], o, lse, do, cp, rank, causal, scale)
+    return dq, exchange.reduce_scatter(dk_part), exchange.reduce_scatter(dv_part)

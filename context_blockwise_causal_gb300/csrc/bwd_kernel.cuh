@@ -60,13 +60,12 @@ enum BwdStatusBits : unsigned int {
   kStatusBwdDrain = 1u << 12,  // copies or MMAs still in flight after the time limit
 };
 
-// Position of query row `row` of (chunk, tile) of head `h` in the
-// tile-padded L/D vectors.
 // Row `row` of tile `tile` of chunk `chunk` of sequence `seq` (tpc tiles per
-// chunk) in the tile-padded L/D vectors [sequences, hq, ntp].
+// chunk) for query head `h` in the tile-padded L/D vectors [sequences, hq,
+// ntp] (only the rank's own tiles in the rank-local form).
 __device__ __forceinline__ int64_t ld_pos(const CpGeom& g, int ntp, int seq, int h, int chunk, int tile, int tpc,
                                           int row) {
-  return int64_t(seq * g.hq + h) * ntp + (chunk * tpc + tile) * kTile + row;
+  return int64_t(seq * g.hq + h) * ntp + ld_tile(g, chunk, tile, tpc) * kTile + row;
 }
 
 // ---------------------------------------------------------------- preprocess
@@ -82,7 +81,8 @@ __global__ void __launch_bounds__(256) cpattn_bwd_pre_kernel(const BwdArgs a) {
   constexpr int kLoads = 32 / kRowsPerLoad;        // loads for the warp's 32 rows
   constexpr int kBatch = 4;                        // loads in flight per lane
   const CpGeom& g = a.g;
-  const int64_t nrows = int64_t(g.b) * g.s * g.hq;
+  const int srows = q_seq_rows(g);  // rows of a sequence in o / dout
+  const int64_t nrows = int64_t(g.b) * srows * g.hq;
   const int lane = threadIdx.x & 31;
   const int li = lane % kLanesPerRow;
   const int lr = lane / kLanesPerRow;  // which of a load's rows this lane reads
@@ -126,8 +126,8 @@ __global__ void __launch_bounds__(256) cpattn_bwd_pre_kernel(const BwdArgs a) {
     const float acc = mine;
     const int h = int(idx % g.hq);
     const int64_t bt = idx / g.hq;
-    const int t = int(bt % g.s);
-    const int bi = int(bt / g.s);
+    const int t = int(bt % srows);
+    const int bi = int(bt / srows);
     // the row's sequence (batch element, or the packed sample holding t)
     int seq = bi, tl = t;
     if (g.nseq > 0) {
@@ -140,8 +140,9 @@ __global__ void __launch_bounds__(256) cpattn_bwd_pre_kernel(const BwdArgs a) {
       tl = t - g.cu[lo];
     }
     const SeqGeom q = seq_geom(g, seq);
-    const int chunk = tl / q.c;
+    int chunk = tl / q.c;  // rank-local form: 0 or 1, the rank's first or second chunk
     const int in = tl - chunk * q.c;
+    if (g.rank >= 0) chunk = chunk ? 2 * g.cp - 1 - g.rank : g.rank;
     const int64_t pos = ld_pos(g, a.ntp, seq, h, chunk, in / kTile, q.tpc, in % kTile);
     a.dvec[pos] = acc;
     a.lvec[pos] = a.lse[(int64_t(bi) * g.hq + h) * a.lse_stride + t] * 1.4426950408889634f;
@@ -357,7 +358,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t nkv = 0;   // K/V tile pairs issued
       int ul = 0;
       auto load_item = [&](const BwdUnit& U, int chunk, int tile, int h) -> bool {
-        const int row = U.tok0 + chunk * U.c + tile * kTile;
+        const int row = U.tok0 + q_chunk_row(g, chunk, U.c) + tile * kTile;
         const uint32_t qs = item % C::kQStages, os = item % C::kOStages;
         if (item >= C::kQStages &&
             !mbar_wait_lean(&q_empty[qs], ((item / C::kQStages) - 1) & 1, abort_flag, kWaitLimitNs))
@@ -539,11 +540,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int idx = snake_unit(rd, blockIdx.x, grid);
       if (idx >= num_units) break;
       const BwdUnit U = bwd_decode_unit(g, idx);
-      if (U.items == 0) continue;  // a tile a shorter packed sample does not have
+      const bool key_ok = jr < U.k_valid;
+      if (U.items == 0) {
+        // No query of this call sees the tile. A tile a shorter packed sample
+        // does not have has no rows (k_valid == 0); a real one (rank-local
+        // form: no query of the rank reaches it) gets a zero share.
+        if (key_ok) {
+          const int64_t off = ((int64_t(U.tok0) + U.k_t0 + jr) * g.hkv + U.g) * D + hf * (D / 2);
+#pragma unroll
+          for (int c0 = 0; c0 < D / 2; c0 += 8) {
+            *reinterpret_cast<uint4*>(a.dv + off + c0) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(a.dk + off + c0) = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        continue;
+      }
       QWalk w(g, U);
       int chunk = 0, tile = 0;
       bool dg = false;
-      const bool key_ok = jr < U.k_valid;
       for (int j = 0; j < U.items && ok; ++j, ++i) {
         if (j % G == 0) w.next(chunk, tile, dg);
         const int rem = U.c - tile * kTile;
@@ -843,7 +857,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         int chunk, tile;
         bool dg;
         while (ok && w.next(chunk, tile, dg)) {
-          const int row = U.tok0 + chunk * U.c + tile * kTile;
+          const int row = U.tok0 + kv_chunk_row(g, chunk, U.c) + tile * kTile;
           // V before K: V is released by the dP MMA, K only after dQ
           ok = load(&tmv, U.g0, row) && load(&tmk, U.g0, row);
         }

@@ -32,15 +32,47 @@ constexpr int kMaxSeqs = 512;  // packed samples per call (their offsets travel 
 // tokens, chunk length c, tpc tiles per chunk) or packed samples (nseq > 0:
 // b == 1, s == total tokens, sample i is tokens [cu[i], cu[i+1]) with its own
 // chunk length; tpc is the largest sample's tile count).
+//
+// Rank-local form (rank >= 0, uniform batch only): the call is the share of
+// one rank of a CP group spread over several GPUs. The query side (q, o,
+// lse, dO, dq) then holds only that rank's two chunks, 2c rows per batch
+// element: chunk `rank` at local rows [0, c), chunk 2cp-1-rank at [c, 2c).
+// The key/value side holds rank-major shards laid out the same way: rank j's
+// shard of batch element bi starts at row j * kv_rank_rows + bi * 2c
+// (kv_rank_rows = b * 2c after an all-gather of every rank's shard; 0 when
+// the buffer holds the one shard a ring step received).
 struct CpGeom {
   int b, s, hq, hkv, cp, causal;
   int c;       // chunk length (uniform batch)
   int tpc;     // tiles per chunk (the largest sample's when packed)
   int npairs;  // query-head pairs per batch element: ceil(hq / 2)
   int nseq = 0;
+  int rank = -1;         // rank-local form: the rank whose queries the call computes
+  int kv_rank_rows = 0;  // rank-local form: rows between consecutive ranks' K/V shards
   int cu[kMaxSeqs + 1];     // packed: sample offsets
   int tile0[kMaxSeqs + 1];  // packed: query tiles (2cp * tpc_i) of the samples before sample i
 };
+
+// Rows of one sequence on the query side: the whole sequence, or one rank's
+// two chunks in the rank-local form.
+__host__ __device__ inline int q_seq_rows(const CpGeom& g) { return g.rank >= 0 ? 2 * g.c : g.s; }
+
+// First row of global chunk `chunk` (chunk length c) relative to its
+// sequence's first row, on the query side and on the key/value side.
+__host__ __device__ inline int q_chunk_row(const CpGeom& g, int chunk, int c) {
+  return g.rank >= 0 ? (chunk < g.cp ? 0 : c) : chunk * c;
+}
+__host__ __device__ inline int kv_chunk_row(const CpGeom& g, int chunk, int c) {
+  if (g.rank < 0) return chunk * c;
+  const int owner = chunk < g.cp ? chunk : 2 * g.cp - 1 - chunk;  // the rank holding the chunk
+  return owner * g.kv_rank_rows + (chunk < g.cp ? 0 : c);
+}
+
+// Tile (chunk, tile) of a sequence in the backward's tile-padded row
+// vectors: all 2cp*tpc tiles, or the rank's own 2*tpc in the rank-local form.
+__host__ __device__ inline int ld_tile(const CpGeom& g, int chunk, int tile, int tpc) {
+  return (g.rank >= 0 ? (chunk < g.cp ? 0 : tpc) : chunk * tpc) + tile;
+}
 
 // Packed geometry from the sample offsets (cu[0..nseq] set): the largest
 // sample's tiles per chunk and the tile prefix sums.
@@ -81,7 +113,7 @@ __host__ __device__ inline int num_seqs(const CpGeom& g) { return g.nseq > 0 ? g
 __host__ __device__ inline SeqGeom seq_geom(const CpGeom& g, int i) {
   SeqGeom q;
   if (g.nseq == 0) {
-    q.tok0 = i * g.s;
+    q.tok0 = i * q_seq_rows(g);
     q.c = g.c;
     q.tpc = g.tpc;
   } else {
@@ -104,17 +136,33 @@ struct FwdUnit {
   int k;         // global chunk index of the query tile
   int u;         // tile index within the chunk
   int r, half;   // owning virtual rank and which of its two chunks
-  int q_t0;      // first token of the query tile (within the sequence)
+  int q_t0;      // first row of the query tile relative to its sequence's first row
+                 // (its position in the sequence; its local position in the rank-local form)
   int q_valid;   // rows of the tile inside the chunk
   int n;         // number of key tiles the unit visits (0: no such tile in a shorter packed sample)
 };
 
-// Units per head group of a call: every sequence's query (or key) tiles.
+// Units per head group of a call: every sequence's key tiles, and its
+// query tiles (only the rank's own in the rank-local form).
 __host__ __device__ inline int all_tiles(const CpGeom& g) {
   return g.nseq > 0 ? g.tile0[g.nseq] : g.b * 2 * g.cp * g.tpc;
 }
+__host__ __device__ inline int query_tiles(const CpGeom& g) {
+  return g.rank >= 0 ? g.b * 2 * g.tpc : all_tiles(g);
+}
 
-__host__ __device__ inline int fwd_num_units(const CpGeom& g) { return g.npairs * all_tiles(g); }
+// Global tile index of the query tile of local position lt (the unit order
+// below walks it from the end): every tile of the sequence, or in the
+// rank-local form the rank's tiles, chunk `rank` first.
+__host__ __device__ inline int query_tile_of(const CpGeom& g, int lt) {
+  if (g.rank < 0) return lt;
+  return (lt < g.tpc ? g.rank : 2 * g.cp - 1 - g.rank) * g.tpc + lt % g.tpc;
+}
+__host__ __device__ inline int query_tiles_per_seq(const CpGeom& g) {
+  return g.rank >= 0 ? 2 * g.tpc : 2 * g.cp * g.tpc;
+}
+
+__host__ __device__ inline int fwd_num_units(const CpGeom& g) { return g.npairs * query_tiles(g); }
 
 // The query tile with global tile index gt of unit U's sequence (U.seq set).
 __host__ __device__ inline void fill_query_tile(const CpGeom& g, FwdUnit& U, int gt) {
@@ -133,7 +181,7 @@ __host__ __device__ inline void fill_query_tile(const CpGeom& g, FwdUnit& U, int
   U.u = gt % U.tpc;
   U.half = U.k >= g.cp ? 1 : 0;
   U.r = U.half ? 2 * g.cp - 1 - U.k : U.k;
-  U.q_t0 = U.k * U.c + U.u * kTile;
+  U.q_t0 = q_chunk_row(g, U.k, U.c) + U.u * kTile;
   const int rem = U.c - U.u * kTile;
   U.q_valid = rem < kTile ? rem : kTile;
   if (g.causal)
@@ -156,7 +204,7 @@ __host__ __device__ inline FwdUnit fwd_decode_unit(const CpGeom& g, int idx) {
     pr = idx % g.npairs;
   } else {
     const int per = g.b * g.npairs;
-    gt = (2 * g.cp * g.tpc - 1) - idx / per;
+    gt = query_tile_of(g, query_tiles_per_seq(g) - 1 - idx / per);
     const int rest = idx % per;
     U.seq = rest / g.npairs;
     pr = rest % g.npairs;
@@ -174,7 +222,7 @@ __host__ __device__ inline FwdUnit fwd_decode_unit(const CpGeom& g, int idx) {
 // dQ work units: one 128-row query tile of one head, longest first: the
 // forward's decomposition with one head per unit (h0 == h1), so the
 // forward's CP-step key walk (KvWalk) applies as is.
-__host__ __device__ inline int dq_num_units(const CpGeom& g) { return g.hq * all_tiles(g); }
+__host__ __device__ inline int dq_num_units(const CpGeom& g) { return g.hq * query_tiles(g); }
 
 __host__ __device__ inline FwdUnit dq_decode_unit(const CpGeom& g, int idx) {
   FwdUnit U;
@@ -186,7 +234,7 @@ __host__ __device__ inline FwdUnit dq_decode_unit(const CpGeom& g, int idx) {
     U.h0 = U.h1 = idx % g.hq;
   } else {
     const int per = g.b * g.hq;
-    gt = (2 * g.cp * g.tpc - 1) - idx / per;
+    gt = query_tile_of(g, query_tiles_per_seq(g) - 1 - idx / per);
     const int rest = idx % per;
     U.seq = rest / g.hq;
     U.h0 = U.h1 = rest % g.hq;
@@ -313,7 +361,10 @@ struct KvWalk {
 // then starts at the same query tiles and moves down at the same pace, so
 // the dQ rows being accumulated (and the Q/dO tiles being read) are shared
 // by the CTAs in flight and stay in L2. dK/dV of the tile accumulate on chip
-// over all its blocks.
+// over all its blocks. In the rank-local form the units are still every key
+// tile of the sequence, but only the rank's own query tiles are visited: the
+// result is the rank's share of every key tile's dK/dV (zero for a tile no
+// query of the rank sees).
 struct BwdUnit {
   int bi, g;      // batch element (0 for packed samples), KV head
   int seq;        // batch element or packed sample
@@ -321,11 +372,17 @@ struct BwdUnit {
   int c, tpc;     // its chunk length and tiles per chunk
   int kc, v;      // key chunk and tile within it
   int gt;         // global tile index of the key tile: kc * tpc + v
-  int k_t0;       // first key token
-  int k_valid;    // keys of the tile inside the chunk
-  int nq;         // number of query tiles that see the tile
-  int items;      // nq * (hq / hkv); 0 for a tile a shorter packed sample does not have
+  int k_t0;       // first row of the key tile relative to its sequence's first row
+  int k_valid;    // keys of the tile inside the chunk (0 for a tile a shorter packed sample does not have)
+  int nq;         // number of query tiles that see the tile (the rank's own in the rank-local form)
+  int items;      // nq * (hq / hkv); 0 when no query sees the tile
 };
+
+// Query tiles of chunk `chunk` at or after global tile gt (tpc per chunk).
+__host__ __device__ inline int tiles_from(int chunk, int tpc, int gt) {
+  const int n = (chunk + 1) * tpc - gt;
+  return n < 0 ? 0 : (n > tpc ? tpc : n);
+}
 
 __host__ __device__ inline int bwd_num_units(const CpGeom& g) { return g.hkv * all_tiles(g); }
 
@@ -357,27 +414,35 @@ __host__ __device__ inline BwdUnit bwd_decode_unit(const CpGeom& g, int idx) {
   }
   U.kc = gt / U.tpc;
   U.v = gt % U.tpc;
-  U.k_t0 = U.kc * U.c + U.v * kTile;
+  U.k_t0 = kv_chunk_row(g, U.kc, U.c) + U.v * kTile;
   const int rem = U.c - U.v * kTile;
   U.k_valid = rem < kTile ? rem : kTile;
-  U.nq = g.causal ? ntile - gt : ntile;
+  if (g.rank >= 0)
+    U.nq = g.causal ? tiles_from(g.rank, U.tpc, gt) + tiles_from(2 * g.cp - 1 - g.rank, U.tpc, gt) : 2 * U.tpc;
+  else
+    U.nq = g.causal ? ntile - gt : ntile;
   U.items = U.nq * (g.hq / g.hkv);
   return U;
 }
 
-// Walks the query tiles of a backward unit, last tile first.
+// Walks the query tiles of a backward unit, last tile first (in the
+// rank-local form only the rank's own tiles: chunk 2cp-1-rank, then chunk
+// rank, each from its end).
 struct QWalk {
-  int tpc, lo, gt_k, causal, gt;
+  int tpc, lo, gt_k, causal, cp, rank, lt;
 
   __host__ __device__ QWalk(const CpGeom& g, const BwdUnit& U)
-      : tpc(U.tpc), lo(g.causal ? U.gt : 0), gt_k(U.gt), causal(g.causal), gt(2 * g.cp * U.tpc - 1) {}
+      : tpc(U.tpc), lo(g.causal ? U.gt : 0), gt_k(U.gt), causal(g.causal), cp(g.cp), rank(g.rank),
+        lt(g.rank >= 0 ? 2 * U.tpc - 1 : 2 * g.cp * U.tpc - 1) {}
 
   __host__ __device__ bool next(int& chunk, int& tile, bool& is_diag) {
-    if (gt < lo) return false;
+    if (lt < 0) return false;
+    const int gt = rank >= 0 ? (lt < tpc ? rank : 2 * cp - 1 - rank) * tpc + lt % tpc : lt;
+    if (gt < lo) return false;  // tiles come in decreasing global order
     chunk = gt / tpc;
     tile = gt % tpc;
     is_diag = causal && gt == gt_k;
-    --gt;
+    --lt;
     return true;
   }
 };

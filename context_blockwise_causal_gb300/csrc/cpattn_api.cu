@@ -140,8 +140,12 @@ double default_scale(int d) { return 1.0 / std::sqrt(double(d)); }
 }  // namespace
 
 namespace {
+// The fused forward. `geom` overrides the uniform geometry (packed samples,
+// or the rank-local form); the query-side tensors then have q_rows rows and
+// the key/value side kv_rows (both b * s by default).
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int b, int s, int hq, int hkv, int d,
-             int cp, int causal, double scale, void* stream, int64_t lse_stride = -1, const CpGeom* packed = nullptr) {
+             int cp, int causal, double scale, void* stream, int64_t lse_stride = -1, const CpGeom* geom = nullptr,
+             uint64_t q_rows = 0, uint64_t kv_rows = 0) {
   if (!q || !k || !v || !o || !lse) return CPATTN_ERR_NULL_PTR;
   int rc = check_geometry(b, s, hq, hkv, d, cp);
   if (rc) return rc;
@@ -150,12 +154,14 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   DeviceInfo* di = nullptr;
   if ((rc = device_info(&di))) return rc;
   CUtensorMap tq, tk, tv;
-  const uint64_t rows = uint64_t(b) * s;
-  if (!encode_bf16_rows_heads_d(&tq, q, rows, hq, d, kTile) || !encode_bf16_rows_heads_d(&tk, k, rows, hkv, d, kTile) ||
-      !encode_bf16_rows_heads_d(&tv, v, rows, hkv, d, kTile))
+  if (q_rows == 0) q_rows = uint64_t(b) * s;
+  if (kv_rows == 0) kv_rows = uint64_t(b) * s;
+  if (!encode_bf16_rows_heads_d(&tq, q, q_rows, hq, d, kTile) ||
+      !encode_bf16_rows_heads_d(&tk, k, kv_rows, hkv, d, kTile) ||
+      !encode_bf16_rows_heads_d(&tv, v, kv_rows, hkv, d, kTile))
     return CPATTN_ERR_CUDA;
   FwdArgs args;
-  args.g = packed ? *packed : make_geom(b, s, hq, hkv, cp, causal);
+  args.g = geom ? *geom : make_geom(b, s, hq, hkv, cp, causal);
   args.o = static_cast<__nv_bfloat16*>(o);
   args.lse = lse;
   args.lse_stride = lse_stride < 0 ? s : lse_stride;
@@ -181,8 +187,12 @@ extern "C" int cpattn_fwd(const void* q, const void* k, const void* v, void* o, 
   return fwd_impl(q, k, v, o, lse, b, s, hq, hkv, d, cp, causal, default_scale(d), stream);
 }
 
-extern "C" int cpattn_fwd_step(const void* q, const void* k, const void* v, float* o_part, float* lse_part, int b,
-                               int s, int hq, int hkv, int d, int cp, int step, int causal, void* stream) {
+namespace {
+// One CP step, unmerged (the step form of the forward kernel); geometry and
+// row counts as for fwd_impl.
+int step_impl(const void* q, const void* k, const void* v, float* o_part, float* lse_part, int b, int s, int hq,
+              int hkv, int d, int cp, int step, int causal, double scale, void* stream, const CpGeom* geom = nullptr,
+              uint64_t q_rows = 0, uint64_t kv_rows = 0, int64_t lse_stride = -1) {
   if (!q || !k || !v || !o_part || !lse_part) return CPATTN_ERR_NULL_PTR;
   int rc = check_geometry(b, s, hq, hkv, d, cp);
   if (rc) return rc;
@@ -192,21 +202,29 @@ extern "C" int cpattn_fwd_step(const void* q, const void* k, const void* v, floa
   DeviceInfo* di = nullptr;
   if ((rc = device_info(&di))) return rc;
   CUtensorMap tq, tk, tv;
-  const uint64_t rows = uint64_t(b) * s;
-  if (!encode_bf16_rows_heads_d(&tq, q, rows, hq, d, kTile) || !encode_bf16_rows_heads_d(&tk, k, rows, hkv, d, kTile) ||
-      !encode_bf16_rows_heads_d(&tv, v, rows, hkv, d, kTile))
+  if (q_rows == 0) q_rows = uint64_t(b) * s;
+  if (kv_rows == 0) kv_rows = uint64_t(b) * s;
+  if (!encode_bf16_rows_heads_d(&tq, q, q_rows, hq, d, kTile) ||
+      !encode_bf16_rows_heads_d(&tk, k, kv_rows, hkv, d, kTile) ||
+      !encode_bf16_rows_heads_d(&tv, v, kv_rows, hkv, d, kTile))
     return CPATTN_ERR_CUDA;
   FwdArgs args;
-  args.g = make_geom(b, s, hq, hkv, cp, causal);
+  args.g = geom ? *geom : make_geom(b, s, hq, hkv, cp, causal);
   args.o = nullptr;
   args.lse = lse_part;
-  args.lse_stride = s;
+  args.lse_stride = lse_stride < 0 ? s : lse_stride;
   args.o_part = o_part;
   args.step = step;
-  args.scale_log2 = float(1.4426950408889634 / std::sqrt(double(d)));
+  args.scale_log2 = float(1.4426950408889634 * scale);
   args.status = di->status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return d == 128 ? launch_fwd<128, true>(tq, tk, tv, args, di, st) : launch_fwd<64, true>(tq, tk, tv, args, di, st);
+}
+}  // namespace
+
+extern "C" int cpattn_fwd_step(const void* q, const void* k, const void* v, float* o_part, float* lse_part, int b,
+                               int s, int hq, int hkv, int d, int cp, int step, int causal, void* stream) {
+  return step_impl(q, k, v, o_part, lse_part, b, s, hq, hkv, d, cp, step, causal, default_scale(d), stream);
 }
 
 extern "C" int cpattn_lse_merge(const float* o_a, const float* lse_a, const float* o_b, const float* lse_b,
@@ -379,7 +397,7 @@ int launch_bwd_stage(int stage, const CUtensorMap& tq, const CUtensorMap& tk, co
     di->bwd_attr[slot].store(true, std::memory_order_release);
   }
   if (stage == 0) {
-    const int64_t rows = int64_t(args.g.b) * args.g.s * args.g.hq;
+    const int64_t rows = int64_t(args.g.b) * q_seq_rows(args.g) * args.g.hq;
     int pre_grid = int((rows + 255) / 256);
     if (pre_grid > di->num_sms * 16) pre_grid = di->num_sms * 16;
     cpattn_bwd_pre_kernel<D><<<pre_grid, 256, 0, st>>>(args);
@@ -420,7 +438,7 @@ namespace {
 int prepare_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int b, int s, int hq, int hkv,
                 int d, int cp, int causal, double scale, CUtensorMap* maps, BwdArgs* args, DeviceInfo** di,
-                int64_t lse_stride = -1, const CpGeom* packed = nullptr) {
+                int64_t lse_stride = -1, const CpGeom* packed = nullptr, const CpGeom* ranked = nullptr) {
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return CPATTN_ERR_NULL_PTR;
   int rc = check_geometry(b, s, hq, hkv, d, cp);
   if (rc) return rc;
@@ -428,17 +446,23 @@ int prepare_bwd(const void* q, const void* k, const void* v, const void* o, cons
                         static_cast<const void*>(dv), static_cast<const void*>(workspace)})
     if (!aligned16(p)) return CPATTN_ERR_MISALIGNED;
   if (reinterpret_cast<uintptr_t>(lse) & 3u) return CPATTN_ERR_MISALIGNED;
-  const BwdLayout L = packed ? bwd_layout_tiles(packed->nseq, packed->tpc, hq, cp) : bwd_layout(b, s, hq, d, cp);
+  // rank-local form: the row vectors hold the rank's 2*tpc tiles per (batch, head)
+  const BwdLayout L = packed   ? bwd_layout_tiles(packed->nseq, packed->tpc, hq, cp)
+                      : ranked ? bwd_layout_tiles(b, ranked->tpc, hq, 1)
+                               : bwd_layout(b, s, hq, d, cp);
   if (workspace_bytes < L.total) return CPATTN_ERR_WORKSPACE_TOO_SMALL;
   if ((rc = device_info(di))) return rc;
-  const uint64_t rows = uint64_t(b) * s;
-  if (!encode_bf16_rows_heads_d(&maps[0], q, rows, hq, d, kTile) ||
-      !encode_bf16_rows_heads_d(&maps[1], k, rows, hkv, d, kTile) ||
-      !encode_bf16_rows_heads_d(&maps[2], v, rows, hkv, d, kTile) ||
-      !encode_bf16_rows_heads_d(&maps[3], dout, rows, hq, d, kTile))
+  // rows of the query-side tensors (q, o, dout, dq) and of the key/value side
+  // (a rank-local call's gathered K/V shards hold cp * b * 2c = b * s rows too)
+  const uint64_t q_rows = ranked ? uint64_t(b) * 2 * ranked->c : uint64_t(b) * s;
+  const uint64_t kv_rows = uint64_t(b) * s;
+  if (!encode_bf16_rows_heads_d(&maps[0], q, q_rows, hq, d, kTile) ||
+      !encode_bf16_rows_heads_d(&maps[1], k, kv_rows, hkv, d, kTile) ||
+      !encode_bf16_rows_heads_d(&maps[2], v, kv_rows, hkv, d, kTile) ||
+      !encode_bf16_rows_heads_d(&maps[3], dout, q_rows, hq, d, kTile))
     return CPATTN_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  args->g = packed ? *packed : make_geom(b, s, hq, hkv, cp, causal);
+  args->g = packed ? *packed : ranked ? *ranked : make_geom(b, s, hq, hkv, cp, causal);
   args->ntp = L.ntp;
   args->o = static_cast<const __nv_bfloat16*>(o);
   args->dout = static_cast<const __nv_bfloat16*>(dout);
@@ -461,12 +485,13 @@ int prepare_bwd(const void* q, const void* k, const void* v, const void* o, cons
 namespace {
 int bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout, void* dq,
              void* dk, void* dv, void* workspace, size_t workspace_bytes, int b, int s, int hq, int hkv, int d, int cp,
-             int causal, double scale, void* stream, int64_t lse_stride = -1, const CpGeom* packed = nullptr) {
+             int causal, double scale, void* stream, int64_t lse_stride = -1, const CpGeom* packed = nullptr,
+             const CpGeom* ranked = nullptr) {
   CUtensorMap maps[4];
   BwdArgs args;
   DeviceInfo* di = nullptr;
   const int rc = prepare_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, b, s, hq, hkv, d, cp,
-                             causal, double(scale), maps, &args, &di, lse_stride, packed);
+                             causal, double(scale), maps, &args, &di, lse_stride, packed, ranked);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return d == 128 ? launch_bwd<128>(maps[0], maps[1], maps[2], maps[3], args, di, st)
@@ -599,6 +624,72 @@ extern "C" int cpattn_bwd_varlen(const void* q, const void* k, const void* v, co
     if (rc) return rc;
   }
   return CPATTN_OK;
+}
+
+// ---------------------------------------------------------------- rank-local form
+namespace {
+// Geometry of one rank's share of a multi-GPU CP group (see CpGeom).
+int rank_geom(int b, int s, int hq, int hkv, int d, int cp, int rank, int causal, int kv_rank_rows, CpGeom* g) {
+  const int rc = check_geometry(b, s, hq, hkv, d, cp);
+  if (rc) return rc;
+  if (rank < 0 || rank >= cp) return CPATTN_ERR_INVALID_ARG;
+  *g = make_geom(b, s, hq, hkv, cp, causal);
+  g->rank = rank;
+  g->kv_rank_rows = kv_rank_rows;
+  return CPATTN_OK;
+}
+
+int rank_scale(float scale, int d, double* out) {
+  if (!(scale == 0.f || valid_scale(scale))) return CPATTN_ERR_INVALID_ARG;
+  *out = scale == 0.f ? default_scale(d) : double(scale);
+  return CPATTN_OK;
+}
+}  // namespace
+
+extern "C" int cpattn_fwd_rank(const void* q, const void* k, const void* v, void* o, float* lse, int b, int s, int hq,
+                               int hkv, int d, int cp, int rank, int causal, float scale, void* stream) {
+  CpGeom g;
+  double sc = 0.0;
+  int rc = rank_scale(scale, d, &sc);
+  if (rc) return rc;
+  if ((rc = rank_geom(b, s, hq, hkv, d, cp, rank, causal, b * (s / cp), &g))) return rc;
+  if (lse && !aligned16(lse)) return CPATTN_ERR_MISALIGNED;
+  const int local = s / cp;  // 2c rows per batch element on the query side
+  return fwd_impl(q, k, v, o, lse, b, s, hq, hkv, d, cp, causal, sc, stream, local, &g, uint64_t(b) * local,
+                  uint64_t(b) * s);
+}
+
+extern "C" int cpattn_fwd_rank_step(const void* q, const void* k, const void* v, float* o_part, float* lse_part,
+                                    int b, int s, int hq, int hkv, int d, int cp, int rank, int step, int causal,
+                                    float scale, void* stream) {
+  CpGeom g;
+  double sc = 0.0;
+  int rc = rank_scale(scale, d, &sc);
+  if (rc) return rc;
+  if ((rc = rank_geom(b, s, hq, hkv, d, cp, rank, causal, 0, &g))) return rc;
+  const int local = s / cp;
+  return step_impl(q, k, v, o_part, lse_part, b, s, hq, hkv, d, cp, step, causal, sc, stream, &g,
+                   uint64_t(b) * local, uint64_t(b) * local, local);
+}
+
+extern "C" size_t cpattn_bwd_rank_workspace_bytes(int b, int s, int hq, int hkv, int d, int cp) {
+  if (check_geometry(b, s, hq, hkv, d, cp)) return 0;
+  const int c = s / (2 * cp);
+  return bwd_layout_tiles(b, (c + kTile - 1) / kTile, hq, 1).total;
+}
+
+extern "C" int cpattn_bwd_rank(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                               const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                               size_t workspace_bytes, int b, int s, int hq, int hkv, int d, int cp, int rank,
+                               int causal, float scale, void* stream) {
+  CpGeom g;
+  double sc = 0.0;
+  int rc = rank_scale(scale, d, &sc);
+  if (rc) return rc;
+  if ((rc = rank_geom(b, s, hq, hkv, d, cp, rank, causal, b * (s / cp), &g))) return rc;
+  if (lse && !aligned16(lse)) return CPATTN_ERR_MISALIGNED;
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, b, s, hq, hkv, d, cp, causal, sc,
+                  stream, s / cp, nullptr, &g);
 }
 
 extern "C" int cpattn_bwd_stage(int stage, const void* q, const void* k, const void* v, const void* o,

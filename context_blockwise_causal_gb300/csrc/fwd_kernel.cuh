@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           return true;
         };
         while (ok && w.next(chunk, tile, dg)) {
-          const int row = U.tok0 + chunk * U.c + tile * kTile;
+          const int row = U.tok0 + kv_chunk_row(g, chunk, U.c) + tile * kTile;
           ok = load(&tmk, U.g0, row) && (shared_kv || load(&tmk, U.g1, row)) && load(&tmv, U.g0, row) &&
                (shared_kv || load(&tmv, U.g1, row));
         }

@@ -269,6 +269,62 @@ int cpattn_bwd_noalloc(const void* q, const void* k, const void* v, const void* 
 size_t cpattn_bwd_noalloc_max_scratch_bytes(void);
 
 /*
+ * ---- Rank-local form: one rank's share of a CP group spread over GPUs ----
+ *
+ * The pages run each CP rank on its own device: rank r holds its zigzag
+ * shard of q, k, v (chunks r and 2cp-1-r, c = s/(2cp) tokens each), and the
+ * ranks exchange K/V either around a ring, one neighbour per step, with the
+ * step's attention computed while the next K/V is in flight ("大模型面试宝典 ·
+ * Megatron-LM 篇", 3.1 point 2 and 3.2 steps 2-5), or by an all-gather of K/V
+ * in the forward and an all-gather of K/V plus a reduce-scatter of dK/dV in
+ * the backward ("超大规模集群下大语言模型训练实操指南", section "超长文本场景
+ * 解决方案"). These calls are the device work of one such rank; the exchange
+ * itself (NCCL) is the caller's. Each launches on the local GPU only and
+ * reads local buffers: nothing here touches another device's memory.
+ *
+ * Layouts (b batch elements; 2c = s/cp rows per element in a shard):
+ *   q, o, dout, dq:  this rank's shard [b, 2c, hq, d] bf16, local rows
+ *                    [0, c) = chunk `rank`, [c, 2c) = chunk 2cp-1-rank;
+ *   lse:             [b, hq, 2c] fp32, natural log, same local rows;
+ *   k_all, v_all:    every rank's shard, rank-major [cp, b, 2c, hkv, d] bf16
+ *                    (what an all-gather of the shards along a new leading
+ *                    dimension gives);
+ *   k_blk, v_blk:    one rank's shard [b, 2c, hkv, d] bf16 (what a ring step
+ *                    receives);
+ *   dk_part, dv_part: [cp, b, 2c, hkv, d] bf16 like k_all: this rank's share
+ *                    of every shard's dK/dV; summing them over the ranks (a
+ *                    reduce-scatter) gives each rank its shard's dK/dV.
+ * s is the full sequence length (s divisible by 2cp); 0 <= rank < cp;
+ * scale 0 selects 1/sqrt(d), otherwise any positive finite value. Other
+ * limits, pointers and errors as cpattn_fwd / cpattn_bwd; rank outside
+ * [0, cp) -> CPATTN_ERR_INVALID_ARG.
+ */
+
+/* Every CP step of rank `rank` in one launch, merged on chip: o and lse of
+ * the rank's shard, equal to those rows of cpattn_fwd's result. */
+int cpattn_fwd_rank(const void* q, const void* k_all, const void* v_all, void* o, float* lse, int b, int s, int hq,
+                    int hkv, int d, int cp, int rank, int causal, float scale, void* stream);
+
+/* CP step `step` of rank `rank` against the shard of rank (rank - step) mod
+ * cp, unmerged (3.2 steps 2 and 4): o_part [b, 2c, hq, d] fp32 and lse_part
+ * [b, hq, 2c] as cpattn_fwd_step's, rows outside the step 0 / -inf. Merging a
+ * rank's cp step results with cpattn_lse_merge (shapes [b, 2c, hq, d]) gives
+ * cpattn_fwd_rank's result. step outside [0, cp) -> CPATTN_ERR_INVALID_ARG. */
+int cpattn_fwd_rank_step(const void* q, const void* k_blk, const void* v_blk, float* o_part, float* lse_part, int b,
+                         int s, int hq, int hkv, int d, int cp, int rank, int step, int causal, float scale,
+                         void* stream);
+
+/* Workspace bytes of cpattn_bwd_rank (0 for an unsupported shape). */
+size_t cpattn_bwd_rank_workspace_bytes(int b, int s, int hq, int hkv, int d, int cp);
+
+/* The backward of rank `rank` from its saved o and lse: dq of its shard, and
+ * its share dk_part, dv_part of every shard's dK/dV (a key tile no query of
+ * the rank sees gets zeros). Deterministic, like cpattn_bwd. */
+int cpattn_bwd_rank(const void* q, const void* k_all, const void* v_all, const void* o, const float* lse,
+                    const void* dout, void* dq, void* dk_part, void* dv_part, void* workspace, size_t workspace_bytes,
+                    int b, int s, int hq, int hkv, int d, int cp, int rank, int causal, float scale, void* stream);
+
+/*
  * Host helper: the zigzag index map. Fills global_of_local (HOST memory,
  * cp * 2c int64 values, row-major [cp][2c]) with the global token position
  * of virtual rank r's local position u: chunk r then chunk 2cp-1-r, each in

@@ -7,8 +7,13 @@
 //     (key-tile) units, every (head, query, key) pair the mask allows is
 //     computed exactly once and no other pair is -- in particular no pair
 //     crosses a packed-sample boundary.
-// Geometries: "U b s hq hkv cp causal grid" (a uniform batch) or
-// "P nseq len_1 .. len_nseq hq hkv cp causal grid" (packed samples).
+// Geometries: "U b s hq hkv cp causal grid" (a uniform batch),
+// "P nseq len_1 .. len_nseq hq hkv cp causal grid" (packed samples), or
+// "R b s hq hkv cp causal grid" (the rank-local form: every rank's call,
+// with its rows mapped back to the sequence, must together cover each pair
+// exactly once -- for the all-gather form, for the ring form step by step,
+// and for the backward's key-tile units -- and every row a call addresses
+// must lie inside its buffer).
 // Prints "ok" per geometry or the first violation, exit code 1 on failure.
 #include <cstdio>
 #include <cstdlib>
@@ -68,10 +73,37 @@ static int mark(std::vector<unsigned char>& count, const Rows& R, int h, int qa,
   return 0;
 }
 
+// Rank-local form: the sequence row (b*s layout) of a row of the rank's
+// query shard [b, 2c], and of a row of the key/value buffer -- rank-major
+// shards (kv_rank_rows = b*2c), or the one shard of rank `owner` (0).
+static int rank_q_row(const CpGeom& g, int row) {
+  const int local = 2 * g.c, bi = row / local, u = row % local;
+  return bi * g.s + (u < g.c ? g.rank * g.c + u : (2 * g.cp - 1 - g.rank) * g.c + (u - g.c));
+}
+static int rank_kv_row(const CpGeom& g, int row, int owner) {
+  const int local = 2 * g.c;
+  int rest = row;
+  if (g.kv_rank_rows > 0) {
+    owner = row / g.kv_rank_rows;
+    rest = row % g.kv_rank_rows;
+  }
+  const int bi = rest / local, u = rest % local;
+  return bi * g.s + (u < g.c ? owner * g.c + u : (2 * g.cp - 1 - owner) * g.c + (u - g.c));
+}
+
+// Buffer rows -> sequence rows, and the buffers' row counts.
+struct RowMap {
+  int q_rows, kv_rows;  // rows of the query-side and key/value buffers
+  int owner;            // ring step form: the rank whose shard the K/V buffer holds
+  int q(const CpGeom& g, int r) const { return g.rank >= 0 ? rank_q_row(g, r) : r; }
+  int kv(const CpGeom& g, int r) const { return g.rank >= 0 ? rank_kv_row(g, r, owner) : r; }
+};
+
+static RowMap natural_map(const CpGeom& g) { return RowMap{g.b * g.s, g.b * g.s, -1}; }
+
 // Walk one query-tile unit (forward sub-tile or dQ unit) and mark its pairs.
 static int walk_query_unit(const CpGeom& g, const Rows& R, const FwdUnit& U, int h, std::vector<unsigned char>& count,
-                           const char* what) {
-  KvWalk w(g, U);
+                           const char* what, KvWalk w, const RowMap& M) {
   int chunk, tile, nt = 0;
   bool dg;
   while (w.next(chunk, tile, dg)) {
@@ -81,11 +113,19 @@ static int walk_query_unit(const CpGeom& g, const Rows& R, const FwdUnit& U, int
     for (int row = 0; row < U.q_valid; ++row)
       for (int col = 0; col < nv; ++col) {
         if (dg && col > row) continue;
-        const int qa = U.tok0 + U.q_t0 + row, ka = U.tok0 + chunk * U.c + tile * kTile + col;
-        if (mark(count, R, h, qa, ka, what)) return -1;
+        const int qb = U.tok0 + U.q_t0 + row, kb = U.tok0 + kv_chunk_row(g, chunk, U.c) + tile * kTile + col;
+        if (qb < 0 || qb >= M.q_rows || kb < 0 || kb >= M.kv_rows) {
+          printf("%s: row outside its buffer (query %d of %d, key %d of %d)\n", what, qb, M.q_rows, kb, M.kv_rows);
+          return -1;
+        }
+        if (mark(count, R, h, M.q(g, qb), M.kv(g, kb), what)) return -1;
       }
   }
   return nt;
+}
+static int walk_query_unit(const CpGeom& g, const Rows& R, const FwdUnit& U, int h, std::vector<unsigned char>& count,
+                           const char* what) {
+  return walk_query_unit(g, R, U, h, count, what, KvWalk(g, U), natural_map(g));
 }
 
 static int check(const CpGeom& g, int grid) {
@@ -187,13 +227,103 @@ static int check(const CpGeom& g, int grid) {
   return verify(g, R, count, "backward");
 }
 
+// The rank-local form: each rank's forward (all-gather form and ring steps),
+// dQ and key-tile backward units, mapped back to sequence rows.
+static int check_rank(const CpGeom& base, int grid) {
+  const Rows R = rows_of(base);
+  const size_t T = R.total;
+  std::vector<unsigned char> fwd(size_t(base.hq) * T * T, 0), ring(fwd.size(), 0), dq(fwd.size(), 0),
+      bwd(fwd.size(), 0);
+  const int G = base.hq / base.hkv;
+  for (int r = 0; r < base.cp; ++r) {
+    CpGeom g = base;
+    g.rank = r;
+    g.kv_rank_rows = g.b * 2 * g.c;
+    const RowMap gathered{g.b * 2 * g.c, g.cp * g.b * 2 * g.c, -1};
+    // ---- forward units: snake assignment, longest first, the rank's tiles only
+    const int nu = fwd_num_units(g);
+    if (nu != g.npairs * g.b * 2 * g.tpc) { printf("rank %d: %d forward units\n", r, nu); return 1; }
+    std::vector<int> seen(nu, 0);
+    for (int bid = 0; bid < grid; ++bid)
+      for (int rd = 0;; ++rd) {
+        const int idx = snake_unit(rd, bid, grid);
+        if (idx >= nu) break;
+        seen[idx]++;
+      }
+    for (int i = 0; i < nu; ++i)
+      if (seen[i] != 1) { printf("rank %d: unit %d assigned %d times\n", r, i, seen[i]); return 1; }
+    int prev_n = 1 << 30;
+    for (int idx = 0; idx < nu; ++idx) {
+      const FwdUnit U = fwd_decode_unit(g, idx);
+      if (U.r != r) { printf("rank %d: unit %d belongs to rank %d\n", r, idx, U.r); return 1; }
+      if (g.causal && U.n > prev_n) { printf("rank %d: units not longest-first at %d\n", r, idx); return 1; }
+      prev_n = U.n;
+      for (int sub = 0; sub < 2; ++sub) {
+        if (sub == 1 && !U.store1) continue;
+        const int h = sub ? U.h1 : U.h0;
+        const int nt = walk_query_unit(g, R, U, h, fwd, "rank forward", KvWalk(g, U), gathered);
+        if (nt < 0) return 1;
+        if (nt != U.n) { printf("rank %d unit %d: walk has %d tiles, n = %d\n", r, idx, nt, U.n); return 1; }
+        // ring form: step st reads only the shard of rank (r - st) mod cp
+        CpGeom gs = g;
+        gs.kv_rank_rows = 0;
+        for (int st = 0; st < g.cp; ++st) {
+          const RowMap one{g.b * 2 * g.c, g.b * 2 * g.c, ((r - st) % g.cp + g.cp) % g.cp};
+          KvWalk w(gs, U);
+          w.only_step(st);
+          if (walk_query_unit(gs, R, U, h, ring, "rank ring step", w, one) < 0) return 1;
+        }
+      }
+    }
+    // ---- dQ units
+    const int nd = dq_num_units(g);
+    for (int idx = 0; idx < nd; ++idx) {
+      const FwdUnit U = dq_decode_unit(g, idx);
+      if (U.r != r) { printf("rank %d: dq unit %d belongs to rank %d\n", r, idx, U.r); return 1; }
+      const int nt = walk_query_unit(g, R, U, U.h0, dq, "rank dq", KvWalk(g, U), gathered);
+      if (nt < 0) return 1;
+      if (nt != U.n) { printf("rank %d dq unit %d: %d tiles, n = %d\n", r, idx, nt, U.n); return 1; }
+    }
+    // ---- backward: every key tile of the gathered shards, the rank's query tiles
+    const int nb = bwd_num_units(g);
+    int prev_items = 1 << 30;
+    for (int idx = 0; idx < nb; ++idx) {
+      const BwdUnit U = bwd_decode_unit(g, idx);
+      if (U.k_valid <= 0) { printf("rank %d: bwd unit %d is not a real key tile\n", r, idx); return 1; }
+      if (g.causal && U.items > prev_items) { printf("rank %d: bwd units not longest-first at %d\n", r, idx); return 1; }
+      prev_items = U.items;
+      QWalk w(g, U);
+      int chunk, tile, nt = 0;
+      bool dg;
+      while (w.next(chunk, tile, dg)) {
+        ++nt;
+        const int rem = U.c - tile * kTile;
+        const int qv = rem < kTile ? rem : kTile;
+        for (int h = U.g * G; h < (U.g + 1) * G; ++h)
+          for (int row = 0; row < qv; ++row)
+            for (int col = 0; col < U.k_valid; ++col) {
+              if (dg && col > row) continue;
+              const int qb = U.tok0 + q_chunk_row(g, chunk, U.c) + tile * kTile + row, kb = U.tok0 + U.k_t0 + col;
+              if (qb >= gathered.q_rows || kb >= gathered.kv_rows) { printf("rank bwd: row outside its buffer\n"); return 1; }
+              if (mark(bwd, R, h, gathered.q(g, qb), gathered.kv(g, kb), "rank bwd")) return 1;
+            }
+      }
+      if (nt != U.nq) { printf("rank %d bwd unit %d: walk has %d tiles, nq = %d\n", r, idx, nt, U.nq); return 1; }
+      if (U.items != nt * G) { printf("rank %d bwd unit %d: items mismatch\n", r, idx); return 1; }
+    }
+  }
+  return verify(base, R, fwd, "rank forward") || verify(base, R, ring, "rank ring steps") ||
+         verify(base, R, dq, "rank dq") || verify(base, R, bwd, "rank backward");
+}
+
 int main(int argc, char** argv) {
   int fails = 0, i = 1;
   while (i < argc) {
     CpGeom g;
     char desc[256];
     int grid;
-    if (!strcmp(argv[i], "U") && i + 7 < argc) {
+    const bool ranked = !strcmp(argv[i], "R");
+    if ((!strcmp(argv[i], "U") || ranked) && i + 7 < argc) {
       g.b = atoi(argv[i + 1]);
       g.s = atoi(argv[i + 2]);
       g.hq = atoi(argv[i + 3]);
@@ -204,8 +334,8 @@ int main(int argc, char** argv) {
       g.c = g.s / (2 * g.cp);
       g.tpc = (g.c + kTile - 1) / kTile;
       g.nseq = 0;
-      snprintf(desc, sizeof desc, "b=%d s=%d hq=%d hkv=%d cp=%d causal=%d grid=%d", g.b, g.s, g.hq, g.hkv, g.cp,
-               g.causal, grid);
+      snprintf(desc, sizeof desc, "%sb=%d s=%d hq=%d hkv=%d cp=%d causal=%d grid=%d", ranked ? "rank-local " : "",
+               g.b, g.s, g.hq, g.hkv, g.cp, g.causal, grid);
       i += 8;
     } else if (!strcmp(argv[i], "P") && i + 1 < argc) {
       const int n = atoi(argv[i + 1]);
@@ -228,7 +358,7 @@ int main(int argc, char** argv) {
       return 1;
     }
     g.npairs = (g.hq + 1) / 2;
-    const int rc = check(g, grid);
+    const int rc = ranked ? check_rank(g, grid) : check(g, grid);
     printf("%s %s\n", rc ? "FAIL" : "ok", desc);
     fails += rc;
   }

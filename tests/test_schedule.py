@@ -113,3 +113,16 @@ def test_random_packed_geometries(checker):
     out = subprocess.run([checker, *args], capture_output=True, text=True)
     assert out.returncode == 0, out.stdout + out.stderr
     assert out.stdout.count("ok") == n
+
+
+def test_rank_local_form_covers_every_pair_once(checker):
+    """One rank's share of a CP group over GPUs (the all-gather form, the ring
+    form step by step, and the backward over every key tile): over all ranks,
+    with local rows mapped back to the sequence, every allowed pair once and
+    every addressed row inside its buffer. Fixed geometries plus seeded random
+    ones."""
+    geoms = [g for g in GEOMS if g[4] <= 4] + _fuzz_geometries(16, seed=4242)
+    args = [str(x) for g in geoms for x in ("R", *g)]
+    out = subprocess.run([checker, *args], capture_output=True, text=True)
+    assert out.returncode == 0, out.stdout + out.stderr
+    assert out.stdout.count("ok") == len(geoms)

@@ -105,7 +105,7 @@ def library():
         lib.cpattn_fwd_rank_step.restype = _i
         lib.cpattn_bwd_rank_workspace_bytes.argtypes = [_i] * 6
         lib.cpattn_bwd_rank_workspace_bytes.restype = _sz
-        lib.cpattn_bwd_rank.argtypes = [_p] * 10 + [_sz] + [_i] * 9 + [ctypes.c_float, _p]
+        lib.cpattn_bwd_rank.argtypes = [_p] * 10 + [_sz] + [_i] * 8 + [ctypes.c_float, _p]
         lib.cpattn_bwd_rank.restype = _i
         lib.cpattn_zigzag_index.argtypes = [_i, _i, _p]
         lib.cpattn_zigzag_index.restype = _i

@@ -44,6 +44,28 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def _declared_arity():
+    """Number of parameters of every function the headers declare."""
+    out = {}
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        for name, params in re.findall(r"\b(cpattn_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", text):
+            params = params.strip()
+            out[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_argtypes_match_the_header(lib):
+    """Every function the binding declares to ctypes takes as many arguments
+    as the header says (a wrong count would shift every later argument)."""
+    arity = _declared_arity()
+    assert arity, "no declarations parsed"
+    for name, n in arity.items():
+        fn = getattr(lib, name)
+        if fn.argtypes is not None:
+            assert len(fn.argtypes) == n, (name, len(fn.argtypes), n)
+
+
 def test_zigzag_index_matches_oracle(lib):
     from context_blockwise_causal_gb300 import cpattn_zigzag_index
 

@@ -404,9 +404,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ++scnt;
         tc_fence_after();
         float s[kTile];
+        float hw_max;
         {
           uint32_t r0[32], r1[32], r2[32], r3[32];
-          tmem_ld32x4(tS, tS + 32, tS + 64, tS + 96, r0, r1, r2, r3);
+          float m4[4];
+          tmem_ld32x4_max(tS, tS + 32, tS + 64, tS + 96, r0, r1, r2, r3, m4);
+          hw_max = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             s[i] = __uint_as_float(r0[i]);
@@ -415,23 +418,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             s[96 + i] = __uint_as_float(r3[i]);
           }
         }
+        // row max: from the load itself, except on a masked tile (the diagonal
+        // or a ragged chunk end), where it is taken over the unmasked scores
+        float m_raw = hw_max;
         if (dg || n_valid < kTile) {
           const int lim = dg ? (row < n_valid - 1 ? row : n_valid - 1) : n_valid - 1;
 #pragma unroll
           for (int i = 0; i < kTile; ++i)
             if (i > lim) s[i] = -INFINITY;
-        }
-        // row max: eight independent chains of 3-input maxima, chain k over
-        // the scores k, k+8, ..., k+120
-        float mx[8];
+          // row max: eight independent chains of 3-input maxima, chain k over
+          // the scores k, k+8, ..., k+120
+          float mx[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          float m = fmax3(s[k], s[k + 8], s[k + 16]);
+          for (int k = 0; k < 8; ++k) {
+            float m = fmax3(s[k], s[k + 8], s[k + 16]);
 #pragma unroll
-          for (int i = 24; i + 8 < kTile; i += 16) m = fmax3(m, s[i + k], s[i + 8 + k]);
-          mx[k] = fmaxf(m, s[kTile - 8 + k]);
+            for (int i = 24; i + 8 < kTile; i += 16) m = fmax3(m, s[i + k], s[i + 8 + k]);
+            mx[k] = fmaxf(m, s[kTile - 8 + k]);
+          }
+          m_raw = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7])));
         }
-        const float m_new = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7]))) * sl2;
+        const float m_new = m_raw * sl2;
         const bool upd = m_new > m_used + kRescaleThreshold;
         float alpha = 1.f;
         if (upd) {
@@ -465,14 +472,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (hh == 0 && rescale) {
             // Rescale O before any P.V of this tile (the MMA warp waits for
             // p_half). This row's O accumulator is idle: P.V of step j-1
-            // completed before S(j) was signalled.
+            // completed before S(j) was signalled. The stores are not waited
+            // for one by one: the P store below waits for all of them before
+            // the fence and the p_half arrival publish the columns.
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
               uint32_t r[32];
               tmem_ld32(tO + c0, r);
 #pragma unroll
               for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-              tmem_st32(tO + c0, r);
+              tmem_st32_nowait(tO + c0, r);
             }
           }
           tmem_st32(tS + hh * 32, pk);

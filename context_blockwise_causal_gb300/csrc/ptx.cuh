@@ -276,6 +276,20 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 #undef CPATTN_W8
 
+// TMEM store of 32 columns without waiting for completion: a later
+// tcgen05.wait::st (before the fence that publishes the columns) covers it.
+__device__ __forceinline__ void tmem_st32_nowait(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+      "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+      "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -412,6 +426,29 @@ __device__ __forceinline__ void tmem_ld32x4(uint32_t ta, uint32_t tb, uint32_t t
 }
 #undef CPATTN_RX8
 
+
+
+// Four TMEM loads of 32 columns that also return the maximum of each load's
+// 32 values (tcgen05.ld.red with .max, new in sm_103a): the loaded row's
+// maximum comes with the load instead of from a chain of max instructions.
+#define CPATTN_RZ8(r, i) "=r"(r[i + 0]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
+                         "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
+__device__ __forceinline__ void tmem_ld32x4_max(uint32_t ta, uint32_t tb, uint32_t tc, uint32_t td, uint32_t (&ra)[32],
+                                                uint32_t (&rb)[32], uint32_t (&rc)[32], uint32_t (&rd)[32], float (&m)[4]) {
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %128, [%132];\n\t"
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, %129, [%133];\n\t"
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 {%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, %130, [%134];\n\t"
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 {%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, %131, [%135];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : CPATTN_RZ8(ra, 0), CPATTN_RZ8(ra, 8), CPATTN_RZ8(ra, 16), CPATTN_RZ8(ra, 24), CPATTN_RZ8(rb, 0),
+        CPATTN_RZ8(rb, 8), CPATTN_RZ8(rb, 16), CPATTN_RZ8(rb, 24), CPATTN_RZ8(rc, 0), CPATTN_RZ8(rc, 8),
+        CPATTN_RZ8(rc, 16), CPATTN_RZ8(rc, 24), CPATTN_RZ8(rd, 0), CPATTN_RZ8(rd, 8), CPATTN_RZ8(rd, 16),
+        CPATTN_RZ8(rd, 24), "=f"(m[0]), "=f"(m[1]), "=f"(m[2]), "=f"(m[3])
+      : "r"(ta), "r"(tb), "r"(tc), "r"(td)
+      : "memory");
+}
+#undef CPATTN_RZ8
 
 // Four TMEM stores of 16 columns (to four addresses) with a single wait.
 #define CPATTN_W4(r) "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])

@@ -7,7 +7,8 @@
 //
 // A forward work unit is one 128-row query tile of one chunk, for a pair of
 // query heads (two sub-tiles that walk the same key tiles), for one batch
-// element. Its key tiles are visited in the order of the rank's CP steps:
+// element -- or, when the head groups are odd (tile_pairs), two adjacent query
+// tiles of one head, so that the two sub-tiles still share their K/V tiles. Its key tiles are visited in the order of the rank's CP steps:
 //   step 0      : the rank's own chunks, causal (the one masked "diagonal"
 //                 tile is where the query tile meets its own chunk);
 //   1 <= i <= r : chunk j = r - i (first half of rank j's pair), unmasked;
@@ -49,6 +50,7 @@ struct CpGeom {
   int nseq = 0;
   int rank = -1;         // rank-local form: the rank whose queries the call computes
   int kv_rank_rows = 0;  // rank-local form: rows between consecutive ranks' K/V shards
+  int tile_pairs = 0;    // forward units pair two query tiles of one head (see fwd_decode_unit)
   int cu[kMaxSeqs + 1];     // packed: sample offsets
   int tile0[kMaxSeqs + 1];  // packed: query tiles (2cp * tpc_i) of the samples before sample i
 };
@@ -139,6 +141,10 @@ struct FwdUnit {
   int q_t0;      // first row of the query tile relative to its sequence's first row
                  // (its position in the sequence; its local position in the rank-local form)
   int q_valid;   // rows of the tile inside the chunk
+  // sub-tile 1's query tile: the same as sub-tile 0's for a head pair; for a
+  // tile pair (tile_pairs) the next tile u of the chunk, sub-tile 0 having
+  // tile u0 = u - 1. The key walk is always that of tile u.
+  int u0, q_t1, q_valid1;
   int n;         // number of key tiles the unit visits (0: no such tile in a shorter packed sample)
 };
 
@@ -162,7 +168,17 @@ __host__ __device__ inline int query_tiles_per_seq(const CpGeom& g) {
   return g.rank >= 0 ? 2 * g.tpc : 2 * g.cp * g.tpc;
 }
 
-__host__ __device__ inline int fwd_num_units(const CpGeom& g) { return g.npairs * query_tiles(g); }
+// Tile pairs replace head pairs in the forward when the query heads of a KV
+// group are odd in number (MHA among them): two heads of a pair would then
+// belong to different KV heads and need separate K/V tiles. Uniform batches
+// with an even number of tiles per chunk only.
+__host__ __device__ inline bool use_tile_pairs(const CpGeom& g) {
+  return g.nseq == 0 && (g.hq / g.hkv) % 2 == 1 && g.tpc % 2 == 0;
+}
+
+__host__ __device__ inline int fwd_num_units(const CpGeom& g) {
+  return g.tile_pairs ? g.hq * (query_tiles(g) / 2) : g.npairs * query_tiles(g);
+}
 
 // The query tile with global tile index gt of unit U's sequence (U.seq set).
 __host__ __device__ inline void fill_query_tile(const CpGeom& g, FwdUnit& U, int gt) {
@@ -174,6 +190,7 @@ __host__ __device__ inline void fill_query_tile(const CpGeom& g, FwdUnit& U, int
   U.tpc = q.tpc;
   if (gt >= 2 * g.cp * U.tpc) {  // beyond this packed sample's tiles
     U.k = U.u = U.half = U.r = U.q_t0 = U.q_valid = 0;
+    U.u0 = U.q_t1 = U.q_valid1 = 0;
     U.n = 0;
     return;
   }
@@ -184,6 +201,9 @@ __host__ __device__ inline void fill_query_tile(const CpGeom& g, FwdUnit& U, int
   U.q_t0 = q_chunk_row(g, U.k, U.c) + U.u * kTile;
   const int rem = U.c - U.u * kTile;
   U.q_valid = rem < kTile ? rem : kTile;
+  U.u0 = U.u;
+  U.q_t1 = U.q_t0;
+  U.q_valid1 = U.q_valid;
   if (g.causal)
     U.n = (U.half ? (2 * g.cp - 1 - U.r) * U.tpc : U.r * U.tpc) + U.u + 1;
   else
@@ -194,9 +214,30 @@ __host__ __device__ inline void fill_query_tile(const CpGeom& g, FwdUnit& U, int
 // tile with global tile index gt is gt+1 key tiles, so index 0 is the last
 // tile of the sequence. Packed samples come one after another (units of one
 // sample share their K/V tiles in L2), each longest tile first.
-__host__ __device__ inline FwdUnit fwd_decode_unit(const CpGeom& g, int idx) {
+// kTilePairs is the geometry's tile_pairs as a compile-time constant: the
+// kernels are instantiated for one or the other, so that neither carries the
+// other's decode (the branch alone measured 6 % slower in the forward).
+template <bool kTilePairs>
+__host__ __device__ inline FwdUnit fwd_decode_unit_t(const CpGeom& g, int idx) {
   FwdUnit U;
   int gt, pr;
+  if constexpr (kTilePairs) {
+    // tiles (u - 1, u), u odd, of one head; longest first by tile u
+    const int per = g.b * g.hq;
+    const int lp = query_tiles_per_seq(g) / 2 - 1 - idx / per;
+    const int rest = idx % per;
+    U.seq = rest / g.hq;
+    U.h0 = U.h1 = rest % g.hq;
+    U.g0 = U.g1 = U.h0 / (g.hq / g.hkv);
+    fill_query_tile(g, U, query_tile_of(g, 2 * lp + 1));
+    U.store1 = true;
+    U.u0 = U.u - 1;
+    U.q_t1 = U.q_t0;
+    U.q_valid1 = U.q_valid;
+    U.q_t0 = U.q_t1 - kTile;
+    U.q_valid = kTile;  // only a chunk's last tile can be ragged
+    return U;
+  }
   if (g.nseq > 0) {
     int local;
     U.seq = packed_sample_of(g, idx / g.npairs, local);
@@ -217,6 +258,10 @@ __host__ __device__ inline FwdUnit fwd_decode_unit(const CpGeom& g, int idx) {
   U.g1 = U.h1 / G;
   fill_query_tile(g, U, gt);
   return U;
+}
+
+__host__ __device__ inline FwdUnit fwd_decode_unit(const CpGeom& g, int idx) {
+  return g.tile_pairs ? fwd_decode_unit_t<true>(g, idx) : fwd_decode_unit_t<false>(g, idx);
 }
 
 // dQ work units: one 128-row query tile of one head, longest first: the
@@ -243,6 +288,26 @@ __host__ __device__ inline FwdUnit dq_decode_unit(const CpGeom& g, int idx) {
   U.store1 = false;
   fill_query_tile(g, U, gt);
   return U;
+}
+
+// Tile pairs: sub-tile 0 (query tile u - 1) follows the key walk of tile u,
+// which has one tile more than its own: the diagonal tile of sub-tile 1,
+// whose keys all lie beyond sub-tile 0's rows. fwd_dead_pos gives that
+// tile's position in the walk (-1 when there is none: head pairs, sub-tile 1,
+// no causal mask, or a single-step walk of a later step). With the causal
+// mask the walk's diagonal run ends step 0, at position (half ? tpc : 0) + u;
+// `step` is the step a single-step walk covers (-1: the whole walk).
+__host__ __device__ inline int fwd_dead_pos(const CpGeom& g, const FwdUnit& U, int sub, int step) {
+  if (sub != 0 || U.u0 == U.u || !g.causal || step > 0) return -1;
+  return (U.half ? U.tpc : 0) + U.u;
+}
+
+// The mask of walk position j for a sub-tile with dead position jd: `dead`
+// (no key counts), else `diag` (each row sees the keys up to its own
+// position): the tile before the dead one is the sub-tile's own diagonal.
+__host__ __device__ inline void fwd_pos_mask(int jd, int j, bool walk_diag, bool& diag, bool& dead) {
+  dead = j == jd;
+  diag = jd >= 0 ? j == jd - 1 : walk_diag;
 }
 
 // Static "snake" assignment of units to persistent CTAs: round q gives CTA

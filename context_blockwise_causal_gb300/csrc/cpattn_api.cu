@@ -37,7 +37,7 @@ struct DeviceInfo {
   int num_sms = 0;
   unsigned int* status = nullptr;
   // kernel attributes already set, per kernel; set once, read by any thread
-  std::atomic<bool> fwd_attr[8] = {};  // [d == 128][step form][five-slot ring]
+  std::atomic<bool> fwd_attr[16] = {};  // [d == 128][step form][five-slot ring][tile pairs]
   std::atomic<bool> bwd_attr[2] = {};
 };
 DeviceInfo g_devs[kMaxDevices];
@@ -93,29 +93,30 @@ CpGeom make_geom(int b, int s, int hq, int hkv, int cp, int causal) {
   g.c = s / (2 * cp);
   g.tpc = (g.c + kTile - 1) / kTile;
   g.npairs = (hq + 1) / 2;
+  g.tile_pairs = use_tile_pairs(g) ? 1 : 0;
   return g;
 }
 
-template <int D, bool kStep, int kRing>
+template <int D, bool kStep, int kRing, bool kTP>
 int launch_fwd_ring(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& args,
                     DeviceInfo* di, cudaStream_t st) {
   using C = FwdCfg<D, kRing>;
-  const int slot = (D == 128 ? 4 : 0) + (kStep ? 2 : 0) + (kRing == fwd_ring<D>(false) ? 0 : 1);
+  const int slot = (D == 128 ? 8 : 0) + (kStep ? 4 : 0) + (kRing == fwd_ring<D>(false) ? 0 : 2) + (kTP ? 1 : 0);
   if (!di->fwd_attr[slot].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(cpattn_fwd_kernel<D, kStep, kRing>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(cpattn_fwd_kernel<D, kStep, kRing, kTP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes) != cudaSuccess)
       return CPATTN_ERR_CUDA;
     // The in-kernel register split assumes exactly kFwdLaunchRegs registers
     // per thread at launch; with fewer, the growing warpgroups would wait
     // for registers that never come free.
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, cpattn_fwd_kernel<D, kStep, kRing>) != cudaSuccess) return CPATTN_ERR_CUDA;
+    if (cudaFuncGetAttributes(&fa, cpattn_fwd_kernel<D, kStep, kRing, kTP>) != cudaSuccess) return CPATTN_ERR_CUDA;
     if (fa.numRegs != kFwdLaunchRegs) return CPATTN_ERR_LAUNCH_FAILED;
     di->fwd_attr[slot].store(true, std::memory_order_release);
   }
   const int units = fwd_num_units(args.g);
   const int grid = units < di->num_sms ? units : di->num_sms;
-  cpattn_fwd_kernel<D, kStep, kRing><<<grid, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, args);
+  cpattn_fwd_kernel<D, kStep, kRing, kTP><<<grid, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, args);
   return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_LAUNCH_FAILED;
 }
 
@@ -123,10 +124,12 @@ int launch_fwd_ring(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensor
 template <int D, bool kStep>
 int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& args,
                DeviceInfo* di, cudaStream_t st) {
+  // head pairs that straddle KV groups need separate K/V tiles (tile pairs share them)
+  if (args.g.tile_pairs) return launch_fwd_ring<D, kStep, fwd_ring<D>(false), true>(tq, tk, tv, args, di, st);
   const bool odd_group = (args.g.hq / args.g.hkv) % 2 != 0;
   if (fwd_ring<D>(odd_group) != fwd_ring<D>(false))
-    return launch_fwd_ring<D, kStep, fwd_ring<D>(true)>(tq, tk, tv, args, di, st);
-  return launch_fwd_ring<D, kStep, fwd_ring<D>(false)>(tq, tk, tv, args, di, st);
+    return launch_fwd_ring<D, kStep, fwd_ring<D>(true), false>(tq, tk, tv, args, di, st);
+  return launch_fwd_ring<D, kStep, fwd_ring<D>(false), false>(tq, tk, tv, args, di, st);
 }
 
 }  // namespace
@@ -525,6 +528,7 @@ namespace {
 CpGeom packed_geom(const int* cu, int nseq, int hq, int hkv, int cp, int causal) {
   CpGeom g = make_geom(1, cu[nseq], hq, hkv, cp, causal);
   g.nseq = nseq;
+  g.tile_pairs = 0;  // packed samples pair heads
   for (int i = 0; i <= nseq; ++i) g.cu[i] = cu[i];
   finish_packed(g);
   return g;

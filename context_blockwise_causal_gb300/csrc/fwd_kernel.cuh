@@ -106,7 +106,8 @@ enum FwdStatusBits : unsigned int {
 // row's softmax over that step's keys only, written as an fp32 partial O and
 // its LSE ("大模型面试宝典 · Megatron-LM 篇", 3.2 step 4, before correction);
 // rows that take no part in the step get O = 0, L = -inf.
-template <int D, bool kStep, int kRing>
+// kTP: units are tile pairs (a.g.tile_pairs), not head pairs.
+template <int D, bool kStep, int kRing, bool kTP>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     cpattn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv, const FwdArgs a) {
@@ -178,7 +179,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       for (int rd = 0; ok; ++rd) {
         const int idx = snake_unit(rd, blockIdx.x, grid);
         if (idx >= num_units) break;
-        const FwdUnit U = fwd_decode_unit(g, idx);
+        const FwdUnit U = fwd_decode_unit_t<kTP>(g, idx);
         if (U.n == 0) continue;  // a tile a shorter packed sample does not have
         KvWalk w(g, U);
         if constexpr (kStep) {
@@ -190,10 +191,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                mbar_wait_bounded(&q_empty[1], (ul - 1) & 1, abort_flag, kWaitLimitNs);
           if (!ok) break;
         }
-        const int qrow = U.tok0 + U.q_t0;
         for (int sub = 0; sub < 2; ++sub) {
           mbar_arrive_expect_tx(&q_full[sub], C::kQBytes);
           const int h = sub ? U.h1 : U.h0;
+          const int qrow = U.tok0 + (sub ? U.q_t1 : U.q_t0);
           for (int x = 0; x < D; x += 64)
             tma_load_3d(sQ + sub * C::kQBytes + (x / 64) * (kTile * 128), &tmq, &q_full[sub], x, h, qrow);
         }
@@ -273,7 +274,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       for (int rd = 0; ok; ++rd) {
         const int idx = snake_unit(rd, blockIdx.x, grid);
         if (idx >= num_units) break;
-        const FwdUnit U = fwd_decode_unit(g, idx);
+        const FwdUnit U = fwd_decode_unit_t<kTP>(g, idx);
         if (U.n == 0) continue;
         const bool shared_kv = U.g0 == U.g1;
         const int n = kStep ? KvWalk(g, U).step_tiles(a.step) : U.n;
@@ -372,8 +373,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     for (int rd = 0; ok; ++rd) {
       const int idx = snake_unit(rd, blockIdx.x, grid);
       if (idx >= num_units) break;
-      const FwdUnit U = fwd_decode_unit(g, idx);
+      const FwdUnit U = fwd_decode_unit_t<kTP>(g, idx);
       if (U.n == 0) continue;
+      // this sub-tile's query rows (a second head, or the next query tile)
+      const int q_t = sub ? U.q_t1 : U.q_t0;
+      const int q_valid = sub ? U.q_valid1 : U.q_valid;
+      // tile pairs: the position of sub-tile 0's fully masked tile (-1: none)
+      const int jd = kTP ? fwd_dead_pos(g, U, sub, kStep ? a.step : -1) : -1;
       KvWalk w(g, U);
       int n = U.n;
       if constexpr (kStep) {
@@ -381,9 +387,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         n = w.step_tiles(a.step);
         if (n == 0) {
           // the unit's rows take no part in this step: O = 0, L = -inf
-          if (row < U.q_valid && (sub == 0 || U.store1)) {
+          if (row < q_valid && (sub == 0 || U.store1)) {
             const int h = sub ? U.h1 : U.h0;
-            const int t = U.q_t0 + row;
+            const int t = q_t + row;
             float4* dst = reinterpret_cast<float4*>(a.o_part + ((int64_t(U.tok0) + t) * g.hq + h) * D);
 #pragma unroll
             for (int c0 = 0; c0 < D / 4; ++c0) dst[c0] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -396,8 +402,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       float l = 0.f;
       for (int j = 0; j < n; ++j) {
         int chunk = 0, tile = 0;
-        bool dg = false;
-        w.next(chunk, tile, dg);
+        bool walk_dg = false, dg = false, dead = false;
+        w.next(chunk, tile, walk_dg);
+        if constexpr (kTP)
+          fwd_pos_mask(jd, j, walk_dg, dg, dead);
+        else
+          dg = walk_dg;
         const int rem = U.c - tile * kTile;
         const int n_valid = rem < kTile ? rem : kTile;
         if (!(ok = mbar_wait_bounded(&s_full[sub], scnt & 1, abort_flag, kWaitLimitNs))) break;
@@ -421,8 +431,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // row max: from the load itself, except on a masked tile (the diagonal
         // or a ragged chunk end), where it is taken over the unmasked scores
         float m_raw = hw_max;
-        if (dg || n_valid < kTile) {
-          const int lim = dg ? (row < n_valid - 1 ? row : n_valid - 1) : n_valid - 1;
+        if (dg || dead || n_valid < kTile) {
+          const int lim = dead ? -1 : dg ? (row < n_valid - 1 ? row : n_valid - 1) : n_valid - 1;
 #pragma unroll
           for (int i = 0; i < kTile; ++i)
             if (i > lim) s[i] = -INFINITY;
@@ -516,10 +526,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_empty[sub]);
-      const bool store = row < U.q_valid && (sub == 0 || U.store1);
+      const bool store = row < q_valid && (sub == 0 || U.store1);
       if (kStep && store) {
         const int h = sub ? U.h1 : U.h0;
-        const int t = U.q_t0 + row;
+        const int t = q_t + row;
         const float inv = 1.f / l;
         float4* dst = reinterpret_cast<float4*>(a.o_part + ((int64_t(U.tok0) + t) * g.hq + h) * D);
 #pragma unroll
@@ -557,17 +567,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const int part = lane & 3;          // 16-byte piece of the 64
             const uint4 v = stg[r * 4 + (part ^ (r & 3))];
             const int trow = wq * 32 + r;       // row within the tile
-            if (write_head && trow < U.q_valid)
-              *reinterpret_cast<uint4*>(a.o + ((int64_t(U.tok0) + U.q_t0 + trow) * g.hq + h) * D + c * 32 + part * 8) = v;
+            if (write_head && trow < q_valid)
+              *reinterpret_cast<uint4*>(a.o + ((int64_t(U.tok0) + q_t + trow) * g.hq + h) * D + c * 32 + part * 8) = v;
           }
           __syncwarp();
         }
         if (store)
-          a.lse[(int64_t(U.bi) * g.hq + h) * a.lse_stride + U.lse_t0 + U.q_t0 + row] =
+          a.lse[(int64_t(U.bi) * g.hq + h) * a.lse_stride + U.lse_t0 + q_t + row] =
               (m_used + log2f(l)) * 0.69314718055994530942f;
       } else if (store) {
         const int h = sub ? U.h1 : U.h0;
-        const int t = U.q_t0 + row;
+        const int t = q_t + row;
         const float inv = 1.f / l;
         __nv_bfloat16* dst = a.o + ((int64_t(U.tok0) + t) * g.hq + h) * D;
 #pragma unroll

@@ -101,19 +101,23 @@ struct RowMap {
 
 static RowMap natural_map(const CpGeom& g) { return RowMap{g.b * g.s, g.b * g.s, -1}; }
 
-// Walk one query-tile unit (forward sub-tile or dQ unit) and mark its pairs.
+// Walk one query-tile unit (forward sub-tile `sub` or a dQ unit) and mark its pairs.
 static int walk_query_unit(const CpGeom& g, const Rows& R, const FwdUnit& U, int h, std::vector<unsigned char>& count,
-                           const char* what, KvWalk w, const RowMap& M) {
+                           const char* what, KvWalk w, const RowMap& M, int sub = 0, int step = -1) {
   int chunk, tile, nt = 0;
-  bool dg;
-  while (w.next(chunk, tile, dg)) {
+  bool walk_dg, dg, dead;
+  const int q_t = sub ? U.q_t1 : U.q_t0, q_valid = sub ? U.q_valid1 : U.q_valid;
+  const int jd = fwd_dead_pos(g, U, sub, step);
+  while (w.next(chunk, tile, walk_dg)) {
+    fwd_pos_mask(jd, nt, walk_dg, dg, dead);
     ++nt;
+    if (dead) continue;
     const int rem = U.c - tile * kTile;
     const int nv = rem < kTile ? rem : kTile;
-    for (int row = 0; row < U.q_valid; ++row)
+    for (int row = 0; row < q_valid; ++row)
       for (int col = 0; col < nv; ++col) {
         if (dg && col > row) continue;
-        const int qb = U.tok0 + U.q_t0 + row, kb = U.tok0 + kv_chunk_row(g, chunk, U.c) + tile * kTile + col;
+        const int qb = U.tok0 + q_t + row, kb = U.tok0 + kv_chunk_row(g, chunk, U.c) + tile * kTile + col;
         if (qb < 0 || qb >= M.q_rows || kb < 0 || kb >= M.kv_rows) {
           printf("%s: row outside its buffer (query %d of %d, key %d of %d)\n", what, qb, M.q_rows, kb, M.kv_rows);
           return -1;
@@ -124,8 +128,8 @@ static int walk_query_unit(const CpGeom& g, const Rows& R, const FwdUnit& U, int
   return nt;
 }
 static int walk_query_unit(const CpGeom& g, const Rows& R, const FwdUnit& U, int h, std::vector<unsigned char>& count,
-                           const char* what) {
-  return walk_query_unit(g, R, U, h, count, what, KvWalk(g, U), natural_map(g));
+                           const char* what, int sub = 0) {
+  return walk_query_unit(g, R, U, h, count, what, KvWalk(g, U), natural_map(g), sub);
 }
 
 static int check(const CpGeom& g, int grid) {
@@ -154,7 +158,7 @@ static int check(const CpGeom& g, int grid) {
       if (sub == 1 && !U.store1) continue;
       const int h = sub ? U.h1 : U.h0;
       if (h / (g.hq / g.hkv) != (sub ? U.g1 : U.g0)) { printf("bad kv head\n"); return 1; }
-      const int nt = walk_query_unit(g, R, U, h, count, "forward");
+      const int nt = walk_query_unit(g, R, U, h, count, "forward", sub);
       if (nt < 0) return 1;
       if (nt != U.n) { printf("unit %d: walk has %d tiles, n = %d\n", idx, nt, U.n); return 1; }
     }
@@ -242,7 +246,10 @@ static int check_rank(const CpGeom& base, int grid) {
     const RowMap gathered{g.b * 2 * g.c, g.cp * g.b * 2 * g.c, -1};
     // ---- forward units: snake assignment, longest first, the rank's tiles only
     const int nu = fwd_num_units(g);
-    if (nu != g.npairs * g.b * 2 * g.tpc) { printf("rank %d: %d forward units\n", r, nu); return 1; }
+    if (nu != (g.tile_pairs ? g.hq * g.b * g.tpc : g.npairs * g.b * 2 * g.tpc)) {
+      printf("rank %d: %d forward units\n", r, nu);
+      return 1;
+    }
     std::vector<int> seen(nu, 0);
     for (int bid = 0; bid < grid; ++bid)
       for (int rd = 0;; ++rd) {
@@ -261,7 +268,7 @@ static int check_rank(const CpGeom& base, int grid) {
       for (int sub = 0; sub < 2; ++sub) {
         if (sub == 1 && !U.store1) continue;
         const int h = sub ? U.h1 : U.h0;
-        const int nt = walk_query_unit(g, R, U, h, fwd, "rank forward", KvWalk(g, U), gathered);
+        const int nt = walk_query_unit(g, R, U, h, fwd, "rank forward", KvWalk(g, U), gathered, sub);
         if (nt < 0) return 1;
         if (nt != U.n) { printf("rank %d unit %d: walk has %d tiles, n = %d\n", r, idx, nt, U.n); return 1; }
         // ring form: step st reads only the shard of rank (r - st) mod cp
@@ -271,7 +278,7 @@ static int check_rank(const CpGeom& base, int grid) {
           const RowMap one{g.b * 2 * g.c, g.b * 2 * g.c, ((r - st) % g.cp + g.cp) % g.cp};
           KvWalk w(gs, U);
           w.only_step(st);
-          if (walk_query_unit(gs, R, U, h, ring, "rank ring step", w, one) < 0) return 1;
+          if (walk_query_unit(gs, R, U, h, ring, "rank ring step", w, one, sub, st) < 0) return 1;
         }
       }
     }
@@ -334,8 +341,9 @@ int main(int argc, char** argv) {
       g.c = g.s / (2 * g.cp);
       g.tpc = (g.c + kTile - 1) / kTile;
       g.nseq = 0;
-      snprintf(desc, sizeof desc, "%sb=%d s=%d hq=%d hkv=%d cp=%d causal=%d grid=%d", ranked ? "rank-local " : "",
-               g.b, g.s, g.hq, g.hkv, g.cp, g.causal, grid);
+      snprintf(desc, sizeof desc, "%sb=%d s=%d hq=%d hkv=%d cp=%d causal=%d grid=%d%s", ranked ? "rank-local " : "",
+               g.b, g.s, g.hq, g.hkv, g.cp, g.causal, grid,
+               (g.hq / g.hkv) % 2 == 1 && (g.s / (2 * g.cp) + kTile - 1) / kTile % 2 == 0 ? " (tile pairs)" : "");
       i += 8;
     } else if (!strcmp(argv[i], "P") && i + 1 < argc) {
       const int n = atoi(argv[i + 1]);
@@ -358,6 +366,7 @@ int main(int argc, char** argv) {
       return 1;
     }
     g.npairs = (g.hq + 1) / 2;
+    g.tile_pairs = use_tile_pairs(g) ? 1 : 0;  // as the library sets it
     const int rc = ranked ? check_rank(g, grid) : check(g, grid);
     printf("%s %s\n", rc ? "FAIL" : "ok", desc);
     fails += rc;

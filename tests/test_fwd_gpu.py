@@ -81,6 +81,9 @@ SMALL = [
     (3, 8, 2, 1, 128, 4, True),       # c = 1: one token per half-chunk, batch 3
     (1, 2, 1, 1, 64, 1, True),        # the smallest case: s = 2, one head
     (1, 6, 3, 3, 64, 3, False),       # c = 1, no mask, odd hq
+    (2, 2048, 4, 4, 128, 2, True),    # MHA, c = 512: units pair two query tiles of one head
+    (1, 1024, 3, 1, 64, 2, False),    # tile pairs without the mask, G = 3
+    (1, 1280, 2, 2, 128, 2, True),    # tile pairs, c = 320: ragged second tile of each last pair
 ]
 
 

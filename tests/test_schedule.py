@@ -31,6 +31,14 @@ GEOMS = [
     (3, 8, 2, 1, 4, 1, 5),
     (1, 6, 3, 3, 3, 0, 2),
     (2, 16, 4, 2, 4, 1, 3),
+    # odd head groups with an even number of tiles per chunk: the forward pairs
+    # two query tiles of one head (MHA, G = 3, no mask, ragged second tile)
+    (1, 2048, 4, 4, 4, 1, 7),
+    (2, 1024, 3, 3, 2, 1, 9),
+    (1, 1024, 3, 1, 2, 0, 5),
+    (1, 4096, 2, 2, 2, 1, 13),
+    (1, 960, 6, 2, 3, 1, 7),
+    (1, 1920, 2, 2, 3, 1, 5),     # three tiles per chunk: head pairs
 ]
 
 

@@ -238,8 +238,8 @@ struct DkdvCfg {
   static constexpr int kLDBytes = 2 * kTile * 4;  // L[128], D[128] fp32 per dO stage
   static constexpr int kOffBar = kOffLD + kOStages * kLDBytes;
   // kv_full kv_empty q_full[3] q_empty[3] o_full[2] o_empty[2]
-  // s_full s_free dp_full p_full dkv_full dkv_empty drain
-  static constexpr int kNumBars = 2 + 2 * kQStages + 2 * kOStages + 7;
+  // s_full s_free dp_full p_full dkv_full dkv_empty drain pt_full
+  static constexpr int kNumBars = 2 + 2 * kQStages + 2 * kOStages + 8;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kLayoutBytes = kOffMisc + 16;
   // The d=128 layout leaves no room for re-alignment: the dynamic shared
@@ -262,11 +262,12 @@ struct DkdvCfg {
 //   dK += dS^T(i) Q,  dV += P^T(i) dO   (A operands packed in [128,256))
 // The element-wise warps read S^T(i) and release its columns at once
 // (s_free), compute P in registers, then read dP^T(i) and write packed bf16
-// P^T and dS^T over it (each warp inside the columns it read: P^T to
-// [128+64h, +32), dS^T to [128+64h+32, +32)). So the tensor core runs
-// S^T(i+1) while the warps finish block i, and the exponentials of block i
-// overlap dK/dV(i-1) and dP^T(i):
-//   tensor core:  S^T(i+1) | dK(i) dV(i) | dP^T(i+1) | S^T(i+2) | ...
+// P^T over it (each warp inside the columns it read: P^T to [128+64h, +32))
+// and release it (pt_full), then form dS^T into [128+64h+32, +32) (p_full).
+// So the tensor core runs S^T(i+1) while the warps finish block i, dV(i)
+// while they form dS(i), and the exponentials of block i overlap dK/dV(i-1)
+// and dP^T(i):
+//   tensor core:  S^T(i+1) | dV(i) dK(i) | dP^T(i+1) | S^T(i+2) | ...
 //   warps:        P(i+1) from S^T(i+1) ..............| dS(i+1)  |
 // Units walk their query tiles from the end of the sequence down (QWalk), so
 // the CTAs in flight read the same Q/dO tiles from L2.
@@ -303,6 +304,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* dkv_full = s_full + 4;
   uint64_t* dkv_empty = s_full + 5;
   uint64_t* drain = s_full + 6;
+  uint64_t* pt_full = s_full + 7;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -332,6 +334,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(dkv_full, 1);
     mbar_init(dkv_empty, 8);
     mbar_init(drain, 1);
+    mbar_init(pt_full, 8);
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -483,23 +486,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             issue_s(i + 1);
             umma_commit_w(s_full);
           }
-          ok = mbar_wait_warp_lean(p_full, i & 1, abort_flag, kWaitLimitNs) &&
+          ok = mbar_wait_warp_lean(pt_full, i & 1, abort_flag, kWaitLimitNs) &&
                (j > 0 || ul == 0 || mbar_wait_warp_lean(dkv_empty, (ul - 1) & 1, abort_flag, kWaitLimitNs));
           if (!ok) break;
           tc_fence_after();
-          // dK += dS^T Q, dV += P^T dO (K = 128 queries, A from TMEM)
+          // dV += P^T dO as soon as P^T is in TMEM, then dK += dS^T Q
           const uint64_t rq = ((i % C::kQStages) * C::kTileBytes) >> 4;
           const uint64_t ro = ((i % C::kOStages) * C::kTileBytes) >> 4;
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            umma_ts_w(tdK, tdP + 32 + half_split_col(kk), dQ_mn + rq + ((kk * 2048) >> 4), idKV,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-          umma_commit_w(&q_empty[i % C::kQStages]);
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
             umma_ts_w(tdV, tdP + half_split_col(kk), ddO_mn + ro + ((kk * 2048) >> 4), idKV,
                       (j > 0 || kk > 0) ? 1u : 0u);
           umma_commit_w(&o_empty[i % C::kOStages]);
+          if (!(ok = mbar_wait_warp_lean(p_full, i & 1, abort_flag, kWaitLimitNs))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            umma_ts_w(tdK, tdP + 32 + half_split_col(kk), dQ_mn + rq + ((kk * 2048) >> 4), idKV,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+          umma_commit_w(&q_empty[i % C::kQStages]);
           if (j + 1 < n) {
             // dP^T(i+1) over P^T/dS^T(i), which the MMAs just issued read first
             if (!(ok = mbar_wait_warp_lean(&o_full[(i + 1) % C::kOStages], ((i + 1) / C::kOStages) & 1, abort_flag,
@@ -609,6 +614,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!(ok = mbar_wait_lean(dp_full, i & 1, abort_flag, kWaitLimitNs))) break;
         tc_fence_after();
         tmem_ld16x256b_2x2(tP, tP + kL16, tP + 32, tP + kL16 + 32, ra, rb);
+        // P^T -> [64h, 64h+32) of the dP^T columns just read: dV may start
+        tmem_st16x128b_2x2(tP, tP + kL16, tP + 16, tP + kL16 + 16, pp[0], pp[1]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pt_full);
         uint32_t pd[2][16];
         if (full) {
           ds_frag<false>(pp[0], ra, dv[0], none, c4, pd[0]);
@@ -617,9 +627,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ds_frag<true>(pp[0], ra, dv[0], valid[0], c4, pd[0]);
           ds_frag<true>(pp[1], rb, dv[1], valid[1], c4, pd[1]);
         }
-        // P^T -> [64h, 64h+32), dS^T -> [64h+32, 64h+64) of the dP^T columns
-        tmem_st16x128b_2x2(tP, tP + kL16, tP + 32, tP + kL16 + 32, pp[0], pd[0]);
-        tmem_st16x128b_2x2(tP + 16, tP + kL16 + 16, tP + 48, tP + kL16 + 48, pp[1], pd[1]);
+        // dS^T -> [64h+32, 64h+64)
+        tmem_st16x128b_2x2(tP + 32, tP + kL16 + 32, tP + 48, tP + kL16 + 48, pd[0], pd[1]);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full);
@@ -716,8 +725,8 @@ struct DqCfg {
   static constexpr int kOffKV = kOffdO + kTileBytes;
   static constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
   // q_full q_empty qa_full qa_empty s_full s_free dp_full p_full dq_full
-  // dq_empty drain, kv_full[] kv_empty[]
-  static constexpr int kNumBars = 11 + 2 * kSlots;
+  // dq_empty drain, kv_full[] kv_empty[], p_half
+  static constexpr int kNumBars = 12 + 2 * kSlots;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kLayoutBytes = kOffMisc + 16;
   // The d=128 layout leaves no room for re-alignment: the dynamic shared
@@ -740,7 +749,10 @@ struct DqCfg {
 // shared memory into TMEM as packed bf16, so every MMA takes its A operand
 // from TMEM and reads only B (a K or V tile) from shared memory:
 //   S(j) = Q K_j^T -> [0,128)     dP(j) = dO V_j^T -> [128,256)
-//   dQ += dS(j) K_j               (dS packed over dP(j))
+//   dQ += dS(j) K_j               (dS packed over dP(j); each warp publishes
+//                                  its first 32 keys' dS (p_half) before
+//                                  forming the other 32, and the MMAs over
+//                                  those keys start at once)
 // The element-wise warps load S(j) and at once release its columns (s_free),
 // compute P in registers, then load dP(j) and write packed bf16 dS over it,
 // each warp inside the columns it read. Tensor-core order per key tile:
@@ -778,6 +790,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* drain = bars + 10;
   uint64_t* kv_full = bars + 11;
   uint64_t* kv_empty = bars + 11 + C::kSlots;
+  uint64_t* p_half = bars + 11 + 2 * C::kSlots;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -800,6 +813,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 8);
     mbar_init(drain, 1);
+    mbar_init(p_half, 8);
     for (int i = 0; i < C::kSlots; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
@@ -946,15 +960,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             issue_s(ks);
             umma_commit_w(s_full);
           }
-          ok = mbar_wait_warp_lean(p_full, jt & 1, abort_flag, kWaitLimitNs) &&
+          ok = mbar_wait_warp_lean(p_half, jt & 1, abort_flag, kWaitLimitNs) &&
                (j > 0 || ul == 0 || mbar_wait_warp_lean(dq_empty, (ul - 1) & 1, abort_flag, kWaitLimitNs));
           if (!ok) break;
           tc_fence_after();
-          // dQ += dS(jt) K_j   (dS from TMEM, K MN-major)
+          // dQ += dS(jt) K_j   (dS from TMEM, K MN-major): first the K-steps of
+          // each warp's first 32 keys (0, 1 and 4, 5), then the rest
           const uint64_t kmn = dKV_mn + ((cur_ks * C::kTileBytes) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
+          for (int q = 0; q < 4; ++q) {
+            const int kk = (q & 1) + 4 * (q >> 1);
             umma_ts_w(tdQ, tdP + half_split_col(kk), kmn + ((kk * 2048) >> 4), idQ, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          if (!(ok = mbar_wait_warp_lean(p_full, jt & 1, abort_flag, kWaitLimitNs))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int kk = 2 + (q & 1) + 4 * (q >> 1);
+            umma_ts_w(tdQ, tdP + half_split_col(kk), kmn + ((kk * 2048) >> 4), idQ, 1u);
+          }
           umma_commit_w(&kv_empty[cur_ks]);
           if (j == n - 1) umma_commit_w(dq_full);
           if (j + 1 < n) {
@@ -1066,15 +1090,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         tmem_ld32x2(tdP, tdP + 32, r0, r1);
         uint32_t pd0[16], pd1[16];
-        if (full) {
+        // dS packed into [64h, 64h+32) of the dP columns (read above), its
+        // first 32 keys published before the second are formed
+        if (full)
           ds_row32<false>(pp0, r0, dd, 0u, pd0);
-          ds_row32<false>(pp1, r1, dd, 0u, pd1);
-        } else {
+        else
           ds_row32<true>(pp0, r0, dd, v0, pd0);
+        tmem_st16(tdP, pd0);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_half);
+        if (full)
+          ds_row32<false>(pp1, r1, dd, 0u, pd1);
+        else
           ds_row32<true>(pp1, r1, dd, v1, pd1);
-        }
-        // dS packed into [64h, 64h+32) of the dP columns (read above)
-        tmem_st16x2(tdP, tdP + 16, pd0, pd1);
+        tmem_st16(tdP + 16, pd1);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full);

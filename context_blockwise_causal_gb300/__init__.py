@@ -111,6 +111,8 @@ def library():
         lib.cpattn_zigzag_index.restype = _i
         lib.cpattn_device_status.argtypes = [_p, ctypes.POINTER(_i)]
         lib.cpattn_device_status.restype = _i
+        lib.cpattn_selftest_abort.argtypes = [_p] * 10 + [_sz] + [_i] * 6 + [ctypes.c_ulonglong, _p]
+        lib.cpattn_selftest_abort.restype = _i
         lib.cpattn_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, _p]
         lib.cpattn_selftest_wait_timeout.restype = _i
         lib.cpattn_strerror.argtypes = [_i]

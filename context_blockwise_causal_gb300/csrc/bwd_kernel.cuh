@@ -50,6 +50,9 @@ struct BwdArgs {
   float scale_log2;  // log2(e) * the softmax scale
   float scale;       // the softmax scale (1 / sqrt(d) by default)
   unsigned int* status;
+  // time limit of the producers' waits for free buffers: kWaitLimitNs, or a
+  // short one in the abort self-test (cpattn_selftest_abort)
+  uint64_t producer_limit_ns;
 };
 
 enum BwdStatusBits : unsigned int {
@@ -271,7 +274,7 @@ struct DkdvCfg {
 //   warps:        P(i+1) from S^T(i+1) ..............| dS(i+1)  |
 // Units walk their query tiles from the end of the sequence down (QWalk), so
 // the CTAs in flight read the same Q/dO tiles from L2.
-template <int D>
+template <int D, bool kShortWaits = false>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     cpattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                            const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
@@ -355,6 +358,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      // the waits for free stages: a short limit only in the abort self-test
+      const uint64_t plimit = kShortWaits ? a.producer_limit_ns : kWaitLimitNs;
       bool ok = true;
       uint32_t item = 0;  // blocks loaded so far (their dO tiles issued)
       uint32_t nq = 0;    // Q tiles issued: item, or item + 1 when a dO wait gave up
@@ -364,14 +369,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int row = U.tok0 + q_chunk_row(g, chunk, U.c) + tile * kTile;
         const uint32_t qs = item % C::kQStages, os = item % C::kOStages;
         if (item >= C::kQStages &&
-            !mbar_wait_lean(&q_empty[qs], ((item / C::kQStages) - 1) & 1, abort_flag, kWaitLimitNs))
+            !mbar_wait_lean(&q_empty[qs], ((item / C::kQStages) - 1) & 1, abort_flag, plimit))
           return false;
         mbar_arrive_expect_tx(&q_full[qs], C::kTileBytes);
         for (int x = 0; x < D; x += 64)
           tma_load_3d(sQ + qs * C::kTileBytes + (x / 64) * (kTile * 128), &tmq, &q_full[qs], x, h, row);
         ++nq;
         if (item >= C::kOStages &&
-            !mbar_wait_lean(&o_empty[os], ((item / C::kOStages) - 1) & 1, abort_flag, kWaitLimitNs))
+            !mbar_wait_lean(&o_empty[os], ((item / C::kOStages) - 1) & 1, abort_flag, plimit))
           return false;
         mbar_arrive_expect_tx(&o_full[os], C::kTileBytes + C::kLDBytes);
         for (int x = 0; x < D; x += 64)
@@ -398,7 +403,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (ok && first) {
               // K/V of this unit, once its first block is on its way.
               first = false;
-              if (ul > 0 && !(ok = mbar_wait_lean(kv_empty, (ul - 1) & 1, abort_flag, kWaitLimitNs))) break;
+              if (ul > 0 && !(ok = mbar_wait_lean(kv_empty, (ul - 1) & 1, abort_flag, plimit))) break;
               mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
               const int krow = U.tok0 + U.k_t0;
               for (int x = 0; x < D; x += 64) {
@@ -759,7 +764,7 @@ struct DqCfg {
 //   S(j+1) | dQ(j) | dP(j+1) | S(j+2) | ...
 // so the exponentials of tile j overlap dQ(j-1) and dP(j), and only the dS
 // step is on the tensor core's critical path.
-template <int D>
+template <int D, bool kShortWaits = false>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     cpattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                          const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
@@ -838,13 +843,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      const uint64_t plimit = kShortWaits ? a.producer_limit_ns : kWaitLimitNs;
       bool ok = true;
       uint32_t nload = 0;
       int ul = 0;
       auto load = [&](const CUtensorMap* map, int head, int row) -> bool {
         const uint32_t slot = nload % C::kSlots;
         if (nload >= (uint32_t)C::kSlots &&
-            !mbar_wait_lean(&kv_empty[slot], ((nload / C::kSlots) - 1) & 1, abort_flag, kWaitLimitNs))
+            !mbar_wait_lean(&kv_empty[slot], ((nload / C::kSlots) - 1) & 1, abort_flag, plimit))
           return false;
         mbar_arrive_expect_tx(&kv_full[slot], C::kTileBytes);
         uint8_t* dst = sKV + slot * C::kTileBytes;
@@ -860,7 +866,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (U.n == 0) continue;  // a tile a shorter packed sample does not have
         // the Q/dO stage is free once the element-wise warps copied the
         // previous unit's tiles into TMEM
-        if (ul > 0 && !(ok = mbar_wait_lean(q_empty, (ul - 1) & 1, abort_flag, kWaitLimitNs))) break;
+        if (ul > 0 && !(ok = mbar_wait_lean(q_empty, (ul - 1) & 1, abort_flag, plimit))) break;
         mbar_arrive_expect_tx(q_full, 2 * C::kTileBytes);
         const int qrow = U.tok0 + U.q_t0;
         for (int x = 0; x < D; x += 64) {

@@ -37,8 +37,8 @@ struct DeviceInfo {
   int num_sms = 0;
   unsigned int* status = nullptr;
   // kernel attributes already set, per kernel; set once, read by any thread
-  std::atomic<bool> fwd_attr[16] = {};  // [d == 128][step form][five-slot ring][tile pairs]
-  std::atomic<bool> bwd_attr[2] = {};
+  std::atomic<bool> fwd_attr[17] = {};  // [d == 128][step form][five-slot ring][tile pairs]; 16: self-test
+  std::atomic<bool> bwd_attr[3] = {};   // [d == 128]; 2: self-test
 };
 DeviceInfo g_devs[kMaxDevices];
 std::mutex g_mu;
@@ -97,26 +97,27 @@ CpGeom make_geom(int b, int s, int hq, int hkv, int cp, int causal) {
   return g;
 }
 
-template <int D, bool kStep, int kRing, bool kTP>
+template <int D, bool kStep, int kRing, bool kTP, bool kShort = false>
 int launch_fwd_ring(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& args,
                     DeviceInfo* di, cudaStream_t st) {
   using C = FwdCfg<D, kRing>;
-  const int slot = (D == 128 ? 8 : 0) + (kStep ? 4 : 0) + (kRing == fwd_ring<D>(false) ? 0 : 2) + (kTP ? 1 : 0);
+  const int slot =
+      kShort ? 16 : (D == 128 ? 8 : 0) + (kStep ? 4 : 0) + (kRing == fwd_ring<D>(false) ? 0 : 2) + (kTP ? 1 : 0);
   if (!di->fwd_attr[slot].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(cpattn_fwd_kernel<D, kStep, kRing, kTP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(cpattn_fwd_kernel<D, kStep, kRing, kTP, kShort>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes) != cudaSuccess)
       return CPATTN_ERR_CUDA;
     // The in-kernel register split assumes exactly kFwdLaunchRegs registers
     // per thread at launch; with fewer, the growing warpgroups would wait
     // for registers that never come free.
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, cpattn_fwd_kernel<D, kStep, kRing, kTP>) != cudaSuccess) return CPATTN_ERR_CUDA;
+    if (cudaFuncGetAttributes(&fa, cpattn_fwd_kernel<D, kStep, kRing, kTP, kShort>) != cudaSuccess) return CPATTN_ERR_CUDA;
     if (fa.numRegs != kFwdLaunchRegs) return CPATTN_ERR_LAUNCH_FAILED;
     di->fwd_attr[slot].store(true, std::memory_order_release);
   }
   const int units = fwd_num_units(args.g);
   const int grid = units < di->num_sms ? units : di->num_sms;
-  cpattn_fwd_kernel<D, kStep, kRing, kTP><<<grid, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, args);
+  cpattn_fwd_kernel<D, kStep, kRing, kTP, kShort><<<grid, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, args);
   return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_LAUNCH_FAILED;
 }
 
@@ -148,7 +149,7 @@ namespace {
 // the key/value side kv_rows (both b * s by default).
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int b, int s, int hq, int hkv, int d,
              int cp, int causal, double scale, void* stream, int64_t lse_stride = -1, const CpGeom* geom = nullptr,
-             uint64_t q_rows = 0, uint64_t kv_rows = 0) {
+             uint64_t q_rows = 0, uint64_t kv_rows = 0, uint64_t producer_limit_ns = kWaitLimitNs) {
   if (!q || !k || !v || !o || !lse) return CPATTN_ERR_NULL_PTR;
   int rc = check_geometry(b, s, hq, hkv, d, cp);
   if (rc) return rc;
@@ -172,7 +173,10 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   args.step = -1;
   args.scale_log2 = float(1.4426950408889634 * scale);
   args.status = di->status;
+  args.producer_limit_ns = producer_limit_ns;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (producer_limit_ns != kWaitLimitNs)  // the abort self-test: d = 128, head pairs sharing K/V (checked there)
+    return launch_fwd_ring<128, false, fwd_ring<128>(false), false, true>(tq, tk, tv, args, di, st);
   return d == 128 ? launch_fwd<128, false>(tq, tk, tv, args, di, st) : launch_fwd<64, false>(tq, tk, tv, args, di, st);
 }
 }  // namespace
@@ -220,6 +224,7 @@ int step_impl(const void* q, const void* k, const void* v, float* o_part, float*
   args.step = step;
   args.scale_log2 = float(1.4426950408889634 * scale);
   args.status = di->status;
+  args.producer_limit_ns = kWaitLimitNs;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return d == 128 ? launch_fwd<128, true>(tq, tk, tv, args, di, st) : launch_fwd<64, true>(tq, tk, tv, args, di, st);
 }
@@ -387,14 +392,14 @@ BwdLayout bwd_layout(int b, int s, int hq, int d, int cp) {
   return bwd_layout_tiles(b, (c + kTile - 1) / kTile, hq, cp);
 }
 
-template <int D>
+template <int D, bool kShort = false>
 int launch_bwd_stage(int stage, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      const CUtensorMap& tdo, const BwdArgs& args, DeviceInfo* di, cudaStream_t st) {
-  const int slot = D == 128 ? 1 : 0;
+  const int slot = kShort ? 2 : D == 128 ? 1 : 0;
   if (!di->bwd_attr[slot].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(cpattn_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(cpattn_bwd_dkdv_kernel<D, kShort>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DkdvCfg<D>::kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(cpattn_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(cpattn_bwd_dq_kernel<D, kShort>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DqCfg<D>::kSmemBytes) != cudaSuccess)
       return CPATTN_ERR_CUDA;
     di->bwd_attr[slot].store(true, std::memory_order_release);
@@ -406,21 +411,21 @@ int launch_bwd_stage(int stage, const CUtensorMap& tq, const CUtensorMap& tk, co
     cpattn_bwd_pre_kernel<D><<<pre_grid, 256, 0, st>>>(args);
   } else if (stage == 1) {
     const int units = bwd_num_units(args.g);
-    cpattn_bwd_dkdv_kernel<D><<<units < di->num_sms ? units : di->num_sms, kBwdThreads, DkdvCfg<D>::kSmemBytes,
-                                st>>>(tq, tk, tv, tdo, args);
+    cpattn_bwd_dkdv_kernel<D, kShort><<<units < di->num_sms ? units : di->num_sms, kBwdThreads,
+                                        DkdvCfg<D>::kSmemBytes, st>>>(tq, tk, tv, tdo, args);
   } else {
     const int units = dq_num_units(args.g);
-    cpattn_bwd_dq_kernel<D><<<units < di->num_sms ? units : di->num_sms, kBwdThreads, DqCfg<D>::kSmemBytes, st>>>(
-        tq, tk, tv, tdo, args);
+    cpattn_bwd_dq_kernel<D, kShort><<<units < di->num_sms ? units : di->num_sms, kBwdThreads, DqCfg<D>::kSmemBytes,
+                                      st>>>(tq, tk, tv, tdo, args);
   }
   return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_LAUNCH_FAILED;
 }
 
-template <int D>
+template <int D, bool kShort = false>
 int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                const BwdArgs& args, DeviceInfo* di, cudaStream_t st) {
   for (int stage = 0; stage < 3; ++stage) {
-    const int rc = launch_bwd_stage<D>(stage, tq, tk, tv, tdo, args, di, st);
+    const int rc = launch_bwd_stage<D, kShort>(stage, tq, tk, tv, tdo, args, di, st);
     if (rc) return rc;
   }
   return CPATTN_OK;
@@ -441,7 +446,8 @@ namespace {
 int prepare_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int b, int s, int hq, int hkv,
                 int d, int cp, int causal, double scale, CUtensorMap* maps, BwdArgs* args, DeviceInfo** di,
-                int64_t lse_stride = -1, const CpGeom* packed = nullptr, const CpGeom* ranked = nullptr) {
+                int64_t lse_stride = -1, const CpGeom* packed = nullptr, const CpGeom* ranked = nullptr,
+                uint64_t producer_limit_ns = kWaitLimitNs) {
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return CPATTN_ERR_NULL_PTR;
   int rc = check_geometry(b, s, hq, hkv, d, cp);
   if (rc) return rc;
@@ -479,6 +485,7 @@ int prepare_bwd(const void* q, const void* k, const void* v, const void* o, cons
   args->scale = float(scale);
   args->scale_log2 = float(1.4426950408889634 * scale);
   args->status = (*di)->status;
+  args->producer_limit_ns = producer_limit_ns;
   return CPATTN_OK;
 }
 
@@ -489,14 +496,16 @@ namespace {
 int bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout, void* dq,
              void* dk, void* dv, void* workspace, size_t workspace_bytes, int b, int s, int hq, int hkv, int d, int cp,
              int causal, double scale, void* stream, int64_t lse_stride = -1, const CpGeom* packed = nullptr,
-             const CpGeom* ranked = nullptr) {
+             const CpGeom* ranked = nullptr, uint64_t producer_limit_ns = kWaitLimitNs) {
   CUtensorMap maps[4];
   BwdArgs args;
   DeviceInfo* di = nullptr;
   const int rc = prepare_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, b, s, hq, hkv, d, cp,
-                             causal, double(scale), maps, &args, &di, lse_stride, packed, ranked);
+                             causal, double(scale), maps, &args, &di, lse_stride, packed, ranked, producer_limit_ns);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (producer_limit_ns != kWaitLimitNs)  // the abort self-test (d = 128, checked there)
+    return launch_bwd<128, true>(maps[0], maps[1], maps[2], maps[3], args, di, st);
   return d == 128 ? launch_bwd<128>(maps[0], maps[1], maps[2], maps[3], args, di, st)
                   : launch_bwd<64>(maps[0], maps[1], maps[2], maps[3], args, di, st);
 }
@@ -777,6 +786,7 @@ extern "C" int cpattn_bwd_noalloc(const void* q, const void* k, const void* v, c
   args.scale = float(1.0 / std::sqrt(double(d)));
   args.scale_log2 = float(1.4426950408889634 / std::sqrt(double(d)));
   args.status = di->status;
+  args.producer_limit_ns = kWaitLimitNs;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return d == 128 ? launch_bwd<128>(tq, tk, tv, tdo, args, di, st) : launch_bwd<64>(tq, tk, tv, tdo, args, di, st);
 }
@@ -819,6 +829,26 @@ extern "C" int cpattn_selftest_wait_timeout(unsigned long long limit_ns, void* s
   if (rc) return rc;
   cpattn_selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(di->status, limit_ns);
   return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_LAUNCH_FAILED;
+}
+
+// Self-test of the abort path in the attention kernels themselves: the fused
+// forward, then the backward's three stages, with the producers' waits for
+// free buffers limited to limit_ns. A producer gives up at its first wait that
+// does not complete at once, raises the CTA's abort flag and records its bit;
+// the other roles leave at their next wait; before the CTA frees anything,
+// every role waits (with the normal limit) for the copies and MMAs it issued.
+// Nothing faults or hangs; the outputs are left incomplete.
+extern "C" int cpattn_selftest_abort(const void* q, const void* k, const void* v, void* o, float* lse,
+                                     const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                                     size_t workspace_bytes, int b, int s, int hq, int hkv, int d, int cp,
+                                     unsigned long long limit_ns, void* stream) {
+  if (limit_ns == 0 || limit_ns >= kWaitLimitNs) return CPATTN_ERR_INVALID_ARG;
+  // the self-test kernels are built for d = 128 with head pairs sharing K/V
+  if (d != 128 || hkv < 1 || hq % hkv != 0 || (hq / hkv) % 2 != 0) return CPATTN_ERR_INVALID_ARG;
+  int rc = fwd_impl(q, k, v, o, lse, b, s, hq, hkv, d, cp, 1, default_scale(d), stream, -1, nullptr, 0, 0, limit_ns);
+  if (rc) return rc;
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, b, s, hq, hkv, d, cp, 1,
+                  default_scale(d), stream, -1, nullptr, nullptr, limit_ns);
 }
 
 extern "C" int cpattn_device_status(void* stream, int* status) {

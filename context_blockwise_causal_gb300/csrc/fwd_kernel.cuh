@@ -60,6 +60,9 @@ struct FwdArgs {
   int step;          // step form: the CP step computed
   float scale_log2;  // log2(e) * the softmax scale
   unsigned int* status;
+  // time limit of the producer's waits for free buffers: kWaitLimitNs, or a
+  // short one in the abort self-test (cpattn_selftest_abort)
+  uint64_t producer_limit_ns;
 };
 
 // K/V ring of kRing slots. When the two sub-tiles share K/V a key tile takes
@@ -107,7 +110,9 @@ enum FwdStatusBits : unsigned int {
 // its LSE ("大模型面试宝典 · Megatron-LM 篇", 3.2 step 4, before correction);
 // rows that take no part in the step get O = 0, L = -inf.
 // kTP: units are tile pairs (a.g.tile_pairs), not head pairs.
-template <int D, bool kStep, int kRing, bool kTP>
+// kShortWaits: the producer's waits for free buffers use a.producer_limit_ns
+// (the abort self-test) instead of the compile-time limit.
+template <int D, bool kStep, int kRing, bool kTP, bool kShortWaits = false>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     cpattn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv, const FwdArgs a) {
@@ -173,6 +178,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      const uint64_t plimit = kShortWaits ? a.producer_limit_ns : kWaitLimitNs;
       bool ok = true;
       uint32_t nload = 0;
       int ul = 0;
@@ -187,8 +193,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (w.step_tiles(a.step) == 0) continue;  // no key tile at this step
         }
         if (ul > 0) {
-          ok = mbar_wait_bounded(&q_empty[0], (ul - 1) & 1, abort_flag, kWaitLimitNs) &&
-               mbar_wait_bounded(&q_empty[1], (ul - 1) & 1, abort_flag, kWaitLimitNs);
+          ok = mbar_wait_bounded(&q_empty[0], (ul - 1) & 1, abort_flag, plimit) &&
+               mbar_wait_bounded(&q_empty[1], (ul - 1) & 1, abort_flag, plimit);
           if (!ok) break;
         }
         for (int sub = 0; sub < 2; ++sub) {
@@ -204,7 +210,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         auto load = [&](const CUtensorMap* map, int head, int row) -> bool {
           const uint32_t slot = nload % C::kSlots;
           if (nload >= (uint32_t)C::kSlots) {
-            if (!mbar_wait_bounded(&kv_empty[slot], ((nload / C::kSlots) - 1) & 1, abort_flag, kWaitLimitNs))
+            if (!mbar_wait_bounded(&kv_empty[slot], ((nload / C::kSlots) - 1) & 1, abort_flag, plimit))
               return false;
           }
           mbar_arrive_expect_tx(&kv_full[slot], C::kKVBytes);

@@ -362,6 +362,25 @@ int cpattn_device_status(void* stream, int* status);
  */
 int cpattn_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
 
+/*
+ * Self-test of the abort path of the attention kernels: runs the fused
+ * forward (writing o, lse) and then the three backward stages, as
+ * cpattn_fwd and cpattn_bwd with causal = 1 would, but with the TMA
+ * producers' waits for free buffers limited to limit_ns nanoseconds
+ * (below the kernels' normal 2 s). A producer then gives up mid-run (status bit 0 for the
+ * forward, 8 for the backward); the other roles leave at their next wait
+ * (bits 1-2, 9-10). Before a CTA frees its shared memory and TMEM, each role
+ * waits, with the normal 2 s limit, for the copies and MMAs it issued itself,
+ * so no fault follows; bits 3 and 12 would say that such a wait ran out.
+ * The outputs are left incomplete. Arguments otherwise as cpattn_bwd, with
+ * d = 128 and an even number of query heads per KV head (the self-test
+ * kernels are built for that case only); CPATTN_ERR_INVALID_ARG for other
+ * shapes or a limit outside 1 .. 2e9 - 1 (before any device work).
+ */
+int cpattn_selftest_abort(const void* q, const void* k, const void* v, void* o, float* lse, const void* dout,
+                          void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int b, int s,
+                          int hq, int hkv, int d, int cp, unsigned long long limit_ns, void* stream);
+
 /* Static description of an error code. */
 const char* cpattn_strerror(int code);
 

@@ -763,7 +763,7 @@ struct DqCfg {
 // each warp inside the columns it read. Tensor-core order per key tile:
 //   S(j+1) | dQ(j) | dP(j+1) | S(j+2) | ...
 // so the exponentials of tile j overlap dQ(j-1) and dP(j), and only the dS
-// step is on the tensor core's critical path.
+// step of each warp's first 32 keys lies on the tensor core's critical path.
 template <int D, bool kShortWaits = false>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     cpattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,

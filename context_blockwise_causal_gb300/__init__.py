@@ -107,6 +107,8 @@ def library():
         lib.cpattn_bwd_rank_workspace_bytes.restype = _sz
         lib.cpattn_bwd_rank.argtypes = [_p] * 10 + [_sz] + [_i] * 8 + [ctypes.c_float, _p]
         lib.cpattn_bwd_rank.restype = _i
+        lib.cpattn_bwd_rank_stage.argtypes = [_i] + [_p] * 10 + [_sz] + [_i] * 8 + [ctypes.c_float, _p]
+        lib.cpattn_bwd_rank_stage.restype = _i
         lib.cpattn_zigzag_index.argtypes = [_i, _i, _p]
         lib.cpattn_zigzag_index.restype = _i
         lib.cpattn_device_status.argtypes = [_p, ctypes.POINTER(_i)]
@@ -487,13 +489,16 @@ def cpattn_bwd_rank_workspace_bytes(b, s, hq, hkv, d, cp):
 
 
 def cpattn_bwd_rank(q, k_all, v_all, o, lse, do, cp, rank, causal=True, scale=None, dq=None, dk_part=None,
-                    dv_part=None, workspace=None, stream=None):
+                    dv_part=None, workspace=None, stream=None, stage=None):
     """One rank's backward in a CP group spread over GPUs (all-gather form).
 
     q, o, do: the rank's shard [b, 2c, hq, d]; lse [b, hq, 2c]; k_all, v_all
     every rank's shard [cp, b, 2c, hkv, d]. Returns (dq [b, 2c, hq, d],
     dk_part, dv_part [cp, b, 2c, hkv, d]): the rank's own dQ, and its share
     of every rank's dK/dV, which a reduce-scatter over the group sums.
+    ``stage`` (0, 1 or 2) runs only that stage (cpattn_bwd_rank_stage): the
+    shares are complete after stage 1, dq after stage 2; stages share the
+    workspace, which the caller then passes to each.
     """
     if k_all.dim() != 5:
         raise ValueError("k_all and v_all must be [cp, b, 2c, hkv, d]")
@@ -513,14 +518,17 @@ def cpattn_bwd_rank(q, k_all, v_all, o, lse, do, cp, rank, causal=True, scale=No
         workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
     if not workspace.is_cuda or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous CUDA tensor")
-    rc = library().cpattn_bwd_rank(q.data_ptr(), k_all.data_ptr(), v_all.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                                   do.data_ptr(), dq.data_ptr(), dk_part.data_ptr(), dv_part.data_ptr(),
-                                   workspace.data_ptr(), workspace.numel() * workspace.element_size(), b, s, hq, hkv,
-                                   d, int(cp), int(rank), 1 if causal else 0, 0.0 if scale is None else float(scale),
-                                   _stream_handle(stream, q, k_all, v_all, o, lse, do, dq, dk_part, dv_part,
-                                                  workspace))
+    ptrs = (q.data_ptr(), k_all.data_ptr(), v_all.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+            dq.data_ptr(), dk_part.data_ptr(), dv_part.data_ptr(), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), b, s, hq, hkv, d, int(cp), int(rank), 1 if causal else 0,
+            0.0 if scale is None else float(scale),
+            _stream_handle(stream, q, k_all, v_all, o, lse, do, dq, dk_part, dv_part, workspace))
+    if stage is None:
+        rc = library().cpattn_bwd_rank(*ptrs)
+    else:
+        rc = library().cpattn_bwd_rank_stage(int(stage), *ptrs)
     if rc:
-        raise CpattnError(rc, "cpattn_bwd_rank")
+        raise CpattnError(rc, "cpattn_bwd_rank" if stage is None else "cpattn_bwd_rank_stage")
     return dq, dk_part, dv_part
 
 

@@ -33,7 +33,7 @@ library is missing.
 import torch
 import torch.distributed as dist
 
-from . import cpattn_bwd_rank, cpattn_fwd_rank, cpattn_fwd_rank_step, cpattn_lse_merge
+from . import cpattn_bwd_rank, cpattn_bwd_rank_workspace_bytes, cpattn_fwd_rank, cpattn_fwd_rank_step, cpattn_lse_merge
 
 __all__ = ["CudaKernels", "GroupExchange", "zigzag_shard", "zigzag_unshard", "cp_forward", "cp_backward"]
 
@@ -61,8 +61,24 @@ class CudaKernels:
         return torch.empty_like(q)
 
     @staticmethod
-    def bwd_rank(q, k_all, v_all, o, lse, do, cp, rank, causal, scale):
-        return cpattn_bwd_rank(q, k_all, v_all, o, lse, do, cp, rank, causal=causal, scale=scale)
+    def bwd_rank_shares(q, k_all, v_all, o, lse, do, cp, rank, causal, scale):
+        """The backward's first two stages: the rank's shares of every shard's
+        dK/dV. Returns (dk_part, dv_part, pending); bwd_rank_dq(pending) then
+        runs the dQ stage."""
+        b, local, hq, d = q.shape
+        ws = torch.empty(max(cpattn_bwd_rank_workspace_bytes(b, local * cp, hq, k_all.shape[3], d, cp), 16),
+                         dtype=torch.uint8, device=q.device)
+        dq, dk_part, dv_part = torch.empty_like(q), torch.empty_like(k_all), torch.empty_like(v_all)
+        call = (q, k_all, v_all, o, lse, do, cp, rank)
+        kw = dict(causal=causal, scale=scale, dq=dq, dk_part=dk_part, dv_part=dv_part, workspace=ws)
+        for stage in (0, 1):
+            cpattn_bwd_rank(*call, stage=stage, **kw)
+        return dk_part, dv_part, (call, kw)
+
+    @staticmethod
+    def bwd_rank_dq(pending):
+        call, kw = pending
+        return cpattn_bwd_rank(*call, stage=2, **kw)[0]
 
 
 class GroupExchange:
@@ -88,13 +104,25 @@ class GroupExchange:
         dist.all_gather_into_tensor(out, x, group=self.group)
         return out.view((self.cp,) + tuple(x.shape))
 
-    def reduce_scatter(self, parts):
-        """parts [cp, *shape] on every rank: this rank gets the sum over the
-        ranks of their parts[rank]."""
-        out = torch.empty(tuple(parts.shape[1:]), dtype=parts.dtype, device=parts.device)
-        flat = parts.contiguous().view((parts.shape[0] * parts.shape[1],) + tuple(parts.shape[2:]))
-        dist.reduce_scatter_tensor(out, flat, op=dist.ReduceOp.SUM, group=self.group)
-        return out
+    def reduce_scatter_start(self, *parts):
+        """For each tensor of parts, [cp, *shape] on every rank, start summing
+        over the ranks so that this rank gets the sum of their parts[rank].
+        Returns a handle for reduce_scatter_finish; the reduction runs while
+        the caller issues more work."""
+        outs, works = [], []
+        for p_ in parts:
+            out = torch.empty(tuple(p_.shape[1:]), dtype=p_.dtype, device=p_.device)
+            flat = p_.contiguous().view((p_.shape[0] * p_.shape[1],) + tuple(p_.shape[2:]))
+            works.append(dist.reduce_scatter_tensor(out, flat, op=dist.ReduceOp.SUM, group=self.group, async_op=True))
+            outs.append(out)
+        return outs, works
+
+    @staticmethod
+    def reduce_scatter_finish(handle):
+        outs, works = handle
+        for w_ in works:
+            w_.wait()
+        return outs
 
     def ring_start(self, send, recv):
         """Post one ring hop: each tensor of ``send`` goes to the next rank,
@@ -195,12 +223,16 @@ def cp_backward(q, k, v, o, lse, do, group=None, causal=True, scale=None, kv_all
                 exchange=None):
     """CP attention backward of this rank from its saved o and lse: all-gather
     K and V (unless ``kv_all`` = (k_all, v_all) from cp_forward is given),
-    the rank's kernels, then a reduce-scatter that sums every rank's share of
-    each shard's dK/dV. Returns (dq, dk, dv) of the rank's shards."""
+    the rank's dK/dV kernels, then a reduce-scatter that sums every rank's
+    share of each shard's dK/dV -- running while the rank's dQ kernel
+    computes. Returns (dq, dk, dv) of the rank's shards."""
     exchange = exchange or GroupExchange(group)
     kernels = kernels or CudaKernels
     rank, cp = exchange.rank, exchange.cp
     if kv_all is None:
         kv_all = (exchange.all_gather(k), exchange.all_gather(v))
-    dq, dk_part, dv_part = kernels.bwd_rank(q, kv_all[0], kv_all[1], o, lse, do, cp, rank, causal, scale)
-    return dq, exchange.reduce_scatter(dk_part), exchange.reduce_scatter(dv_part)
+    dk_part, dv_part, pending = kernels.bwd_rank_shares(q, kv_all[0], kv_all[1], o, lse, do, cp, rank, causal, scale)
+    handle = exchange.reduce_scatter_start(dk_part, dv_part)
+    dq = kernels.bwd_rank_dq(pending)
+    dk, dv = exchange.reduce_scatter_finish(handle)
+    return dq, dk, dv

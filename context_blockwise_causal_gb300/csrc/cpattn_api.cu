@@ -705,6 +705,28 @@ extern "C" int cpattn_bwd_rank(const void* q, const void* k, const void* v, cons
                   stream, s / cp, nullptr, &g);
 }
 
+extern "C" int cpattn_bwd_rank_stage(int stage, const void* q, const void* k, const void* v, const void* o,
+                                     const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                     void* workspace, size_t workspace_bytes, int b, int s, int hq, int hkv, int d,
+                                     int cp, int rank, int causal, float scale, void* stream) {
+  if (stage < 0 || stage > 2) return CPATTN_ERR_INVALID_ARG;
+  CpGeom g;
+  double sc = 0.0;
+  int rc = rank_scale(scale, d, &sc);
+  if (rc) return rc;
+  if ((rc = rank_geom(b, s, hq, hkv, d, cp, rank, causal, b * (s / cp), &g))) return rc;
+  if (lse && !aligned16(lse)) return CPATTN_ERR_MISALIGNED;
+  CUtensorMap maps[4];
+  BwdArgs args;
+  DeviceInfo* di = nullptr;
+  if ((rc = prepare_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, b, s, hq, hkv, d, cp, causal,
+                        sc, maps, &args, &di, s / cp, nullptr, &g)))
+    return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return d == 128 ? launch_bwd_stage<128>(stage, maps[0], maps[1], maps[2], maps[3], args, di, st)
+                  : launch_bwd_stage<64>(stage, maps[0], maps[1], maps[2], maps[3], args, di, st);
+}
+
 extern "C" int cpattn_bwd_stage(int stage, const void* q, const void* k, const void* v, const void* o,
                                 const float* lse, const void* dout, void* dq, void* dk, void* dv, void* workspace,
                                 size_t workspace_bytes, int b, int s, int hq, int hkv, int d, int cp, int causal,

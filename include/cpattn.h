@@ -324,6 +324,15 @@ int cpattn_bwd_rank(const void* q, const void* k_all, const void* v_all, const v
                     const void* dout, void* dq, void* dk_part, void* dv_part, void* workspace, size_t workspace_bytes,
                     int b, int s, int hq, int hkv, int d, int cp, int rank, int causal, float scale, void* stream);
 
+/* One stage of cpattn_bwd_rank (as cpattn_bwd_stage is of cpattn_bwd): 0 the
+ * row vectors, 1 the shares dk_part/dv_part, 2 dq. After stage 1 the shares
+ * are complete, so their reduce-scatter can run while stage 2 computes dq.
+ * Arguments as cpattn_bwd_rank; stage outside 0..2 -> CPATTN_ERR_INVALID_ARG. */
+int cpattn_bwd_rank_stage(int stage, const void* q, const void* k_all, const void* v_all, const void* o,
+                          const float* lse, const void* dout, void* dq, void* dk_part, void* dv_part,
+                          void* workspace, size_t workspace_bytes, int b, int s, int hq, int hkv, int d, int cp,
+                          int rank, int causal, float scale, void* stream);
+
 /*
  * Host helper: the zigzag index map. Fills global_of_local (HOST memory,
  * cp * 2c int64 values, row-major [cp][2c]) with the global token position

@@ -78,6 +78,15 @@ class OracleKernels:
             cls.lse_merge(o_acc, l_acc, o_i, l_i, o_acc, l_acc, None)
         return o_acc, l_acc
 
+    @classmethod
+    def bwd_rank_shares(cls, q, k_all, v_all, o, lse, do, cp, rank, causal, scale):
+        dq, dk_part, dv_part = cls.bwd_rank(q, k_all, v_all, o, lse, do, cp, rank, causal, scale)
+        return dk_part, dv_part, dq
+
+    @staticmethod
+    def bwd_rank_dq(pending):
+        return pending
+
     @staticmethod
     def bwd_rank(q, k_all, v_all, o, lse, do, cp, rank, causal, scale):
         """The rank's dQ, and its share of every shard's dK/dV: the plain
@@ -125,9 +134,13 @@ class RecordingKernels:
         b, local, hq, d = q.shape
         return torch.zeros(b, local, hq, d, dtype=_F64), torch.zeros(b, hq, local, dtype=_F64)
 
-    def bwd_rank(self, q, k_all, v_all, o, lse, do, cp, rank, causal, scale):
+    def bwd_rank_shares(self, q, k_all, v_all, o, lse, do, cp, rank, causal, scale):
         self.gathered.append((k_all.clone(), v_all.clone()))
         # share of shard j from rank r: 1000 * (r + 1) + j, small integers, so
         # the reduce-scatter's sum is exact in any float type
         parts = torch.stack([torch.full(k_all.shape[1:], 1000.0 * (rank + 1) + j, dtype=_F64) for j in range(cp)])
-        return torch.zeros(q.shape, dtype=_F64), parts, -parts
+        return parts, -parts, torch.zeros(q.shape, dtype=_F64)
+
+    @staticmethod
+    def bwd_rank_dq(pending):
+        return pending

@@ -575,14 +575,23 @@ extern "C" int cpattn_fwd_varlen(const void* q, const void* k, const void* v, vo
     if (!packed_units_fit(g)) return CPATTN_ERR_INVALID_ARG;
     return fwd_impl(q, k, v, o, lse, 1, int(total), hq, hkv, d, cp, causal, sc, stream, total, &g);
   }
-  // more samples than one launch's parameters hold: a launch per sample
-  for (int i = 0; i < nseq; ++i) {
-    const int start = cu_seqlens[i], len = cu_seqlens[i + 1] - cu_seqlens[i];
+  // More samples than one launch's parameters hold: groups of up to
+  // kMaxSeqs consecutive samples, one launch per group. Each group's rows,
+  // its LSE columns (row stride still the packed total) and its sample
+  // offsets are taken relative to its first token.
+  if (hq < 1 || hkv < 1) return CPATTN_ERR_INVALID_ARG;
+  for (int first = 0; first < nseq; first += kMaxSeqs) {
+    const int n = nseq - first < kMaxSeqs ? nseq - first : kMaxSeqs;
+    const int start = cu_seqlens[first], len = cu_seqlens[first + n] - start;
     if (len == 0) continue;
+    int cu[kMaxSeqs + 1];
+    for (int i = 0; i <= n; ++i) cu[i] = cu_seqlens[first + i] - start;
+    const CpGeom g = packed_geom(cu, n, hq, hkv, cp, causal);
+    if (!packed_units_fit(g)) return CPATTN_ERR_INVALID_ARG;
     const size_t qo = size_t(start) * hq * d * 2, ko = size_t(start) * hkv * d * 2;
     const int rc = fwd_impl(static_cast<const uint8_t*>(q) + qo, static_cast<const uint8_t*>(k) + ko,
                             static_cast<const uint8_t*>(v) + ko, static_cast<uint8_t*>(o) + qo, lse + start, 1, len,
-                            hq, hkv, d, cp, causal, sc, stream, total);
+                            hq, hkv, d, cp, causal, sc, stream, total, &g);
     if (rc) return rc;
   }
   return CPATTN_OK;
@@ -590,16 +599,18 @@ extern "C" int cpattn_fwd_varlen(const void* q, const void* k, const void* v, vo
 
 extern "C" size_t cpattn_bwd_varlen_workspace_bytes(const int* cu_seqlens, int nseq, int hq, int hkv, int d, int cp) {
   if (check_cu(cu_seqlens, nseq, cp) < 0 || hq < 1 || hkv < 1 || hq % hkv || (d != 64 && d != 128)) return 0;
-  if (nseq <= kMaxSeqs) {
-    const CpGeom g = packed_geom(cu_seqlens, nseq, hq, hkv, cp, 1);
-    return g.tpc > 0 ? bwd_layout_tiles(nseq, g.tpc, hq, cp).total : 16;
-  }
-  size_t need = 0;
-  for (int i = 0; i < nseq; ++i) {
-    const int len = cu_seqlens[i + 1] - cu_seqlens[i];
-    if (len == 0) continue;
-    const size_t n = bwd_layout(1, len, hq, d, cp).total;
-    need = n > need ? n : need;
+  // one launch per group of up to kMaxSeqs samples; the groups share the
+  // workspace, so it is sized for the largest
+  size_t need = 16;
+  for (int first = 0; first < nseq; first += kMaxSeqs) {
+    const int n = nseq - first < kMaxSeqs ? nseq - first : kMaxSeqs;
+    int cu[kMaxSeqs + 1];
+    for (int i = 0; i <= n; ++i) cu[i] = cu_seqlens[first + i] - cu_seqlens[first];
+    const CpGeom g = packed_geom(cu, n, hq, hkv, cp, 1);
+    if (g.tpc > 0) {
+      const size_t b = bwd_layout_tiles(n, g.tpc, hq, cp).total;
+      need = b > need ? b : need;
+    }
   }
   return need;
 }
@@ -623,17 +634,24 @@ extern "C" int cpattn_bwd_varlen(const void* q, const void* k, const void* v, co
     return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, 1, int(total), hq, hkv, d, cp,
                     causal, sc, stream, total, &g);
   }
-  // More samples than one launch's parameters hold: a launch per sample,
-  // one after another on the stream, sharing the workspace.
-  for (int i = 0; i < nseq; ++i) {
-    const int start = cu_seqlens[i], len = cu_seqlens[i + 1] - cu_seqlens[i];
+  // More samples than one launch's parameters hold: groups of up to
+  // kMaxSeqs consecutive samples (as in the forward), one after another on
+  // the stream, sharing the workspace.
+  if (hq < 1 || hkv < 1) return CPATTN_ERR_INVALID_ARG;
+  for (int first = 0; first < nseq; first += kMaxSeqs) {
+    const int n = nseq - first < kMaxSeqs ? nseq - first : kMaxSeqs;
+    const int start = cu_seqlens[first], len = cu_seqlens[first + n] - start;
     if (len == 0) continue;
+    int cu[kMaxSeqs + 1];
+    for (int i = 0; i <= n; ++i) cu[i] = cu_seqlens[first + i] - start;
+    const CpGeom g = packed_geom(cu, n, hq, hkv, cp, causal);
+    if (!packed_units_fit(g)) return CPATTN_ERR_INVALID_ARG;
     const size_t qo = size_t(start) * hq * d * 2, ko = size_t(start) * hkv * d * 2;
     const int rc = bwd_impl(static_cast<const uint8_t*>(q) + qo, static_cast<const uint8_t*>(k) + ko,
                             static_cast<const uint8_t*>(v) + ko, static_cast<const uint8_t*>(o) + qo, lse + start,
                             static_cast<const uint8_t*>(dout) + qo, static_cast<uint8_t*>(dq) + qo,
                             static_cast<uint8_t*>(dk) + ko, static_cast<uint8_t*>(dv) + ko, workspace,
-                            workspace_bytes, 1, len, hq, hkv, d, cp, causal, sc, stream, total);
+                            workspace_bytes, 1, len, hq, hkv, d, cp, causal, sc, stream, total, &g);
     if (rc) return rc;
   }
   return CPATTN_OK;

@@ -155,11 +155,11 @@ int cpattn_lse_merge(const float* o_a, const float* lse_a, const float* o_b, con
  *   scale:      0 selects 1/sqrt(d); otherwise as cpattn_fwd_ex.
  * Up to 512 samples run in one launch per kernel (the offsets travel as
  * kernel parameters; work units are dealt longest tile first across all
- * samples); with more samples each sample is launched on its own, one after
- * another on `stream`. cpattn_bwd_varlen needs a workspace of
- * cpattn_bwd_varlen_workspace_bytes(...) bytes (per sample two fp32 vectors
- * padded to the longest sample's tiles; for more than 512 samples, the
- * longest sample's alone). Errors as cpattn_fwd / cpattn_bwd; malformed
+ * samples); more samples run as consecutive groups of up to 512, one launch
+ * per group and kernel, one after another on `stream`. cpattn_bwd_varlen
+ * needs a workspace of cpattn_bwd_varlen_workspace_bytes(...) bytes (per
+ * sample of a group two fp32 vectors padded to the group's longest sample's
+ * tiles; the largest group's). Errors as cpattn_fwd / cpattn_bwd; malformed
  * offsets -> CPATTN_ERR_INVALID_ARG.
  */
 int cpattn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,

@@ -98,18 +98,21 @@ def _packed_case(lens, hq, hkv, d, seed):
 
 @pytest.mark.parametrize("cp,hq,hkv,d", [(1, 4, 2, 64), (2, 2, 1, 128)])
 def test_more_samples_than_one_launch_holds(cp, hq, hkv, d):
-    """More than 512 samples: the library falls back to one launch per sample,
-    each addressing its rows, its LSE columns (lse + start, row stride the
-    packed total) and the shared workspace itself. 600 samples of 0..64
-    tokens; with cp = 1 the lengths are even but not all multiples of 4, so
-    many samples start at an LSE column that is not 16-byte aligned. Every
-    element against the oracle."""
+    """More than 512 samples: the library runs consecutive groups of up to
+    512, one launch per group, each addressing its rows, its LSE columns
+    (lse + the group's first token, row stride the packed total), its sample
+    offsets relative to that token and the shared workspace itself. 600
+    samples of 0..64 tokens; with cp = 1 the lengths are even but not all
+    multiples of 4, so the second group starts at an LSE column that need not
+    be 16-byte aligned. Every element against the oracle."""
     g = torch.Generator(device="cpu").manual_seed(600 + cp)
     unit = 2 * cp
     lens = [int(x) * unit for x in torch.randint(0, 64 // unit + 1, (600,), generator=g)]
     lens[0], lens[1], lens[7] = 0, unit, 64  # an empty sample first, a shortest one, a longest one
+    if cp == 1 and sum(lens[:512]) % 4 == 0:  # the second group's first LSE column off a 16-byte boundary
+        lens[2] += 2 if lens[2] < 64 else -2
     cu, q, k, v, do = _packed_case(lens, hq, hkv, d, seed=700 + cp)
-    assert len(lens) > 512 and (cp != 1 or any(c % 4 for c in cu))
+    assert len(lens) > 512 and (cp != 1 or cu[512] % 4 != 0)
     qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
     o, lse = cpattn_fwd_varlen(qd, kd, vd, cu, cp)
     dq, dk, dv = cpattn_bwd_varlen(qd, kd, vd, o, lse, dod, cu, cp)

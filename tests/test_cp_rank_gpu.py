@@ -188,3 +188,56 @@ def test_driver_with_a_one_rank_nccl_group():
                 assert torch.equal(a, b_)
     finally:
         dist.destroy_process_group()
+
+
+def _random_rank_geometries(n, seed):
+    """Half of them with odd head groups and an even number of tiles per
+    chunk, where the forward pairs query tiles of one head."""
+    import random
+    rng = random.Random(seed)
+    out = []
+    while len(out) < n:
+        cp = rng.randint(2, 4)
+        c = rng.randint(1, 300)
+        b = rng.randint(1, 2)
+        hkv = rng.randint(1, 2)
+        hq = hkv * rng.randint(1, 4)
+        tile_pairs = (hq // hkv) % 2 == 1 and ((c + 127) // 128) % 2 == 0
+        if b * 2 * cp * c * hq > 8192 or tile_pairs != (len(out) % 2 == 0):
+            continue
+        out.append((b, 2 * cp * c, hq, hkv, rng.choice([64, 128]), cp, rng.random() < 0.75))
+    return out
+
+
+@pytest.mark.parametrize("b,s,hq,hkv,d,cp,causal", _random_rank_geometries(6, seed=23))
+def test_rank_local_random_geometries_match_single_gpu_rows(b, s, hq, hkv, d, cp, causal):
+    """Seeded random geometries (ragged chunks, head groups 1-4 -- tile pairs
+    among them --, d 64/128, either mask): every rank's forward, step results
+    and dQ bit for bit against the single-GPU launches' rows, its dK/dV shares
+    summed over the ranks within the backward's tolerance."""
+    w = Workload("rank_rand", b=b, s=s, hq=hq, hkv=hkv, d=d, cp=cp, causal=causal, backward=True, seed=s + 31 * hq)
+    x = make_inputs(w, device="cuda")
+    o, lse = cpattn_fwd(x["q"], x["k"], x["v"], cp, causal=causal)
+    dq, dk, dv = cpattn_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], cp, causal=causal)
+    steps = [cpattn_fwd_step(x["q"], x["k"], x["v"], cp, i, causal=causal) for i in range(cp)]
+    sh = {n: [zigzag_shard(t, cp, r) for r in range(cp)] for n, t in x.items()}
+    k_all, v_all = torch.stack(sh["k"]), torch.stack(sh["v"])
+    dk_sum = torch.zeros(k_all.shape, device="cuda")
+    dv_sum = torch.zeros(v_all.shape, device="cuda")
+    for r in range(cp):
+        o_r, l_r = cpattn_fwd_rank(sh["q"][r], k_all, v_all, cp, r, causal=causal)
+        assert torch.equal(o_r, zigzag_shard(o, cp, r)) and torch.equal(l_r, zigzag_shard(lse, cp, r, dim=2))
+        for i in range(cp):
+            j = (r - i) % cp
+            op, lp = cpattn_fwd_rank_step(sh["q"][r], sh["k"][j], sh["v"][j], cp, r, i, causal=causal)
+            assert torch.equal(op, zigzag_shard(steps[i][0], cp, r)) and torch.equal(
+                lp, zigzag_shard(steps[i][1], cp, r, dim=2)), (r, i)
+        dq_r, dk_p, dv_p = cpattn_bwd_rank(sh["q"][r], k_all, v_all, o_r, l_r, sh["do"][r], cp, r, causal=causal)
+        assert torch.equal(dq_r, zigzag_shard(dq, cp, r))
+        dk_sum += dk_p.float()
+        dv_sum += dv_p.float()
+    torch.cuda.synchronize()
+    assert cpattn_device_status() == 0
+    for r in range(cp):
+        assert _rel(dk_sum[r], zigzag_shard(dk, cp, r).float()) <= REL_L2
+        assert _rel(dv_sum[r], zigzag_shard(dv, cp, r).float()) <= REL_L2

@@ -444,6 +444,47 @@ def run_ours(args, w):
     varlen = {"mixed": packed([w.s // 2, w.s // 4, w.s // 8, w.s // 16, w.s // 16]),
               "short": packed([2048] * (w.s // 2048))}
 
+    # ---- one CP group spread over GPUs, its compute side on this GPU: each
+    # rank's forward (all-gather form) and backward on its shard, one rank
+    # after another; the slowest rank bounds a group step. No exchange is
+    # timed (one GPU here); the all-gathered K/V are built locally.
+    cp_ranks = None
+    if not args.no_cp_ranks and w.cp > 1:
+        from context_blockwise_causal_gb300 import cpattn_bwd_rank, cpattn_fwd_rank
+        from context_blockwise_causal_gb300.cp_group import zigzag_shard
+
+        sh = {n: [zigzag_shard(t, w.cp, r) for r in range(w.cp)] for n, t in (("q", q), ("k", k), ("v", v), ("do", do))}
+        k_all, v_all = torch.stack(sh["k"]), torch.stack(sh["v"])
+        per = []
+        for r in range(w.cp):
+            o_r, l_r = cpattn_fwd_rank(sh["q"][r], k_all, v_all, w.cp, r, causal=w.causal, stream=stream)
+            g_r = cpattn_bwd_rank(sh["q"][r], k_all, v_all, o_r, l_r, sh["do"][r], w.cp, r, causal=w.causal,
+                                  stream=stream)
+            tf, tb = [], []
+            for _ in range(3):
+                e0c, e1c, e2c = ev(), ev(), ev()
+                e0c.record(stream)
+                cpattn_fwd_rank(sh["q"][r], k_all, v_all, w.cp, r, causal=w.causal, o=o_r, lse=l_r, stream=stream)
+                e1c.record(stream)
+                cpattn_bwd_rank(sh["q"][r], k_all, v_all, o_r, l_r, sh["do"][r], w.cp, r, causal=w.causal,
+                                dq=g_r[0], dk_part=g_r[1], dv_part=g_r[2], stream=stream)
+                e2c.record(stream)
+                e2c.synchronize()
+                tf.append(e0c.elapsed_time(e1c))
+                tb.append(e1c.elapsed_time(e2c))
+            per.append({"rank": r, "fwd_ms": statistics.median(tf), "bwd_ms": statistics.median(tb)})
+        if cpattn_device_status(stream) != 0:
+            raise RuntimeError("a kernel reported a timeout in the per-rank run")
+        mf = max(p_["fwd_ms"] for p_ in per)
+        mb = max(p_["bwd_ms"] for p_ in per)
+        cp_ranks = {"ranks": w.cp, "per_rank": per, "max_fwd_ms": mf, "max_bwd_ms": mb,
+                    "compute_scaling": {"fwd": kern_ms["fwd"] / w.cp / mf,
+                                        "bwd": (kern_ms["bwd_pre"] + kern_ms["bwd_dkdv"] + kern_ms["bwd_dq"]) / w.cp / mb},
+                    "what": "each rank's cpattn_fwd_rank and cpattn_bwd_rank on its zigzag shard with every rank's "
+                            "K/V gathered locally, on this one GPU; compute_scaling = (fused single-GPU time / cp) / "
+                            "slowest rank's time; the K/V exchange is not timed"}
+        del sh, k_all, v_all
+
     # ---- the forward on the other configurations (each: warm-up, then the
     # median of several launches, L2 flushed before each)
     sweep = {}
@@ -525,6 +566,8 @@ def run_ours(args, w):
         rope["hbm_frac"] = rope["gbs"] / peaks["hbm_gbs"]
         line["rope"] = rope
         line["varlen"] = varlen
+        if cp_ranks is not None:
+            line["cp_ranks"] = cp_ranks
         if sweep:
             for v_ in sweep.values():
                 v_["frac_burst"] = v_["fwd_tflops"] / peaks["bf16_tflops"]
@@ -565,6 +608,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-unfused", action="store_true", help="skip timing the unfused forward")
     ap.add_argument("--no-sweep", action="store_true", help="skip the forward on the other configurations")
+    ap.add_argument("--no-cp-ranks", action="store_true",
+                    help="skip timing each CP rank's share of the workload (the multi-GPU form's compute)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

@@ -51,6 +51,8 @@ struct CpGeom {
   int rank = -1;         // rank-local form: the rank whose queries the call computes
   int kv_rank_rows = 0;  // rank-local form: rows between consecutive ranks' K/V shards
   int tile_pairs = 0;    // forward units pair two query tiles of one head (see fwd_decode_unit)
+  int tp_block = 0;      // tile pairs: (sequence, query head) combinations per unit block (0: one block)
+  int tp_slots = 0;      // tile pairs: unit slots per block (its units, then empty slots)
   int cu[kMaxSeqs + 1];     // packed: sample offsets
   int tile0[kMaxSeqs + 1];  // packed: query tiles (2cp * tpc_i) of the samples before sample i
 };
@@ -177,7 +179,32 @@ __host__ __device__ inline bool use_tile_pairs(const CpGeom& g) {
 }
 
 __host__ __device__ inline int fwd_num_units(const CpGeom& g) {
+  if (g.tile_pairs && g.tp_block > 0) return (g.b * g.hq + g.tp_block - 1) / g.tp_block * g.tp_slots;
   return g.tile_pairs ? g.hq * (query_tiles(g) / 2) : g.npairs * query_tiles(g);
+}
+
+// Tile-pair units in blocks. When the heads' K/V is larger than L2 keeps,
+// units of all heads in flight at once read it from DRAM again and again;
+// the (sequence, query head) combinations are then cut into blocks spanning
+// at most about kv_per_block (sequence, KV head) pairs, numbered block after
+// block, each block longest first. A block is padded with empty slots to a
+// whole number of double rounds of the snake assignment (2 * grid), so each
+// block balances the CTAs' work on its own; a block holds at least 1.5 * grid
+// units, so the padding stays a small part of it. kv_per_block <= 0, or
+// blocks of at least half the pairs, leave one block (no padding).
+__host__ __device__ inline void set_tile_pair_blocks(CpGeom& g, int grid, int kv_per_block) {
+  g.tp_block = 0;
+  g.tp_slots = 0;
+  const int pairs = g.b * g.hkv;
+  const int units_per_pair = (g.hq / g.hkv) * (query_tiles_per_seq(g) / 2);
+  if (!g.tile_pairs || kv_per_block <= 0) return;
+  const int kv_min = (3 * grid + 2 * units_per_pair - 1) / (2 * units_per_pair);
+  if (kv_per_block < kv_min) kv_per_block = kv_min;
+  if (2 * kv_per_block >= pairs) return;
+  const int nblk = (pairs + kv_per_block - 1) / kv_per_block;
+  const int kv = (pairs + nblk - 1) / nblk;  // KV pairs per block, evened out
+  g.tp_block = kv * (g.hq / g.hkv);
+  g.tp_slots = (kv * units_per_pair + 2 * grid - 1) / (2 * grid) * (2 * grid);
 }
 
 // The query tile with global tile index gt of unit U's sequence (U.seq set).
@@ -222,12 +249,31 @@ __host__ __device__ inline FwdUnit fwd_decode_unit_t(const CpGeom& g, int idx) {
   FwdUnit U;
   int gt, pr;
   if constexpr (kTilePairs) {
-    // tiles (u - 1, u), u odd, of one head; longest first by tile u
+    // tiles (u - 1, u), u odd, of one head; longest first by tile u (within
+    // a block of (sequence, head) combinations, see set_tile_pair_blocks)
     const int per = g.b * g.hq;
-    const int lp = query_tiles_per_seq(g) / 2 - 1 - idx / per;
-    const int rest = idx % per;
-    U.seq = rest / g.hq;
-    U.h0 = U.h1 = rest % g.hq;
+    const int qp = query_tiles_per_seq(g) / 2;
+    int lp, combo;
+    if (g.tp_block > 0) {
+      const int blk = idx / g.tp_slots;
+      const int i = idx - blk * g.tp_slots;
+      const int c0 = blk * g.tp_block;
+      const int nc = per - c0 < g.tp_block ? per - c0 : g.tp_block;
+      if (i >= nc * qp) {  // an empty slot
+        U.seq = U.bi = U.tok0 = U.lse_t0 = U.c = U.tpc = U.h0 = U.h1 = U.g0 = U.g1 = 0;
+        U.store1 = false;
+        U.k = U.u = U.half = U.r = U.q_t0 = U.q_valid = U.u0 = U.q_t1 = U.q_valid1 = 0;
+        U.n = 0;
+        return U;
+      }
+      lp = qp - 1 - i / nc;
+      combo = c0 + i % nc;
+    } else {
+      lp = qp - 1 - idx / per;
+      combo = idx % per;
+    }
+    U.seq = combo / g.hq;
+    U.h0 = U.h1 = combo % g.hq;
     U.g0 = U.g1 = U.h0 / (g.hq / g.hkv);
     fill_query_tile(g, U, query_tile_of(g, 2 * lp + 1));
     U.store1 = true;

@@ -97,8 +97,12 @@ CpGeom make_geom(int b, int s, int hq, int hkv, int cp, int causal) {
   return g;
 }
 
+// K/V bytes of the heads whose tile-pair units may be in flight together
+// (see set_tile_pair_blocks): a quarter of L2.
+constexpr int64_t kTilePairKvBudget = 32ll << 20;
+
 template <int D, bool kStep, int kRing, bool kTP, bool kShort = false>
-int launch_fwd_ring(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& args,
+int launch_fwd_ring(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& args_in,
                     DeviceInfo* di, cudaStream_t st) {
   using C = FwdCfg<D, kRing>;
   const int slot =
@@ -114,6 +118,11 @@ int launch_fwd_ring(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensor
     if (cudaFuncGetAttributes(&fa, cpattn_fwd_kernel<D, kStep, kRing, kTP, kShort>) != cudaSuccess) return CPATTN_ERR_CUDA;
     if (fa.numRegs != kFwdLaunchRegs) return CPATTN_ERR_LAUNCH_FAILED;
     di->fwd_attr[slot].store(true, std::memory_order_release);
+  }
+  FwdArgs args = args_in;
+  if (kTP) {  // K/V of one (sequence, KV head): s tokens of K and of V
+    const int64_t per_pair = 4ll * args.g.s * D;
+    set_tile_pair_blocks(args.g, di->num_sms, int(kTilePairKvBudget / per_pair));
   }
   const int units = fwd_num_units(args.g);
   const int grid = units < di->num_sms ? units : di->num_sms;

@@ -149,8 +149,9 @@ static int check(const CpGeom& g, int grid) {
   int prev_n = 1 << 30, prev_seq = -1;
   for (int idx = 0; idx < nu; ++idx) {
     const FwdUnit U = fwd_decode_unit(g, idx);
-    if (U.n == 0) continue;  // an empty packed sample
+    if (U.n == 0) continue;  // an empty packed sample, or an empty slot of a unit block
     if (g.nseq > 0 && U.seq != prev_seq) prev_n = 1 << 30;  // packed samples come one after another
+    if (g.tp_block > 0 && idx % g.tp_slots == 0) prev_n = 1 << 30;  // unit blocks come one after another
     prev_seq = U.seq;
     if (g.causal && U.n > prev_n) { printf("units not in longest-first order at %d\n", idx); return 1; }
     prev_n = U.n;
@@ -233,7 +234,7 @@ static int check(const CpGeom& g, int grid) {
 
 // The rank-local form: each rank's forward (all-gather form and ring steps),
 // dQ and key-tile backward units, mapped back to sequence rows.
-static int check_rank(const CpGeom& base, int grid) {
+static int check_rank(const CpGeom& base, int grid, int kv_per_block) {
   const Rows R = rows_of(base);
   const size_t T = R.total;
   std::vector<unsigned char> fwd(size_t(base.hq) * T * T, 0), ring(fwd.size(), 0), dq(fwd.size(), 0),
@@ -243,10 +244,12 @@ static int check_rank(const CpGeom& base, int grid) {
     CpGeom g = base;
     g.rank = r;
     g.kv_rank_rows = g.b * 2 * g.c;
+    set_tile_pair_blocks(g, grid, kv_per_block);  // as the library sets it, per launch
     const RowMap gathered{g.b * 2 * g.c, g.cp * g.b * 2 * g.c, -1};
     // ---- forward units: snake assignment, longest first, the rank's tiles only
     const int nu = fwd_num_units(g);
-    if (nu != (g.tile_pairs ? g.hq * g.b * g.tpc : g.npairs * g.b * 2 * g.tpc)) {
+    const int blocks = g.tp_block > 0 ? (g.b * g.hq + g.tp_block - 1) / g.tp_block : 0;
+    if (nu != (blocks ? blocks * g.tp_slots : g.tile_pairs ? g.hq * g.b * g.tpc : g.npairs * g.b * 2 * g.tpc)) {
       printf("rank %d: %d forward units\n", r, nu);
       return 1;
     }
@@ -261,7 +264,9 @@ static int check_rank(const CpGeom& base, int grid) {
       if (seen[i] != 1) { printf("rank %d: unit %d assigned %d times\n", r, i, seen[i]); return 1; }
     int prev_n = 1 << 30;
     for (int idx = 0; idx < nu; ++idx) {
+      if (g.tp_block > 0 && idx % g.tp_slots == 0) prev_n = 1 << 30;
       const FwdUnit U = fwd_decode_unit(g, idx);
+      if (U.n == 0) continue;  // an empty slot of a unit block
       if (U.r != r) { printf("rank %d: unit %d belongs to rank %d\n", r, idx, U.r); return 1; }
       if (g.causal && U.n > prev_n) { printf("rank %d: units not longest-first at %d\n", r, idx); return 1; }
       prev_n = U.n;
@@ -325,7 +330,13 @@ static int check_rank(const CpGeom& base, int grid) {
 
 int main(int argc, char** argv) {
   int fails = 0, i = 1;
+  int kv_per_block = 0;  // "K n": tile-pair unit blocks of n KV pairs for the geometries that follow
   while (i < argc) {
+    if (!strcmp(argv[i], "K") && i + 1 < argc) {
+      kv_per_block = atoi(argv[i + 1]);
+      i += 2;
+      continue;
+    }
     CpGeom g;
     char desc[256];
     int grid;
@@ -367,7 +378,17 @@ int main(int argc, char** argv) {
     }
     g.npairs = (g.hq + 1) / 2;
     g.tile_pairs = use_tile_pairs(g) ? 1 : 0;  // as the library sets it
-    const int rc = ranked ? check_rank(g, grid) : check(g, grid);
+    {
+      CpGeom t = g;
+      if (ranked) t.rank = 0;
+      set_tile_pair_blocks(t, grid, kv_per_block);
+      if (t.tp_block > 0) {
+        const size_t n = strlen(desc);
+        snprintf(desc + n, sizeof desc - n, " [blocks of %d heads, %d slots]", t.tp_block, t.tp_slots);
+      }
+      if (!ranked) g = t;
+    }
+    const int rc = ranked ? check_rank(g, grid, kv_per_block) : check(g, grid);
     printf("%s %s\n", rc ? "FAIL" : "ok", desc);
     fails += rc;
   }

@@ -52,6 +52,35 @@ def checker(tmp_path_factory):
     return exe
 
 
+# tile pairs in unit blocks (b, s, hq, hkv, cp, causal, grid, KV pairs per block): the
+# blocks the library forms for large K/V, forced here on small shapes -- MHA, G = 3,
+# no mask, a ragged second tile
+BLOCKED = [
+    (2, 2048, 8, 8, 4, 1, 7, 3),
+    (2, 1024, 9, 3, 2, 1, 5, 1),
+    (1, 1024, 5, 5, 2, 0, 3, 2),
+    (3, 800, 4, 4, 2, 1, 5, 2),
+    (4, 4096, 4, 4, 4, 1, 19, 2),
+]
+
+
+def test_tile_pair_unit_blocks_cover_every_pair_once(checker):
+    """Blocks change only the order of the forward's units: every allowed pair is
+    still computed once (whole sequence and rank-local form), each block longest
+    first, and the padded slots decode to empty units."""
+    args = []
+    for *g, kv in BLOCKED:
+        args += ["K", str(kv), "U", *map(str, g), "R", *map(str, g)]
+    out = subprocess.run([checker, *args], capture_output=True, text=True)
+    assert out.returncode == 0 and "FAIL" not in out.stdout, out.stdout
+    lines = out.stdout.strip().splitlines()
+    assert len(lines) == 2 * len(BLOCKED) and all(ln.startswith("ok ") for ln in lines)
+    # every whole-sequence geometry forms blocks; a rank's share has fewer
+    # units per head, so some of them stay one block
+    assert all("[blocks of" in ln for ln in lines if "rank-local" not in ln), out.stdout
+    assert sum("[blocks of" in ln for ln in lines if "rank-local" in ln) >= 2, out.stdout
+
+
 # packed samples: lengths (each divisible by 2cp, 0 allowed), hq, hkv, cp, causal, grid
 PACKED = [
     ([512, 256, 1024], 4, 2, 2, 1, 7),

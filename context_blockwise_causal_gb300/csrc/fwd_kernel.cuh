@@ -86,10 +86,10 @@ struct FwdCfg {
   // barriers: q_full[2] q_empty[2] s_full[2] p_full[2] o_full[2] o_empty[2]
   //           drain, kv_full[kSlots] kv_empty[kSlots], p_half[2]
   static constexpr int kNumBars = 15 + 2 * kSlots;
-  // Epilogue staging: 2 KB per softmax warp (32 rows x 64 bytes) to turn its
-  // O stores into whole 64-byte row segments; only where the ring leaves room
-  // (not with the five-slot ring at d = 128).
-  static constexpr int kStageBytes = kRing == fwd_ring<D>(false) ? 8 * 32 * 64 : 0;
+  // Epilogue staging: 4 KB per softmax warp (32 rows x 128 bytes) to turn its
+  // O stores into whole 128-byte lines; only where the ring leaves room (not
+  // with the five-slot ring at d = 128).
+  static constexpr int kStageBytes = kRing == fwd_ring<D>(false) ? 8 * 32 * 128 : 0;
   static constexpr int kOffStage = (kOffBar + kNumBars * 8 + 127) & ~127;
   static constexpr int kOffMisc = kOffStage + kStageBytes;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
@@ -544,37 +544,37 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                                     __uint_as_float(ov[c0 + 2]) * inv, __uint_as_float(ov[c0 + 3]) * inv);
         a.lse[(int64_t(U.bi) * g.hq + h) * a.lse_stride + U.lse_t0 + t] = (m_used + log2f(l)) * 0.69314718055994530942f;
       } else if (!kStep && C::kStageBytes > 0) {
-        // O through the warp's staging buffer, 32 columns at a time: each
-        // thread writes its row's 64 bytes (16-byte pieces at slot k ^ (row & 3),
-        // so neither pass has bank conflicts beyond the minimum), then each
-        // store covers 8 rows x 64 contiguous bytes. Every lane takes part;
-        // rows outside the tile's valid part or of a repeated head are not
-        // written.
+        // O through the warp's staging buffer, 64 columns at a time: each
+        // thread writes its row's 128 bytes (16-byte pieces at slot
+        // k ^ (row & 7), so neither pass has bank conflicts), then each store
+        // covers 4 rows x 128 contiguous bytes, whole lines. Every lane takes
+        // part; rows outside the tile's valid part or of a repeated head are
+        // not written.
         const int h = sub ? U.h1 : U.h0;
         const float inv = 1.f / l;
         const bool write_head = sub == 0 || U.store1;
-        uint4* stg = reinterpret_cast<uint4*>(smem + C::kOffStage + warp * (32 * 64));
+        uint4* stg = reinterpret_cast<uint4*>(smem + C::kOffStage + warp * (32 * 128));
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int c0 = c * 32 + k * 8;
+          for (int k = 0; k < 8; ++k) {
+            const int c0 = c * 64 + k * 8;
             uint4 pkv;
             pkv.x = pack_bf16x2(__uint_as_float(ov[c0 + 0]) * inv, __uint_as_float(ov[c0 + 1]) * inv);
             pkv.y = pack_bf16x2(__uint_as_float(ov[c0 + 2]) * inv, __uint_as_float(ov[c0 + 3]) * inv);
             pkv.z = pack_bf16x2(__uint_as_float(ov[c0 + 4]) * inv, __uint_as_float(ov[c0 + 5]) * inv);
             pkv.w = pack_bf16x2(__uint_as_float(ov[c0 + 6]) * inv, __uint_as_float(ov[c0 + 7]) * inv);
-            stg[lane * 4 + (k ^ (lane & 3))] = pkv;
+            stg[lane * 8 + (k ^ (lane & 7))] = pkv;
           }
           __syncwarp();
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int r = 8 * i + (lane >> 2);  // the warp's row
-            const int part = lane & 3;          // 16-byte piece of the 64
-            const uint4 v = stg[r * 4 + (part ^ (r & 3))];
+          for (int i = 0; i < 8; ++i) {
+            const int r = 4 * i + (lane >> 3);  // the warp's row
+            const int part = lane & 7;          // 16-byte piece of the 128
+            const uint4 v = stg[r * 8 + (part ^ (r & 7))];
             const int trow = wq * 32 + r;       // row within the tile
             if (write_head && trow < q_valid)
-              *reinterpret_cast<uint4*>(a.o + ((int64_t(U.tok0) + q_t + trow) * g.hq + h) * D + c * 32 + part * 8) = v;
+              *reinterpret_cast<uint4*>(a.o + ((int64_t(U.tok0) + q_t + trow) * g.hq + h) * D + c * 64 + part * 8) = v;
           }
           __syncwarp();
         }

@@ -29,6 +29,31 @@ namespace cpattn {
 constexpr int kTile = 128;
 constexpr int kMaxSeqs = 512;  // packed samples per call (their offsets travel as kernel parameters)
 
+// Division by a value fixed for a launch, as a multiply and a shift
+// (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", PLDI 1994): for 0 <= n < 2^31 and 1 <= d <= 2^31, with
+// s = ceil(log2 d) and m = ceil(2^(31+s) / d), which is below 2^32,
+// floor(n / d) = floor(n * m / 2^(31+s)): n*m / 2^(31+s) exceeds n/d by
+// less than 2^-s <= 1/d. The backward's unit decodes run once per work unit
+// in every role of a CTA; a plain integer division there is a long
+// dependent chain.
+struct FastDiv {
+  int d = 1;
+  uint32_t m = 0x80000000u;
+  int shift = 31;
+  __host__ __device__ int div(int n) const { return int((uint64_t(uint32_t(n)) * m) >> shift); }
+  __host__ __device__ int mod(int n) const { return n - div(n) * d; }
+};
+__host__ __device__ inline FastDiv make_fastdiv(int d) {
+  FastDiv f;
+  f.d = d;
+  int s = 0;
+  while ((int64_t(1) << s) < d) ++s;
+  f.m = uint32_t(((uint64_t(1) << (31 + s)) + uint64_t(d) - 1) / uint64_t(d));
+  f.shift = 31 + s;
+  return f;
+}
+
 // Geometry of a call. Either a uniform batch (nseq == 0: b sequences of s
 // tokens, chunk length c, tpc tiles per chunk) or packed samples (nseq > 0:
 // b == 1, s == total tokens, sample i is tokens [cu[i], cu[i+1]) with its own
@@ -53,9 +78,21 @@ struct CpGeom {
   int tile_pairs = 0;    // forward units pair two query tiles of one head (see fwd_decode_unit)
   int tp_block = 0;      // tile pairs: (sequence, query head) combinations per unit block (0: one block)
   int tp_slots = 0;      // tile pairs: unit slots per block (its units, then empty slots)
+  // divisors of the backward's unit decodes (set_fast_divs; set again
+  // whenever b, hq, hkv or tpc change)
+  FastDiv fd_hq, fd_hkv, fd_G, fd_tpc, fd_bhq, fd_bhkv;
   int cu[kMaxSeqs + 1];     // packed: sample offsets
   int tile0[kMaxSeqs + 1];  // packed: query tiles (2cp * tpc_i) of the samples before sample i
 };
+
+__host__ __device__ inline void set_fast_divs(CpGeom& g) {
+  g.fd_hq = make_fastdiv(g.hq);
+  g.fd_hkv = make_fastdiv(g.hkv);
+  g.fd_G = make_fastdiv(g.hq / g.hkv);
+  g.fd_tpc = make_fastdiv(g.tpc > 0 ? g.tpc : 1);
+  g.fd_bhq = make_fastdiv(g.b * g.hq);
+  g.fd_bhkv = make_fastdiv(g.b * g.hkv);
+}
 
 // Rows of one sequence on the query side: the whole sequence, or one rank's
 // two chunks in the rank-local form.
@@ -92,6 +129,7 @@ __host__ __device__ inline void finish_packed(CpGeom& g) {
     g.tpc = tpc > g.tpc ? tpc : g.tpc;
     g.tile0[i + 1] = g.tile0[i] + 2 * g.cp * tpc;
   }
+  set_fast_divs(g);
 }
 
 // Packed samples: the sample holding global tile position p (a binary
@@ -162,9 +200,12 @@ __host__ __device__ inline int query_tiles(const CpGeom& g) {
 // Global tile index of the query tile of local position lt (the unit order
 // below walks it from the end): every tile of the sequence, or in the
 // rank-local form the rank's tiles, chunk `rank` first.
+// kFast: divide with the geometry's FastDiv (the backward's decodes; the
+// forward's measured slower with it, its register budget being tighter).
+template <bool kFast = false>
 __host__ __device__ inline int query_tile_of(const CpGeom& g, int lt) {
   if (g.rank < 0) return lt;
-  return (lt < g.tpc ? g.rank : 2 * g.cp - 1 - g.rank) * g.tpc + lt % g.tpc;
+  return (lt < g.tpc ? g.rank : 2 * g.cp - 1 - g.rank) * g.tpc + (kFast ? g.fd_tpc.mod(lt) : lt % g.tpc);
 }
 __host__ __device__ inline int query_tiles_per_seq(const CpGeom& g) {
   return g.rank >= 0 ? 2 * g.tpc : 2 * g.cp * g.tpc;
@@ -208,6 +249,7 @@ __host__ __device__ inline void set_tile_pair_blocks(CpGeom& g, int grid, int kv
 }
 
 // The query tile with global tile index gt of unit U's sequence (U.seq set).
+template <bool kFast = false>
 __host__ __device__ inline void fill_query_tile(const CpGeom& g, FwdUnit& U, int gt) {
   const SeqGeom q = seq_geom(g, U.seq);
   U.bi = g.nseq > 0 ? 0 : U.seq;
@@ -221,8 +263,13 @@ __host__ __device__ inline void fill_query_tile(const CpGeom& g, FwdUnit& U, int
     U.n = 0;
     return;
   }
-  U.k = gt / U.tpc;
-  U.u = gt % U.tpc;
+  if (kFast && g.nseq == 0) {  // uniform batch: every sequence has g.tpc tiles per chunk
+    U.k = g.fd_tpc.div(gt);
+    U.u = gt - U.k * U.tpc;
+  } else {
+    U.k = gt / U.tpc;
+    U.u = gt % U.tpc;
+  }
   U.half = U.k >= g.cp ? 1 : 0;
   U.r = U.half ? 2 * g.cp - 1 - U.k : U.k;
   U.q_t0 = q_chunk_row(g, U.k, U.c) + U.u * kTile;
@@ -324,15 +371,15 @@ __host__ __device__ inline FwdUnit dq_decode_unit(const CpGeom& g, int idx) {
     gt = (g.tile0[U.seq + 1] - g.tile0[U.seq]) - 1 - local;
     U.h0 = U.h1 = idx % g.hq;
   } else {
-    const int per = g.b * g.hq;
-    gt = query_tile_of(g, query_tiles_per_seq(g) - 1 - idx / per);
-    const int rest = idx % per;
-    U.seq = rest / g.hq;
-    U.h0 = U.h1 = rest % g.hq;
+    const int q = g.fd_bhq.div(idx);
+    gt = query_tile_of<true>(g, query_tiles_per_seq(g) - 1 - q);
+    const int rest = idx - q * (g.b * g.hq);
+    U.seq = g.fd_hq.div(rest);
+    U.h0 = U.h1 = rest - U.seq * g.hq;
   }
-  U.g0 = U.g1 = U.h0 / (g.hq / g.hkv);
+  U.g0 = U.g1 = g.fd_G.div(U.h0);
   U.store1 = false;
-  fill_query_tile(g, U, gt);
+  fill_query_tile<true>(g, U, gt);
   return U;
 }
 
@@ -506,11 +553,10 @@ __host__ __device__ inline BwdUnit bwd_decode_unit(const CpGeom& g, int idx) {
     U.seq = packed_sample_of(g, idx / g.hkv, gt);
     U.g = idx % g.hkv;
   } else {
-    const int per = g.b * g.hkv;
-    gt = idx / per;
-    const int rest = idx % per;
-    U.seq = rest / g.hkv;
-    U.g = rest % g.hkv;
+    gt = g.fd_bhkv.div(idx);
+    const int rest = idx - gt * (g.b * g.hkv);
+    U.seq = g.fd_hkv.div(rest);
+    U.g = rest - U.seq * g.hkv;
   }
   U.bi = g.nseq > 0 ? 0 : U.seq;
   const SeqGeom q = seq_geom(g, U.seq);
@@ -523,8 +569,13 @@ __host__ __device__ inline BwdUnit bwd_decode_unit(const CpGeom& g, int idx) {
     U.kc = U.v = U.k_t0 = U.k_valid = U.nq = U.items = 0;
     return U;
   }
-  U.kc = gt / U.tpc;
-  U.v = gt % U.tpc;
+  if (g.nseq == 0) {
+    U.kc = g.fd_tpc.div(gt);
+    U.v = gt - U.kc * U.tpc;
+  } else {
+    U.kc = gt / U.tpc;
+    U.v = gt % U.tpc;
+  }
   U.k_t0 = kv_chunk_row(g, U.kc, U.c) + U.v * kTile;
   const int rem = U.c - U.v * kTile;
   U.k_valid = rem < kTile ? rem : kTile;
@@ -539,21 +590,29 @@ __host__ __device__ inline BwdUnit bwd_decode_unit(const CpGeom& g, int idx) {
 // Walks the query tiles of a backward unit, last tile first (in the
 // rank-local form only the rank's own tiles: chunk 2cp-1-rank, then chunk
 // rank, each from its end).
+// The position is kept as (chunk, tile) and stepped down one tile at a time
+// (no division per tile).
 struct QWalk {
-  int tpc, lo, gt_k, causal, cp, rank, lt;
+  int tpc, lo, gt_k, causal, low_chunk, left;
+  int ch, t;  // the next tile: chunk and tile within it
 
   __host__ __device__ QWalk(const CpGeom& g, const BwdUnit& U)
-      : tpc(U.tpc), lo(g.causal ? U.gt : 0), gt_k(U.gt), causal(g.causal), cp(g.cp), rank(g.rank),
-        lt(g.rank >= 0 ? 2 * U.tpc - 1 : 2 * g.cp * U.tpc - 1) {}
+      : tpc(U.tpc), lo(g.causal ? U.gt : 0), gt_k(U.gt), causal(g.causal),
+        low_chunk(g.rank >= 0 ? g.rank : -1), left(g.rank >= 0 ? 2 * U.tpc : 2 * g.cp * U.tpc),
+        ch(g.rank >= 0 ? 2 * g.cp - 1 - g.rank : 2 * g.cp - 1), t(U.tpc - 1) {}
 
   __host__ __device__ bool next(int& chunk, int& tile, bool& is_diag) {
-    if (lt < 0) return false;
-    const int gt = rank >= 0 ? (lt < tpc ? rank : 2 * cp - 1 - rank) * tpc + lt % tpc : lt;
+    if (left <= 0) return false;
+    const int gt = ch * tpc + t;
     if (gt < lo) return false;  // tiles come in decreasing global order
-    chunk = gt / tpc;
-    tile = gt % tpc;
+    chunk = ch;
+    tile = t;
     is_diag = causal && gt == gt_k;
-    --lt;
+    --left;
+    if (--t < 0) {  // on to the chunk before: the previous one, or the rank's lower chunk
+      t = tpc - 1;
+      ch = low_chunk >= 0 ? low_chunk : ch - 1;
+    }
     return true;
   }
 };

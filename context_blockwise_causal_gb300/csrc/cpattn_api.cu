@@ -94,6 +94,7 @@ CpGeom make_geom(int b, int s, int hq, int hkv, int cp, int causal) {
   g.tpc = (g.c + kTile - 1) / kTile;
   g.npairs = (hq + 1) / 2;
   g.tile_pairs = use_tile_pairs(g) ? 1 : 0;
+  set_fast_divs(g);
   return g;
 }
 

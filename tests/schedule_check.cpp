@@ -328,7 +328,44 @@ static int check_rank(const CpGeom& base, int grid, int kv_per_block) {
          verify(base, R, dq, "rank dq") || verify(base, R, bwd, "rank backward");
 }
 
+// FastDiv against plain division: every divisor up to 5000 with dividends
+// around each multiple and at the ends of the range, and pseudo-random
+// (divisor, dividend) pairs over the whole range (xorshift, fixed seed).
+static int check_fastdiv() {
+  auto one = [](int d, int n) {
+    const FastDiv f = make_fastdiv(d);
+    if (f.div(n) != n / d || f.mod(n) != n % d) {
+      printf("fastdiv %d / %d: %d (expected %d)\n", n, d, f.div(n), n / d);
+      return 1;
+    }
+    return 0;
+  };
+  for (int d = 1; d <= 5000; ++d) {
+    for (int k = 0; k <= 64; ++k)
+      for (int e = -2; e <= 2; ++e) {
+        const int64_t n = int64_t(k) * d + e;
+        if (n >= 0 && one(d, int(n))) return 1;
+      }
+    for (int e = 0; e < 4; ++e)
+      if (one(d, 0x7fffffff - e)) return 1;
+  }
+  uint64_t x = 0x9e3779b97f4a7c15ull;
+  for (int i = 0; i < 2000000; ++i) {
+    x ^= x << 13;
+    x ^= x >> 7;
+    x ^= x << 17;
+    const int d = int((x >> 33) % 0x7fffffffu) + 1, n = int(x & 0x7fffffffu);
+    if (one(d, n) || one(d & 0xffff ? d & 0xffff : 1, n)) return 1;
+  }
+  return 0;
+}
+
 int main(int argc, char** argv) {
+  if (argc == 2 && !strcmp(argv[1], "D")) {
+    const int rc = check_fastdiv();
+    printf("%s fastdiv\n", rc ? "FAIL" : "ok");
+    return rc;
+  }
   int fails = 0, i = 1;
   int kv_per_block = 0;  // "K n": tile-pair unit blocks of n KV pairs for the geometries that follow
   while (i < argc) {
@@ -378,6 +415,7 @@ int main(int argc, char** argv) {
     }
     g.npairs = (g.hq + 1) / 2;
     g.tile_pairs = use_tile_pairs(g) ? 1 : 0;  // as the library sets it
+    set_fast_divs(g);
     {
       CpGeom t = g;
       if (ranked) t.rank = 0;

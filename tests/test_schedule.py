@@ -52,6 +52,14 @@ def checker(tmp_path_factory):
     return exe
 
 
+def test_fast_division_matches_integer_division(checker):
+    """The unit decodes divide by multiply and shift (FastDiv): exact against
+    plain integer division for every divisor up to 5000 around each multiple,
+    at the top of the range, and for two million random pairs."""
+    out = subprocess.run([checker, "D"], capture_output=True, text=True)
+    assert out.returncode == 0 and out.stdout.strip() == "ok fastdiv", out.stdout
+
+
 # tile pairs in unit blocks (b, s, hq, hkv, cp, causal, grid, KV pairs per block): the
 # blocks the library forms for large K/V, forced here on small shapes -- MHA, G = 3,
 # no mask, a ragged second tile

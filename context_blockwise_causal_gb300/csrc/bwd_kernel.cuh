@@ -568,8 +568,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       QWalk w(g, U);
       int chunk = 0, tile = 0;
       bool dg = false;
-      for (int j = 0; j < U.items && ok; ++j, ++i) {
-        if (j % G == 0) w.next(chunk, tile, dg);
+      int jh = 0;  // item j's head within the group (j mod G, counted)
+      for (int j = 0; j < U.items && ok; ++j, ++i, jh = jh + 1 == G ? 0 : jh + 1) {
+        if (jh == 0) w.next(chunk, tile, dg);
         const int rem = U.c - tile * kTile;
         const int q_valid = rem < kTile ? rem : kTile;
         const uint32_t os = i % C::kOStages;

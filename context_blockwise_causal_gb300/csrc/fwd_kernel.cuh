@@ -406,16 +406,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       float m_used = -INFINITY;
       float l = 0.f;
+      // Without ragged tiles (and outside the step form) the walk's only
+      // masked position is the query tile's diagonal, where step 0 ends: the
+      // softmax warps then follow the positions without the walk itself.
+      const bool walkless = !kStep && (U.c & (kTile - 1)) == 0;
+      const int jdiag = g.causal ? (U.half ? U.tpc : 0) + U.u : -1;
       for (int j = 0; j < n; ++j) {
         int chunk = 0, tile = 0;
         bool walk_dg = false, dg = false, dead = false;
-        w.next(chunk, tile, walk_dg);
+        int n_valid = kTile;
+        if (walkless) {
+          walk_dg = j == jdiag;
+        } else {
+          w.next(chunk, tile, walk_dg);
+          const int rem = U.c - tile * kTile;
+          n_valid = rem < kTile ? rem : kTile;
+        }
         if constexpr (kTP)
           fwd_pos_mask(jd, j, walk_dg, dg, dead);
         else
           dg = walk_dg;
-        const int rem = U.c - tile * kTile;
-        const int n_valid = rem < kTile ? rem : kTile;
         if (!(ok = mbar_wait_bounded(&s_full[sub], scnt & 1, abort_flag, kWaitLimitNs))) break;
         ++scnt;
         tc_fence_after();

@@ -1064,12 +1064,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float l2 = a.lvec[pos];
       const float dd = a.dvec[pos];
       KvWalk w(g, U);
+      // Without ragged tiles the walk's only masked position is the query
+      // tile's diagonal, where step 0 ends: follow the positions without the
+      // walk itself (as the forward's softmax warps do).
+      const bool walkless = (U.c & (kTile - 1)) == 0;
+      const int jdiag = g.causal ? (U.half ? U.tpc : 0) + U.u : -1;
       for (int j = 0; j < U.n && ok; ++j, ++jt) {
         int chunk = 0, tile = 0;
         bool dg = false;
-        w.next(chunk, tile, dg);
-        const int rem = U.c - tile * kTile;
-        const int n_valid = rem < kTile ? rem : kTile;
+        int n_valid = kTile;
+        if (walkless) {
+          dg = j == jdiag;
+        } else {
+          w.next(chunk, tile, dg);
+          const int rem = U.c - tile * kTile;
+          n_valid = rem < kTile ? rem : kTile;
+        }
         if (!(ok = mbar_wait_lean(s_full, jt & 1, abort_flag, kWaitLimitNs))) break;
         tc_fence_after();
         uint32_t r0[32], r1[32];

@@ -149,6 +149,28 @@ def test_fwd_full_size_workloads(name):
     assert raw32 <= O_TOL and l32_err <= LSE_TOL
 
 
+def test_fwd_tile_pair_blocks_match_unblocked_bitwise():
+    """Odd head groups (G = 3, tile pairs) whose K/V outgrows L2 (b8 s4096 hq24
+    hkv8: 128 MB) run their units in L2-sized head blocks; one batch element
+    alone (16 MB) runs them unblocked. The units are the same, only their
+    order differs, so every batch element's output is bit-identical to its
+    own launch; sampled rows of two elements also meet the oracle bar."""
+    w = Workload("tp_blocks", b=8, s=4096, hq=24, hkv=8, d=128, cp=4, seed=4242)
+    x = make_inputs(w, device="cuda", with_grad=False)
+    o, lse = cpattn_fwd(x["q"], x["k"], x["v"], w.cp)
+    torch.cuda.synchronize()
+    assert cpattn_device_status() == 0
+    for bi in range(w.b):
+        one = [x[n][bi:bi + 1].contiguous() for n in ("q", "k", "v")]
+        o1, l1 = cpattn_fwd(*one, w.cp)
+        torch.cuda.synchronize()
+        assert torch.equal(o1[0], o[bi]) and torch.equal(l1[0], lse[bi]), f"batch element {bi}"
+    rows = sample_rows(w, 48, seed=9)
+    for bi in (0, w.b - 1):
+        o_ref, l_ref = oracle.attention_forward(*[x[n][bi:bi + 1].cpu() for n in ("q", "k", "v")], rows=rows)
+        _check(o[bi:bi + 1, rows].cpu(), lse[bi:bi + 1][:, :, rows].cpu(), o_ref, l_ref, name=f"tp_blocks b{bi}")
+
+
 @pytest.mark.parametrize("std,cp,d", [(8.0, 4, 128), (16.0, 2, 64)])
 def test_fwd_peaky_scores_all_elements(std, cp, d):
     """Q, K ~ N(0, std^2): scores of several hundred, a row's maximum moves

@@ -171,6 +171,24 @@ def test_fwd_tile_pair_blocks_match_unblocked_bitwise():
         _check(o[bi:bi + 1, rows].cpu(), lse[bi:bi + 1][:, :, rows].cpu(), o_ref, l_ref, name=f"tp_blocks b{bi}")
 
 
+@pytest.mark.parametrize("d", [128, 64])
+def test_fwd_output_only_16_byte_aligned(d):
+    """The ABI asks o for 16-byte alignment only: an o 16 bytes past a 32-byte
+    boundary gets the same result as an aligned one, bit for bit, and nothing
+    around it is written."""
+    w = Workload("off16", b=2, s=1024, hq=4, hkv=2, d=d, cp=2, seed=5)
+    x = make_inputs(w, device="cuda", with_grad=False)
+    o_ref, l_ref = cpattn_fwd(x["q"], x["k"], x["v"], w.cp)
+    buf = torch.zeros(x["q"].numel() + 16, dtype=torch.bfloat16, device="cuda")
+    o_off = buf[8:8 + x["q"].numel()].view(x["q"].shape)
+    assert o_off.data_ptr() % 32 == 16
+    o2, l2 = cpattn_fwd(x["q"], x["k"], x["v"], w.cp, o=o_off)
+    torch.cuda.synchronize()
+    assert cpattn_device_status() == 0
+    assert torch.equal(o2, o_ref) and torch.equal(l2, l_ref)
+    assert not buf[:8].any() and not buf[8 + x["q"].numel():].any()  # nothing outside o written
+
+
 @pytest.mark.parametrize("std,cp,d", [(8.0, 4, 128), (16.0, 2, 64)])
 def test_fwd_peaky_scores_all_elements(std, cp, d):
     """Q, K ~ N(0, std^2): scores of several hundred, a row's maximum moves

@@ -12,7 +12,7 @@ import os
 
 import torch
 
-from ._build import LIB_PATH, build  # noqa: F401
+from ._build import CHECKED_LIB_PATH, LIB_PATH, build  # noqa: F401
 
 __all__ = [
     "CpattnError",
@@ -60,69 +60,93 @@ _LIB = None
 _i, _p, _sz = ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
 
 
+_CHECKED = None
+
+
 def library():
     """Load libcpattn.so (once). Raises if it has not been built."""
     global _LIB
     if _LIB is None:
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(f"{LIB_PATH} is missing: build it with context_blockwise_causal_gb300.build()")
-        lib = ctypes.CDLL(LIB_PATH)
-        lib.cpattn_fwd.argtypes = [_p, _p, _p, _p, _p] + [_i] * 7 + [_p]
-        lib.cpattn_fwd.restype = _i
-        lib.cpattn_fwd_ex.argtypes = [_p, _p, _p, _p, _p] + [_i] * 7 + [ctypes.c_float, _p]
-        lib.cpattn_fwd_ex.restype = _i
-        lib.cpattn_bwd_ex.argtypes = [_p] * 10 + [_sz] + [_i] * 7 + [ctypes.c_float, _p]
-        lib.cpattn_bwd_ex.restype = _i
-        lib.cpattn_fwd_step.argtypes = [_p] * 5 + [_i] * 8 + [_p]
-        lib.cpattn_fwd_step.restype = _i
-        lib.cpattn_lse_merge.argtypes = [_p] * 7 + [_i] * 4 + [_p]
-        lib.cpattn_lse_merge.restype = _i
-        lib.cpattn_fwd_unfused_workspace_bytes.argtypes = [_i] * 4
-        lib.cpattn_fwd_unfused_workspace_bytes.restype = _sz
-        lib.cpattn_fwd_unfused.argtypes = [_p] * 6 + [_sz] + [_i] * 7 + [_p]
-        lib.cpattn_fwd_unfused.restype = _i
-        lib.cpattn_rope.argtypes = [_p] + [_i] * 7 + [_p, _i, ctypes.c_float, _i, _p]
-        lib.cpattn_rope.restype = _i
-        lib.cpattn_fwd_varlen.argtypes = [_p] * 6 + [_i] * 6 + [ctypes.c_float, _p]
-        lib.cpattn_fwd_varlen.restype = _i
-        lib.cpattn_bwd_varlen_workspace_bytes.argtypes = [_p] + [_i] * 5
-        lib.cpattn_bwd_varlen_workspace_bytes.restype = _sz
-        lib.cpattn_bwd_varlen.argtypes = [_p] * 10 + [_sz, _p] + [_i] * 6 + [ctypes.c_float, _p]
-        lib.cpattn_bwd_varlen.restype = _i
-        lib.cpattn_bwd.argtypes = [_p] * 10 + [_sz] + [_i] * 7 + [_p]
-        lib.cpattn_bwd.restype = _i
-        lib.cpattn_bwd_stage.argtypes = [_i] + [_p] * 10 + [_sz] + [_i] * 7 + [_p]
-        lib.cpattn_bwd_stage.restype = _i
-        lib.cpattn_bwd_noalloc.argtypes = [_p] * 9 + [_i] * 7 + [_p]
-        lib.cpattn_bwd_noalloc.restype = _i
-        lib.cpattn_bwd_noalloc_max_scratch_bytes.argtypes = []
-        lib.cpattn_bwd_noalloc_max_scratch_bytes.restype = _sz
-        lib.cpattn_bwd_workspace_bytes.argtypes = [_i] * 6
-        lib.cpattn_bwd_workspace_bytes.restype = _sz
-        lib.cpattn_fwd_rank.argtypes = [_p] * 5 + [_i] * 8 + [ctypes.c_float, _p]
-        lib.cpattn_fwd_rank.restype = _i
-        lib.cpattn_fwd_rank_step.argtypes = [_p] * 5 + [_i] * 9 + [ctypes.c_float, _p]
-        lib.cpattn_fwd_rank_step.restype = _i
-        lib.cpattn_bwd_rank_workspace_bytes.argtypes = [_i] * 6
-        lib.cpattn_bwd_rank_workspace_bytes.restype = _sz
-        lib.cpattn_bwd_rank.argtypes = [_p] * 10 + [_sz] + [_i] * 8 + [ctypes.c_float, _p]
-        lib.cpattn_bwd_rank.restype = _i
-        lib.cpattn_bwd_rank_stage.argtypes = [_i] + [_p] * 10 + [_sz] + [_i] * 8 + [ctypes.c_float, _p]
-        lib.cpattn_bwd_rank_stage.restype = _i
-        lib.cpattn_zigzag_index.argtypes = [_i, _i, _p]
-        lib.cpattn_zigzag_index.restype = _i
-        lib.cpattn_device_status.argtypes = [_p, ctypes.POINTER(_i)]
-        lib.cpattn_device_status.restype = _i
-        lib.cpattn_selftest_abort.argtypes = [_p] * 10 + [_sz] + [_i] * 6 + [ctypes.c_ulonglong, _p]
-        lib.cpattn_selftest_abort.restype = _i
-        lib.cpattn_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, _p]
-        lib.cpattn_selftest_wait_timeout.restype = _i
-        lib.cpattn_strerror.argtypes = [_i]
-        lib.cpattn_strerror.restype = ctypes.c_char_p
-        lib.cpattn_version.argtypes = []
-        lib.cpattn_version.restype = _i
-        _LIB = lib
+        _LIB = _declare(ctypes.CDLL(LIB_PATH))
     return _LIB
+
+
+def checked_library():
+    """Load libcpattn_checked.so (once), the build whose kernels test every
+    global access against the buffers' extents (bit 20 of the status word).
+    A debugging aid with the same entry points and results; raises if it has
+    not been built."""
+    global _CHECKED
+    if _CHECKED is None:
+        if not os.path.exists(CHECKED_LIB_PATH):
+            raise RuntimeError(f"{CHECKED_LIB_PATH} is missing: build it with context_blockwise_causal_gb300.build()")
+        _CHECKED = _declare(ctypes.CDLL(CHECKED_LIB_PATH))
+    return _CHECKED
+
+
+def _declare(lib):
+    """Argument and result types of every entry point of a loaded library."""
+    lib.cpattn_fwd.argtypes = [_p, _p, _p, _p, _p] + [_i] * 7 + [_p]
+    lib.cpattn_fwd.restype = _i
+    lib.cpattn_fwd_ex.argtypes = [_p, _p, _p, _p, _p] + [_i] * 7 + [ctypes.c_float, _p]
+    lib.cpattn_fwd_ex.restype = _i
+    lib.cpattn_bwd_ex.argtypes = [_p] * 10 + [_sz] + [_i] * 7 + [ctypes.c_float, _p]
+    lib.cpattn_bwd_ex.restype = _i
+    lib.cpattn_fwd_step.argtypes = [_p] * 5 + [_i] * 8 + [_p]
+    lib.cpattn_fwd_step.restype = _i
+    lib.cpattn_lse_merge.argtypes = [_p] * 7 + [_i] * 4 + [_p]
+    lib.cpattn_lse_merge.restype = _i
+    lib.cpattn_fwd_unfused_workspace_bytes.argtypes = [_i] * 4
+    lib.cpattn_fwd_unfused_workspace_bytes.restype = _sz
+    lib.cpattn_fwd_unfused.argtypes = [_p] * 6 + [_sz] + [_i] * 7 + [_p]
+    lib.cpattn_fwd_unfused.restype = _i
+    lib.cpattn_rope.argtypes = [_p] + [_i] * 7 + [_p, _i, ctypes.c_float, _i, _p]
+    lib.cpattn_rope.restype = _i
+    lib.cpattn_fwd_varlen.argtypes = [_p] * 6 + [_i] * 6 + [ctypes.c_float, _p]
+    lib.cpattn_fwd_varlen.restype = _i
+    lib.cpattn_bwd_varlen_workspace_bytes.argtypes = [_p] + [_i] * 5
+    lib.cpattn_bwd_varlen_workspace_bytes.restype = _sz
+    lib.cpattn_bwd_varlen.argtypes = [_p] * 10 + [_sz, _p] + [_i] * 6 + [ctypes.c_float, _p]
+    lib.cpattn_bwd_varlen.restype = _i
+    lib.cpattn_bwd.argtypes = [_p] * 10 + [_sz] + [_i] * 7 + [_p]
+    lib.cpattn_bwd.restype = _i
+    lib.cpattn_bwd_stage.argtypes = [_i] + [_p] * 10 + [_sz] + [_i] * 7 + [_p]
+    lib.cpattn_bwd_stage.restype = _i
+    lib.cpattn_bwd_noalloc.argtypes = [_p] * 9 + [_i] * 7 + [_p]
+    lib.cpattn_bwd_noalloc.restype = _i
+    lib.cpattn_bwd_noalloc_max_scratch_bytes.argtypes = []
+    lib.cpattn_bwd_noalloc_max_scratch_bytes.restype = _sz
+    lib.cpattn_bwd_workspace_bytes.argtypes = [_i] * 6
+    lib.cpattn_bwd_workspace_bytes.restype = _sz
+    lib.cpattn_fwd_rank.argtypes = [_p] * 5 + [_i] * 8 + [ctypes.c_float, _p]
+    lib.cpattn_fwd_rank.restype = _i
+    lib.cpattn_fwd_rank_step.argtypes = [_p] * 5 + [_i] * 9 + [ctypes.c_float, _p]
+    lib.cpattn_fwd_rank_step.restype = _i
+    lib.cpattn_bwd_rank_workspace_bytes.argtypes = [_i] * 6
+    lib.cpattn_bwd_rank_workspace_bytes.restype = _sz
+    lib.cpattn_bwd_rank.argtypes = [_p] * 10 + [_sz] + [_i] * 8 + [ctypes.c_float, _p]
+    lib.cpattn_bwd_rank.restype = _i
+    lib.cpattn_bwd_rank_stage.argtypes = [_i] + [_p] * 10 + [_sz] + [_i] * 8 + [ctypes.c_float, _p]
+    lib.cpattn_bwd_rank_stage.restype = _i
+    lib.cpattn_zigzag_index.argtypes = [_i, _i, _p]
+    lib.cpattn_zigzag_index.restype = _i
+    lib.cpattn_device_status.argtypes = [_p, ctypes.POINTER(_i)]
+    lib.cpattn_device_status.restype = _i
+    lib.cpattn_selftest_abort.argtypes = [_p] * 10 + [_sz] + [_i] * 6 + [ctypes.c_ulonglong, _p]
+    lib.cpattn_selftest_abort.restype = _i
+    lib.cpattn_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, _p]
+    lib.cpattn_selftest_wait_timeout.restype = _i
+    lib.cpattn_strerror.argtypes = [_i]
+    lib.cpattn_strerror.restype = ctypes.c_char_p
+    lib.cpattn_version.argtypes = []
+    lib.cpattn_version.restype = _i
+    lib.cpattn_checked_build.argtypes = []
+    lib.cpattn_checked_build.restype = _i
+    lib.cpattn_selftest_bounds.argtypes = [_p] * 5 + [_i] * 6 + [_p]
+    lib.cpattn_selftest_bounds.restype = _i
+    return lib
 
 
 def _stream_handle(stream, *tensors):

@@ -53,6 +53,9 @@ struct BwdArgs {
   // time limit of the producers' waits for free buffers: kWaitLimitNs, or a
   // short one in the abort self-test (cpattn_selftest_abort)
   uint64_t producer_limit_ns;
+  // extents for the checked build (bounds_ok): rows of the query-side and
+  // key/value-side tensors, floats of lse and of each row vector
+  int64_t q_rows, kv_rows, lse_len, vec_len;
 };
 
 enum BwdStatusBits : unsigned int {
@@ -86,6 +89,7 @@ __global__ void __launch_bounds__(256) cpattn_bwd_pre_kernel(const BwdArgs a) {
   const CpGeom& g = a.g;
   const int srows = q_seq_rows(g);  // rows of a sequence in o / dout
   const int64_t nrows = int64_t(g.b) * srows * g.hq;
+  if (!bounds_ok(nrows <= a.q_rows * g.hq, a.status)) return;  // o and dout hold q_rows rows
   const int lane = threadIdx.x & 31;
   const int li = lane % kLanesPerRow;
   const int lr = lane / kLanesPerRow;  // which of a load's rows this lane reads
@@ -147,8 +151,10 @@ __global__ void __launch_bounds__(256) cpattn_bwd_pre_kernel(const BwdArgs a) {
     const int in = tl - chunk * q.c;
     if (g.rank >= 0) chunk = chunk ? 2 * g.cp - 1 - g.rank : g.rank;
     const int64_t pos = ld_pos(g, a.ntp, seq, h, chunk, in / kTile, q.tpc, in % kTile);
+    const int64_t li = (int64_t(bi) * g.hq + h) * a.lse_stride + t;
+    if (!bounds_ok(pos >= 0 && pos < a.vec_len && li < a.lse_len && idx < a.q_rows * g.hq, a.status)) continue;
     a.dvec[pos] = acc;
-    a.lvec[pos] = a.lse[(int64_t(bi) * g.hq + h) * a.lse_stride + t] * 1.4426950408889634f;
+    a.lvec[pos] = a.lse[li] * 1.4426950408889634f;
   }
 }
 
@@ -367,6 +373,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int ul = 0;
       auto load_item = [&](const BwdUnit& U, int chunk, int tile, int h) -> bool {
         const int row = U.tok0 + q_chunk_row(g, chunk, U.c) + tile * kTile;
+        bounds_ok(row >= 0 && row < a.q_rows && h >= 0 && h < g.hq, a.status);
         const uint32_t qs = item % C::kQStages, os = item % C::kOStages;
         if (item >= C::kQStages &&
             !mbar_wait_lean(&q_empty[qs], ((item / C::kQStages) - 1) & 1, abort_flag, plimit))
@@ -381,7 +388,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive_expect_tx(&o_full[os], C::kTileBytes + C::kLDBytes);
         for (int x = 0; x < D; x += 64)
           tma_load_3d(sdO + os * C::kTileBytes + (x / 64) * (kTile * 128), &tmdo, &o_full[os], x, h, row);
-        const int64_t pos = ld_pos(g, a.ntp, U.seq, h, chunk, tile, U.tpc, 0);
+        int64_t pos = ld_pos(g, a.ntp, U.seq, h, chunk, tile, U.tpc, 0);
+        if (!bounds_ok(pos >= 0 && pos + kTile <= a.vec_len, a.status)) pos = 0;  // stays inside the vectors
         bulk_load(reinterpret_cast<uint8_t*>(sLD) + os * C::kLDBytes, a.lvec + pos, kTile * 4, &o_full[os]);
         bulk_load(reinterpret_cast<uint8_t*>(sLD) + os * C::kLDBytes + kTile * 4, a.dvec + pos, kTile * 4,
                   &o_full[os]);
@@ -406,6 +414,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               if (ul > 0 && !(ok = mbar_wait_lean(kv_empty, (ul - 1) & 1, abort_flag, plimit))) break;
               mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
               const int krow = U.tok0 + U.k_t0;
+              bounds_ok(krow >= 0 && krow < a.kv_rows && U.g < g.hkv, a.status);
               for (int x = 0; x < D; x += 64) {
                 tma_load_3d(sK + (x / 64) * (kTile * 128), &tmk, kv_full, x, U.g, krow);
                 tma_load_3d(sV + (x / 64) * (kTile * 128), &tmv, kv_full, x, U.g, krow);
@@ -555,7 +564,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // No query of this call sees the tile. A tile a shorter packed sample
         // does not have has no rows (k_valid == 0); a real one (rank-local
         // form: no query of the rank reaches it) gets a zero share.
-        if (key_ok) {
+        if (key_ok && bounds_ok(int64_t(U.tok0) + U.k_t0 + jr < a.kv_rows && U.g < g.hkv, a.status)) {
           const int64_t off = ((int64_t(U.tok0) + U.k_t0 + jr) * g.hkv + U.g) * D + hf * (D / 2);
 #pragma unroll
           for (int c0 = 0; c0 < D / 2; c0 += 8) {
@@ -655,7 +664,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(dkv_empty);
         }
-        if (key_ok) {
+        if (key_ok && bounds_ok(int64_t(U.tok0) + U.k_t0 + jr < a.kv_rows && U.g < g.hkv, a.status)) {
 #pragma unroll
           for (int q = 0; q < 32; q += 8) {
             uint4 pv, pk;
@@ -849,6 +858,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t nload = 0;
       int ul = 0;
       auto load = [&](const CUtensorMap* map, int head, int row) -> bool {
+        bounds_ok(row >= 0 && row < a.kv_rows && head >= 0 && head < g.hkv, a.status);
         const uint32_t slot = nload % C::kSlots;
         if (nload >= (uint32_t)C::kSlots &&
             !mbar_wait_lean(&kv_empty[slot], ((nload / C::kSlots) - 1) & 1, abort_flag, plimit))
@@ -870,6 +880,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (ul > 0 && !(ok = mbar_wait_lean(q_empty, (ul - 1) & 1, abort_flag, plimit))) break;
         mbar_arrive_expect_tx(q_full, 2 * C::kTileBytes);
         const int qrow = U.tok0 + U.q_t0;
+        bounds_ok(qrow >= 0 && qrow < a.q_rows && U.h0 < g.hq, a.status);
         for (int x = 0; x < D; x += 64) {
           tma_load_3d(sQ + (x / 64) * (kTile * 128), &tmq, q_full, x, U.h0, qrow);
           tma_load_3d(sdO + (x / 64) * (kTile * 128), &tmdo, q_full, x, U.h0, qrow);
@@ -1060,7 +1071,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       // this row's L*log2e and D (padded rows of a ragged tile read arbitrary
       // values; their dQ is never stored)
-      const int64_t pos = ld_pos(g, a.ntp, U.seq, U.h0, U.k, U.u, U.tpc, jr);
+      int64_t pos = ld_pos(g, a.ntp, U.seq, U.h0, U.k, U.u, U.tpc, jr);
+      if (!bounds_ok(pos >= 0 && pos < a.vec_len, a.status)) pos = 0;  // stays inside the vectors
       const float l2 = a.lvec[pos];
       const float dd = a.dvec[pos];
       KvWalk w(g, U);
@@ -1144,7 +1156,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(dq_empty);
-      if (jr < U.q_valid) {
+      if (jr < U.q_valid && bounds_ok(int64_t(U.tok0) + U.q_t0 + jr < a.q_rows && U.h0 < g.hq, a.status)) {
         __nv_bfloat16* dst = a.dq + ((int64_t(U.tok0) + U.q_t0 + jr) * g.hq + U.h0) * D + hf * (D / 2);
 #pragma unroll
         for (int i = 0; i < D / 2; i += 8) {

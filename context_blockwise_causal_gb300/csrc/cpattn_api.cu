@@ -179,6 +179,9 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   args.o = static_cast<__nv_bfloat16*>(o);
   args.lse = lse;
   args.lse_stride = lse_stride < 0 ? s : lse_stride;
+  args.q_rows = int64_t(q_rows);
+  args.kv_rows = int64_t(kv_rows);
+  args.lse_len = int64_t(b) * hq * args.lse_stride;
   args.o_part = nullptr;
   args.step = -1;
   args.scale_log2 = float(1.4426950408889634 * scale);
@@ -230,6 +233,9 @@ int step_impl(const void* q, const void* k, const void* v, float* o_part, float*
   args.o = nullptr;
   args.lse = lse_part;
   args.lse_stride = lse_stride < 0 ? s : lse_stride;
+  args.q_rows = int64_t(q_rows);
+  args.kv_rows = int64_t(kv_rows);
+  args.lse_len = int64_t(b) * hq * args.lse_stride;
   args.o_part = o_part;
   args.step = step;
   args.scale_log2 = float(1.4426950408889634 * scale);
@@ -487,6 +493,10 @@ int prepare_bwd(const void* q, const void* k, const void* v, const void* o, cons
   args->dout = static_cast<const __nv_bfloat16*>(dout);
   args->lse = lse;
   args->lse_stride = lse_stride < 0 ? s : lse_stride;
+  args->q_rows = int64_t(q_rows);
+  args->kv_rows = int64_t(kv_rows);
+  args->lse_len = int64_t(b) * hq * args->lse_stride;
+  args->vec_len = int64_t(num_seqs(args->g)) * hq * L.ntp;
   args->lvec = reinterpret_cast<float*>(ws + L.lvec);
   args->dvec = reinterpret_cast<float*>(ws + L.dvec);
   args->dq = static_cast<__nv_bfloat16*>(dq);
@@ -828,6 +838,10 @@ extern "C" int cpattn_bwd_noalloc(const void* q, const void* k, const void* v, c
   args.dout = static_cast<const __nv_bfloat16*>(dout);
   args.lse = lse;
   args.lse_stride = s;
+  args.q_rows = int64_t(rows);
+  args.kv_rows = int64_t(rows);
+  args.lse_len = int64_t(b) * hq * s;
+  args.vec_len = int64_t(b) * hq * L.ntp;
   args.lvec = reinterpret_cast<float*>(ws + L.lvec);
   args.dvec = reinterpret_cast<float*>(ws + L.dvec);
   args.dq = static_cast<__nv_bfloat16*>(dq);
@@ -899,6 +913,33 @@ extern "C" int cpattn_selftest_abort(const void* q, const void* k, const void* v
   if (rc) return rc;
   return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, b, s, hq, hkv, d, cp, 1,
                   default_scale(d), stream, -1, nullptr, nullptr, limit_ns);
+}
+
+// Self-test of a checked build's bounds tests: the fused forward told that
+// the query-side tensors hold one row fewer than they do. The last row's
+// stores then fail their test and are skipped, and bit 20 of the status word
+// is set; the buffers do hold that row, so nothing outside them is touched
+// whether or not a test fires. Builds without the tests return
+// CPATTN_ERR_INVALID_ARG before any device work.
+extern "C" int cpattn_selftest_bounds(const void* q, const void* k, const void* v, void* o, float* lse, int b, int s,
+                                      int hq, int hkv, int d, int cp, void* stream) {
+#ifdef CPATTN_CHECKS
+  if (b < 1 || s < 2) return CPATTN_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, o, lse, b, s, hq, hkv, d, cp, 1, default_scale(d), stream, -1, nullptr,
+                  uint64_t(b) * s - 1, 0);
+#else
+  (void)q, (void)k, (void)v, (void)o, (void)lse, (void)b, (void)s, (void)hq, (void)hkv, (void)d, (void)cp,
+      (void)stream;
+  return CPATTN_ERR_INVALID_ARG;
+#endif
+}
+
+extern "C" int cpattn_checked_build(void) {
+#ifdef CPATTN_CHECKS
+  return 1;
+#else
+  return 0;
+#endif
 }
 
 extern "C" int cpattn_device_status(void* stream, int* status) {

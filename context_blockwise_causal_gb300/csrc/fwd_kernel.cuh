@@ -63,6 +63,9 @@ struct FwdArgs {
   // time limit of the producer's waits for free buffers: kWaitLimitNs, or a
   // short one in the abort self-test (cpattn_selftest_abort)
   uint64_t producer_limit_ns;
+  // extents for the checked build (bounds_ok): rows of the query-side and
+  // key/value-side tensors, floats of lse
+  int64_t q_rows, kv_rows, lse_len;
 };
 
 // K/V ring of kRing slots. When the two sub-tiles share K/V a key tile takes
@@ -201,6 +204,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           mbar_arrive_expect_tx(&q_full[sub], C::kQBytes);
           const int h = sub ? U.h1 : U.h0;
           const int qrow = U.tok0 + (sub ? U.q_t1 : U.q_t0);
+          bounds_ok(qrow >= 0 && qrow < a.q_rows && h >= 0 && h < g.hq, a.status);
           for (int x = 0; x < D; x += 64)
             tma_load_3d(sQ + sub * C::kQBytes + (x / 64) * (kTile * 128), &tmq, &q_full[sub], x, h, qrow);
         }
@@ -208,6 +212,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         int chunk, tile;
         bool dg;
         auto load = [&](const CUtensorMap* map, int head, int row) -> bool {
+          bounds_ok(row >= 0 && row < a.kv_rows && head >= 0 && head < g.hkv, a.status);
           const uint32_t slot = nload % C::kSlots;
           if (nload >= (uint32_t)C::kSlots) {
             if (!mbar_wait_bounded(&kv_empty[slot], ((nload / C::kSlots) - 1) & 1, abort_flag, plimit))
@@ -396,10 +401,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (row < q_valid && (sub == 0 || U.store1)) {
             const int h = sub ? U.h1 : U.h0;
             const int t = q_t + row;
-            float4* dst = reinterpret_cast<float4*>(a.o_part + ((int64_t(U.tok0) + t) * g.hq + h) * D);
+            const int64_t li = (int64_t(U.bi) * g.hq + h) * a.lse_stride + U.lse_t0 + t;
+            if (bounds_ok(int64_t(U.tok0) + t < a.q_rows && h < g.hq && li < a.lse_len, a.status)) {
+              float4* dst = reinterpret_cast<float4*>(a.o_part + ((int64_t(U.tok0) + t) * g.hq + h) * D);
 #pragma unroll
-            for (int c0 = 0; c0 < D / 4; ++c0) dst[c0] = make_float4(0.f, 0.f, 0.f, 0.f);
-            a.lse[(int64_t(U.bi) * g.hq + h) * a.lse_stride + U.lse_t0 + t] = -INFINITY;
+              for (int c0 = 0; c0 < D / 4; ++c0) dst[c0] = make_float4(0.f, 0.f, 0.f, 0.f);
+              a.lse[li] = -INFINITY;
+            }
           }
           continue;
         }
@@ -547,12 +555,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int h = sub ? U.h1 : U.h0;
         const int t = q_t + row;
         const float inv = 1.f / l;
-        float4* dst = reinterpret_cast<float4*>(a.o_part + ((int64_t(U.tok0) + t) * g.hq + h) * D);
+        const int64_t li = (int64_t(U.bi) * g.hq + h) * a.lse_stride + U.lse_t0 + t;
+        if (bounds_ok(int64_t(U.tok0) + t < a.q_rows && h < g.hq && li < a.lse_len, a.status)) {
+          float4* dst = reinterpret_cast<float4*>(a.o_part + ((int64_t(U.tok0) + t) * g.hq + h) * D);
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 4)
-          dst[c0 / 4] = make_float4(__uint_as_float(ov[c0]) * inv, __uint_as_float(ov[c0 + 1]) * inv,
-                                    __uint_as_float(ov[c0 + 2]) * inv, __uint_as_float(ov[c0 + 3]) * inv);
-        a.lse[(int64_t(U.bi) * g.hq + h) * a.lse_stride + U.lse_t0 + t] = (m_used + log2f(l)) * 0.69314718055994530942f;
+          for (int c0 = 0; c0 < D; c0 += 4)
+            dst[c0 / 4] = make_float4(__uint_as_float(ov[c0]) * inv, __uint_as_float(ov[c0 + 1]) * inv,
+                                      __uint_as_float(ov[c0 + 2]) * inv, __uint_as_float(ov[c0 + 3]) * inv);
+          a.lse[li] = (m_used + log2f(l)) * 0.69314718055994530942f;
+        }
       } else if (!kStep && C::kStageBytes > 0) {
         // O through the warp's staging buffer, 64 columns at a time: each
         // thread writes its row's 128 bytes (16-byte pieces at slot
@@ -583,15 +594,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const int part = lane & 7;          // 16-byte piece of the 128
             const uint4 v = stg[r * 8 + (part ^ (r & 7))];
             const int trow = wq * 32 + r;       // row within the tile
-            if (write_head && trow < q_valid)
+            if (write_head && trow < q_valid &&
+                bounds_ok(int64_t(U.tok0) + q_t + trow < a.q_rows && h < g.hq, a.status))
               *reinterpret_cast<uint4*>(a.o + ((int64_t(U.tok0) + q_t + trow) * g.hq + h) * D + c * 64 + part * 8) = v;
           }
           __syncwarp();
         }
-        if (store)
-          a.lse[(int64_t(U.bi) * g.hq + h) * a.lse_stride + U.lse_t0 + q_t + row] =
-              (m_used + log2f(l)) * 0.69314718055994530942f;
-      } else if (store) {
+        const int64_t li = (int64_t(U.bi) * g.hq + h) * a.lse_stride + U.lse_t0 + q_t + row;
+        if (store && bounds_ok(li < a.lse_len, a.status)) a.lse[li] = (m_used + log2f(l)) * 0.69314718055994530942f;
+      } else if (store && bounds_ok(int64_t(U.tok0) + q_t + row < a.q_rows &&
+                                        (int64_t(U.bi) * g.hq + (sub ? U.h1 : U.h0)) * a.lse_stride + U.lse_t0 +
+                                                q_t + row < a.lse_len,
+                                    a.status)) {
         const int h = sub ? U.h1 : U.h0;
         const int t = q_t + row;
         const float inv = 1.f / l;

@@ -45,6 +45,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Checked builds (compiled with -DCPATTN_CHECKS, the library's debug form in
+// place of a memory checker): the kernels test the rows, heads and vector
+// positions of their global accesses against the extents of the buffers and
+// record a failure in bit 20 of the device status word; a store out of range
+// is skipped and a plain bulk copy's source clamped, so a checked run touches
+// nothing outside its buffers (tensor copies clip by themselves). In other
+// builds bounds_ok() is constant true and the tests compile away.
+constexpr unsigned int kStatusBounds = 1u << 20;
+#ifdef CPATTN_CHECKS
+__device__ __forceinline__ bool bounds_ok(bool ok, unsigned int* status) {
+  if (!ok) atomicOr(status, kStatusBounds);
+  return ok;
+}
+#else
+__device__ __forceinline__ bool bounds_ok(bool, unsigned int*) { return true; }
+#endif
+
 // Time limit of every wait on a barrier inside the kernels.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 

@@ -348,7 +348,8 @@ int cpattn_zigzag_index(int s, int cp, int64_t* global_of_local);
  * error code. Bits: forward producer / MMA / softmax role gave up (0, 1, 2);
  * forward copies or MMAs still in flight at the end after the time limit (3);
  * the same for the backward kernels (8, 9, 10; 12); a backward kernel's
- * shared memory base not 1024-byte aligned (11); the timeout self-test (16).
+ * shared memory base not 1024-byte aligned (11); the timeout self-test (16);
+ * a bounds test of a checked build failed (20).
  * A role that gives up makes the others leave too, but every role first waits
  * for the copies and MMAs it already issued, so no kernel frees memory that
  * asynchronous work still writes.
@@ -389,6 +390,28 @@ int cpattn_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
 int cpattn_selftest_abort(const void* q, const void* k, const void* v, void* o, float* lse, const void* dout,
                           void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int b, int s,
                           int hq, int hkv, int d, int cp, unsigned long long limit_ns, void* stream);
+
+/*
+ * Checked builds (libcpattn_checked.so, compiled with -DCPATTN_CHECKS; the
+ * library's debug form in place of a memory checker): every kernel tests the
+ * rows, heads and vector positions of its global accesses against the
+ * extents of the buffers, records a failure in bit 20 (0x100000) of the
+ * device status word, skips a store out of range and keeps a plain bulk copy
+ * inside its source; results are otherwise those of the normal build, bit
+ * for bit. cpattn_checked_build() returns 1 in a checked build, else 0.
+ */
+int cpattn_checked_build(void);
+
+/*
+ * Self-test of a checked build's bounds tests: runs the fused forward (as
+ * cpattn_fwd with causal = 1) told that q and o hold one row fewer than they
+ * do, so the stores of the last row fail their test and are skipped and bit
+ * 20 is set (no access leaves the buffers either way). The last row of o and
+ * of lse is left unwritten. Arguments as cpattn_fwd (s >= 2). Returns
+ * CPATTN_ERR_INVALID_ARG in builds without the tests, before any device work.
+ */
+int cpattn_selftest_bounds(const void* q, const void* k, const void* v, void* o, float* lse, int b, int s, int hq,
+                           int hkv, int d, int cp, void* stream);
 
 /* Static description of an error code. */
 const char* cpattn_strerror(int code);

@@ -96,6 +96,19 @@ def test_strerror_and_version(lib):
     assert lib.cpattn_version() >= 100
 
 
+def test_checked_build_loads_and_reports_itself(lib):
+    """The checked build (kernels' bounds tests compiled in) exports the same
+    entry points; each build reports which one it is, and the bounds
+    self-test refuses to run where no tests were compiled."""
+    import context_blockwise_causal_gb300 as pkg
+
+    chk = pkg.checked_library()
+    for name in _declared():
+        assert hasattr(chk, name), name
+    assert lib.cpattn_checked_build() == 0 and chk.cpattn_checked_build() == 1
+    assert lib.cpattn_selftest_bounds(None, None, None, None, None, 1, 256, 2, 2, 128, 2, None) == -1
+
+
 def test_fwd_argument_errors_are_reported_before_any_device_work(lib):
     p = ctypes.c_void_p(4096)  # never dereferenced: validation fails first
     f = lib.cpattn_fwd

@@ -14,9 +14,11 @@
  *     merged: L = log(sum_i e^{L_i}), O = sum_i e^{L_i - L} O_i.
  * The result equals plain causal softmax attention over the uncut sequence
  * (3.2: each rank's output equals the matching part of the non-CP output).
- * All cp virtual ranks run inside one kernel launch on one GPU; there is no
- * KV exchange between devices. The per-step correction is carried on chip,
- * so partial outputs never reach device memory.
+ * All cp virtual ranks run inside one kernel launch on one GPU; the library
+ * itself moves no data between devices (the rank-local calls further down
+ * compute one rank's share of a CP group spread over GPUs, and the caller
+ * exchanges K/V). The per-step correction is carried on chip, so partial
+ * outputs never reach device memory.
  *
  * Conventions shared by every entry point
  *   - Tensors are in natural token order (the zigzag is applied inside).

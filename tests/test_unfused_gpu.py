@@ -42,6 +42,8 @@ SMALL = [
     (1, 640, 3, 1, 64, 2, True),     # odd hq, MQA, ragged
     (1, 768, 4, 4, 128, 3, False),   # no mask
     (1, 256, 2, 2, 128, 1, True),    # cp = 1
+    (1, 2048, 2, 2, 128, 2, True),   # MHA, two tiles per chunk: tile-pair units in every step
+    (1, 1536, 3, 1, 64, 3, False),   # G = 3, c = 256: tile pairs without the mask
 ]
 
 

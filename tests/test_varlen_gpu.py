@@ -1,6 +1,7 @@
 """Packed samples (cpattn_fwd_varlen / cpattn_bwd_varlen) through the C ABI
 against the CPU fp64 oracle (oracle.varlen_attention_*): mixed lengths,
-empty samples, ragged tiles, GQA, d = 64 and 128, a custom scale.
+empty samples, ragged tiles, GQA, d = 64 and 128, a custom scale, with and
+without the causal mask.
 Tolerances as for one sequence: max |O err| <= 1e-2 beyond the bf16
 output's half ulp, max |LSE err| <= 1e-3, relative L2 <= 2e-2 per gradient."""
 import pytest
@@ -23,17 +24,19 @@ def _rel(x, ref):
 
 
 CASES = [
-    # lengths, hq, hkv, d, cp, scale
-    ([512, 1024, 256], 4, 2, 128, 2, None),
-    ([960, 0, 192, 384], 6, 2, 64, 3, None),     # empty sample, ragged chunks
-    ([2048, 128], 8, 1, 128, 4, 0.05),          # MQA, custom scale
-    ([96], 2, 2, 128, 3, None),                 # one sample, c = 16
-    ([4, 8, 0, 4], 2, 1, 128, 2, None),         # one- and two-token chunks
+    # lengths, hq, hkv, d, cp, scale, causal
+    ([512, 1024, 256], 4, 2, 128, 2, None, True),
+    ([960, 0, 192, 384], 6, 2, 64, 3, None, True),     # empty sample, ragged chunks
+    ([2048, 128], 8, 1, 128, 4, 0.05, True),          # MQA, custom scale
+    ([96], 2, 2, 128, 3, None, True),                 # one sample, c = 16
+    ([4, 8, 0, 4], 2, 1, 128, 2, None, True),         # one- and two-token chunks
+    ([640, 0, 384, 1152], 4, 2, 128, 2, None, False),  # no mask: every key of the sample
+    ([96, 32, 480], 3, 1, 64, 4, 0.1, False),          # no mask, ragged chunks, custom scale
 ]
 
 
-@pytest.mark.parametrize("lengths,hq,hkv,d,cp,scale", CASES)
-def test_varlen_forward_backward(lengths, hq, hkv, d, cp, scale):
+@pytest.mark.parametrize("lengths,hq,hkv,d,cp,scale,causal", CASES)
+def test_varlen_forward_backward(lengths, hq, hkv, d, cp, scale, causal):
     cu = [0]
     for n in lengths:
         cu.append(cu[-1] + n)
@@ -44,15 +47,15 @@ def test_varlen_forward_backward(lengths, hq, hkv, d, cp, scale):
     v = torch.randn(total, hkv, d, generator=g).to(torch.bfloat16)
     do = torch.randn(total, hq, d, generator=g).to(torch.bfloat16)
     qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
-    o, lse = cpattn_fwd_varlen(qd, kd, vd, cu, cp, scale=scale)
-    dq, dk, dv = cpattn_bwd_varlen(qd, kd, vd, o, lse, dod, cu, cp, scale=scale)
+    o, lse = cpattn_fwd_varlen(qd, kd, vd, cu, cp, causal=causal, scale=scale)
+    dq, dk, dv = cpattn_bwd_varlen(qd, kd, vd, o, lse, dod, cu, cp, causal=causal, scale=scale)
     torch.cuda.synchronize()
     assert cpattn_device_status() == 0
-    o_r, l_r = oracle.varlen_attention_forward(q, k, v, cu, scale=scale)
+    o_r, l_r = oracle.varlen_attention_forward(q, k, v, cu, causal=causal, scale=scale)
     err = (o.double().cpu() - o_r).abs()
     assert (err <= 1e-2 + _half_ulp_bf16(o_r)).all(), err.max().item()
     assert (lse.double().cpu() - l_r).abs().max().item() <= 1e-3
-    dq_r, dk_r, dv_r = oracle.varlen_attention_backward(q, k, v, do, cu, scale=scale)
+    dq_r, dk_r, dv_r = oracle.varlen_attention_backward(q, k, v, do, cu, causal=causal, scale=scale)
     for name, got, ref in (("dq", dq, dq_r), ("dk", dk, dk_r), ("dv", dv, dv_r)):
         assert _rel(got.float().cpu(), ref) <= 2e-2, name
 

@@ -5,6 +5,8 @@ import ctypes
 import glob
 import os
 import re
+import subprocess
+import sys
 
 import pytest
 import torch
@@ -209,3 +211,35 @@ def test_sizes_beyond_the_index_range_are_rejected(lib):
     s = (1 << 31) - 2
     assert lib.cpattn_fwd(p, p, p, p, p, 1, s, 1, 1, 64, 1, 1, None) == -1
     assert lib.cpattn_bwd_workspace_bytes(1, s, 1, 1, 64, 1) == 0
+
+
+def test_product_fails_loudly_without_the_library(tmp_path):
+    """With the library absent, the binding's entry points raise: no CPU or
+    PyTorch fallback answers in its place. Run in a fresh interpreter whose
+    package points at a path with no library."""
+    code = f"""
+import context_blockwise_causal_gb300 as pkg
+import torch
+pkg.LIB_PATH = {str(tmp_path / 'libcpattn.so')!r}
+pkg._LIB = None
+q = torch.zeros(1, 256, 2, 64, dtype=torch.bfloat16)
+calls = {{
+    "library": lambda: pkg.library(),
+    "cpattn_zigzag_index": lambda: pkg.cpattn_zigzag_index(256, 2),
+    "cpattn_fwd": lambda: pkg.cpattn_fwd(q, q, q, 2),
+}}
+for name, call in calls.items():
+    try:
+        call()
+    except (RuntimeError, TypeError, ValueError) as e:
+        print(name, type(e).__name__, "missing" in str(e) or "CUDA" in str(e))
+    else:
+        print(name, "returned")
+"""
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = dict(ln.split(" ", 1) for ln in r.stdout.strip().splitlines())
+    assert lines["library"] == "RuntimeError True"
+    assert lines["cpattn_zigzag_index"] == "RuntimeError True"
+    # a CPU tensor is refused before the library is reached; either way nothing computes it
+    assert not lines["cpattn_fwd"].startswith("returned")

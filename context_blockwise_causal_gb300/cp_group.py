@@ -28,14 +28,18 @@ directly.
 The ``kernels`` and ``exchange`` arguments exist so that the exchange logic
 can be checked on its own: tests pass recording or CPU stand-ins. The
 default kernels are the CUDA library's, and it fails loudly when that
-library is missing.
+library is missing. ``exchange=CheckedExchange(group)`` fingerprints every
+collective across the ranks (a debugging aid, see its docstring).
 """
+import zlib
+
 import torch
 import torch.distributed as dist
 
 from . import cpattn_bwd_rank, cpattn_bwd_rank_workspace_bytes, cpattn_fwd_rank, cpattn_fwd_rank_step, cpattn_lse_merge
 
-__all__ = ["CudaKernels", "GroupExchange", "zigzag_shard", "zigzag_unshard", "cp_forward", "cp_backward"]
+__all__ = ["CudaKernels", "GroupExchange", "CheckedExchange", "ExchangeMismatch", "zigzag_shard", "zigzag_unshard",
+           "cp_forward", "cp_backward"]
 
 
 class CudaKernels:
@@ -95,8 +99,9 @@ class GroupExchange:
     def _global(self, r):
         return r if self.group is None else dist.get_global_rank(self.group, r)
 
-    def all_gather(self, x):
-        """Every rank's x stacked rank-major: [cp, *x.shape]."""
+    def all_gather(self, x, tag=None):
+        """Every rank's x stacked rank-major: [cp, *x.shape]. ``tag`` names
+        the logical tensor (used by CheckedExchange)."""
         x = x.contiguous()
         # gathered as the concatenation along dimension 0 (the form every
         # backend takes), then viewed rank-major
@@ -104,7 +109,7 @@ class GroupExchange:
         dist.all_gather_into_tensor(out, x, group=self.group)
         return out.view((self.cp,) + tuple(x.shape))
 
-    def reduce_scatter_start(self, *parts):
+    def reduce_scatter_start(self, *parts, tag=None):
         """For each tensor of parts, [cp, *shape] on every rank, start summing
         over the ranks so that this rank gets the sum of their parts[rank].
         Returns a handle for reduce_scatter_finish; the reduction runs while
@@ -124,7 +129,7 @@ class GroupExchange:
             w_.wait()
         return outs
 
-    def ring_start(self, send, recv):
+    def ring_start(self, send, recv, tag=None):
         """Post one ring hop: each tensor of ``send`` goes to the next rank,
         each of ``recv`` is filled from the previous one. Returns the
         requests; the send and receive pairs are issued together, so no
@@ -137,6 +142,115 @@ class GroupExchange:
     def ring_wait(reqs):
         for r in reqs or ():
             r.wait()
+
+
+class ExchangeMismatch(RuntimeError):
+    """The ranks of a CheckedExchange disagreed on a collective, or received
+    bytes that differ from what their peer sent."""
+
+
+_OPS = {"all_gather": 1, "reduce_scatter": 2, "ring": 3}
+_DTYPES = (torch.bfloat16, torch.float16, torch.float32, torch.float64, torch.int64, torch.int32, torch.int16)
+_MAX_TENSORS, _MAX_DIMS = 4, 6
+_FIELDS = ("sequence", "operation", "logical id", "dimensions") + tuple(f"size {i}" for i in range(_MAX_DIMS)) + (
+    "dtype", "checksum")
+
+
+def _checksum(t):
+    """A position-weighted sum of the tensor's 16-bit words, modulo 2^64
+    (integer arithmetic, so every rank gets the same value for the same
+    bytes). A debugging checksum, not part of any attention step."""
+    w = t.detach().contiguous().view(-1).view(torch.int16).to(torch.int64) & 0xFFFF
+    pos = torch.arange(w.numel(), dtype=torch.int64, device=w.device) % 65521 + 1
+    return int((w * pos).sum().item())
+
+
+class CheckedExchange(GroupExchange):
+    """GroupExchange that fingerprints every logical collective.
+
+    Page "Megatron 面试题（一）：模型抽象与训练数据流", item M024 (follow-up):
+    collectives of the same shape issued in a different order on some rank
+    can complete and give finite but wrong results, so each logical
+    collective records its group, sequence number, operation, shape, dtype
+    and an input checksum, and business tensors a logical id; comparing the
+    records across ranks shows the first point where they diverge.
+
+    Here, before each collective every rank all-gathers a fixed-size record
+    (sequence number, operation, the caller's tag as logical id, and per
+    tensor its shape, dtype and checksum). All ranks must agree on
+    everything but the checksums; each rank sees every record, so on a
+    mismatch every rank raises ExchangeMismatch before the collective itself
+    runs, and none is left waiting in it. After an all-gather each rank's
+    block is checked against its owner's checksum, after a ring hop the
+    received tensors against the sender's; the ranks then agree (one more
+    small all-gather) so that a failure on one raises on all. The checks add
+    two small collectives and a pass over the data per collective: a
+    debugging aid, off unless a caller passes this exchange.
+    """
+
+    def __init__(self, group=None):
+        super().__init__(group)
+        self.sequence = 0
+
+    def _record(self, op, tag, tensors):
+        if len(tensors) > _MAX_TENSORS:
+            raise ValueError(f"at most {_MAX_TENSORS} tensors per checked collective")
+        rows = []
+        for t in tensors:
+            if t.dim() > _MAX_DIMS or t.dtype not in _DTYPES:
+                raise ValueError("tensor outside the checked exchange's shapes or dtypes")
+            rows.append([self.sequence, _OPS[op], zlib.crc32(str(tag).encode()), t.dim()]
+                        + list(t.shape) + [-1] * (_MAX_DIMS - t.dim()) + [_DTYPES.index(t.dtype), _checksum(t)])
+        rows += [[self.sequence, _OPS[op], zlib.crc32(str(tag).encode())] + [-2] * (len(_FIELDS) - 3)] * (
+            _MAX_TENSORS - len(tensors))
+        dev = tensors[0].device if tensors else torch.device("cpu")
+        mine = torch.tensor(rows, dtype=torch.int64, device=dev)
+        every = torch.empty((self.cp * _MAX_TENSORS, len(_FIELDS)), dtype=torch.int64, device=dev)
+        dist.all_gather_into_tensor(every, mine, group=self.group)
+        every = every.view(self.cp, _MAX_TENSORS, len(_FIELDS)).cpu()
+        meta = every[:, :, :-1]
+        if not bool((meta == meta[0]).all()):
+            r = int((meta != meta[0]).flatten(1).any(1).nonzero()[0])
+            ti, fi = [int(x) for x in (meta[r] != meta[0]).nonzero()[0]]
+            raise ExchangeMismatch(
+                f"collective #{self.sequence} ({op} {tag!r}): rank {r} differs from rank 0 in the "
+                f"{_FIELDS[fi]} of tensor {ti} ({int(meta[r, ti, fi])} against {int(meta[0, ti, fi])})")
+        self.sequence += 1
+        return every[:, :, -1]  # checksums [rank, tensor]
+
+    def _agree(self, ok, what, dev):
+        flags = torch.empty(self.cp, dtype=torch.int64, device=dev)
+        dist.all_gather_into_tensor(flags, torch.tensor([0 if ok else 1], dtype=torch.int64, device=dev),
+                                    group=self.group)
+        bad = [r for r, f in enumerate(flags.cpu().tolist()) if f]
+        if bad:
+            raise ExchangeMismatch(f"{what}: received bytes differ from those sent on rank(s) {bad}")
+
+    def all_gather(self, x, tag=None):
+        sums = self._record("all_gather", tag, [x])
+        out = super().all_gather(x, tag)
+        ok = all(_checksum(out[r]) == int(sums[r, 0]) for r in range(self.cp))
+        self._agree(ok, f"all_gather {tag!r}", x.device)
+        return out
+
+    def reduce_scatter_start(self, *parts, tag=None):
+        self._record("reduce_scatter", tag, list(parts))
+        return super().reduce_scatter_start(*parts, tag=tag)
+
+    def ring_start(self, send, recv, tag=None):
+        sums = self._record("ring", tag, list(send))
+        return (super().ring_start(send, recv, tag), recv, sums[(self.rank - 1) % self.cp], tag)
+
+    def ring_wait(self, handle):
+        if handle is None:
+            return
+        GroupExchange.ring_wait(handle[0])
+        self._verify_ring(handle)
+
+    def _verify_ring(self, handle):
+        _, recv, sums, tag = handle
+        ok = all(_checksum(t) == int(sums[i]) for i, t in enumerate(recv))
+        self._agree(ok, f"ring hop {tag!r}", recv[0].device)
 
 
 def zigzag_shard(x, cp, rank, dim=1):
@@ -175,7 +289,7 @@ def _ring_forward(q, k, v, rank, cp, causal, scale, kernels, exchange):
     o_acc = l_acc = o_part = l_part = lse = None
     for i in range(cp):
         nxt = recv[i % 2] if i + 1 < cp else None
-        reqs = exchange.ring_start(kv, nxt) if nxt is not None else None  # in flight during step i
+        reqs = exchange.ring_start(kv, nxt, tag=f"kv hop {i + 1}") if nxt is not None else None  # during step i
         if i == 0:
             o_acc, l_acc = kernels.fwd_rank_step(q, kv[0], kv[1], cp, rank, 0, causal, scale)
         else:
@@ -213,8 +327,8 @@ def cp_forward(q, k, v, group=None, causal=True, scale=None, form="allgather", k
         return _ring_forward(q, k, v, rank, cp, causal, scale, kernels, exchange)
     if form != "allgather":
         raise ValueError("form must be 'allgather' or 'ring'")
-    k_all = exchange.all_gather(k)
-    v_all = exchange.all_gather(v)
+    k_all = exchange.all_gather(k, tag="k")
+    v_all = exchange.all_gather(v, tag="v")
     o, lse = kernels.fwd_rank(q, k_all, v_all, cp, rank, causal, scale)
     return (o, lse, k_all, v_all) if keep_kv else (o, lse)
 
@@ -230,9 +344,9 @@ def cp_backward(q, k, v, o, lse, do, group=None, causal=True, scale=None, kv_all
     kernels = kernels or CudaKernels
     rank, cp = exchange.rank, exchange.cp
     if kv_all is None:
-        kv_all = (exchange.all_gather(k), exchange.all_gather(v))
+        kv_all = (exchange.all_gather(k, tag="k"), exchange.all_gather(v, tag="v"))
     dk_part, dv_part, pending = kernels.bwd_rank_shares(q, kv_all[0], kv_all[1], o, lse, do, cp, rank, causal, scale)
-    handle = exchange.reduce_scatter_start(dk_part, dv_part)
+    handle = exchange.reduce_scatter_start(dk_part, dv_part, tag="dk dv")
     dq = kernels.bwd_rank_dq(pending)
     dk, dv = exchange.reduce_scatter_finish(handle)
     return dq, dk, dv

@@ -10,6 +10,11 @@ checked with gloo process groups of 2 and 3 ranks on the CPU.
 * End to end with the oracle's fp64 stand-ins for the kernels: each rank's
   forward (both forms) and backward equal the uncut oracle's rows within
   1e-12, and the shards are the zigzag map's rows.
+* The checked exchange ("Megatron 面试题（一）：模型抽象与训练数据流", M024
+  follow-up: a fingerprint of every logical collective): it leaves results
+  bit-identical, and every rank raises together when one rank issues the
+  collectives in another order, passes another shape, or receives bytes
+  other than those sent (faults made on the host).
 """
 import os
 import socket
@@ -119,6 +124,83 @@ def _oracle_group_matches_uncut(rank, cp):
         assert (dq - dq_ref[:, rows]).abs().max().item() <= 1e-12
         assert (dk - zigzag_shard(dk_ref, cp, rank)).abs().max().item() <= 1e-12
         assert (dv - zigzag_shard(dv_ref, cp, rank)).abs().max().item() <= 1e-12
+
+
+def _checked_exchange_changes_nothing(rank, cp):
+    from cp_oracle_kernels import OracleKernels
+
+    from context_blockwise_causal_gb300.cp_group import CheckedExchange, cp_backward, cp_forward, zigzag_shard
+
+    b, c, hq, hkv, d = 1, 4, 4, 2, 8
+    q, k, v, do = _inputs(b, 2 * cp * c, hq, hkv, d, seed=14, dtype=torch.float64)
+    sh = lambda x: zigzag_shard(x, cp, rank)  # noqa: E731
+    ex = CheckedExchange()
+    for form in ("ring", "allgather"):
+        plain = cp_forward(sh(q), sh(k), sh(v), form=form, kernels=OracleKernels)
+        checked = cp_forward(sh(q), sh(k), sh(v), form=form, kernels=OracleKernels, exchange=ex)
+        assert all(torch.equal(a, b_) for a, b_ in zip(plain, checked)), form
+    o, lse = plain
+    grads = cp_backward(sh(q), sh(k), sh(v), o, lse, sh(do), kernels=OracleKernels)
+    grads_c = cp_backward(sh(q), sh(k), sh(v), o, lse, sh(do), kernels=OracleKernels, exchange=ex)
+    assert all(torch.equal(a, b_) for a, b_ in zip(grads, grads_c))
+    # ring: cp - 1 hops; all-gather forward: 2; backward: 2 gathers + 1 reduce-scatter
+    assert ex.sequence == (cp - 1) + 2 + 3
+
+
+def _checked_exchange_catches_order_swap(rank, cp):
+    from context_blockwise_causal_gb300.cp_group import CheckedExchange, ExchangeMismatch
+
+    ex = CheckedExchange()
+    k = torch.full((2, 3), float(rank), dtype=torch.bfloat16)
+    v = torch.full((2, 3), 10.0 + rank, dtype=torch.bfloat16)
+    # same shapes and dtypes: without the check the gathers would complete
+    # and mix K and V; rank 1 issues them in the other order
+    order = [("k", k), ("v", v)] if rank == 0 else [("v", v), ("k", k)]
+    with pytest.raises(ExchangeMismatch, match="logical id"):
+        ex.all_gather(order[0][1], tag=order[0][0])
+
+
+def _checked_exchange_catches_shape(rank, cp):
+    from context_blockwise_causal_gb300.cp_group import CheckedExchange, ExchangeMismatch
+
+    ex = CheckedExchange()
+    x = torch.zeros(2, 3 + (rank == cp - 1), dtype=torch.bfloat16)
+    with pytest.raises(ExchangeMismatch, match=f"rank {cp - 1} differs from rank 0 in the size 1"):
+        ex.all_gather(x, tag="k")
+
+
+def _checked_exchange_catches_corrupt_hop(rank, cp):
+    from cp_oracle_kernels import RecordingKernels
+
+    from context_blockwise_causal_gb300.cp_group import (CheckedExchange, ExchangeMismatch, GroupExchange, cp_forward,
+                                                         zigzag_shard)
+
+    class CorruptsOnRank0(CheckedExchange):
+        # the hop completes, then rank 0's received K changes in one element
+        # (a transfer fault made on the host) before the check
+        def ring_wait(self, handle):
+            if handle is None:
+                return
+            GroupExchange.ring_wait(handle[0])
+            if self.rank == 0:
+                handle[1][0].view(-1)[0] += 1
+            self._verify_ring(handle)
+
+    q, k, v, _ = _inputs(1, 8 * cp, 2, 1, 8, seed=15, dtype=torch.bfloat16)
+    sh = lambda x: zigzag_shard(x, cp, rank)  # noqa: E731
+    with pytest.raises(ExchangeMismatch, match=r"ring hop 'kv hop 1'.*rank\(s\) \[0\]"):
+        cp_forward(sh(q), sh(k), sh(v), form="ring", kernels=RecordingKernels(), exchange=CorruptsOnRank0())
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_checked_exchange_changes_nothing(world):
+    _run(_checked_exchange_changes_nothing, world)
+
+
+@pytest.mark.parametrize("case", [_checked_exchange_catches_order_swap, _checked_exchange_catches_shape,
+                                  _checked_exchange_catches_corrupt_hop])
+def test_checked_exchange_raises_on_every_rank(case):
+    _run(case, 2)
 
 
 @pytest.mark.parametrize("world", [2, 3])

@@ -50,7 +50,7 @@ class LocalRing:
     def __init__(self, k_shards, v_shards, rank):
         self.k, self.v, self.rank, self.cp, self.hop = k_shards, v_shards, rank, len(k_shards), 0
 
-    def ring_start(self, send, recv):
+    def ring_start(self, send, recv, tag=None):
         self.hop += 1
         j = (self.rank - self.hop) % self.cp
         recv[0].copy_(self.k[j])

@@ -13,7 +13,7 @@ ranks' shards.
   results and dQ are those rows of cpattn_fwd / cpattn_fwd_step / cpattn_bwd
   (the same work units, computed the same way).
 * The driver with a one-rank NCCL group: the collectives' code path on CUDA
-  tensors.
+  tensors, plain and checked (every collective fingerprinted).
 """
 import datetime
 import socket
@@ -24,7 +24,7 @@ import torch
 import oracle
 from context_blockwise_causal_gb300 import (cpattn_bwd, cpattn_bwd_rank, cpattn_device_status, cpattn_fwd,
                                             cpattn_fwd_rank, cpattn_fwd_rank_step, cpattn_fwd_step)
-from context_blockwise_causal_gb300.cp_group import cp_backward, cp_forward, zigzag_shard
+from context_blockwise_causal_gb300.cp_group import CheckedExchange, cp_backward, cp_forward, zigzag_shard
 from context_blockwise_causal_gb300.workloads import Workload, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -186,6 +186,15 @@ def test_driver_with_a_one_rank_nccl_group():
         for got in (g, g2):
             for a, b_ in zip(got, (dq, dk, dv)):
                 assert torch.equal(a, b_)
+        # the checked exchange: fingerprints and checksums of CUDA tensors
+        # through NCCL, results unchanged
+        ex = CheckedExchange()
+        o_c, l_c = cp_forward(x["q"], x["k"], x["v"], exchange=ex)
+        g3 = cp_backward(x["q"], x["k"], x["v"], o_c, l_c, x["do"], exchange=ex)
+        torch.cuda.synchronize()
+        assert torch.equal(o_c, o) and torch.equal(l_c, lse) and ex.sequence == 5
+        for a, b_ in zip(g3, (dq, dk, dv)):
+            assert torch.equal(a, b_)
     finally:
         dist.destroy_process_group()
 

@@ -192,6 +192,48 @@ def _checked_exchange_catches_corrupt_hop(rank, cp):
         cp_forward(sh(q), sh(k), sh(v), form="ring", kernels=RecordingKernels(), exchange=CorruptsOnRank0())
 
 
+def _rank_leaves_worker(rank, world, port, out):
+    # rank 1 leaves between steps (its process ends without entering the
+    # exchange); rank 0's next collective must end in an error, not wait
+    import datetime
+
+    sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=10))
+    if rank == 1:
+        dist.destroy_process_group()
+        return
+    from cp_oracle_kernels import RecordingKernels
+
+    from context_blockwise_causal_gb300.cp_group import cp_forward, zigzag_shard
+
+    q, k, v, _ = _inputs(1, 8 * world, 2, 1, 8, seed=16, dtype=torch.bfloat16)
+    sh = lambda x: zigzag_shard(x, world, rank)  # noqa: E731
+    import time
+
+    t0 = time.time()
+    try:
+        cp_forward(sh(q), sh(k), sh(v), form="allgather", kernels=RecordingKernels())
+        out[rank] = "returned"
+    except Exception as e:  # the collective reports the lost peer
+        out[rank] = f"raised {type(e).__name__} after {time.time() - t0:.1f} s"
+    finally:
+        try:
+            dist.destroy_process_group()
+        except Exception:
+            pass
+
+
+@pytest.mark.timeout(120)
+def test_a_rank_that_leaves_ends_the_others_collective_with_an_error():
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_rank_leaves_worker, args=(2, _free_port(), out), nprocs=2, join=True)
+        got = dict(out)
+    assert got[0].startswith("raised"), got
+
+
 @pytest.mark.parametrize("world", [2, 3])
 def test_checked_exchange_changes_nothing(world):
     _run(_checked_exchange_changes_nothing, world)

@@ -75,3 +75,25 @@ def test_timed_region_takes_the_slowest_rank_gloo():
 
     assert bench._max_over_ranks(3.5, torch.device("cpu"), 1) == 3.5
 
+
+
+def test_profile_traffic_only_for_the_current_kernel_source(tmp_path, monkeypatch):
+    """bench.py reports a kernel's DRAM traffic from its committed ncu summary
+    only when the summary was taken on the kernel source as it is now (the
+    sha256 in the summary matches); otherwise traffic is null."""
+    import hashlib
+
+    import bench
+
+    src_dir = tmp_path / "context_blockwise_causal_gb300" / "csrc"
+    src_dir.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    src = src_dir / "k.cuh"
+    src.write_bytes(b"__global__ void k() {}\n")
+    sha = hashlib.sha256(src.read_bytes()).hexdigest()
+    (tmp_path / "profiles" / "k_w.md").write_text(f"kernel_source_sha256: {sha}\ndram_bytes_per_launch: 12345\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench._profile_traffic("k.cuh", "k_w.md") == 12345.0
+    src.write_bytes(b"__global__ void k() { }\n")  # the kernel changed since the capture
+    assert bench._profile_traffic("k.cuh", "k_w.md") is None
+    assert bench._profile_traffic("k.cuh", "missing.md") is None

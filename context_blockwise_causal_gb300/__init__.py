@@ -16,6 +16,7 @@ from ._build import CHECKED_LIB_PATH, LIB_PATH, build  # noqa: F401
 
 __all__ = [
     "CpattnError",
+    "cpattn_set_max_ctas",
     "cpattn_fwd",
     "cpattn_fwd_step",
     "cpattn_lse_merge",
@@ -88,6 +89,8 @@ def checked_library():
 
 def _declare(lib):
     """Argument and result types of every entry point of a loaded library."""
+    lib.cpattn_set_max_ctas.argtypes = [_i]
+    lib.cpattn_set_max_ctas.restype = _i
     lib.cpattn_fwd.argtypes = [_p, _p, _p, _p, _p] + [_i] * 7 + [_p]
     lib.cpattn_fwd.restype = _i
     lib.cpattn_fwd_ex.argtypes = [_p, _p, _p, _p, _p] + [_i] * 7 + [ctypes.c_float, _p]
@@ -554,6 +557,15 @@ def cpattn_bwd_rank(q, k_all, v_all, o, lse, do, cp, rank, causal=True, scale=No
     if rc:
         raise CpattnError(rc, "cpattn_bwd_rank" if stage is None else "cpattn_bwd_rank_stage")
     return dq, dk_part, dv_part
+
+
+def cpattn_set_max_ctas(max_ctas):
+    """Cap the persistent attention kernels' grid at max_ctas CTAs (one per
+    SM; 0 = every SM), leaving the other SMs to kernels on other streams.
+    Outputs are bit-identical for any cap. Process-wide."""
+    rc = library().cpattn_set_max_ctas(int(max_ctas))
+    if rc:
+        raise CpattnError(rc, "cpattn_set_max_ctas")
 
 
 def cpattn_zigzag_index(s, cp):

@@ -30,6 +30,10 @@ can be checked on its own: tests pass recording or CPU stand-ins. The
 default kernels are the CUDA library's, and it fails loudly when that
 library is missing. ``exchange=CheckedExchange(group)`` fingerprints every
 collective across the ranks (a debugging aid, see its docstring).
+
+The attention kernels take a whole SM per CTA, so a send/receive kernel of
+the communication library runs during a ring step only on SMs they leave
+free: cpattn_set_max_ctas caps their grid (outputs unchanged).
 """
 import zlib
 

@@ -42,6 +42,16 @@ struct DeviceInfo {
 };
 DeviceInfo g_devs[kMaxDevices];
 std::mutex g_mu;
+// Cap on the grid of the persistent attention kernels (0: one CTA per SM).
+std::atomic<int> g_max_ctas{0};
+
+// Grid of a persistent kernel over `units` work units: one CTA per SM, at
+// most the cap set by cpattn_set_max_ctas, at most one per unit.
+int persistent_grid(const DeviceInfo* di, int64_t units) {
+  const int cap_set = g_max_ctas.load(std::memory_order_relaxed);
+  const int cap = cap_set > 0 && cap_set < di->num_sms ? cap_set : di->num_sms;
+  return units < cap ? int(units) : cap;
+}
 
 int device_info(DeviceInfo** out) {
   int dev = 0;
@@ -123,10 +133,10 @@ int launch_fwd_ring(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensor
   FwdArgs args = args_in;
   if (kTP) {  // K/V of one (sequence, KV head): s tokens of K and of V
     const int64_t per_pair = 4ll * args.g.s * D;
-    set_tile_pair_blocks(args.g, di->num_sms, int(kTilePairKvBudget / per_pair));
+    set_tile_pair_blocks(args.g, persistent_grid(di, int64_t(1) << 31), int(kTilePairKvBudget / per_pair));
   }
   const int units = fwd_num_units(args.g);
-  const int grid = units < di->num_sms ? units : di->num_sms;
+  const int grid = persistent_grid(di, units);
   cpattn_fwd_kernel<D, kStep, kRing, kTP, kShort><<<grid, kFwdThreads, C::kSmemBytes, st>>>(tq, tk, tv, args);
   return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_LAUNCH_FAILED;
 }
@@ -427,11 +437,11 @@ int launch_bwd_stage(int stage, const CUtensorMap& tq, const CUtensorMap& tk, co
     cpattn_bwd_pre_kernel<D><<<pre_grid, 256, 0, st>>>(args);
   } else if (stage == 1) {
     const int units = bwd_num_units(args.g);
-    cpattn_bwd_dkdv_kernel<D, kShort><<<units < di->num_sms ? units : di->num_sms, kBwdThreads,
+    cpattn_bwd_dkdv_kernel<D, kShort><<<persistent_grid(di, units), kBwdThreads,
                                         DkdvCfg<D>::kSmemBytes, st>>>(tq, tk, tv, tdo, args);
   } else {
     const int units = dq_num_units(args.g);
-    cpattn_bwd_dq_kernel<D, kShort><<<units < di->num_sms ? units : di->num_sms, kBwdThreads, DqCfg<D>::kSmemBytes,
+    cpattn_bwd_dq_kernel<D, kShort><<<persistent_grid(di, units), kBwdThreads, DqCfg<D>::kSmemBytes,
                                       st>>>(tq, tk, tv, tdo, args);
   }
   return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_LAUNCH_FAILED;
@@ -955,6 +965,12 @@ extern "C" int cpattn_device_status(void* stream, int* status) {
     return CPATTN_ERR_CUDA;
   *status = int(h);
   return h ? CPATTN_ERR_TIMEOUT : CPATTN_OK;
+}
+
+extern "C" int cpattn_set_max_ctas(int max_ctas) {
+  if (max_ctas < 0) return CPATTN_ERR_INVALID_ARG;
+  g_max_ctas.store(max_ctas, std::memory_order_relaxed);
+  return CPATTN_OK;
 }
 
 extern "C" const char* cpattn_strerror(int code) {

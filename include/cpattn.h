@@ -364,6 +364,20 @@ int cpattn_zigzag_index(int s, int cp, int64_t* global_of_local);
 int cpattn_device_status(void* stream, int* status);
 
 /*
+ * Caps the grid of the persistent attention kernels (forward in every form,
+ * dK/dV, dQ) at max_ctas CTAs, one per SM; 0 (the default) uses every SM.
+ * Each CTA takes a whole SM (all its registers and nearly all its shared
+ * memory), so a kernel launched on another stream -- say a communication
+ * library's send/receive kernel during a ring CP step ("大模型面试宝典 ·
+ * Megatron-LM 篇", 3.2: the next shard travels while a step computes) --
+ * runs meanwhile only on SMs the cap leaves free. Results do not depend on
+ * the grid: every work unit is computed the same way on whichever CTA takes
+ * it, so outputs are bit-identical. Process-wide; applies to launches made
+ * after the call. Returns CPATTN_ERR_INVALID_ARG for max_ctas < 0.
+ */
+int cpattn_set_max_ctas(int max_ctas);
+
+/*
  * Self-test of the timeout path: launches one block whose single waiting
  * thread waits on a barrier phase that nothing completes, giving up after
  * limit_ns nanoseconds (1 .. 2e9) exactly as the kernels' waits do. It then

@@ -243,3 +243,9 @@ for name, call in calls.items():
     assert lines["cpattn_zigzag_index"] == "RuntimeError True"
     # a CPU tensor is refused before the library is reached; either way nothing computes it
     assert not lines["cpattn_fwd"].startswith("returned")
+
+
+def test_grid_cap_argument(lib):
+    assert lib.cpattn_set_max_ctas(-1) == -1  # CPATTN_ERR_INVALID_ARG
+    assert lib.cpattn_set_max_ctas(37) == 0
+    assert lib.cpattn_set_max_ctas(0) == 0

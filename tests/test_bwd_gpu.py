@@ -190,3 +190,53 @@ def test_random_geometries_forward_and_backward(b, s, hq, hkv, d, cp, causal):
     for name, got, ref in (("dq", dq, refs[0]), ("dk", dk, refs[1]), ("dv", dv, refs[2])):
         err = rel_l2(got.float().cpu(), ref)
         assert err <= REL_L2, f"{name} rel L2 {err:.3e}"
+
+
+@pytest.mark.parametrize("cap", [1, 37])
+def test_grid_cap_gives_bit_identical_results(cap):
+    """cpattn_set_max_ctas: the persistent kernels on fewer CTAs than SMs
+    (one CTA, or 37) compute every output bit for bit as on the full grid --
+    forward, step form and backward; head pairs, tile pairs, ragged chunks,
+    no mask, d = 64."""
+    from context_blockwise_causal_gb300 import cpattn_fwd_step, cpattn_set_max_ctas
+
+    geoms = [(1, 960, 6, 2, 128, 3, True), (2, 2048, 4, 4, 128, 2, True), (1, 768, 3, 1, 64, 3, False)]
+    for b, s, hq, hkv, d, cp, causal in geoms:
+        w = Workload("cap", b=b, s=s, hq=hq, hkv=hkv, d=d, cp=cp, causal=causal, backward=True, seed=41 + s)
+        x = make_inputs(w, device="cuda")
+
+        def run():
+            o, lse = cpattn_fwd(x["q"], x["k"], x["v"], cp, causal=causal)
+            grads = cpattn_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], cp, causal=causal)
+            step = cpattn_fwd_step(x["q"], x["k"], x["v"], cp, cp - 1, causal=causal)
+            return (o, lse, *grads, *step)
+
+        ref = run()
+        try:
+            cpattn_set_max_ctas(cap)
+            got = run()
+        finally:
+            cpattn_set_max_ctas(0)
+        torch.cuda.synchronize()
+        assert cpattn_device_status() == 0
+        for a, b_ in zip(ref, got):
+            assert torch.equal(a, b_), (b, s, hq, hkv, d, cp, causal)
+
+
+def test_grid_cap_with_tile_pair_blocks():
+    """Tile-pair units in L2-sized head blocks are padded to whole rounds of
+    the grid: a capped grid changes the padding and the order of the units,
+    not the outputs."""
+    from context_blockwise_causal_gb300 import cpattn_set_max_ctas
+
+    w = Workload("capblk", b=8, s=4096, hq=24, hkv=8, d=128, cp=2, causal=True, seed=43)
+    x = make_inputs(w, device="cuda")
+    ref = cpattn_fwd(x["q"], x["k"], x["v"], w.cp)
+    try:
+        cpattn_set_max_ctas(37)
+        got = cpattn_fwd(x["q"], x["k"], x["v"], w.cp)
+    finally:
+        cpattn_set_max_ctas(0)
+    torch.cuda.synchronize()
+    assert cpattn_device_status() == 0
+    assert torch.equal(ref[0], got[0]) and torch.equal(ref[1], got[1])
